@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for the MoE decode layer step.
+
+Shared by the tests, the bench and the smoke check. This module only draws and
+encodes inputs (normal draws, bf16 rounding, NVFP4 quantisation); it holds none of
+the layer's arithmetic, and no expected value is ever computed here.
+
+Recipe (the pages publish no weights, so all inputs are synthetic):
+  * weights ~ N(0, 0.02^2), rounded to bf16 (torch RNG on the target device,
+    drawn in chunks of experts so a 6 GB layer needs no 24 GB float32 temporary);
+  * hidden rows ~ N(0, 1) as float32, rounded to bf16. With rho > 0 the rows are
+    correlated: x_m = sqrt(rho) z_0 + sqrt(1 - rho) z_m, with z_0 shared, so the
+    rows of a speculative verify chain route to partly overlapping experts;
+  * every row draws its z_m from its own stream keyed (seed, row, attempt), so a
+    caller that needs a top-k margin can redraw one row alone;
+  * NVFP4 weights come from the same bf16-free N(0, 0.02^2) float32 draws,
+    quantised with tensor scale amax / (6 * 448), e4m3 block scales
+    amax_block / (6 * tensor_scale) and e2m1 codes rounded to nearest-even.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class LayerShape:
+    """Sizes of one MoE layer: H hidden, I expert intermediate, E routed experts."""
+
+    hidden: int
+    inter: int
+    num_experts: int
+    top_k: int
+    num_shared: int = 1
+    wdtype: str = "bf16"  # "bf16" or "nvfp4"
+
+    def expert_bytes(self) -> int:
+        """HBM bytes of one expert's gate/up/down weights (codes + block scales)."""
+        h, i = self.hidden, self.inter
+        if self.wdtype == "bf16":
+            return 3 * h * i * 2
+        return 3 * h * i // 2 + 3 * h * i // 16
+
+    def router_bytes(self) -> int:
+        return self.num_experts * self.hidden * 2
+
+
+# The layer shapes the pages describe (model tables of the Ling-3.0-flash and
+# Muse Spark posts) plus a tiny one for fast checks.
+TINY = LayerShape(hidden=256, inter=128, num_experts=16, top_k=2, num_shared=1)
+LING = LayerShape(hidden=2560, inter=768, num_experts=512, top_k=8, num_shared=1)
+MUSE_NVFP4 = LayerShape(hidden=4096, inter=1024, num_experts=256, top_k=8,
+                        num_shared=0, wdtype="nvfp4")
+
+
+def algorithmic_bytes(shape: LayerShape, distinct_routed: int) -> int:
+    """Bytes one layer step must read: router + each distinct routed expert + shared."""
+    return shape.router_bytes() + (distinct_routed + shape.num_shared) * shape.expert_bytes()
+
+
+# ----------------------------------------------------------------------------
+# hidden rows
+# ----------------------------------------------------------------------------
+
+
+def hidden_rows(m_rows: int, hidden: int, seed: int, rho: float = 0.0,
+                attempts=None) -> torch.Tensor:
+    """bf16 [M, H] hidden rows on the CPU (see the module recipe)."""
+    rng0 = np.random.default_rng([seed, 0x5EED, 0])
+    z0 = rng0.standard_normal(hidden)
+    rows = np.empty((m_rows, hidden), np.float64)
+    for m in range(m_rows):
+        a = 0 if attempts is None else int(attempts[m])
+        zm = np.random.default_rng([seed, 0x5EED, 1 + m, a]).standard_normal(hidden)
+        rows[m] = math.sqrt(rho) * z0 + math.sqrt(1.0 - rho) * zm
+    return torch.from_numpy(rows.astype(np.float32)).to(torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------
+# weights
+# ----------------------------------------------------------------------------
+
+
+def _normal(shape, gen, device, std):
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * std
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _bf16_experts(n, rows, cols, seed, device, std, chunk_bytes=1 << 29):
+    out = torch.empty((n, rows, cols), dtype=torch.bfloat16, device=device)
+    per = max(1, chunk_bytes // (rows * cols * 4))
+    for s in range(0, n, per):
+        e = min(n, s + per)
+        g = _gen(seed * 1000003 + s, device)
+        out[s:e] = _normal((e - s, rows, cols), g, device, std).to(torch.bfloat16)
+    return out
+
+
+def _e2m1_codes(q: torch.Tensor) -> torch.Tensor:
+    """Round float32 values to e2m1 (nearest, ties to even code), saturating at 6."""
+    mag = q.abs()
+    code = torch.zeros_like(mag, dtype=torch.uint8)
+    # (lower bound, inclusive?) -> code; the tie at each midpoint goes to the even code
+    code = torch.where(mag > 0.25, 1, code)
+    code = torch.where(mag >= 0.75, 2, code)
+    code = torch.where(mag > 1.25, 3, code)
+    code = torch.where(mag >= 1.75, 4, code)
+    code = torch.where(mag > 2.5, 5, code)
+    code = torch.where(mag >= 3.5, 6, code)
+    code = torch.where(mag > 5.0, 7, code).to(torch.uint8)
+    sign = ((q < 0) & (code != 0)).to(torch.uint8) << 3
+    return code | sign
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """Quantise float32 [..., R, K] to NVFP4 with one tensor scale over the last two dims.
+
+    Returns (codes uint8 [..., R, K/2], scales uint8 [..., R, K/16], tensor_scale
+    float32 [...]).
+    """
+    *lead, r, k = w.shape
+    amax = w.abs().amax(dim=(-2, -1))
+    ts = (amax / (6.0 * 448.0)).to(torch.float32)
+    ts = torch.where(ts > 0, ts, torch.ones_like(ts))
+    tsx = ts[..., None, None]
+    blocks = w.reshape(*lead, r, k // 16, 16)
+    bmax = blocks.abs().amax(dim=-1)
+    sb = (bmax / (6.0 * tsx)).clamp(max=448.0).to(torch.float8_e4m3fn)
+    sbv = sb.to(torch.float32)
+    denom = (sbv * tsx)[..., None]
+    q = torch.where(denom > 0, blocks / torch.where(denom > 0, denom, torch.ones_like(denom)),
+                    torch.zeros_like(blocks))
+    codes = _e2m1_codes(q).reshape(*lead, r, k)
+    packed = codes[..., 0::2] | (codes[..., 1::2] << 4)
+    return packed.contiguous(), sb.view(torch.uint8).contiguous(), ts
+
+
+def _nvfp4_experts(n, inter, hidden, seed, device, std):
+    """NVFP4 gate/up [n, 2I, H] and down [n, H, I] with per-projection tensor scales."""
+    w13q = torch.empty((n, 2 * inter, hidden // 2), dtype=torch.uint8, device=device)
+    w13s = torch.empty((n, 2 * inter, hidden // 16), dtype=torch.uint8, device=device)
+    w13g = torch.empty((n, 2), dtype=torch.float32, device=device)
+    w2q = torch.empty((n, hidden, inter // 2), dtype=torch.uint8, device=device)
+    w2s = torch.empty((n, hidden, inter // 16), dtype=torch.uint8, device=device)
+    w2g = torch.empty((n,), dtype=torch.float32, device=device)
+    per = max(1, (1 << 29) // (3 * hidden * inter * 4))
+    for s in range(0, n, per):
+        e = min(n, s + per)
+        g = _gen(seed * 1000003 + s, device)
+        w13 = _normal((e - s, 2 * inter, hidden), g, device, std)
+        w2 = _normal((e - s, hidden, inter), g, device, std)
+        for p in range(2):  # gate rows, then up rows: one tensor scale each
+            q, sc, ts = quantize_nvfp4(w13[:, p * inter:(p + 1) * inter])
+            w13q[s:e, p * inter:(p + 1) * inter] = q
+            w13s[s:e, p * inter:(p + 1) * inter] = sc
+            w13g[s:e, p] = ts
+        q, sc, ts = quantize_nvfp4(w2)
+        w2q[s:e], w2s[s:e], w2g[s:e] = q, sc, ts
+    return w13q, w13s, w13g, w2q, w2s, w2g
+
+
+def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) -> dict:
+    """All weights of one layer as torch tensors on ``device``.
+
+    bf16:  router_w [E, H], w13 [E, 2I, H], w2 [E, H, I], sh_w13 [S, 2I, H], sh_w2 [S, H, I]
+    nvfp4: router_w bf16 [E, H]; w13_q uint8 [E, 2I, H/2], w13_s uint8 [E, 2I, H/16],
+           w13_gs f32 [E, 2], w2_q uint8 [E, H, I/2], w2_s uint8 [E, H, I/16],
+           w2_gs f32 [E]; the same with an ``sh_`` prefix for the S shared experts.
+    """
+    h, i, e, s = shape.hidden, shape.inter, shape.num_experts, shape.num_shared
+    g = _gen(seed * 7919 + 1, device)
+    layer = {"router_w": _normal((e, h), g, device, std).to(torch.bfloat16)}
+    if shape.wdtype == "bf16":
+        layer["w13"] = _bf16_experts(e, 2 * i, h, seed * 7919 + 2, device, std)
+        layer["w2"] = _bf16_experts(e, h, i, seed * 7919 + 3, device, std)
+        layer["sh_w13"] = _bf16_experts(s, 2 * i, h, seed * 7919 + 4, device, std)
+        layer["sh_w2"] = _bf16_experts(s, h, i, seed * 7919 + 5, device, std)
+    elif shape.wdtype == "nvfp4":
+        names = ("w13_q", "w13_s", "w13_gs", "w2_q", "w2_s", "w2_gs")
+        for n, t in zip(names, _nvfp4_experts(e, i, h, seed * 7919 + 2, device, std)):
+            layer[n] = t
+        for n, t in zip(names, _nvfp4_experts(s, i, h, seed * 7919 + 4, device, std)):
+            layer["sh_" + n] = t
+    else:
+        raise ValueError(f"unknown weight dtype {shape.wdtype!r}")
+    return layer
