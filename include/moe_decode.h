@@ -1,0 +1,202 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 small-batch MoE decode layer step.
+ *
+ * One call computes, for M = 1..8 token rows, the MoE block of a decoder layer:
+ *
+ *   1. router GEMV      l[m,e] = sum_h x[m,h] Wr[e,h]          (bf16 in, fp32 acc)
+ *   2. top-k select     the k largest l[m,:], ties to the lower expert id, with
+ *                       renormalised weights w_j = exp(l_j - l_max) / sum_sel exp(.)
+ *                       (= softmax over all experts -> top-k -> renormalise)
+ *   3. routed experts   h = silu(Wg_e x) * (Wu_e x),  y_e = Wd_e h   (fp32)
+ *   4. shared experts   the same SwiGLU MLP with the shared weights, weight 1
+ *   5. combine          out = bf16_rne(r + routed_scale * sum_j w_j y_{e_j} + sum_s y_s)
+ *
+ * Sources: the Ling-3.0-flash batch-1 decode blog (LMSYS) -- section "PDL:
+ * stacking the latency floors of small kernels" (router chain norm -> gate
+ * matvec -> top-k; the MoE chain up-GEMM -> activation -> down-GEMM -> combine;
+ * the combine is one fp32 sum times a scale with a single final cast), section
+ * "Two fusions and a retune" (silu(gate) * up in fp32 inside the up-GEMM, w13 =
+ * [gate; up]), section "bf16 router gate and lm_head" (bf16 router matvec), and
+ * its model table (512 routed + 1 shared expert, top-8(+1), moe_intermediate 768,
+ * hidden 2560); "Muse Spark Open Ultrafast", section "The model" (8 of 256
+ * experts, NVFP4 expert weights); "SGLang Low-Latency Mode: kernels and
+ * runtime", section "Low-Latency-Specific Optimizations" item 3 (at most eight
+ * rows: expert row sets placed by bitmap and population count). The pages do not
+ * fix the scoring rule; softmax -> top-k -> renormalise is the one implemented.
+ *
+ * Threading: a handle may be used from one host thread at a time. Runs on one
+ * handle must not overlap on the GPU (they share the handle's scratch); issue
+ * them on one stream, or order the streams.
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_DECODE_ABI_VERSION 1
+
+/* A cudaStream_t. NULL means the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, M out of range, bad option */
+  MOE_ERR_UNSUPPORTED = 2,    /* a config outside the supported shapes (see below)   */
+  MOE_ERR_CUDA = 3,           /* a CUDA runtime call failed                          */
+  MOE_ERR_DEVICE_TIMEOUT = 4, /* a device-side wait ran past its limit (see get_status) */
+  MOE_ERR_OOM = 5             /* device allocation failed in create                  */
+} moe_status;
+
+typedef enum moe_wdtype {
+  MOE_W_BF16 = 0,  /* expert weights bf16                                     */
+  MOE_W_NVFP4 = 1  /* expert weights e2m1 codes + e4m3 block-16 scales + fp32 */
+} moe_wdtype;
+
+typedef enum moe_score {
+  MOE_SCORE_SOFTMAX_TOPK_RENORM = 0 /* softmax over E -> top-k -> renormalise */
+} moe_score;
+
+typedef enum moe_sched {
+  MOE_SCHED_PERSISTENT = 0, /* one cooperative kernel; phases hand off through tagged data */
+  MOE_SCHED_PDL_CHAIN = 1,  /* three kernels (router, gate/up, down) chained with PDL      */
+  MOE_SCHED_CHAIN = 2       /* the same three kernels without PDL (plain stream order)     */
+} moe_sched;
+
+/*
+ * Layer configuration. Supported (create/config_check return MOE_ERR_UNSUPPORTED
+ * otherwise):
+ *   2 <= num_experts <= 1024, even;  1 <= top_k <= min(16, num_experts);
+ *   0 <= num_shared <= 4;  1 <= max_rows <= 8;
+ *   bf16:  hidden % 8 == 0, 64 <= hidden <= 4096; inter % 8 == 0 and inter / 8
+ *          either a power of two <= 32 or a multiple of 32 no larger than 384;
+ *   nvfp4: hidden % 256 == 0, 256 <= hidden <= 8192; inter % 256 == 0, inter <= 12288;
+ *   routed_scale finite; rms_eps > 0 when pre_rmsnorm.
+ */
+typedef struct moe_decode_config {
+  int32_t hidden;      /* H: model width                                      */
+  int32_t inter;       /* I: expert intermediate size (shared experts too)    */
+  int32_t num_experts; /* E: routed experts                                   */
+  int32_t top_k;       /* k: experts per row                                  */
+  int32_t num_shared;  /* S: always-on shared experts (weight 1)              */
+  int32_t max_rows;    /* largest M passed to run                             */
+  int32_t wdtype;      /* moe_wdtype                                          */
+  int32_t score;       /* moe_score                                           */
+  float routed_scale;  /* multiplies the routed sum (1.0 when unused)         */
+  int32_t pre_rmsnorm; /* 1: the layer input is bf16(RMSNorm(x)), gamma = 1  */
+  float rms_eps;       /* RMSNorm epsilon (1e-6)                              */
+  int32_t sched;       /* moe_sched                                           */
+} moe_decode_config;
+
+/*
+ * Weight pointers: device memory, BORROWED (the caller keeps ownership and must
+ * keep them alive and unchanged until destroy). Every pointer 16-byte aligned.
+ * Row-major, no padding:
+ *   router_w        bf16  [E, H]
+ *   bf16:   w13     bf16  [E, 2I, H]   rows 0..I-1 gate, I..2I-1 up
+ *           w2      bf16  [E, H, I]
+ *   nvfp4:  w13     uint8 [E, 2I, H/2] e2m1 codes, element 2i in the low nibble
+ *           w13_scale uint8 [E, 2I, H/16] e4m3 scale per 16 consecutive elements
+ *           w13_gscale fp32 [E, 2]     tensor scale of the gate rows, of the up rows
+ *           w2      uint8 [E, H, I/2], w2_scale uint8 [E, H, I/16], w2_gscale fp32 [E]
+ *   sh_*            the same for the S shared experts (leading dim S)
+ * Unused pointers (scales for bf16, shared for S = 0) may be NULL.
+ */
+typedef struct moe_decode_weights {
+  const void* router_w;
+  const void* w13;
+  const void* w2;
+  const void* w13_scale;
+  const void* w2_scale;
+  const float* w13_gscale;
+  const float* w2_gscale;
+  const void* sh_w13;
+  const void* sh_w2;
+  const void* sh_w13_scale;
+  const void* sh_w2_scale;
+  const float* sh_w13_gscale;
+  const float* sh_w2_gscale;
+} moe_decode_weights;
+
+typedef struct moe_decode_handle moe_decode_handle;
+
+/* Validates a config on the host. Makes no CUDA call. */
+moe_status moe_decode_config_check(const moe_decode_config* cfg);
+
+/*
+ * Builds a handle for the current CUDA device: validates cfg and the weight
+ * pointers, allocates the handle's device scratch (control words, tagged
+ * logits and intermediate activations, host-call staging buffers) and plans the
+ * launch shape from the device's SM count and shared memory. Copies nothing and
+ * repacks no weight. On error *out is NULL and nothing stays allocated.
+ */
+moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weights* w,
+                             moe_decode_handle** out);
+
+/*
+ * Enqueues one layer step on `stream`; returns without waiting.
+ *   x        bf16 [M, H] device, layer input (normalised inside when pre_rmsnorm)
+ *   residual bf16 [M, H] device
+ *   out      bf16 [M, H] device; may be the same buffer as residual and/or x
+ *   m_rows   1 <= M <= cfg.max_rows
+ *   topk_idx int32 [M, k] device or NULL: chosen experts, descending weight
+ *   topk_w   fp32  [M, k] device or NULL: their renormalised weights
+ * All device pointers 16-byte aligned. Allocates nothing, never synchronises and
+ * never reads device memory back, so it can be captured in a CUDA graph. Returns
+ * only argument and launch errors; device-side wait timeouts are reported by
+ * moe_decode_get_status.
+ */
+moe_status moe_decode_run(moe_decode_handle* h, const void* x, const void* residual, void* out,
+                          int32_t m_rows, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/*
+ * The same step from host memory: copies x and residual (bf16 [M, H], host) into
+ * the handle's staging buffers, runs, copies out (and topk_idx / topk_w when not
+ * NULL, host) back, and synchronises `stream`. Host buffers should be pinned for
+ * speed; pageable memory works. Returns the device status as get_status does.
+ */
+moe_status moe_decode_run_host(moe_decode_handle* h, const void* x_host, const void* residual_host,
+                               void* out_host, int32_t m_rows, int32_t* topk_idx_host,
+                               float* topk_w_host, moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the handle's device status word.
+ * MOE_ERR_DEVICE_TIMEOUT means some device-side wait of an earlier run on this
+ * handle gave up after the wait limit; that run's outputs are undefined.
+ */
+moe_status moe_decode_get_status(moe_decode_handle* h, moe_stream_t stream);
+
+/* Options for moe_decode_set_option / moe_decode_get_info. */
+enum {
+  MOE_OPT_SCHED = 1,           /* moe_sched of later runs                           */
+  MOE_OPT_WAIT_TIMEOUT_NS = 2, /* device wait limit in ns (default 1e9)             */
+  MOE_OPT_TEST_FLAGS = 3,      /* testing only: 1 = router results are never published,
+                                  so every wait on them runs into the limit          */
+  MOE_INFO_GRID = 16,          /* CTAs per kernel                                   */
+  MOE_INFO_THREADS = 17,       /* threads per CTA                                   */
+  MOE_INFO_SMEM = 18,          /* dynamic shared memory per CTA, bytes              */
+  MOE_INFO_RING_SLOTS = 19,    /* shared-memory weight ring: slots                  */
+  MOE_INFO_SLOT_BYTES = 20,    /*                            bytes per slot         */
+  MOE_INFO_KERNELS_PER_RUN = 21,
+  MOE_INFO_SCRATCH_BYTES = 22
+};
+moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value);
+moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value);
+
+/* Frees the handle's scratch (waits for the device first). NULL is a no-op. */
+moe_status moe_decode_destroy(moe_decode_handle* h);
+
+/* Static text for a status code. */
+const char* moe_decode_status_string(moe_status s);
+
+/* MOE_DECODE_ABI_VERSION of the loaded library. */
+int32_t moe_decode_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DECODE_H */

@@ -1,0 +1,408 @@
+// C ABI of the MoE decode layer step: config validation, launch planning,
+// scratch ownership and kernel launches. See include/moe_decode.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/moe_decode.h"
+#include "kernel_table.h"
+#include "moe_params.h"
+
+using moe::Params;
+
+struct moe_decode_handle {
+  moe_decode_config cfg;
+  Params base;       // everything but the per-run pointers and M
+  int device = 0;
+  int sched = MOE_SCHED_PERSISTENT;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  uint16_t* stage_x = nullptr;  // run_host staging
+  uint16_t* stage_r = nullptr;
+  uint16_t* stage_out = nullptr;
+  int32_t* stage_idx = nullptr;
+  float* stage_w = nullptr;
+};
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+moe_status check_config(const moe_decode_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  const int H = c->hidden, I = c->inter, E = c->num_experts, K = c->top_k;
+  if (H <= 0 || I <= 0 || E <= 0 || K <= 0 || c->num_shared < 0 || c->max_rows <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX_TOPK_RENORM) return MOE_ERR_UNSUPPORTED;
+  if (c->sched < MOE_SCHED_PERSISTENT || c->sched > MOE_SCHED_CHAIN) return MOE_ERR_UNSUPPORTED;
+  if (E < 2 || E > 1024 || (E & 1)) return MOE_ERR_UNSUPPORTED;
+  if (K > 16 || K > E) return MOE_ERR_UNSUPPORTED;
+  if (c->num_shared > 4 || c->max_rows > 8) return MOE_ERR_UNSUPPORTED;
+  if (!std::isfinite(c->routed_scale)) return MOE_ERR_INVALID_ARG;
+  if (c->pre_rmsnorm && !(c->rms_eps > 0.0f && std::isfinite(c->rms_eps))) return MOE_ERR_INVALID_ARG;
+  if (c->wdtype == MOE_W_BF16) {
+    if (H % 8 || H < 64 || H > 4096) return MOE_ERR_UNSUPPORTED;
+    const int tg = I / 8;
+    if (I % 8) return MOE_ERR_UNSUPPORTED;
+    if (!((tg <= 32 && pow2(tg)) || (tg % 32 == 0 && tg <= moe::kNC * 32))) return MOE_ERR_UNSUPPORTED;
+  } else if (c->wdtype == MOE_W_NVFP4) {
+    if (H % 256 || H < 256 || H > 4096) return MOE_ERR_UNSUPPORTED;
+    if (I % 256 || I / 32 > moe::kNC * 32) return MOE_ERR_UNSUPPORTED;
+  } else {
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+// Plans the per-CTA layout for a device with `sms` SMs and `smem_optin` bytes
+// of opt-in shared memory per block.
+moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) {
+  std::memset(&p, 0, sizeof(p));
+  const int H = c.hidden, I = c.inter, E = c.num_experts, K = c.top_k, S = c.num_shared;
+  const int maxm = c.max_rows;
+  p.H = H; p.I = I; p.E = E; p.K = K; p.S = S; p.maxm = maxm;
+  p.fmt = c.wdtype == MOE_W_BF16 ? moe::FMT_BF16 : moe::FMT_NVFP4;
+  p.routed_scale = c.routed_scale;
+  p.rms_eps = c.rms_eps;
+  p.pre_rmsnorm = c.pre_rmsnorm ? 1 : 0;
+  if (p.fmt == moe::FMT_BF16) {
+    p.nchunk_h = H / 8; p.row13 = 2 * H; p.sc13 = 0;
+    p.nchunk_i = I / 8; p.row2 = 2 * I; p.sc2 = 0;
+  } else {
+    p.nchunk_h = H / 32; p.row13 = H / 2; p.sc13 = H / 16;
+    p.nchunk_i = I / 32; p.row2 = I / 2; p.sc2 = I / 16;
+  }
+  p.tg = p.nchunk_i;
+  p.ng = moe::kNC * 32 / p.tg;
+  p.pair_bytes = 2 * (p.row13 + p.sc13);
+  p.rpair_bytes = 4 * H;
+  p.grid = sms;
+  p.nslot_max = S + std::min(E, maxm * K);
+  // fixed shared-memory blocks
+  size_t off = 0;
+  auto take = [&](size_t bytes, size_t align) {
+    off = round_up(off, align);
+    const size_t at = off;
+    off += bytes;
+    return static_cast<int>(at);
+  };
+  p.off_full = take(moe::kMaxSlots * 8, 8);
+  p.off_empty = take(moe::kMaxSlots * 8, 8);
+  p.off_x = take((size_t)maxm * H * 2, 16);
+  p.off_hs = take((size_t)2 * maxm * I * 4, 16);
+  p.off_sel_e = take((size_t)maxm * K * 4, 4);
+  p.off_sel_w = take((size_t)maxm * K * 4, 4);
+  p.off_emask = take((size_t)E * 4, 4);
+  p.off_slot_of = take((size_t)E * 4, 4);
+  p.off_slot_e = take((size_t)p.nslot_max * 4, 4);
+  p.off_slot_mask = take((size_t)p.nslot_max * 4, 4);
+  p.off_slot_w = take((size_t)p.nslot_max * maxm * 4, 4);
+  p.off_red = take((size_t)moe::kNC * moe::kRpgMax * 8 * 4, 16);
+  p.off_misc = take(moe::MISC_WORDS * 4, 16);
+  p.off_ring = take(0, 128);
+  const long long budget = (long long)smem_optin - 1024 - p.off_ring;
+  const int rows_per_cta = (H + p.grid - 1) / p.grid;
+  int drs = std::min(rows_per_cta, moe::kRpgMax * p.ng);
+  for (;;) {
+    const size_t need = std::max({(size_t)p.rpair_bytes, (size_t)p.pair_bytes,
+                                  (size_t)drs * (p.row2 + p.sc2)});
+    const size_t slot = round_up(need, 128);
+    const long long ns = budget > 0 ? budget / (long long)slot : 0;
+    if (ns >= 3 || drs == 1) {
+      if (ns < 2) return MOE_ERR_UNSUPPORTED;
+      p.slot_bytes = (int)slot;
+      p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
+      break;
+    }
+    drs = (drs + 1) / 2;
+  }
+  p.d_rows_stage = drs;
+  p.pps = std::max(1, std::min(8, p.slot_bytes / p.pair_bytes));
+  p.pps_r = std::max(1, std::min(8, p.slot_bytes / p.rpair_bytes));
+  p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
+  p.timeout_ns = kDefaultTimeoutNs;
+  return MOE_OK;
+}
+
+const void* kernel_for(const Params& p, int maxm_t, int phases) {
+  return p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, phases) : moe::kernel_nvfp4(maxm_t, phases);
+}
+
+moe_status check_weights(const moe_decode_config& c, const moe_decode_weights* w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  auto need = [](const void* q) { return q != nullptr && aligned16(q); };
+  if (!need(w->router_w) || !need(w->w13) || !need(w->w2)) return MOE_ERR_INVALID_ARG;
+  const bool fp4 = c.wdtype == MOE_W_NVFP4;
+  if (fp4 && (!need(w->w13_scale) || !need(w->w2_scale) || !w->w13_gscale || !w->w2_gscale))
+    return MOE_ERR_INVALID_ARG;
+  if (c.num_shared > 0) {
+    if (!need(w->sh_w13) || !need(w->sh_w2)) return MOE_ERR_INVALID_ARG;
+    if (fp4 && (!need(w->sh_w13_scale) || !need(w->sh_w2_scale) || !w->sh_w13_gscale ||
+                !w->sh_w2_gscale))
+      return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
+  const int maxm_t = p.M == 1 ? 1 : 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(moe::kThreads);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  void* args[] = {const_cast<Params*>(&p)};
+  if (h->sched == MOE_SCHED_PERSISTENT) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, kernel_for(p, maxm_t, moe::PH_ALL), args) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  const int phases[3] = {moe::PH_R, moe::PH_U, moe::PH_D};
+  for (int i = 0; i < 3; ++i) {
+    cfg.numAttrs = 0;
+    if (h->sched == MOE_SCHED_PDL_CHAIN) {
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelExC(&cfg, kernel_for(p, maxm_t, phases[i]), args) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_decode_abi_version(void) { return MOE_DECODE_ABI_VERSION; }
+
+const char* moe_decode_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_OOM: return "device allocation failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_decode_config_check(const moe_decode_config* cfg) { return check_config(cfg); }
+
+moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weights* w,
+                             moe_decode_handle** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(*cfg, w)) != MOE_OK) return st;
+  int dev = 0, sms = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  Params p;
+  if ((st = plan(*cfg, sms, optin, p)) != MOE_OK) return st;
+  // Every kernel this handle may launch gets the shared-memory size, and one
+  // CTA of the single-kernel schedule must fit on every SM.
+  const int phases[4] = {moe::PH_ALL, moe::PH_R, moe::PH_U, moe::PH_D};
+  for (int mt : {1, 8}) {
+    for (int ph : phases) {
+      const void* k = kernel_for(p, mt, ph);
+      if (!k) return MOE_ERR_UNSUPPORTED;
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      int blocks = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, moe::kThreads, p.smem_bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (blocks < 1) return MOE_ERR_UNSUPPORTED;
+    }
+  }
+  // scratch: control words | logits | h | x flags | run_host staging
+  const size_t H = cfg->hidden, I = cfg->inter, E = cfg->num_experts, K = cfg->top_k;
+  const size_t maxm = cfg->max_rows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  const size_t o_ctrl = take(moe::CTRL_WORDS * 4);
+  const size_t o_logits = take(maxm * E * 8);
+  const size_t o_h = take((size_t)p.nslot_max * maxm * I * 8);
+  const size_t o_xf = take((size_t)p.grid * 8);
+  const size_t tag_end = off;
+  const size_t o_sx = take(maxm * H * 2);
+  const size_t o_sr = take(maxm * H * 2);
+  const size_t o_so = take(maxm * H * 2);
+  const size_t o_si = take(maxm * K * 4);
+  const size_t o_sw = take(maxm * K * 4);
+  auto* h = new (std::nothrow) moe_decode_handle();
+  if (!h) return MOE_ERR_OOM;
+  if (cudaMalloc(&h->scratch, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return MOE_ERR_OOM;
+  }
+  uint8_t* base = static_cast<uint8_t*>(h->scratch);
+  if (cudaMemset(base, 0, o_logits) != cudaSuccess ||
+      cudaMemset(base + o_logits, 0xff, tag_end - o_logits) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(h->scratch);
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  h->cfg = *cfg;
+  h->device = dev;
+  h->sched = cfg->sched;
+  h->scratch_bytes = off;
+  p.router_w = static_cast<const uint8_t*>(w->router_w);
+  p.w13 = static_cast<const uint8_t*>(w->w13);
+  p.w2 = static_cast<const uint8_t*>(w->w2);
+  p.w13_s = static_cast<const uint8_t*>(w->w13_scale);
+  p.w2_s = static_cast<const uint8_t*>(w->w2_scale);
+  p.w13_gs = w->w13_gscale;
+  p.w2_gs = w->w2_gscale;
+  p.sh_w13 = static_cast<const uint8_t*>(w->sh_w13);
+  p.sh_w2 = static_cast<const uint8_t*>(w->sh_w2);
+  p.sh_w13_s = static_cast<const uint8_t*>(w->sh_w13_scale);
+  p.sh_w2_s = static_cast<const uint8_t*>(w->sh_w2_scale);
+  p.sh_w13_gs = w->sh_w13_gscale;
+  p.sh_w2_gs = w->sh_w2_gscale;
+  p.ctrl = reinterpret_cast<uint32_t*>(base + o_ctrl);
+  p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
+  p.hbuf = reinterpret_cast<unsigned long long*>(base + o_h);
+  p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
+  h->stage_x = reinterpret_cast<uint16_t*>(base + o_sx);
+  h->stage_r = reinterpret_cast<uint16_t*>(base + o_sr);
+  h->stage_out = reinterpret_cast<uint16_t*>(base + o_so);
+  h->stage_idx = reinterpret_cast<int32_t*>(base + o_si);
+  h->stage_w = reinterpret_cast<float*>(base + o_sw);
+  h->base = p;
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_decode_run(moe_decode_handle* h, const void* x, const void* residual, void* out,
+                          int32_t m_rows, int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  if (!h || !x || !residual || !out) return MOE_ERR_INVALID_ARG;
+  if (m_rows < 1 || m_rows > h->cfg.max_rows) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  Params p = h->base;
+  p.M = m_rows;
+  p.x = static_cast<const uint16_t*>(x);
+  p.resid = static_cast<const uint16_t*>(residual);
+  p.out = static_cast<uint16_t*>(out);
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  const size_t bytes = (size_t)m_rows * p.H * 2;
+  p.out_aliases_x = overlaps(x, bytes, out, bytes) ? 1 : 0;
+  return launch(h, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_decode_get_status(moe_decode_handle* h, moe_stream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t ctrl[4] = {0, 0, 0, 0};
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(ctrl, h->base.ctrl, sizeof(ctrl), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ctrl[moe::CTRL_STATUS] == 0) return MOE_OK;
+  if (cudaMemsetAsync(h->base.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_ERR_DEVICE_TIMEOUT;
+}
+
+moe_status moe_decode_run_host(moe_decode_handle* h, const void* x_host, const void* residual_host,
+                               void* out_host, int32_t m_rows, int32_t* topk_idx_host,
+                               float* topk_w_host, moe_stream_t stream) {
+  if (!h || !x_host || !residual_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (m_rows < 1 || m_rows > h->cfg.max_rows) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)m_rows * h->cfg.hidden * 2;
+  const size_t kb = (size_t)m_rows * h->cfg.top_k * 4;
+  if (cudaMemcpyAsync(h->stage_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(h->stage_r, residual_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = moe_decode_run(h, h->stage_x, h->stage_r, h->stage_out, m_rows,
+                                 topk_idx_host ? h->stage_idx : nullptr,
+                                 topk_w_host ? h->stage_w : nullptr, stream);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(out_host, h->stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (topk_idx_host &&
+      cudaMemcpyAsync(topk_idx_host, h->stage_idx, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (topk_w_host && cudaMemcpyAsync(topk_w_host, h->stage_w, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return moe_decode_get_status(h, stream);
+}
+
+moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  switch (option) {
+    case MOE_OPT_SCHED:
+      if (value < MOE_SCHED_PERSISTENT || value > MOE_SCHED_CHAIN) return MOE_ERR_INVALID_ARG;
+      h->sched = (int)value;
+      return MOE_OK;
+    case MOE_OPT_WAIT_TIMEOUT_NS:
+      if (value <= 0) return MOE_ERR_INVALID_ARG;
+      h->base.timeout_ns = (unsigned long long)value;
+      return MOE_OK;
+    case MOE_OPT_TEST_FLAGS:
+      if (value < 0 || value > moe::TEST_SKIP_LOGITS) return MOE_ERR_INVALID_ARG;
+      h->base.test_flags = (int)value;
+      return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value) {
+  if (!h || !value) return MOE_ERR_INVALID_ARG;
+  switch (what) {
+    case MOE_OPT_SCHED: *value = h->sched; return MOE_OK;
+    case MOE_OPT_WAIT_TIMEOUT_NS: *value = (int64_t)h->base.timeout_ns; return MOE_OK;
+    case MOE_OPT_TEST_FLAGS: *value = h->base.test_flags; return MOE_OK;
+    case MOE_INFO_GRID: *value = h->base.grid; return MOE_OK;
+    case MOE_INFO_THREADS: *value = moe::kThreads; return MOE_OK;
+    case MOE_INFO_SMEM: *value = h->base.smem_bytes; return MOE_OK;
+    case MOE_INFO_RING_SLOTS: *value = h->base.nslots; return MOE_OK;
+    case MOE_INFO_SLOT_BYTES: *value = h->base.slot_bytes; return MOE_OK;
+    case MOE_INFO_KERNELS_PER_RUN: *value = h->sched == MOE_SCHED_PERSISTENT ? 1 : 3; return MOE_OK;
+    case MOE_INFO_SCRATCH_BYTES: *value = (int64_t)h->scratch_bytes; return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_decode_destroy(moe_decode_handle* h) {
+  if (!h) return MOE_OK;
+  cudaError_t e = cudaFree(h->scratch);  // cudaFree waits for outstanding work
+  delete h;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,9 @@
+// Host-side access to the kernel instantiations (one translation unit per
+// weight format, so the two compile in parallel).
+#pragma once
+
+namespace moe {
+// Kernel entry for (maxm_t in {1, 8}, phases in Phase). NULL if not instantiated.
+const void* kernel_bf16(int maxm_t, int phases);
+const void* kernel_nvfp4(int maxm_t, int phases);
+}  // namespace moe

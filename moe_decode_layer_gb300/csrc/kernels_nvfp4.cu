@@ -1,0 +1,24 @@
+// nvfp4 instantiations of the MoE decode layer kernels.
+#include "kernel_table.h"
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+template <int MAXM>
+static const void* pick(int phases) {
+  switch (phases) {
+    case PH_ALL: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_ALL>);
+    case PH_R: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_R>);
+    case PH_U: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_U>);
+    case PH_D: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_D>);
+    default: return nullptr;
+  }
+}
+
+const void* kernel_nvfp4(int maxm_t, int phases) {
+  if (maxm_t == 1) return pick<1>(phases);
+  if (maxm_t == 8) return pick<8>(phases);
+  return nullptr;
+}
+
+}  // namespace moe

@@ -1,0 +1,91 @@
+// Launch parameters shared by the host planner and the device kernels.
+#pragma once
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kNC = 12;                  // consumer warps per CTA
+constexpr int kThreads = (kNC + 1) * 32; // + one producer warp
+constexpr int kRpgMax = 6;               // down-projection rows per thread group per stage
+constexpr int kMaxSlots = 64;            // ring slots (upper bound for the barrier arrays)
+constexpr int kCplBf16 = 16;             // 16-byte x chunks per lane kept in registers (H <= 4096)
+constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVFP4 (H <= 4096)
+
+enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
+
+// Phases a kernel runs: router + shared gate/up (R), routed gate/up (U),
+// down + combine + residual (D).
+enum Phase : int { PH_R = 1, PH_U = 2, PH_D = 4, PH_ALL = 7 };
+
+// Control words at the start of the handle's scratch.
+enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3, CTRL_WORDS = 64 };
+// Device status bits and the wait that gave up first.
+enum DevErr : uint32_t { DEV_ERR_TIMEOUT = 1u };
+enum WaitSite : uint32_t {
+  SITE_RING_FULL = 1,
+  SITE_RING_EMPTY = 2,
+  SITE_LOGITS = 3,
+  SITE_HIDDEN = 4,
+  SITE_XFLAGS = 5,
+  SITE_DRAIN = 6
+};
+// Test flags.
+enum TestFlag : int { TEST_SKIP_LOGITS = 1 };
+
+// Shared-memory words kept in the misc block.
+enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_WTOT = 8, MISC_WORDS = 32 };
+
+struct Params {
+  // shapes
+  int H, I, E, K, S, M, maxm, fmt;
+  float routed_scale;
+  float rms_eps;
+  int pre_rmsnorm;
+  // weights (device, borrowed)
+  const uint8_t* router_w;
+  const uint8_t* w13;
+  const uint8_t* w13_s;
+  const float* w13_gs;
+  const uint8_t* w2;
+  const uint8_t* w2_s;
+  const float* w2_gs;
+  const uint8_t* sh_w13;
+  const uint8_t* sh_w13_s;
+  const float* sh_w13_gs;
+  const uint8_t* sh_w2;
+  const uint8_t* sh_w2_s;
+  const float* sh_w2_gs;
+  // activations
+  const uint16_t* x;
+  const uint16_t* resid;
+  uint16_t* out;
+  int32_t* topk_idx;
+  float* topk_w;
+  // scratch (device, owned by the handle)
+  unsigned long long* logits;  // [maxm][E] tagged
+  unsigned long long* hbuf;    // [nslot_max][maxm][I] tagged
+  unsigned long long* xflags;  // [grid] tagged: this CTA has read x
+  uint32_t* ctrl;              // CTRL_WORDS
+  int out_aliases_x;
+  // planned layout
+  int nchunk_h;      // 16-byte code chunks per gate/up row
+  int row13, sc13;   // code / scale bytes per gate/up row
+  int nchunk_i;      // 16-byte code chunks per down row
+  int row2, sc2;     // code / scale bytes per down row
+  int pair_bytes;    // one gate row + one up row (codes and scales)
+  int rpair_bytes;   // two router rows
+  int pps, pps_r;    // pairs per stage (expert / router)
+  int slot_bytes, nslots;
+  int d_rows_stage;  // down rows per stage
+  int tg, ng;        // threads per down group, groups
+  int grid;
+  int nslot_max;     // S + min(E, maxm * K)
+  // shared-memory offsets from the aligned base
+  int off_full, off_empty, off_x, off_hs, off_sel_e, off_sel_w, off_emask, off_slot_of;
+  int off_slot_e, off_slot_mask, off_slot_w, off_red, off_misc, off_ring;
+  int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
+  unsigned long long timeout_ns;
+  int test_flags;
+};
+
+}  // namespace moe

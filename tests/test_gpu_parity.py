@@ -1,0 +1,208 @@
+"""GPU (CUDA path through the C ABI) against the float64 oracle.
+
+Expert index sets must match exactly (inputs are drawn with a top-k logit gap of
+at least 0.05), routing weights within 1e-5, outputs within max-abs 2e-2 and
+relative L2 5e-3 of the oracle. Cases span the tiny layer, the Ling-shaped layer
+at full size (M = 1 and M = 6 correlated rows) in the launch configuration the
+bench times, ragged and degenerate shapes, all three schedules (which must agree
+bit for bit), in-place outputs, repeated runs, graph capture and the host-buffer
+entry point.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from moe_decode_layer_gb300 import _lib, synth
+from moe_decode_layer_gb300.layer import MoEDecodeLayer
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = ["persistent", "pdl_chain", "chain"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _needs_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return synth.make_layer(synth.TINY, seed=0, device="cuda")
+
+
+@pytest.fixture(scope="module")
+def ling():
+    layer = synth.make_layer(synth.LING, seed=1, device="cuda")
+    yield layer
+    del layer
+    torch.cuda.empty_cache()
+
+
+def _run(shape, layer, x, residual=None, sched="persistent", max_rows=None, **kw):
+    m = x.shape[0]
+    mod = MoEDecodeLayer(shape, layer, max_rows or m, sched=sched, **kw)
+    xd = x.cuda()
+    rd = xd if residual is None else residual.cuda()
+    out = torch.empty_like(xd)
+    idx = torch.full((m, shape.top_k), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((m, shape.top_k), dtype=torch.float32, device="cuda")
+    mod.run(xd, rd, out, idx, w)
+    assert mod.status() == _lib.MOE_OK
+    torch.cuda.synchronize()
+    return mod, out.cpu(), idx.cpu(), w.cpu()
+
+
+def _check(shape, layer, x, out, idx, w, residual=None):
+    ref, ridx, rw = helpers.oracle_layer(shape, layer, x, x if residual is None else residual)
+    helpers.assert_routing(idx, w, ridx, rw)
+    return helpers.assert_close(out, ref)
+
+
+# ----------------------------------------------------------------------------- tiny layer
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_tiny_m1(tiny, sched):
+    x = helpers.hidden_with_margin(tiny["router_w"], 1, synth.TINY.top_k, seed=0)
+    _, out, idx, w = _run(synth.TINY, tiny, x, sched=sched)
+    _check(synth.TINY, tiny, x, out, idx, w)
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("m", [2, 6, 8])
+def test_tiny_multi_row(tiny, sched, m):
+    x = helpers.hidden_with_margin(tiny["router_w"], m, synth.TINY.top_k, seed=m, rho=0.5)
+    _, out, idx, w = _run(synth.TINY, tiny, x, sched=sched, max_rows=8)
+    _check(synth.TINY, tiny, x, out, idx, w)
+
+
+def test_tiny_moe_part_alone(tiny):
+    """Zero residual: the bf16 output is the MoE sum itself, so the tolerance
+    bites on the expert arithmetic rather than on the residual's rounding."""
+    x = helpers.hidden_with_margin(tiny["router_w"], 3, synth.TINY.top_k, seed=5, rho=0.5)
+    r = torch.zeros_like(x)
+    _, out, idx, w = _run(synth.TINY, tiny, x, residual=r)
+    ref, _, _ = helpers.oracle_layer(synth.TINY, tiny, x, r)
+    helpers.assert_close(out, ref)
+    # tighter than the contract: bf16 rounding of the sum only
+    g = helpers.f64(out)
+    assert np.linalg.norm(g - ref) / np.linalg.norm(ref) < 3e-3
+
+
+def test_schedules_bitwise_identical(tiny):
+    x = helpers.hidden_with_margin(tiny["router_w"], 4, synth.TINY.top_k, seed=9, rho=0.5)
+    outs = [_run(synth.TINY, tiny, x, sched=s)[1] for s in SCHEDS]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_repeated_runs_and_inplace(tiny):
+    x = helpers.hidden_with_margin(tiny["router_w"], 2, synth.TINY.top_k, seed=11)
+    mod = MoEDecodeLayer(synth.TINY, tiny, 2)
+    xd = x.cuda()
+    first = mod.run(xd, xd).clone()
+    for _ in range(50):
+        again = mod.run(xd, xd)
+        assert torch.equal(again, first)
+    # in place: x, residual and out are one buffer
+    buf = xd.clone()
+    mod.run(buf, buf, buf)
+    assert mod.status() == _lib.MOE_OK
+    assert torch.equal(buf, first)
+
+
+def test_zero_rows_give_zero(tiny):
+    x = torch.zeros((3, synth.TINY.hidden), dtype=torch.bfloat16)
+    _, out, _, w = _run(synth.TINY, tiny, x)
+    assert torch.count_nonzero(out.float()) == 0
+    np.testing.assert_allclose(w.numpy(), 1.0 / synth.TINY.top_k, rtol=0, atol=1e-7)
+
+
+def test_run_host_matches_device(tiny):
+    x = helpers.hidden_with_margin(tiny["router_w"], 2, synth.TINY.top_k, seed=13)
+    mod, out_dev, idx_dev, w_dev = _run(synth.TINY, tiny, x)
+    out = torch.empty_like(x)
+    idx = torch.empty((2, synth.TINY.top_k), dtype=torch.int32)
+    w = torch.empty((2, synth.TINY.top_k), dtype=torch.float32)
+    mod.run_host(x.contiguous(), x.contiguous(), out, idx, w)
+    assert torch.equal(out, out_dev) and torch.equal(idx, idx_dev) and torch.equal(w, w_dev)
+
+
+def test_graph_capture_replays(tiny):
+    x = helpers.hidden_with_margin(tiny["router_w"], 2, synth.TINY.top_k, seed=17)
+    for sched in SCHEDS:
+        mod = MoEDecodeLayer(synth.TINY, tiny, 2, sched=sched)
+        xd = x.cuda()
+        out = torch.empty_like(xd)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            mod.run(xd, xd, out, stream=s)  # warm-up outside capture
+        torch.cuda.synchronize()
+        ref = out.clone()
+        out.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            mod.run(xd, xd, out, stream=s)
+        for _ in range(3):
+            out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref), sched
+        assert mod.status() == _lib.MOE_OK
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(hidden=256, inter=128, num_experts=16, top_k=16, num_shared=1),   # k = E
+    dict(hidden=256, inter=128, num_experts=16, top_k=2, num_shared=0),    # no shared expert
+    dict(hidden=256, inter=128, num_experts=16, top_k=4, num_shared=2),    # two shared experts
+    dict(hidden=200, inter=64, num_experts=10, top_k=3, num_shared=1),     # ragged chunks
+    dict(hidden=512, inter=256, num_experts=64, top_k=1, num_shared=1),    # top-1
+    dict(hidden=1024, inter=768, num_experts=2, top_k=1, num_shared=1),    # E = 2, 96-thread groups
+])
+@pytest.mark.parametrize("m", [1, 5])
+def test_shapes(cfg, m):
+    shape = synth.LayerShape(**cfg)
+    layer = synth.make_layer(shape, seed=3, device="cuda")
+    margin = 0.05 if cfg["top_k"] < cfg["num_experts"] else 0.0
+    x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=21, rho=0.5, margin=margin)
+    outs = []
+    for sched in SCHEDS:
+        _, out, idx, w = _run(shape, layer, x, sched=sched, max_rows=8)
+        if cfg["top_k"] < cfg["num_experts"]:
+            _check(shape, layer, x, out, idx, w)
+        else:
+            ref, _, _ = helpers.oracle_layer(shape, layer, x, x)
+            helpers.assert_close(out, ref)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+# ----------------------------------------------------------------------------- Ling-shaped layer
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_ling_m1(ling, sched):
+    x = helpers.hidden_with_margin(ling["router_w"], 1, synth.LING.top_k, seed=0)
+    _, out, idx, w = _run(synth.LING, ling, x, sched=sched)
+    _check(synth.LING, ling, x, out, idx, w)
+
+
+@pytest.mark.parametrize("sched", ["persistent", "pdl_chain"])
+def test_ling_m6_correlated(ling, sched):
+    x = helpers.hidden_with_margin(ling["router_w"], 6, synth.LING.top_k, seed=1, rho=0.5)
+    _, out, idx, w = _run(synth.LING, ling, x, sched=sched)
+    _check(synth.LING, ling, x, out, idx, w)
+    distinct = len(set(idx.flatten().tolist()))
+    assert 8 <= distinct <= 48
+
+
+def test_ling_moe_part_alone(ling):
+    x = helpers.hidden_with_margin(ling["router_w"], 2, synth.LING.top_k, seed=4)
+    r = torch.zeros_like(x)
+    _, out, idx, w = _run(synth.LING, ling, x, residual=r)
+    ref, _, _ = helpers.oracle_layer(synth.LING, ling, x, r)
+    helpers.assert_close(out, ref)
