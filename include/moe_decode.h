@@ -176,6 +176,7 @@ enum {
   MOE_OPT_WAIT_TIMEOUT_NS = 2, /* device wait limit in ns (default 1e9)             */
   MOE_OPT_TEST_FLAGS = 3,      /* testing only: 1 = router results are never published,
                                   so every wait on them runs into the limit          */
+  MOE_OPT_RING_SLOTS = 4,      /* shared-memory ring slots used, 2 .. the planned count */
   MOE_INFO_GRID = 16,          /* CTAs per kernel                                   */
   MOE_INFO_THREADS = 17,       /* threads per CTA                                   */
   MOE_INFO_SMEM = 18,          /* dynamic shared memory per CTA, bytes              */

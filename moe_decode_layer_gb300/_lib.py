@@ -31,6 +31,7 @@ SCHED_NAMES = {"persistent": MOE_SCHED_PERSISTENT, "pdl_chain": MOE_SCHED_PDL_CH
 MOE_OPT_SCHED = 1
 MOE_OPT_WAIT_TIMEOUT_NS = 2
 MOE_OPT_TEST_FLAGS = 3
+MOE_OPT_RING_SLOTS = 4
 MOE_INFO_GRID = 16
 MOE_INFO_THREADS = 17
 MOE_INFO_SMEM = 18

@@ -19,6 +19,7 @@ struct moe_decode_handle {
   Params base;       // everything but the per-run pointers and M
   int device = 0;
   int sched = MOE_SCHED_PERSISTENT;
+  int max_slots = 0;  // ring slots the planned shared memory holds
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   uint16_t* stage_x = nullptr;  // run_host staging
@@ -96,6 +97,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   };
   p.off_full = take(moe::kMaxSlots * 8, 8);
   p.off_empty = take(moe::kMaxSlots * 8, 8);
+  p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
   p.off_x = take((size_t)maxm * H * 2, 16);
   p.off_hs = take((size_t)2 * maxm * I * 4, 16);
   p.off_sel_e = take((size_t)maxm * K * 4, 4);
@@ -299,6 +301,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->stage_idx = reinterpret_cast<int32_t*>(base + o_si);
   h->stage_w = reinterpret_cast<float*>(base + o_sw);
   h->base = p;
+  h->max_slots = p.nslots;
   *out = h;
   return MOE_OK;
 }
@@ -377,6 +380,10 @@ moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t v
       if (value < 0 || value > moe::TEST_SKIP_LOGITS) return MOE_ERR_INVALID_ARG;
       h->base.test_flags = (int)value;
       return MOE_OK;
+    case MOE_OPT_RING_SLOTS:
+      if (value < 2 || value > h->max_slots) return MOE_ERR_INVALID_ARG;
+      h->base.nslots = (int)value;
+      return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -387,6 +394,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_OPT_SCHED: *value = h->sched; return MOE_OK;
     case MOE_OPT_WAIT_TIMEOUT_NS: *value = (int64_t)h->base.timeout_ns; return MOE_OK;
     case MOE_OPT_TEST_FLAGS: *value = h->base.test_flags; return MOE_OK;
+    case MOE_OPT_RING_SLOTS: *value = h->base.nslots; return MOE_OK;
     case MOE_INFO_GRID: *value = h->base.grid; return MOE_OK;
     case MOE_INFO_THREADS: *value = moe::kThreads; return MOE_OK;
     case MOE_INFO_SMEM: *value = h->base.smem_bytes; return MOE_OK;

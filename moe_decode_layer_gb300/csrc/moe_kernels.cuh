@@ -68,12 +68,14 @@ struct Ctx {
   const Params& p;
   uint8_t* sm;
   int* misc;
+  volatile int* slot_seq;  // [nslots] ring stage that currently owns each slot
   uint32_t full0, empty0;
   uint64_t t0;
   int tid, warp, lane;
 
   __device__ Ctx(const Params& pp, uint8_t* base) : p(pp), sm(base) {
     misc = reinterpret_cast<int*>(sm + p.off_misc);
+    slot_seq = reinterpret_cast<volatile int*>(sm + p.off_slot_seq);
     full0 = smem_u32(sm + p.off_full);
     empty0 = smem_u32(sm + p.off_empty);
     t0 = global_ns();
@@ -94,10 +96,21 @@ struct Ctx {
   __device__ uint8_t* slot_ptr(int slot) const { return sm + p.off_ring + (size_t)slot * p.slot_bytes; }
 
   // Bounded wait for ring stage `seq` to be full. False on abort / timeout.
+  // Consumer warps take stages round-robin, so a warp may ask for a stage more
+  // than one lap ahead of its slot; an mbarrier parity only tells adjacent
+  // phases apart. The producer therefore records which stage owns a slot before
+  // arming it, and the parity wait starts only once `seq` owns the slot.
   __device__ bool wait_full(long long seq) const {
     const int slot = (int)(seq % p.nslots);
     const uint32_t par = (uint32_t)((seq / p.nslots) & 1);
     const uint32_t bar = full0 + 8u * slot;
+    while (slot_seq[slot] != (int)seq) {
+      if (aborted()) return false;
+      if (expired()) {
+        fail(SITE_RING_FULL);
+        return false;
+      }
+    }
     while (!mbar_try_wait(bar, par)) {
       if (aborted()) return false;
       if (expired()) {
@@ -812,6 +825,7 @@ struct Producer {
     const int slot = (int)(seq % c.p.nslots);
     dst = smem_u32(c.slot_ptr(slot));
     bar = c.full0 + 8u * slot;
+    c.slot_seq[slot] = (int)seq;  // before arming: see Ctx::wait_full
     mbar_arrive_expect_tx(bar, bytes);
     issued = seq + 1;
     return true;
@@ -945,6 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     for (int i = 0; i < p.nslots; ++i) {
       mbar_init(c.full0 + 8u * i, 1);
       mbar_init(c.empty0 + 8u * i, kNC);
+      c.slot_seq[i] = -1;
     }
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;

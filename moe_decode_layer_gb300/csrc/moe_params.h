@@ -81,7 +81,7 @@ struct Params {
   int grid;
   int nslot_max;     // S + min(E, maxm * K)
   // shared-memory offsets from the aligned base
-  int off_full, off_empty, off_x, off_hs, off_sel_e, off_sel_w, off_emask, off_slot_of;
+  int off_full, off_empty, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w, off_emask, off_slot_of;
   int off_slot_e, off_slot_mask, off_slot_w, off_red, off_misc, off_ring;
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;

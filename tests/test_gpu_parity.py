@@ -206,3 +206,20 @@ def test_ling_moe_part_alone(ling):
     _, out, idx, w = _run(synth.LING, ling, x, residual=r)
     ref, _, _ = helpers.oracle_layer(synth.LING, ling, x, r)
     helpers.assert_close(out, ref)
+
+
+@pytest.mark.parametrize("slots", [2, 3, 5])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_small_ring_wraps(tiny, slots, sched):
+    """Few ring slots force every phase to wrap the shared-memory ring many times;
+    results must not change by a bit."""
+    x = helpers.hidden_with_margin(tiny["router_w"], 6, synth.TINY.top_k, seed=31, rho=0.5)
+    _, ref_out, _, _ = _run(synth.TINY, tiny, x, sched=sched, max_rows=8)
+    mod = MoEDecodeLayer(synth.TINY, tiny, 8, sched=sched)
+    mod.set_option(_lib.MOE_OPT_RING_SLOTS, slots)
+    assert mod.info(_lib.MOE_OPT_RING_SLOTS) == slots
+    xd = x.cuda()
+    for _ in range(3):
+        out = mod.run(xd, xd)
+        assert mod.status() == _lib.MOE_OK
+        assert torch.equal(out.cpu(), ref_out)
