@@ -42,23 +42,7 @@ METRIC = "MoE decode layer-step µs and achieved HBM GB/s (% of roofline), M=1 a
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
-WORKLOADS = {
-    "ling_m1": dict(shape="LING", m=1, rho=0.0, layers=1,
-                    desc="Ling-3.0-flash-shaped MoE layer, H=2560, E=512 top-8 + 1 shared, I=768, M=1"),
-    "ling_m6": dict(shape="LING", m=6, rho=0.5, layers=1,
-                    desc="Ling-3.0-flash-shaped MoE layer, H=2560, E=512 top-8 + 1 shared, I=768, "
-                         "M=6 verify rows correlated rho=0.5"),
-    "stack_m6": dict(shape="LING", m=6, rho=0.5, layers=12,
-                     desc="12 distinct Ling-shaped MoE layers back to back, RMSNorm(1e-6) + residual "
-                          "between layers, M=6 rho=0.5"),
-    "nvfp4_m1": dict(shape="MUSE_NVFP4", m=1, rho=0.0, layers=1,
-                     desc="NVFP4 experts (e2m1, e4m3 block-16 scales, fp32 tensor scale), H=4096, "
-                          "E=256 top-8, I=1024, no shared expert, M=1"),
-    "nvfp4_m6": dict(shape="MUSE_NVFP4", m=6, rho=0.5, layers=1,
-                     desc="NVFP4 experts, H=4096, E=256 top-8, I=1024, M=6 rho=0.5"),
-    "tiny_m1": dict(shape="TINY", m=1, rho=0.0, layers=1,
-                    desc="tiny MoE layer H=256, E=16 top-2 + 1 shared, I=128, M=1"),
-}
+from moe_decode_layer_gb300.synth import WORKLOADS  # noqa: E402
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -150,7 +134,7 @@ def run_ours(args, rank, world, dist):
     from moe_decode_layer_gb300.layer import MoEDecodeLayer
 
     wl = WORKLOADS[args.workload]
-    shape = getattr(synth, wl["shape"])
+    shape = synth.workload_shape(args.workload)
     m, nl = wl["m"], wl["layers"]
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
@@ -161,6 +145,9 @@ def run_ours(args, rank, world, dist):
     copies = nl if nl > 1 else args.copies
     layers = [synth.make_layer(shape, seed=1000 + 97 * rank + i, device="cuda") for i in range(copies)]
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=args.sched, pre_rmsnorm=nl > 1) for i in range(copies)]
+    if args.ring_slots:
+        for md in mods:
+            md.set_option(_lib.MOE_OPT_RING_SLOTS, min(args.ring_slots, md.info(_lib.MOE_INFO_RING_SLOTS)))
     n_in = 64
     xs = [synth.hidden_rows(m, shape.hidden, seed=50_000 + 1000 * rank + j, rho=wl["rho"]).cuda()
           for j in range(n_in)]
@@ -414,7 +401,7 @@ def cores_used():
 def cpu_baseline(workload, target_s):
     from moe_decode_layer_gb300 import synth
     wl = WORKLOADS[workload]
-    shape = getattr(synth, wl["shape"])
+    shape = synth.workload_shape(workload)
     t_step, b_step, n = oracle_step_time(shape, wl["m"], wl["rho"], target_s)
     t_step *= wl["layers"]  # the stack runs the same layer arithmetic per layer
     b_step *= wl["layers"]
@@ -431,7 +418,7 @@ def run_reference(args, rank, world):
         return None
     from moe_decode_layer_gb300 import synth
     wl = WORKLOADS[args.workload]
-    shape = getattr(synth, wl["shape"])
+    shape = synth.workload_shape(args.workload)
     # each step is a bounded sample; total CPU time ~ a few minutes at most
     per = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     t_step, b_step, n = oracle_step_time(shape, wl["m"], wl["rho"], per * (args.steps + args.warmup))
@@ -464,6 +451,7 @@ def main(argv=None):
     ap.add_argument("--sched", default="persistent", choices=["persistent", "pdl_chain", "chain"])
     ap.add_argument("--copies", type=int, default=8, help="distinct layer copies (single-layer workloads)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--ring-slots", type=int, default=0, help="cap on shared-memory ring slots (0 = planned)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle CPU baseline sample length")
     ap.add_argument("--secondary", default="ling_m6",
                     help="extra workload measured in the same run ('' to skip)")
@@ -503,7 +491,7 @@ def main(argv=None):
         res["secondary"] = {k: sec[k] for k in ("value", "unit", "ms_per_step", "us_per_layer_step",
                                                 "tokens_per_s_equiv", "bytes_per_step_avg", "roofline",
                                                 "config", "steps", "clocks")}
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -177,6 +177,9 @@ enum {
   MOE_OPT_TEST_FLAGS = 3,      /* testing only: 1 = router results are never published,
                                   so every wait on them runs into the limit          */
   MOE_OPT_RING_SLOTS = 4,      /* shared-memory ring slots used, 2 .. the planned count */
+  MOE_OPT_STAMPS = 5,          /* device pointer (as int64) to a uint64 buffer of
+                                  MOE_INFO_GRID x 16 words, or 0: each CTA stores the
+                                  %globaltimer ns at its phase boundaries (profiling)  */
   MOE_INFO_GRID = 16,          /* CTAs per kernel                                   */
   MOE_INFO_THREADS = 17,       /* threads per CTA                                   */
   MOE_INFO_SMEM = 18,          /* dynamic shared memory per CTA, bytes              */

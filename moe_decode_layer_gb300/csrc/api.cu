@@ -384,6 +384,10 @@ moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t v
       if (value < 2 || value > h->max_slots) return MOE_ERR_INVALID_ARG;
       h->base.nslots = (int)value;
       return MOE_OK;
+    case MOE_OPT_STAMPS:
+      if (value & 7) return MOE_ERR_INVALID_ARG;
+      h->base.stamps = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+      return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -395,6 +399,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_OPT_WAIT_TIMEOUT_NS: *value = (int64_t)h->base.timeout_ns; return MOE_OK;
     case MOE_OPT_TEST_FLAGS: *value = h->base.test_flags; return MOE_OK;
     case MOE_OPT_RING_SLOTS: *value = h->base.nslots; return MOE_OK;
+    case MOE_OPT_STAMPS: *value = (int64_t)reinterpret_cast<uintptr_t>(h->base.stamps); return MOE_OK;
     case MOE_INFO_GRID: *value = h->base.grid; return MOE_OK;
     case MOE_INFO_THREADS: *value = moe::kThreads; return MOE_OK;
     case MOE_INFO_SMEM: *value = h->base.smem_bytes; return MOE_OK;

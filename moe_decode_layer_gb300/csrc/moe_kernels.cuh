@@ -94,6 +94,10 @@ struct Ctx {
   __device__ bool peer_failed() const { return ld_relaxed_u32(&p.ctrl[CTRL_STATUS]) != 0; }
   __device__ uint32_t epoch() const { return static_cast<uint32_t>(misc[MISC_EPOCH]); }
   __device__ uint8_t* slot_ptr(int slot) const { return sm + p.off_ring + (size_t)slot * p.slot_bytes; }
+  // Phase timestamp (one plain store; off unless the handle has a stamp buffer).
+  __device__ void stamp(int ev) const {
+    if (p.stamps) p.stamps[(size_t)blockIdx.x * kStampSlots + ev] = global_ns();
+  }
 
   // Bounded wait for ring stage `seq` to be full. False on abort / timeout.
   // Consumer warps take stages round-robin, so a warp may ask for a stage more
@@ -692,6 +696,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, l
       const bool got = ok && !c.aborted() && c.wait_full(seq);
       ok = got;
       bar_sync(kBarConsumers, kNC * 32);
+      if (rb == 0 && sl == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
       if (ok && !c.aborted() && active) {
         const uint8_t* st = c.slot_ptr((int)(seq % p.nslots));
         float gsc = 1.0f;
@@ -976,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       if (c.lane == 0) {
         pr.router(seq);
         pr.pairs(true, rt, seq);
+        c.stamp(ST_P_R_ISSUED);
         if (PHASES & PH_D) pr.prefetch_shared_down();
       }
     } else if (PHASES == PH_D) {
@@ -987,11 +993,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       bar_sync(kBarRoute, kThreads);
     }
     if (c.lane == 0) {
-      if (PHASES & PH_U) pr.pairs(false, rt, seq);
+      c.stamp(ST_P_ROUTE);
+      if (PHASES & PH_U) {
+        pr.pairs(false, rt, seq);
+        c.stamp(ST_P_U_ISSUED);
+      }
       if (PHASES & PH_D) {
         const int nsl = p.S + c.misc[MISC_NROUTED];
         const int first = PHASES == PH_D ? p.S : 0;  // the chain issued these before routing
         for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl, seq);
+        c.stamp(ST_P_D_ISSUED);
       }
       if (c.aborted()) pr.drain();
     }
@@ -1000,8 +1011,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     // ------------------------------------------------------------ consumers
     if (kChain) pdl_wait();
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
+    if (c.tid == 0) c.stamp(ST_START);
     if (kNeedX) load_x(c);
     bar_sync(kBarConsumers, kNC * 32);
+    if (c.tid == 0) c.stamp(ST_X_LOADED);
     if (PHASES == PH_ALL && p.out_aliases_x && c.tid == 0)
       st_tagged(p.xflags + blockIdx.x, c.epoch(), 0.0f);
     long long seq = 0;
@@ -1010,17 +1023,21 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       load_xregs<FMT, MAXM>(c, xr);
       consume_router<FMT, MAXM>(c, xr, seq);
       consume_pairs<FMT, MAXM>(c, rt, xr, true, seq);
+      if (c.tid == 0) c.stamp(ST_R_DONE);
     }
     if (kRoute) {
       route_rows(c, rt, (PHASES & PH_U) != 0);
       bar_arrive(kBarRoute, kThreads);
+      if (c.tid == 0) c.stamp(ST_ROUTED);
     }
     if (PHASES & PH_U) {
       XRegs<FMT, MAXM> xr;
       load_xregs<FMT, MAXM>(c, xr);
       consume_pairs<FMT, MAXM>(c, rt, xr, false, seq);
+      if (c.tid == 0) c.stamp(ST_U_DONE);
     }
     if (PHASES & PH_D) consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, seq);
+    if (c.tid == 0) c.stamp(ST_D_DONE);
   }
   __syncthreads();
   if (kLast && c.tid == 0) {

@@ -31,6 +31,22 @@ enum WaitSite : uint32_t {
 };
 // Test flags.
 enum TestFlag : int { TEST_SKIP_LOGITS = 1 };
+// Per-CTA phase timestamps (%globaltimer, ns) when Params::stamps is set:
+// stamps[cta * kStampSlots + event].
+enum Stamp : int {
+  ST_START = 0,       // kernel entry
+  ST_X_LOADED = 1,    // x rows in shared memory (consumers)
+  ST_R_DONE = 2,      // this CTA's router + shared gate/up stages consumed (warp 0 view)
+  ST_ROUTED = 3,      // top-k and expert union ready
+  ST_U_DONE = 4,      // routed gate/up stages consumed (warp 0 view)
+  ST_D_FIRST = 5,     // first down stage's inputs staged
+  ST_D_DONE = 6,      // outputs written
+  ST_P_R_ISSUED = 8,  // producer: last router / shared stage issued
+  ST_P_ROUTE = 9,     // producer: routing received
+  ST_P_U_ISSUED = 10, // producer: last routed gate/up stage issued
+  ST_P_D_ISSUED = 11, // producer: last down stage issued
+  kStampSlots = 16
+};
 
 // Shared-memory words kept in the misc block.
 enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_WTOT = 8, MISC_WORDS = 32 };
@@ -86,6 +102,7 @@ struct Params {
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;
   int test_flags;
+  unsigned long long* stamps;  // optional [grid][kStampSlots]
 };
 
 }  // namespace moe

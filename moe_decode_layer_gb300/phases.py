@@ -1,0 +1,85 @@
+"""Phase timeline of the single-kernel MoE decode step from the kernel's own
+timestamps (each CTA stores %globaltimer at its phase boundaries).
+
+    python -m moe_decode_layer_gb300.phases --workload ling_m1 [--copies 8]
+           [--runs 200] [--ring-slots N]
+
+Prints, per phase boundary, the median / 10th / 90th percentile over CTAs and
+runs of the time since the earliest CTA entered the kernel, in microseconds.
+Weights rotate over several layer copies so they are cold as in the bench.
+"""
+
+from __future__ import annotations
+
+import argparse
+import statistics
+
+import torch
+
+from . import _lib, synth
+from .layer import MoEDecodeLayer
+
+
+def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: str = "persistent"):
+    wl = synth.WORKLOADS[workload]
+    shape = synth.workload_shape(workload)
+    m = wl["m"]
+    layers = [synth.make_layer(shape, seed=2000 + i, device="cuda") for i in range(copies)]
+    mods = [MoEDecodeLayer(shape, layers[i], m, sched=sched) for i in range(copies)]
+    grid = mods[0].info(_lib.MOE_INFO_GRID)
+    stamps = torch.zeros((grid, 16), dtype=torch.int64, device="cuda")
+    for md in mods:
+        if ring_slots:
+            md.set_option(_lib.MOE_OPT_RING_SLOTS, ring_slots)
+    xs = [synth.hidden_rows(m, shape.hidden, seed=70_000 + j, rho=wl["rho"]).cuda() for j in range(64)]
+    out = torch.empty_like(xs[0])
+    per_event = {k: [] for k in _lib.STAMP_NAMES}
+    totals = []
+    for r in range(runs + 5):
+        md = mods[r % copies]
+        md.set_option(_lib.MOE_OPT_STAMPS, stamps.data_ptr() if r >= 5 else 0)
+        stamps.zero_()
+        md.run(xs[r % 64], xs[r % 64], out)
+        torch.cuda.synchronize()
+        if r < 5:
+            continue
+        st = stamps.cpu()
+        t0 = int(st[:, 0].min())
+        for k in _lib.STAMP_NAMES:
+            col = st[:, k]
+            for v in col.tolist():
+                if v:
+                    per_event[k].append((v - t0) / 1000.0)
+        totals.append((int(st[:, 6].max()) - t0) / 1000.0)
+    for md in mods:
+        md.set_option(_lib.MOE_OPT_STAMPS, 0)
+        assert md.status() == _lib.MOE_OK
+    rows = []
+    for k, name in _lib.STAMP_NAMES.items():
+        v = sorted(per_event[k])
+        if not v:
+            continue
+        q = lambda f: v[min(len(v) - 1, int(f * len(v)))]  # noqa: E731
+        rows.append((name, statistics.median(v), q(0.1), q(0.9), v[-1]))
+    return rows, statistics.median(totals), mods[0].info(_lib.MOE_OPT_RING_SLOTS)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="ling_m1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--copies", type=int, default=8)
+    ap.add_argument("--runs", type=int, default=200)
+    ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--sweep-ring", default="", help="comma list of ring slot counts to compare")
+    a = ap.parse_args()
+    sweep = [int(v) for v in a.sweep_ring.split(",") if v] or [a.ring_slots]
+    for rs in sweep:
+        rows, total, used = timeline(a.workload, a.copies, a.runs, rs)
+        print(f"# {a.workload}: ring slots {used}, median first-entry -> last-exit {total:.2f} us")
+        print(f"{'event':>16} {'median':>8} {'p10':>8} {'p90':>8} {'max':>8}")
+        for name, med, p10, p90, mx in rows:
+            print(f"{name:>16} {med:8.2f} {p10:8.2f} {p90:8.2f} {mx:8.2f}")
+
+
+if __name__ == "__main__":
+    main()

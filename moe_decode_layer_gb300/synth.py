@@ -54,6 +54,38 @@ TINY = LayerShape(hidden=256, inter=128, num_experts=16, top_k=2, num_shared=1)
 LING = LayerShape(hidden=2560, inter=768, num_experts=512, top_k=8, num_shared=1)
 MUSE_NVFP4 = LayerShape(hidden=4096, inter=1024, num_experts=256, top_k=8,
                         num_shared=0, wdtype="nvfp4")
+LING_E64 = LayerShape(hidden=2560, inter=768, num_experts=64, top_k=8, num_shared=1)
+
+
+# Workloads of the bench and the profiling tools: layer shape, rows, row
+# correlation, layers per step.
+WORKLOADS = {
+    "ling_m1": dict(shape="LING", m=1, rho=0.0, layers=1,
+                    desc="Ling-3.0-flash-shaped MoE layer, H=2560, E=512 top-8 + 1 shared, I=768, M=1"),
+    "ling_m6": dict(shape="LING", m=6, rho=0.5, layers=1,
+                    desc="Ling-3.0-flash-shaped MoE layer, H=2560, E=512 top-8 + 1 shared, I=768, "
+                         "M=6 verify rows correlated rho=0.5"),
+    "stack_m6": dict(shape="LING", m=6, rho=0.5, layers=12,
+                     desc="12 distinct Ling-shaped MoE layers back to back, RMSNorm(1e-6) + residual "
+                          "between layers, M=6 rho=0.5"),
+    "nvfp4_m1": dict(shape="MUSE_NVFP4", m=1, rho=0.0, layers=1,
+                     desc="NVFP4 experts (e2m1, e4m3 block-16 scales, fp32 tensor scale), H=4096, "
+                          "E=256 top-8, I=1024, no shared expert, M=1"),
+    "nvfp4_m6": dict(shape="MUSE_NVFP4", m=6, rho=0.5, layers=1,
+                     desc="NVFP4 experts, H=4096, E=256 top-8, I=1024, M=6 rho=0.5"),
+    "tiny_m1": dict(shape="TINY", m=1, rho=0.0, layers=1,
+                    desc="tiny MoE layer H=256, E=16 top-2 + 1 shared, I=128, M=1"),
+    # profiling case: Ling-shaped experts, 64 of them (0.76 GB per copy), same
+    # bytes per step as Ling M=1 but for the smaller router
+    "ling_e64_m1": dict(shape="LING_E64", m=1, rho=0.0, layers=1,
+                        desc="Ling-shaped experts with E=64 top-8 + 1 shared (profiling case), M=1"),
+    "ling_e64_m6": dict(shape="LING_E64", m=6, rho=0.5, layers=1,
+                        desc="Ling-shaped experts with E=64 top-8 + 1 shared (profiling case), M=6"),
+}
+
+
+def workload_shape(name: str) -> LayerShape:
+    return globals()[WORKLOADS[name]["shape"]]
 
 
 def algorithmic_bytes(shape: LayerShape, distinct_routed: int) -> int:
