@@ -87,6 +87,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.rpair_bytes = 4 * H;
   p.grid = sms;
   p.nslot_max = S + std::min(E, maxm * K);
+  p.npair_max = S * maxm + maxm * K;
   // fixed shared-memory blocks
   size_t off = 0;
   auto take = [&](size_t bytes, size_t align) {
@@ -97,38 +98,50 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   };
   p.off_full = take(moe::kMaxSlots * 8, 8);
   p.off_empty = take(moe::kMaxSlots * 8, 8);
+  p.off_xbar = take(8, 8);
   p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
-  p.off_x = take((size_t)maxm * H * 2, 16);
-  p.off_hs = take((size_t)2 * maxm * I * 4, 16);
+  p.off_x = take((size_t)maxm * H * 2, 128);
   p.off_sel_e = take((size_t)maxm * K * 4, 4);
   p.off_sel_w = take((size_t)maxm * K * 4, 4);
   p.off_emask = take((size_t)E * 4, 4);
+  p.off_bitmap = take((size_t)(E + 31) / 32 * 4, 4);
   p.off_slot_of = take((size_t)E * 4, 4);
   p.off_slot_e = take((size_t)p.nslot_max * 4, 4);
   p.off_slot_mask = take((size_t)p.nslot_max * 4, 4);
   p.off_slot_w = take((size_t)p.nslot_max * maxm * 4, 4);
+  p.off_pair_base = take((size_t)(p.nslot_max + 1) * 4, 4);
   p.off_red = take((size_t)moe::kNC * moe::kRpgMax * 8 * 4, 16);
   p.off_misc = take(moe::MISC_WORDS * 4, 16);
-  p.off_ring = take(0, 128);
-  const long long budget = (long long)smem_optin - 1024 - p.off_ring;
+  const size_t fixed = round_up(off, 128);
+  const long long avail = (long long)smem_optin - 1024 - (long long)fixed;
+  // ring slot: one stage of ~kStageTarget bytes, at least one router pair, one
+  // gate/up pair and one down stage of this CTA's rows
   const int rows_per_cta = (H + p.grid - 1) / p.grid;
   int drs = std::min(rows_per_cta, moe::kRpgMax * p.ng);
+  size_t slot = 0;
   for (;;) {
-    const size_t need = std::max({(size_t)p.rpair_bytes, (size_t)p.pair_bytes,
-                                  (size_t)drs * (p.row2 + p.sc2)});
-    const size_t slot = round_up(need, 128);
-    const long long ns = budget > 0 ? budget / (long long)slot : 0;
-    if (ns >= 3 || drs == 1) {
-      if (ns < 2) return MOE_ERR_UNSUPPORTED;
-      p.slot_bytes = (int)slot;
-      p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
-      break;
-    }
+    slot = round_up(std::max({(size_t)moe::kStageTarget, (size_t)p.rpair_bytes, (size_t)p.pair_bytes,
+                              (size_t)drs * (p.row2 + p.sc2)}), 128);
+    if ((long long)(moe::kMinSlots * slot) <= avail - (long long)maxm * I * 4 || drs == 1) break;
     drs = (drs + 1) / 2;
   }
+  // h staging area: all (expert, row) pairs when they fit next to kMinSlots ring
+  // slots, else as many as fit (at least one slot's worth: maxm rows)
+  const size_t per_pair = (size_t)I * 4;
+  long long hs_room = avail - (long long)(moe::kMinSlots * slot);
+  int hs_pairs = (int)std::min<long long>(p.npair_max, hs_room > 0 ? hs_room / (long long)per_pair : 0);
+  if (hs_pairs < maxm) hs_pairs = maxm;
+  p.hs_pairs = hs_pairs;
+  p.off_hs = (int)fixed;
+  p.off_ring = (int)round_up(fixed + (size_t)hs_pairs * per_pair, 128);
+  const long long ring_budget = (long long)smem_optin - 1024 - p.off_ring;
+  const long long ns = ring_budget > 0 ? ring_budget / (long long)slot : 0;
+  if (ns < 2) return MOE_ERR_UNSUPPORTED;
+  p.slot_bytes = (int)slot;
+  p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
   p.d_rows_stage = drs;
-  p.pps = std::max(1, std::min(8, p.slot_bytes / p.pair_bytes));
-  p.pps_r = std::max(1, std::min(8, p.slot_bytes / p.rpair_bytes));
+  p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
+  p.qr = std::max(1, std::min(moe::kNC, p.slot_bytes / p.rpair_bytes));
   p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
   p.timeout_ns = kDefaultTimeoutNs;
   return MOE_OK;

@@ -1,23 +1,27 @@
 // Kernels of the small-batch MoE decode layer step (sm_103a).
 //
 // Every CTA has kNC consumer warps and one producer warp. The producer streams
-// weight rows from HBM into a ring of shared-memory slots with 1-D bulk (TMA)
-// copies tagged evict-first in L2, each slot guarded by a "full" mbarrier (the
-// copy engine counts the bytes in) and an "empty" mbarrier (consumers hand the
-// slot back). Consumers turn slots into dot products against the token rows.
+// weights from HBM into a ring of shared-memory slots with 1-D bulk (TMA)
+// copies tagged evict-first in L2. A stage is a block of consecutive rows
+// (several router row pairs, several gate/up row pairs of one expert as one
+// gate block and one up block, or one expert's down rows for this CTA's output
+// features), so each stage needs few large copies: the copy engine's rate per SM
+// is bounded by copies and stages issued, not by bytes in flight. Each slot has
+// a "full" mbarrier (the copy engine counts the bytes in) and an "empty"
+// mbarrier (the consumers hand the slot back).
 //
 // Phases (Ling-3.0-flash batch-1 decode blog, section "PDL: stacking the latency
 // floors of small kernels": router chain norm -> gate matvec -> top-k, MoE chain
 // up-GEMM -> activation -> down-GEMM -> combine):
 //   R  router rows (bf16) and the shared experts' gate/up rows: router logits and
-//      the shared experts' silu(g) * u; both need no routing decision.
+//      the shared experts' silu(g) * u; neither needs a routing decision.
 //   T  every CTA reads all logits and selects the top-k of each row itself, then
-//      forms the union of chosen experts with one row bitmask per expert and a
-//      popcount prefix over the expert ids (SGLang Low-Latency Mode page,
-//      section "Low-Latency-Specific Optimizations", item 3).
-//   U  gate/up rows of the chosen experts: h = w * silu(g) * u per (expert, row);
+//      forms the union of chosen experts from a bitmap with one row mask per
+//      expert and a popcount prefix over the expert ids (SGLang Low-Latency Mode
+//      page, section "Low-Latency-Specific Optimizations", item 3).
+//   U  gate/up rows of the chosen experts: h = w * silu(g) * u per (expert, row),
 //      SwiGLU in fp32 right after the dot products (blog section "Two fusions and
-//      a retune").
+//      a retune"). Row pairs of a stage go to different consumer warps.
 //   D  down rows: each CTA owns a contiguous block of output features, sums
 //      W2_e h_e over all chosen and shared experts in fp32 and writes
 //      bf16(residual + sum) with one rounding (blog section "PDL: ...": the combine
@@ -46,6 +50,7 @@ namespace moe {
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kBarConsumers = 1;  // named barrier: the kNC consumer warps
 constexpr int kBarRoute = 2;      // named barrier: consumers -> producer, routing ready
+constexpr int kStageBatch = 8;    // tagged words in flight per thread when staging h
 
 // --------------------------------------------------------------------------
 // small helpers
@@ -64,12 +69,18 @@ __device__ __forceinline__ void split_range(long long n, int c, int g, long long
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 struct Ctx {
   const Params& p;
   uint8_t* sm;
   int* misc;
   volatile int* slot_seq;  // [nslots] ring stage that currently owns each slot
-  uint32_t full0, empty0;
+  uint32_t full0, empty0, xbar;
   uint64_t t0;
   int tid, warp, lane;
 
@@ -78,6 +89,7 @@ struct Ctx {
     slot_seq = reinterpret_cast<volatile int*>(sm + p.off_slot_seq);
     full0 = smem_u32(sm + p.off_full);
     empty0 = smem_u32(sm + p.off_empty);
+    xbar = smem_u32(sm + p.off_xbar);
     t0 = global_ns();
     tid = threadIdx.x;
     warp = tid >> 5;
@@ -99,15 +111,25 @@ struct Ctx {
     if (p.stamps) p.stamps[(size_t)blockIdx.x * kStampSlots + ev] = global_ns();
   }
 
-  // Bounded wait for ring stage `seq` to be full. False on abort / timeout.
-  // Consumer warps take stages round-robin, so a warp may ask for a stage more
-  // than one lap ahead of its slot; an mbarrier parity only tells adjacent
-  // phases apart. The producer therefore records which stage owns a slot before
-  // arming it, and the parity wait starts only once `seq` owns the slot.
+  // Bounded wait on an mbarrier phase. False on abort / timeout.
+  __device__ bool wait_bar(uint32_t bar, uint32_t par, uint32_t site) const {
+    while (!mbar_try_wait(bar, par)) {
+      if (aborted()) return false;
+      if (expired()) {
+        fail(site);
+        return false;
+      }
+    }
+    return true;
+  }
+
+  // Bounded wait for ring stage `seq` to be full. Consumer warps take stages
+  // out of step with each other, so a warp may ask for a stage more than one lap
+  // ahead of its slot; an mbarrier parity only tells adjacent phases apart. The
+  // producer therefore records which stage owns a slot before arming it, and the
+  // parity wait starts only once `seq` owns the slot.
   __device__ bool wait_full(long long seq) const {
     const int slot = (int)(seq % p.nslots);
-    const uint32_t par = (uint32_t)((seq / p.nslots) & 1);
-    const uint32_t bar = full0 + 8u * slot;
     while (slot_seq[slot] != (int)seq) {
       if (aborted()) return false;
       if (expired()) {
@@ -115,28 +137,12 @@ struct Ctx {
         return false;
       }
     }
-    while (!mbar_try_wait(bar, par)) {
-      if (aborted()) return false;
-      if (expired()) {
-        fail(SITE_RING_FULL);
-        return false;
-      }
-    }
-    return true;
+    return wait_bar(full0 + 8u * slot, (uint32_t)((seq / p.nslots) & 1), SITE_RING_FULL);
   }
   // Producer side: bounded wait for the slot of stage `seq` to be free.
   __device__ bool wait_empty(long long seq) const {
     const int slot = (int)(seq % p.nslots);
-    const uint32_t par = (uint32_t)(((seq / p.nslots) & 1) ^ 1);
-    const uint32_t bar = empty0 + 8u * slot;
-    while (!mbar_try_wait(bar, par)) {
-      if (aborted()) return false;
-      if (expired()) {
-        fail(SITE_RING_EMPTY);
-        return false;
-      }
-    }
-    return true;
+    return wait_bar(empty0 + 8u * slot, (uint32_t)(((seq / p.nslots) & 1) ^ 1), SITE_RING_EMPTY);
   }
   __device__ void release(long long seq, uint32_t count) const {
     mbar_arrive(empty0 + 8u * (uint32_t)(seq % p.nslots), count);
@@ -145,73 +151,89 @@ struct Ctx {
 
 // Routing tables in shared memory.
 struct Route {
-  int* sel_e;          // [maxm][K]
-  float* sel_w;        // [maxm][K]
-  uint32_t* emask;     // [E] row mask per expert
-  int* slot_of;        // [E]
-  int* slot_e;         // [nslot_max] expert id, or -1 - s for shared expert s
-  uint32_t* slot_mask; // [nslot_max]
-  float* slot_w;       // [nslot_max][maxm] combine weight (routed_scale folded in)
+  int* sel_e;           // [maxm][K] chosen experts, descending weight
+  float* sel_w;         // [maxm][K]
+  uint32_t* emask;      // [E] row mask per expert
+  uint32_t* bitmap;     // [E / 32] experts chosen by any row
+  int* slot_of;         // [E] union slot of a chosen expert
+  int* slot_e;          // [nslot_max] expert id, or -1 - s for shared expert s
+  uint32_t* slot_mask;  // [nslot_max] rows that use the slot
+  float* slot_w;        // [nslot_max][maxm] combine weight (routed_scale folded in)
+  int* pair_base;       // [nslot_max + 1] first (slot, row) pair index of each slot
   __device__ Route(const Params& p, uint8_t* sm)
       : sel_e(reinterpret_cast<int*>(sm + p.off_sel_e)),
         sel_w(reinterpret_cast<float*>(sm + p.off_sel_w)),
         emask(reinterpret_cast<uint32_t*>(sm + p.off_emask)),
+        bitmap(reinterpret_cast<uint32_t*>(sm + p.off_bitmap)),
         slot_of(reinterpret_cast<int*>(sm + p.off_slot_of)),
         slot_e(reinterpret_cast<int*>(sm + p.off_slot_e)),
         slot_mask(reinterpret_cast<uint32_t*>(sm + p.off_slot_mask)),
-        slot_w(reinterpret_cast<float*>(sm + p.off_slot_w)) {}
+        slot_w(reinterpret_cast<float*>(sm + p.off_slot_w)),
+        pair_base(reinterpret_cast<int*>(sm + p.off_pair_base)) {}
 };
 
 // --------------------------------------------------------------------------
-// consumer: x rows into shared memory (optionally RMS-normalised)
+// stage schedule: the same walk on the producer and the consumer side
 // --------------------------------------------------------------------------
-static __device__ void load_x(const Ctx& c) {
+// Items of the gate/up phases are (slot u, row j) pairs flattened as u * I + j;
+// a stage holds up to q consecutive items of one slot (expert). Router items are
+// row pairs; a stage holds up to qr of them (I = 0: no slot boundaries).
+__device__ __forceinline__ long long stage_end(long long a, long long hi, int q, int I) {
+  long long b = a + q;
+  if (I > 0) {
+    const long long bound = (a / I + 1) * I;
+    b = b < bound ? b : bound;
+  }
+  return b < hi ? b : hi;
+}
+
+// This warp's item in stage [a, b) of a range starting at lo (item t goes to
+// warp (t - lo) % kNC); b or later when the warp has none.
+__device__ __forceinline__ long long warp_item(long long a, long long lo, int warp) {
+  return a + ((warp - (int)((a - lo) % kNC)) + kNC) % kNC;
+}
+
+// --------------------------------------------------------------------------
+// consumer: x rows (arrive by bulk copy; optionally RMS-normalised in place)
+// --------------------------------------------------------------------------
+static __device__ __noinline__ void prepare_x(const Ctx& c) {
   const Params& p = c.p;
+  if (!c.wait_bar(c.xbar, 0, SITE_RING_FULL)) return;
+  if (!p.pre_rmsnorm) return;
   uint4* xs = reinterpret_cast<uint4*>(c.sm + p.off_x);
   const int nch = p.H / 8;
-  const uint4* xg = reinterpret_cast<const uint4*>(p.x);
-  for (int m = c.warp; m < p.maxm; m += kNC) {
-    if (m >= p.M) {
-      for (int ch = c.lane; ch < nch; ch += 32) xs[m * nch + ch] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    float scale = 1.0f;
-    if (p.pre_rmsnorm) {
-      float ss = 0.0f;
-      for (int ch = c.lane; ch < nch; ch += 32) {
-        const uint4 v = xg[m * nch + ch];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float a = bf16lo(w[q]), b = bf16hi(w[q]);
-          ss = fmaf(a, a, ss);
-          ss = fmaf(b, b, ss);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-      scale = 1.0f / sqrtf(ss / (float)p.H + p.rms_eps);
-    }
+  for (int m = c.warp; m < p.M; m += kNC) {
+    float ss = 0.0f;
     for (int ch = c.lane; ch < nch; ch += 32) {
-      uint4 v = xg[m * nch + ch];
-      if (p.pre_rmsnorm) {
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint4 v = xs[m * nch + ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t lo = f32_to_bf16_bits(bf16lo(w[q]) * scale);
-          const uint32_t hi = f32_to_bf16_bits(bf16hi(w[q]) * scale);
-          w[q] = lo | (hi << 16);
-        }
-        v = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int q = 0; q < 4; ++q) {
+        const float a = bf16lo(w[q]), b = bf16hi(w[q]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
       }
-      xs[m * nch + ch] = v;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    const float scale = 1.0f / sqrtf(ss / (float)p.H + p.rms_eps);
+    for (int ch = c.lane; ch < nch; ch += 32) {
+      const uint4 v = xs[m * nch + ch];
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = f32_to_bf16_bits(bf16lo(w[q]) * scale);
+        const uint32_t hi = f32_to_bf16_bits(bf16hi(w[q]) * scale);
+        w[q] = lo | (hi << 16);
+      }
+      xs[m * nch + ch] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
 
 // --------------------------------------------------------------------------
-// consumer: dot products of one gate/up (or router) row pair with the rows in
-// `mask`. Results are warp-reduced (butterfly), so every lane holds all sums.
+// consumer: dot products of one row pair with the token rows in `mask`.
+// Results are warp-reduced (butterfly), so every lane holds all sums.
 // --------------------------------------------------------------------------
 template <int MAXM>
 struct PairAcc {
@@ -219,26 +241,45 @@ struct PairAcc {
   float u[MAXM];
 };
 
-// bf16 rows: `row_bytes` per row, stage = [row a][row b]. xr: lane's x chunks
-// (MAXM == 1); xs: x rows in shared memory (MAXM > 1).
-template <int MAXM, bool XREG>
-__device__ __forceinline__ void pair_dot_bf16(const uint8_t* st, int row_bytes, int nch,
-                                              const uint4* xr, const uint4* xs, uint32_t mask,
-                                              int lane, PairAcc<MAXM>& a) {
+template <int MAXM>
+__device__ __forceinline__ void warp_reduce_pair(PairAcc<MAXM>& a, uint32_t mask) {
 #pragma unroll
-  for (int m = 0; m < MAXM; ++m) a.g[m] = a.u[m] = 0.0f;
-  const uint4* wa = reinterpret_cast<const uint4*>(st);
-  const uint4* wb = reinterpret_cast<const uint4*>(st + row_bytes);
-  if (MAXM == 1 && XREG) {
+  for (int m = 0; m < MAXM; ++m) {
+    if (mask >> m & 1u) {
 #pragma unroll
-    for (int i = 0; i < kCplBf16; ++i) {
-      const int ch = lane + 32 * i;
-      if (ch < nch) {
-        dot8_bf16(a.g[0], wa[ch], xr[i]);
-        dot8_bf16(a.u[0], wb[ch], xr[i]);
+      for (int o = 16; o; o >>= 1) {
+        a.g[m] += __shfl_xor_sync(kFull, a.g[m], o);
+        a.u[m] += __shfl_xor_sync(kFull, a.u[m], o);
       }
     }
+  }
+}
+
+// bf16 rows a, b against x. XREG (MAXM == 1 only): the lane's x chunks in
+// registers; otherwise x rows from shared memory. Two partial sums per row
+// (even / odd chunk) shorten the dependent FMA chain.
+template <int MAXM, bool XREG>
+__device__ __forceinline__ void pair_dot_bf16(const uint4* wa, const uint4* wb, int nch, const uint4* xr,
+                                              const uint4* xs, uint32_t mask, int lane, PairAcc<MAXM>& a) {
+  if (MAXM == 1 && XREG) {
+    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kCplBf16; i += 2) {
+      const int ch0 = lane + 32 * i, ch1 = ch0 + 32;
+      if (ch0 < nch) {
+        dot8_bf16(g0, wa[ch0], xr[i]);
+        dot8_bf16(u0, wb[ch0], xr[i]);
+      }
+      if (ch1 < nch) {
+        dot8_bf16(g1, wa[ch1], xr[i + 1]);
+        dot8_bf16(u1, wb[ch1], xr[i + 1]);
+      }
+    }
+    a.g[0] = g0 + g1;
+    a.u[0] = u0 + u1;
   } else {
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) a.g[m] = a.u[m] = 0.0f;
     for (int ch = lane; ch < nch; ch += 32) {
       const uint4 va = wa[ch], vb = wb[ch];
 #pragma unroll
@@ -251,16 +292,7 @@ __device__ __forceinline__ void pair_dot_bf16(const uint8_t* st, int row_bytes, 
       }
     }
   }
-#pragma unroll
-  for (int m = 0; m < MAXM; ++m) {
-    if (mask >> m & 1u) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        a.g[m] += __shfl_xor_sync(kFull, a.g[m], o);
-        a.u[m] += __shfl_xor_sync(kFull, a.u[m], o);
-      }
-    }
-  }
+  warp_reduce_pair<MAXM>(a, mask);
 }
 
 // One NVFP4 chunk: 32 e2m1 codes (16 bytes) in two 16-element blocks with their
@@ -300,18 +332,15 @@ __device__ __forceinline__ void bf16x8_to_f16x8(const uint4 v, uint32_t* o) {
   }
 }
 
-// NVFP4 gate/up pair. Stage layout: [codes a][codes b][scales a][scales b].
-// xr: lane's x chunks as fp16 (MAXM == 1, 16 words per chunk); xs: bf16 x rows.
+// NVFP4 rows a, b (codes qa, qb; scales sa, sb). xr: lane's x chunks as fp16
+// (MAXM == 1, 16 words per chunk); xs: bf16 x rows (MAXM > 1).
 template <int MAXM>
-__device__ __forceinline__ void pair_dot_fp4(const uint8_t* st, int row_bytes, int sc_bytes, int nch,
-                                             const uint32_t* xr, const uint4* xs, int H,
-                                             uint32_t mask, int lane, PairAcc<MAXM>& a) {
+__device__ __forceinline__ void pair_dot_fp4(const uint4* qa, const uint4* qb, const uint16_t* sa,
+                                             const uint16_t* sb, int nch, const uint32_t* xr,
+                                             const uint4* xs, int H, uint32_t mask, int lane,
+                                             PairAcc<MAXM>& a) {
 #pragma unroll
   for (int m = 0; m < MAXM; ++m) a.g[m] = a.u[m] = 0.0f;
-  const uint4* qa = reinterpret_cast<const uint4*>(st);
-  const uint4* qb = reinterpret_cast<const uint4*>(st + row_bytes);
-  const uint16_t* sa = reinterpret_cast<const uint16_t*>(st + 2 * row_bytes);
-  const uint16_t* sb = reinterpret_cast<const uint16_t*>(st + 2 * row_bytes + sc_bytes);
   if (MAXM == 1) {
 #pragma unroll
     for (int i = 0; i < kCplFp4; ++i) {
@@ -338,16 +367,7 @@ __device__ __forceinline__ void pair_dot_fp4(const uint8_t* st, int row_bytes, i
       }
     }
   }
-#pragma unroll
-  for (int m = 0; m < MAXM; ++m) {
-    if (mask >> m & 1u) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        a.g[m] += __shfl_xor_sync(kFull, a.g[m], o);
-        a.u[m] += __shfl_xor_sync(kFull, a.u[m], o);
-      }
-    }
-  }
+  warp_reduce_pair<MAXM>(a, mask);
 }
 
 // --------------------------------------------------------------------------
@@ -356,7 +376,7 @@ __device__ __forceinline__ void pair_dot_fp4(const uint8_t* st, int row_bytes, i
 template <int FMT, int MAXM>
 struct XRegs {
   // MAXM == 1: the lane's x chunks, loaded once per phase.
-  uint4 b[(MAXM == 1 && FMT == FMT_BF16) ? kCplBf16 : 1];         // bf16 chunks
+  uint4 b[(MAXM == 1 && FMT == FMT_BF16) ? kCplBf16 : 1];          // bf16 chunks
   uint32_t h[(MAXM == 1 && FMT == FMT_NVFP4) ? 16 * kCplFp4 : 1];  // fp16 chunks (NVFP4)
 };
 
@@ -384,220 +404,241 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
   }
 }
 
-// Router stages: consecutive router row pairs. Writes tagged logits.
+// Router stages: up to qr consecutive row pairs per stage; item t of the CTA's
+// range goes to consumer warp (t - lo) % kNC. Writes tagged logits.
 template <int FMT, int MAXM>
 __device__ void consume_router(const Ctx& c, const XRegs<FMT, MAXM>& xr, long long& seq) {
   const Params& p = c.p;
   long long lo, hi;
   split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
-  const long long nst = (hi - lo + p.pps_r - 1) / p.pps_r;
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
   const uint32_t mask = (1u << p.M) - 1u;
   const uint32_t ep = c.epoch();
-  for (long long s = c.warp; s < nst; s += kNC) {
-    const long long q = seq + s;
-    const bool got = !c.aborted() && c.wait_full(q);
-    if (got) {
-      const uint8_t* st = c.slot_ptr((int)(q % p.nslots));
-      for (int it = 0; it < p.pps_r; ++it) {
-        const long long item = lo + s * p.pps_r + it;
-        if (item >= hi) break;
-        PairAcc<MAXM> a;
-        pair_dot_bf16<MAXM, FMT == FMT_BF16>(st + (size_t)it * p.rpair_bytes, p.H * 2, p.H / 8, xr.b,
-                                             xs, mask, c.lane, a);
-        if (!(p.test_flags & TEST_SKIP_LOGITS)) {
+  for (long long a = lo; a < hi; ++seq) {
+    const long long b = stage_end(a, hi, p.qr, 0);
+    const long long t = warp_item(a, lo, c.warp);
+    if (t < b && !c.aborted() && c.wait_full(seq)) {
+      const uint8_t* st = c.slot_ptr((int)(seq % p.nslots)) + (size_t)(t - a) * p.rpair_bytes;
+      PairAcc<MAXM> acc;
+      pair_dot_bf16<MAXM, FMT == FMT_BF16>(reinterpret_cast<const uint4*>(st),
+                                           reinterpret_cast<const uint4*>(st + 2 * p.H), p.H / 8, xr.b,
+                                           xs, mask, c.lane, acc);
+      if (!(p.test_flags & TEST_SKIP_LOGITS)) {
 #pragma unroll
-          for (int m = 0; m < MAXM; ++m) {
-            if (c.lane == m && m < p.M) {
-              st_tagged(&p.logits[(size_t)m * p.E + 2 * item], ep, a.g[m]);
-              st_tagged(&p.logits[(size_t)m * p.E + 2 * item + 1], ep, a.u[m]);
-            }
+        for (int m = 0; m < MAXM; ++m) {
+          if (c.lane == m && m < p.M) {
+            st_tagged(&p.logits[(size_t)m * p.E + 2 * t], ep, acc.g[m]);
+            st_tagged(&p.logits[(size_t)m * p.E + 2 * t + 1], ep, acc.u[m]);
           }
         }
       }
+      __syncwarp();
+      if (c.lane == 0) c.release(seq, t == a ? (uint32_t)(kNC - (b - a) + 1) : 1u);
     }
-    __syncwarp();
-    if (got && c.lane == 0) c.release(q, kNC);
+    a = b;
   }
-  seq += nst;
 }
 
-// Gate/up stages for expert pairs. `shared_phase`: items are (shared s, j) and
-// the result has weight 1; otherwise items are (routed union slot u, j).
+// Gate/up stages. `shared_phase`: items are (shared s, j), weight 1; otherwise
+// (routed union slot u, j) with the row's routing weight folded into h.
 template <int FMT, int MAXM>
 __device__ void consume_pairs(const Ctx& c, const Route& rt, const XRegs<FMT, MAXM>& xr,
                               bool shared_phase, long long& seq) {
   const Params& p = c.p;
-  const int n_routed = c.misc[MISC_NROUTED];
-  const long long n = shared_phase ? (long long)p.S * p.I : (long long)n_routed * p.I;
+  const long long n = shared_phase ? (long long)p.S * p.I : (long long)c.misc[MISC_NROUTED] * p.I;
   long long lo, hi;
   split_range(n, blockIdx.x, p.grid, lo, hi);
-  const long long nst = (hi - lo + p.pps - 1) / p.pps;
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
   const uint32_t ep = c.epoch();
-  for (long long s = c.warp; s < nst; s += kNC) {
-    const long long q = seq + s;
-    const bool got = !c.aborted() && c.wait_full(q);
-    if (got) {
-      const uint8_t* st = c.slot_ptr((int)(q % p.nslots));
-      for (int it = 0; it < p.pps; ++it) {
-        const long long item = lo + s * p.pps + it;
-        if (item >= hi) break;
-        const int slot = (int)(item / p.I) + (shared_phase ? 0 : p.S);
-        const int j = (int)(item % p.I);
-        const uint32_t mask = shared_phase ? (1u << p.M) - 1u : rt.slot_mask[slot];
-        PairAcc<MAXM> a;
-        const uint8_t* pst = st + (size_t)it * p.pair_bytes;
-        if (FMT == FMT_BF16)
-          pair_dot_bf16<MAXM, true>(pst, p.row13, p.nchunk_h, xr.b, xs, mask, c.lane, a);
-        else
-          pair_dot_fp4<MAXM>(pst, p.row13, p.sc13, p.nchunk_h, xr.h, xs, p.H, mask, c.lane, a);
-        float gsg = 1.0f, gsu = 1.0f;
-        if (FMT == FMT_NVFP4) {
-          const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
-          const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
-          gsg = gs[0];
-          gsu = gs[1];
-        }
+  const int slot0 = shared_phase ? 0 : p.S;
+  for (long long a = lo; a < hi; ++seq) {
+    const long long b = stage_end(a, hi, p.q, p.I);
+    const long long t = warp_item(a, lo, c.warp);
+    if (t < b && !c.aborted() && c.wait_full(seq)) {
+      const int nq = (int)(b - a), iq = (int)(t - a);
+      const int slot = (int)(t / p.I) + slot0;
+      const int j = (int)(t % p.I);
+      const uint32_t mask = shared_phase ? (1u << p.M) - 1u : rt.slot_mask[slot];
+      const uint8_t* st = c.slot_ptr((int)(seq % p.nslots));
+      PairAcc<MAXM> acc;
+      float gsg = 1.0f, gsu = 1.0f;
+      if (FMT == FMT_BF16) {
+        pair_dot_bf16<MAXM, true>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
+                                  reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
+                                  p.nchunk_h, xr.b, xs, mask, c.lane, acc);
+      } else {
+        const uint8_t* scb = st + (size_t)2 * nq * p.row13;
+        pair_dot_fp4<MAXM>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
+                           reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
+                           reinterpret_cast<const uint16_t*>(scb + (size_t)iq * p.sc13),
+                           reinterpret_cast<const uint16_t*>(scb + (size_t)(nq + iq) * p.sc13), p.nchunk_h,
+                           xr.h, xs, p.H, mask, c.lane, acc);
+        const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
+        const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
+        gsg = gs[0];
+        gsu = gs[1];
+      }
 #pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-          if (c.lane == m && (mask >> m & 1u)) {
-            const float g = a.g[m] * gsg, u = a.u[m] * gsu;
-            float h = silu_f32(g) * u;
-            if (!shared_phase) h *= rt.slot_w[slot * p.maxm + m];
-            st_tagged(&p.hbuf[((size_t)slot * p.maxm + m) * p.I + j], ep, h);
-          }
+      for (int m = 0; m < MAXM; ++m) {
+        if (c.lane == m && (mask >> m & 1u)) {
+          float h = silu_f32(acc.g[m] * gsg) * (acc.u[m] * gsu);
+          if (!shared_phase) h *= rt.slot_w[slot * p.maxm + m];
+          st_tagged(&p.hbuf[((size_t)slot * p.maxm + m) * p.I + j], ep, h);
         }
       }
+      __syncwarp();
+      if (c.lane == 0) c.release(seq, t == a ? (uint32_t)(kNC - nq + 1) : 1u);
     }
-    __syncwarp();
-    if (got && c.lane == 0) c.release(q, kNC);
+    a = b;
   }
-  seq += nst;
 }
 
 // --------------------------------------------------------------------------
 // consumer phase T: top-k per row and the expert union
 // --------------------------------------------------------------------------
-static __device__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
+// Row m's top-k on warp m: lane l holds the logits of experts [l*P, l*P+P) as
+// order-preserving keys; each round takes the warp-wide max (ties: lowest lane,
+// then lowest index, i.e. the lower expert id) and the winning lane rescans.
+template <int PM>
+__device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
   const Params& p = c.p;
-  const int ctid = c.tid;  // consumers are threads [0, kNC * 32)
   const uint32_t ep = c.epoch();
-  if (c.warp < p.M) {
-    const int m = c.warp;
-    const int P = (p.E + 31) / 32;  // logits per lane, contiguous ids
-    const int base = c.lane * P;
-    uint32_t key[32];
-    const unsigned long long* row = p.logits + (size_t)m * p.E;
-    uint64_t spins = 0;
-    for (;;) {
-      uint32_t bad = 0;
+  const int P = (p.E + 31) / 32;
+  const int base = c.lane * P;
+  const unsigned long long* row = p.logits + (size_t)m * p.E;
+  uint32_t key[PM];
+  uint64_t spins = 0;
+  for (;;) {
+    uint32_t bad = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        key[i] = 0;
-        if (i < P && base + i < p.E) {
-          unsigned long long v;
-          asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(row + base + i) : "memory");
-          bad |= (uint32_t)(v >> 32) != ep;
-          key[i] = f32_order_key(__uint_as_float((uint32_t)v));
-        }
-      }
-      if (!__any_sync(kFull, bad)) break;
-      bool stop = c.aborted();
-      if (!stop && (++spins & 63) == 0 && c.peer_failed()) stop = true;
-      if (!stop && c.expired()) {
-        if (c.lane == 0) c.fail(SITE_LOGITS);
-        stop = true;
-      }
-      if (__any_sync(kFull, stop)) {
-        if (c.lane == 0) *reinterpret_cast<volatile int*>(c.misc + MISC_ABORT) = 1;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) key[i] = (i < P && base + i < p.E) ? 1u : 0u;  // any valid ids
-        break;
+    for (int i = 0; i < PM; ++i) {
+      key[i] = 0;
+      if (i < P && base + i < p.E) {
+        const unsigned long long v = ld_relaxed_u64(row + base + i);
+        bad |= (uint32_t)(v >> 32) != ep;
+        key[i] = f32_order_key(__uint_as_float((uint32_t)v));
       }
     }
-    uint32_t lmax = 0;
-    int lidx = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (key[i] > lmax) {
-        lmax = key[i];
-        lidx = i;
-      }
-    int my_e = 0;
-    float my_v = 0.0f;
-    for (int j = 0; j < p.K; ++j) {
-      const uint32_t gmax = warp_max_u32(lmax);
-      const int winner = __ffs(__ballot_sync(kFull, lmax == gmax)) - 1;
-      const int e = __shfl_sync(kFull, base + lidx, winner);
-      if (c.lane == j) {
-        my_e = e;
-        my_v = order_key_f32(gmax);
-      }
-      if (c.lane == winner) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i == lidx) key[i] = 0;
-        lmax = 0;
-        lidx = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key[i] > lmax) {
-            lmax = key[i];
-            lidx = i;
-          }
-      }
+    if (!__any_sync(kFull, bad)) break;
+    bool stop = c.aborted();
+    if (!stop && (++spins & 63) == 0 && c.peer_failed()) stop = true;
+    if (!stop && c.expired()) {
+      if (c.lane == 0) c.fail(SITE_LOGITS);
+      stop = true;
     }
-    const float v0 = __shfl_sync(kFull, my_v, 0);
-    float ex = c.lane < p.K ? expf(my_v - v0) : 0.0f;
-    float sum = ex;
+    if (__any_sync(kFull, stop)) {
+      if (c.lane == 0) *reinterpret_cast<volatile int*>(c.misc + MISC_ABORT) = 1;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-    if (c.lane < p.K) {
-      const float w = ex / sum;
-      rt.sel_e[m * p.K + c.lane] = my_e;
-      rt.sel_w[m * p.K + c.lane] = w;
-      if (write_topk && blockIdx.x == 0) {
-        if (p.topk_idx) p.topk_idx[m * p.K + c.lane] = my_e;
-        if (p.topk_w) p.topk_w[m * p.K + c.lane] = w;
-      }
+      for (int i = 0; i < PM; ++i) key[i] = (i < P && base + i < p.E) ? 1u : 0u;  // any valid ids
+      break;
     }
   }
-  bar_sync(kBarConsumers, kNC * 32);
-  for (int t = ctid; t < p.M * p.K; t += kNC * 32) atomicOr(&rt.emask[rt.sel_e[t]], 1u << (t / p.K));
-  bar_sync(kBarConsumers, kNC * 32);
-  // Compact the experts with a non-zero row mask, ascending id (popcount prefix).
-  int* wtot = c.misc + MISC_WTOT;
-  int running = 0;
-  for (int e0 = 0; e0 < p.E; e0 += kNC * 32) {
-    const int e = e0 + ctid;
-    const bool nz = e < p.E && rt.emask[e] != 0u;
-    const uint32_t bal = __ballot_sync(kFull, nz);
-    if (c.lane == 0) wtot[c.warp] = __popc(bal);
-    bar_sync(kBarConsumers, kNC * 32);
-    int before = 0, total = 0;
-    for (int w = 0; w < kNC; ++w) {
-      const int v = wtot[w];
-      before += w < c.warp ? v : 0;
-      total += v;
+  // lane-local best as (key << 32 | (PM - 1 - i)): larger key, then lower index
+  auto best = [&]() {
+    unsigned long long v[PM];
+#pragma unroll
+    for (int i = 0; i < PM; ++i) v[i] = ((unsigned long long)key[i] << 32) | (unsigned)(PM - 1 - i);
+#pragma unroll
+    for (int w = PM / 2; w; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) v[i] = v[i] > v[i + w] ? v[i] : v[i + w];
+    return v[0];
+  };
+  unsigned long long lb = best();
+  int my_e = 0;
+  float my_v = 0.0f;
+  for (int j = 0; j < p.K; ++j) {
+    const uint32_t lmax = (uint32_t)(lb >> 32);
+    const uint32_t gmax = warp_max_u32(lmax);
+    const int winner = __ffs(__ballot_sync(kFull, lmax == gmax)) - 1;
+    const int lidx = PM - 1 - (int)(lb & 0xffffffffu);
+    const int e = __shfl_sync(kFull, base + lidx, winner);
+    if (c.lane == j) {
+      my_e = e;
+      my_v = order_key_f32(gmax);
     }
-    if (nz) {
-      const int s = p.S + running + before + __popc(bal & lanemask_lt());
+    if (c.lane == winner) {
+#pragma unroll
+      for (int i = 0; i < PM; ++i)
+        if (i == lidx) key[i] = 0;
+      lb = best();
+    }
+  }
+  const float v0 = __shfl_sync(kFull, my_v, 0);
+  const float ex = c.lane < p.K ? expf(my_v - v0) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+  if (c.lane < p.K) {
+    const float w = ex / sum;
+    rt.sel_e[m * p.K + c.lane] = my_e;
+    rt.sel_w[m * p.K + c.lane] = w;
+    atomicOr(&rt.emask[my_e], 1u << m);
+    atomicOr(&rt.bitmap[my_e >> 5], 1u << (my_e & 31));
+    if (write_topk && blockIdx.x == 0) {
+      if (p.topk_idx) p.topk_idx[m * p.K + c.lane] = my_e;
+      if (p.topk_w) p.topk_w[m * p.K + c.lane] = w;
+    }
+  }
+}
+
+static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
+  const Params& p = c.p;
+  if (c.warp < p.M) {
+    if (p.E <= 16 * 32)
+      topk_row<16>(c, rt, c.warp, write_topk);
+    else
+      topk_row<32>(c, rt, c.warp, write_topk);
+  }
+  bar_sync(kBarConsumers, kNC * 32);
+  if (c.warp == 0) {
+    // Union slots S.. in ascending expert id: popcount prefix over the bitmap.
+    const int words = (p.E + 31) / 32;
+    const uint32_t w = c.lane < words ? rt.bitmap[c.lane] : 0u;
+    const int cnt = __popc(w);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (c.lane >= o) incl += v;
+    }
+    int s = p.S + incl - cnt;
+    for (uint32_t bits = w; bits; bits &= bits - 1) {
+      const int e = c.lane * 32 + __ffs(bits) - 1;
       rt.slot_of[e] = s;
       rt.slot_e[s] = e;
       rt.slot_mask[s] = rt.emask[e];
+      ++s;
     }
-    running += total;
-    bar_sync(kBarConsumers, kNC * 32);
+    const int n_routed = __shfl_sync(kFull, incl, 31);
+    for (int t = c.lane; t < p.S; t += 32) {
+      rt.slot_e[t] = -1 - t;
+      rt.slot_mask[t] = (1u << p.M) - 1u;
+      for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
+    }
+    __syncwarp();
+    for (int t = c.lane; t < p.M * p.K; t += 32)
+      rt.slot_w[rt.slot_of[rt.sel_e[t]] * p.maxm + t / p.K] = rt.sel_w[t] * p.routed_scale;
+    // (slot, row) pair index of each slot: prefix of the row-mask popcounts
+    const int nsl = p.S + n_routed;
+    int carry = 0;
+    for (int s0 = 0; s0 < nsl; s0 += 32) {
+      const int sl = s0 + c.lane;
+      const int pc = sl < nsl ? __popc(rt.slot_mask[sl]) : 0;
+      int in = pc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, in, o);
+        if (c.lane >= o) in += v;
+      }
+      if (sl < nsl) rt.pair_base[sl] = carry + in - pc;
+      carry += __shfl_sync(kFull, in, 31);
+    }
+    if (c.lane == 0) {
+      rt.pair_base[nsl] = carry;
+      c.misc[MISC_NROUTED] = n_routed;
+    }
   }
-  if (ctid == 0) c.misc[MISC_NROUTED] = running;
-  for (int t = ctid; t < p.S; t += kNC * 32) {
-    rt.slot_e[t] = -1 - t;
-    rt.slot_mask[t] = (1u << p.M) - 1u;
-    for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
-  }
-  for (int t = ctid; t < p.M * p.K; t += kNC * 32)
-    rt.slot_w[rt.slot_of[rt.sel_e[t]] * p.maxm + t / p.K] = rt.sel_w[t] * p.routed_scale;
   bar_sync(kBarConsumers, kNC * 32);
 }
 
@@ -611,16 +652,15 @@ __device__ __forceinline__ void cta_rows(const Params& p, int& r_lo, int& r_hi) 
   r_hi = (int)hi;
 }
 
-// Wait until every CTA has copied x into shared memory (only needed when the
-// output overwrites x in the single-kernel schedule).
-static __device__ bool wait_xflags(const Ctx& c) {
+// Wait until every CTA has its copy of x (only needed when the output
+// overwrites x in the single-kernel schedule).
+static __device__ __noinline__ bool wait_xflags(const Ctx& c) {
   const Params& p = c.p;
   const uint32_t ep = c.epoch();
   uint64_t spins = 0;
   for (int i = c.tid; i < p.grid; i += kNC * 32) {
     for (;;) {
-      unsigned long long v;
-      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.xflags + i) : "memory");
+      const unsigned long long v = ld_relaxed_u64(p.xflags + i);
       if ((uint32_t)(v >> 32) == ep) break;
       if (c.aborted() || ((++spins & 63) == 0 && c.peer_failed())) return false;
       if (c.expired()) {
@@ -632,8 +672,66 @@ static __device__ bool wait_xflags(const Ctx& c) {
   return true;
 }
 
-// check_xflags: the output overwrites x and other CTAs of this kernel may still
-// be reading x (single-kernel schedule only).
+// Copies the h rows of slots [sl0, sl1) (tagged, produced by all CTAs) into hs
+// in (slot, row) pair order, kStageBatch 16-byte loads in flight per thread,
+// re-polling only the words whose tag is not current yet. False on abort /
+// timeout.
+static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float* hs, int sl0, int sl1) {
+  const Params& p = c.p;
+  const uint32_t ep = c.epoch();
+  const int p0 = rt.pair_base[sl0];
+  const int half = p.I / 2;
+  const int n = (rt.pair_base[sl1] - p0) * half;  // 16-byte units
+  uint64_t spins = 0;
+  for (int base = c.tid; base < n; base += kNC * 32 * kStageBatch) {
+    uint32_t pending = 0;
+    const unsigned long long* src[kStageBatch];
+    float* dst[kStageBatch];
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const int u = base + k * kNC * 32;
+      src[k] = p.hbuf;
+      dst[k] = hs;
+      if (u < n) {
+        const int pr = p0 + u / half, kk = 2 * (u % half);
+        // pair pr -> (slot, row): the slot whose pair range holds pr, then the
+        // row of that slot's mask with this rank
+        int sl = sl0;
+        while (rt.pair_base[sl + 1] <= pr) ++sl;
+        uint32_t msk = rt.slot_mask[sl];
+        for (int r = pr - rt.pair_base[sl]; r > 0; --r) msk &= msk - 1;
+        const int m = __ffs(msk) - 1;
+        src[k] = p.hbuf + ((size_t)sl * p.maxm + m) * p.I + kk;
+        dst[k] = hs + (size_t)(pr - p0) * p.I + kk;
+        pending |= 1u << k;
+      }
+    }
+    while (pending) {
+      unsigned long long v0[kStageBatch], v1[kStageBatch];
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        v0[k] = v1[k] = 0;
+        if (pending >> k & 1u) ld_tagged2(src[k], v0[k], v1[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        if ((pending >> k & 1u) && (uint32_t)(v0[k] >> 32) == ep && (uint32_t)(v1[k] >> 32) == ep) {
+          dst[k][0] = __uint_as_float((uint32_t)v0[k]);
+          dst[k][1] = __uint_as_float((uint32_t)v1[k]);
+          pending &= ~(1u << k);
+        }
+      }
+      if (!pending) break;
+      if (c.aborted() || ((++spins & 63) == 0 && c.peer_failed())) return false;
+      if (c.expired()) {
+        c.fail(SITE_HIDDEN);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 template <int FMT, int MAXM>
 __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, long long& seq) {
   const Params& p = c.p;
@@ -643,15 +741,13 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, l
   const int nrb = (r_hi - r_lo + drs - 1) / drs;
   const int nsl = p.S + c.misc[MISC_NROUTED];
   const int ctid = c.tid;
-  const int g = ctid / p.tg;        // thread group
-  const int ch = ctid % p.tg;       // 16-byte code chunk of a down row
+  const int g = ctid / p.tg;   // thread group
+  const int ch = ctid % p.tg;  // 16-byte code chunk of a down row
   const bool active = g < p.ng;
-  const uint32_t ep = c.epoch();
-  float* hs0 = reinterpret_cast<float*>(c.sm + p.off_hs);
+  float* hs = reinterpret_cast<float*>(c.sm + p.off_hs);
   float* red = reinterpret_cast<float*>(c.sm + p.off_red);
-  const int hs_words = p.maxm * p.I;
   constexpr int CH_EL = FMT == FMT_BF16 ? 8 : 32;  // elements per chunk
-  int buf = 0;
+  bool first_batch = true;
   for (int rb = 0; rb < nrb; ++rb) {
     const int rb_lo = r_lo + rb * drs;
     const int nr = min(drs, r_hi - rb_lo);
@@ -660,102 +756,80 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, l
     for (int ri = 0; ri < kRpgMax; ++ri)
 #pragma unroll
       for (int m = 0; m < MAXM; ++m) acc[ri][m] = 0.0f;
-    for (int sl = 0; sl < nsl; ++sl, ++seq) {
-      const uint32_t mask = rt.slot_mask[sl];
-      float* hs = hs0 + buf * hs_words;
-      // Stage this expert's h rows (tagged, from every CTA) into shared memory.
-      bool ok = !c.aborted();
-      if (ok) {
-        uint64_t spins = 0;
-        const int pairs = p.M * p.I / 2;
-        for (int t = ctid; t < pairs && ok; t += kNC * 32) {
-          const int m = (2 * t) / p.I;
-          if (!(mask >> m & 1u)) continue;
-          const int k = (2 * t) % p.I;
-          const unsigned long long* src = p.hbuf + ((size_t)sl * p.maxm + m) * p.I + k;
-          for (;;) {
-            unsigned long long v0, v1;
-            ld_tagged2(src, v0, v1);
-            if ((uint32_t)(v0 >> 32) == ep && (uint32_t)(v1 >> 32) == ep) {
-              hs[m * p.I + k] = __uint_as_float((uint32_t)v0);
-              hs[m * p.I + k + 1] = __uint_as_float((uint32_t)v1);
-              break;
-            }
-            if (c.aborted() || ((++spins & 63) == 0 && c.peer_failed())) {
-              ok = false;
-              break;
-            }
-            if (c.expired()) {
-              c.fail(SITE_HIDDEN);
-              ok = false;
-              break;
-            }
-          }
-        }
-      }
-      const bool got = ok && !c.aborted() && c.wait_full(seq);
-      ok = got;
+    for (int sl0 = 0; sl0 < nsl;) {
+      // the batch of slots whose h rows fit in hs at once
+      int sl1 = sl0 + 1;
+      while (sl1 < nsl && rt.pair_base[sl1 + 1] - rt.pair_base[sl0] <= p.hs_pairs) ++sl1;
+      if (!first_batch) bar_sync(kBarConsumers, kNC * 32);  // hs is free again
+      first_batch = false;
+      if (!c.aborted()) stage_h(c, rt, hs, sl0, sl1);
       bar_sync(kBarConsumers, kNC * 32);
-      if (rb == 0 && sl == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
-      if (ok && !c.aborted() && active) {
-        const uint8_t* st = c.slot_ptr((int)(seq % p.nslots));
-        float gsc = 1.0f;
-        if (FMT == FMT_NVFP4) {
-          const int e = rt.slot_e[sl];
-          gsc = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];
-        }
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-          if (!(mask >> m & 1u)) continue;
-          float hv[CH_EL];
-          const float4* hp = reinterpret_cast<const float4*>(hs + m * p.I + ch * CH_EL);
-#pragma unroll
-          for (int q = 0; q < CH_EL / 4; ++q) {
-            const float4 f = hp[q];
-            hv[4 * q] = f.x * gsc;
-            hv[4 * q + 1] = f.y * gsc;
-            hv[4 * q + 2] = f.z * gsc;
-            hv[4 * q + 3] = f.w * gsc;
+      if (rb == 0 && sl0 == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
+      for (int sl = sl0; sl < sl1; ++sl, ++seq) {
+        const uint32_t mask = rt.slot_mask[sl];
+        const bool got = !c.aborted() && c.wait_full(seq);
+        if (got && active) {
+          const uint8_t* st = c.slot_ptr((int)(seq % p.nslots));
+          float gsc = 1.0f;
+          if (FMT == FMT_NVFP4) {
+            const int e = rt.slot_e[sl];
+            gsc = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];
           }
+          int hp = rt.pair_base[sl] - rt.pair_base[sl0];
 #pragma unroll
-          for (int ri = 0; ri < kRpgMax; ++ri) {
-            const int r = g + ri * p.ng;
-            if (r < nr) {
-              if (FMT == FMT_BF16) {
-                const uint4 w = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
-                dot8_bf16_f32(acc[ri][m], w, hv);
-              } else {
-                const uint4 qv = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
-                const uint32_t sc = reinterpret_cast<const uint16_t*>(
-                    st + (size_t)drs * p.row2 + (size_t)r * p.sc2)[ch];
-                const uint32_t sf = e4m3x2_to_f16x2(sc);
-                const float s[2] = {__half2float(__ushort_as_half((unsigned short)(sf & 0xffffu))),
-                                    __half2float(__ushort_as_half((unsigned short)(sf >> 16)))};
-                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+          for (int m = 0; m < MAXM; ++m) {
+            if (!(mask >> m & 1u)) continue;
+            float hv[CH_EL];
+            const float4* hq = reinterpret_cast<const float4*>(hs + (size_t)hp * p.I + ch * CH_EL);
+            ++hp;
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                  float part = 0.0f;
+            for (int q = 0; q < CH_EL / 4; ++q) {
+              const float4 f = hq[q];
+              hv[4 * q] = f.x * gsc;
+              hv[4 * q + 1] = f.y * gsc;
+              hv[4 * q + 2] = f.z * gsc;
+              hv[4 * q + 3] = f.w * gsc;
+            }
 #pragma unroll
-                  for (int wi = 0; wi < 2; ++wi) {
+            for (int ri = 0; ri < kRpgMax; ++ri) {
+              const int r = g + ri * p.ng;
+              if (r < nr) {
+                if (FMT == FMT_BF16) {
+                  const uint4 w = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
+                  dot8_bf16_f32(acc[ri][m], w, hv);
+                } else {
+                  const uint4 qv = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
+                  const uint32_t sc = reinterpret_cast<const uint16_t*>(
+                      st + (size_t)drs * p.row2 + (size_t)r * p.sc2)[ch];
+                  const uint32_t sf = e4m3x2_to_f16x2(sc);
+                  const float s[2] = {__half2float(__ushort_as_half((unsigned short)(sf & 0xffffu))),
+                                      __half2float(__ushort_as_half((unsigned short)(sf >> 16)))};
+                  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                    for (int by = 0; by < 4; ++by) {
-                      const uint32_t wv = e2m1x2_to_f16x2((qw[blk * 2 + wi] >> (8 * by)) & 0xffu);
-                      const int e0 = blk * 16 + wi * 8 + by * 2;
-                      const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
-                      part = fmaf(__low2float(wh), hv[e0], part);
-                      part = fmaf(__high2float(wh), hv[e0 + 1], part);
+                  for (int blk = 0; blk < 2; ++blk) {
+                    float part = 0.0f;
+#pragma unroll
+                    for (int wi = 0; wi < 2; ++wi) {
+#pragma unroll
+                      for (int by = 0; by < 4; ++by) {
+                        const uint32_t wv = e2m1x2_to_f16x2((qw[blk * 2 + wi] >> (8 * by)) & 0xffu);
+                        const int e0 = blk * 16 + wi * 8 + by * 2;
+                        const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
+                        part = fmaf(__low2float(wh), hv[e0], part);
+                        part = fmaf(__high2float(wh), hv[e0 + 1], part);
+                      }
                     }
+                    acc[ri][m] = fmaf(s[blk], part, acc[ri][m]);
                   }
-                  acc[ri][m] = fmaf(s[blk], part, acc[ri][m]);
                 }
               }
             }
           }
         }
+        __syncwarp();
+        if (got && c.lane == 0) c.release(seq, 1);
       }
-      __syncwarp();
-      if (got && c.lane == 0) c.release(seq, 1);
-      buf ^= 1;
+      sl0 = sl1;
     }
     // Reduce each row's partial sums over the group's threads and write out.
     if (check_xflags && rb == 0) {
@@ -836,54 +910,60 @@ struct Producer {
     return true;
   }
 
+  // x rows straight into shared memory, ahead of any weights.
+  __device__ void x_rows() {
+    const Params& p = c.p;
+    const uint32_t bytes = (uint32_t)p.M * p.H * 2;
+    mbar_arrive_expect_tx(c.xbar, bytes);
+    bulk_g2s(smem_u32(c.sm + p.off_x), p.x, bytes, c.xbar, pol);
+  }
+
   __device__ void router(long long& seq) {
     const Params& p = c.p;
     long long lo, hi;
     split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
-    const long long nst = (hi - lo + p.pps_r - 1) / p.pps_r;
-    for (long long s = 0; s < nst; ++s) {
-      const long long a = lo + s * p.pps_r, b = min(hi, a + p.pps_r);
+    for (long long a = lo; a < hi; ++seq) {
+      const long long b = stage_end(a, hi, p.qr, 0);
       const uint32_t bytes = (uint32_t)((b - a) * p.rpair_bytes);
       uint32_t dst, bar;
-      if (!begin(seq + s, bytes, dst, bar)) break;
+      if (!begin(seq, bytes, dst, bar)) return;
       bulk_g2s(dst, p.router_w + (size_t)a * p.rpair_bytes, bytes, bar, pol);
+      a = b;
     }
-    seq += nst;
   }
 
-  // Gate/up row pairs: shared experts (shared_phase) or the routed union.
+  // Gate/up stages: consecutive rows of one expert as a gate block and an up
+  // block (plus the two scale blocks for NVFP4).
   __device__ void pairs(bool shared_phase, const Route& rt, long long& seq) {
     const Params& p = c.p;
-    const int n_routed = c.misc[MISC_NROUTED];
-    const long long n = shared_phase ? (long long)p.S * p.I : (long long)n_routed * p.I;
+    const long long n = shared_phase ? (long long)p.S * p.I : (long long)c.misc[MISC_NROUTED] * p.I;
     long long lo, hi;
     split_range(n, blockIdx.x, p.grid, lo, hi);
-    const long long nst = (hi - lo + p.pps - 1) / p.pps;
-    for (long long s = 0; s < nst; ++s) {
-      const long long a = lo + s * p.pps, b = min(hi, a + p.pps);
+    for (long long a = lo; a < hi; ++seq) {
+      const long long b = stage_end(a, hi, p.q, p.I);
+      const int nq = (int)(b - a);
+      const int slot = (int)(a / p.I) + (shared_phase ? 0 : p.S);
+      const int j = (int)(a % p.I);
       uint32_t dst, bar;
-      if (!begin(seq + s, (uint32_t)((b - a) * p.pair_bytes), dst, bar)) break;
-      for (long long item = a; item < b; ++item) {
-        const int slot = (int)(item / p.I) + (shared_phase ? 0 : p.S);
-        const int j = (int)(item % p.I);
-        const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
-        const uint8_t* w = e >= 0 ? p.w13 : p.sh_w13;
-        const uint8_t* ws = e >= 0 ? p.w13_s : p.sh_w13_s;
-        const size_t ex = (size_t)(e >= 0 ? e : -1 - e);
-        const size_t rg = ex * 2 * p.I + j, ru = rg + p.I;  // gate row, up row
-        const uint32_t d = dst + (uint32_t)((item - a) * p.pair_bytes);
-        bulk_g2s(d, w + rg * p.row13, p.row13, bar, pol);
-        bulk_g2s(d + p.row13, w + ru * p.row13, p.row13, bar, pol);
-        if (p.sc13) {
-          bulk_g2s(d + 2 * p.row13, ws + rg * p.sc13, p.sc13, bar, pol);
-          bulk_g2s(d + 2 * p.row13 + p.sc13, ws + ru * p.sc13, p.sc13, bar, pol);
-        }
+      if (!begin(seq, (uint32_t)nq * p.pair_bytes, dst, bar)) return;
+      const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
+      const uint8_t* w = e >= 0 ? p.w13 : p.sh_w13;
+      const uint8_t* ws = e >= 0 ? p.w13_s : p.sh_w13_s;
+      const size_t ex = (size_t)(e >= 0 ? e : -1 - e);
+      const size_t rg = ex * 2 * p.I + j, ru = rg + p.I;  // first gate row, first up row
+      const uint32_t cb = (uint32_t)nq * p.row13;
+      bulk_g2s(dst, w + rg * p.row13, cb, bar, pol);
+      bulk_g2s(dst + cb, w + ru * p.row13, cb, bar, pol);
+      if (p.sc13) {
+        const uint32_t sb = (uint32_t)nq * p.sc13;
+        bulk_g2s(dst + 2 * cb, ws + rg * p.sc13, sb, bar, pol);
+        bulk_g2s(dst + 2 * cb + sb, ws + ru * p.sc13, sb, bar, pol);
       }
+      a = b;
     }
-    seq += nst;
   }
 
-  // Down stages (row block rb, union slot sl) for sl in [sl_lo, sl_hi) of block rb.
+  // Down stages (row block rb, union slot sl) for sl in [sl_lo, sl_hi).
   __device__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi, long long& seq) {
     const Params& p = c.p;
     int r_lo, r_hi;
@@ -926,7 +1006,7 @@ struct Producer {
     }
   }
 
-  // After an abort: wait (bounded) for this CTA's copies still in flight.
+  // Before exit: wait (bounded) for this CTA's copies still in flight.
   __device__ void drain() {
     const Params& p = c.p;
     const long long first = issued > p.nslots ? issued - p.nslots : 0;
@@ -966,27 +1046,42 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       mbar_init(c.empty0 + 8u * i, kNC);
       c.slot_seq[i] = -1;
     }
+    mbar_init(c.xbar, 1);
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;
     c.misc[MISC_NROUTED] = 0;
   }
   for (int e = c.tid; e < p.E; e += kThreads) rt.emask[e] = 0u;
+  for (int e = c.tid; e < (p.E + 31) / 32; e += kThreads) rt.bitmap[e] = 0u;
   __syncthreads();
 
+  bool x_issued = false;
   if (c.warp == kNC) {
     // ------------------------------------------------------------ producer
     Producer pr(c);
     long long seq = 0;
-    if (PHASES & PH_R) {
-      if (c.lane == 0) {
-        pr.router(seq);
+    if (c.lane == 0) {
+      c.stamp(ST_START);
+      if (PHASES == PH_ALL) {
+        pr.x_rows();
+        x_issued = true;
+      }
+      if (PHASES & PH_R) pr.router(seq);
+      if (kChain && kNeedX) {
+        pdl_wait();  // x may be the previous kernel's output
+        if (!c.aborted()) {
+          pr.x_rows();
+          x_issued = true;
+        }
+      }
+      if (PHASES & PH_R) {
         pr.pairs(true, rt, seq);
         c.stamp(ST_P_R_ISSUED);
         if (PHASES & PH_D) pr.prefetch_shared_down();
+      } else if (PHASES == PH_D) {
+        // The shared experts' down rows of the first row block need no routing.
+        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, seq);
       }
-    } else if (PHASES == PH_D) {
-      // The shared experts' down rows of the first row block need no routing.
-      if (c.lane == 0 && pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, seq);
     }
     if (kRoute) {
       __syncwarp();
@@ -1005,14 +1100,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         c.stamp(ST_P_D_ISSUED);
       }
       if (c.aborted()) pr.drain();
+      // the x copy may still be in flight if the consumers gave up before it landed
+      if (x_issued && c.aborted()) {
+        const uint64_t t = global_ns();
+        while (!mbar_try_wait(c.xbar, 0) && global_ns() - t < p.timeout_ns) {
+        }
+      }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers
     if (kChain) pdl_wait();
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
-    if (c.tid == 0) c.stamp(ST_START);
-    if (kNeedX) load_x(c);
+    if (kNeedX) prepare_x(c);
     bar_sync(kBarConsumers, kNC * 32);
     if (c.tid == 0) c.stamp(ST_X_LOADED);
     if (PHASES == PH_ALL && p.out_aliases_x && c.tid == 0)

@@ -10,6 +10,8 @@ constexpr int kRpgMax = 6;               // down-projection rows per thread grou
 constexpr int kMaxSlots = 64;            // ring slots (upper bound for the barrier arrays)
 constexpr int kCplBf16 = 16;             // 16-byte x chunks per lane kept in registers (H <= 4096)
 constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVFP4 (H <= 4096)
+constexpr int kStageTarget = 32768;      // ring slot size aimed for (bytes)
+constexpr int kMinSlots = 4;             // ring slots kept before shrinking the h staging area
 
 enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
 
@@ -90,15 +92,18 @@ struct Params {
   int row2, sc2;     // code / scale bytes per down row
   int pair_bytes;    // one gate row + one up row (codes and scales)
   int rpair_bytes;   // two router rows
-  int pps, pps_r;    // pairs per stage (expert / router)
+  int q, qr;         // gate/up pairs per stage, router row pairs per stage (<= kNC)
   int slot_bytes, nslots;
   int d_rows_stage;  // down rows per stage
   int tg, ng;        // threads per down group, groups
   int grid;
   int nslot_max;     // S + min(E, maxm * K)
+  int npair_max;     // S * maxm + maxm * K: (expert, row) pairs with an h row
+  int hs_pairs;      // h rows the down phase stages in shared memory at once
   // shared-memory offsets from the aligned base
-  int off_full, off_empty, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w, off_emask, off_slot_of;
-  int off_slot_e, off_slot_mask, off_slot_w, off_red, off_misc, off_ring;
+  int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
+  int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;
+  int off_red, off_misc, off_ring;
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;
   int test_flags;
