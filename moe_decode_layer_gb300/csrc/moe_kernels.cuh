@@ -130,11 +130,14 @@ struct Ctx {
   // parity wait starts only once `seq` owns the slot.
   __device__ bool wait_full(long long seq) const {
     const int slot = (int)(seq % p.nslots);
-    while (slot_seq[slot] != (int)seq) {
-      if (aborted()) return false;
-      if (expired()) {
-        fail(SITE_RING_FULL);
-        return false;
+    for (uint32_t spin = 0; slot_seq[slot] != (int)seq; ++spin) {
+      __nanosleep(64);  // leave the issue slots to the warps doing arithmetic
+      if ((spin & 15) == 15) {
+        if (aborted()) return false;
+        if (expired()) {
+          fail(SITE_RING_FULL);
+          return false;
+        }
       }
     }
     return wait_bar(full0 + 8u * slot, (uint32_t)((seq / p.nslots) & 1), SITE_RING_FULL);
@@ -520,6 +523,7 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
       }
     }
     if (!__any_sync(kFull, bad)) break;
+    __nanosleep(32);
     bool stop = c.aborted();
     if (!stop && (++spins & 63) == 0 && c.peer_failed()) stop = true;
     if (!stop && c.expired()) {
@@ -722,6 +726,7 @@ static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float
         }
       }
       if (!pending) break;
+      __nanosleep(32);
       if (c.aborted() || ((++spins & 63) == 0 && c.peer_failed())) return false;
       if (c.expired()) {
         c.fail(SITE_HIDDEN);

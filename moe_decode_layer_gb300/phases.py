@@ -20,7 +20,8 @@ from . import _lib, synth
 from .layer import MoEDecodeLayer
 
 
-def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: str = "persistent"):
+def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: str = "persistent",
+             n_inputs: int = 64):
     wl = synth.WORKLOADS[workload]
     shape = synth.workload_shape(workload)
     m = wl["m"]
@@ -30,8 +31,8 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
     stamps = torch.zeros((grid, 16), dtype=torch.int64, device="cuda")
     for md in mods:
         if ring_slots:
-            md.set_option(_lib.MOE_OPT_RING_SLOTS, ring_slots)
-    xs = [synth.hidden_rows(m, shape.hidden, seed=70_000 + j, rho=wl["rho"]).cuda() for j in range(64)]
+            md.set_option(_lib.MOE_OPT_RING_SLOTS, min(ring_slots, md.info(_lib.MOE_INFO_RING_SLOTS)))
+    xs = [synth.hidden_rows(m, shape.hidden, seed=70_000 + j, rho=wl["rho"]).cuda() for j in range(n_inputs)]
     out = torch.empty_like(xs[0])
     per_event = {k: [] for k in _lib.STAMP_NAMES}
     totals = []
@@ -39,7 +40,7 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
         md = mods[r % copies]
         md.set_option(_lib.MOE_OPT_STAMPS, stamps.data_ptr() if r >= 5 else 0)
         stamps.zero_()
-        md.run(xs[r % 64], xs[r % 64], out)
+        md.run(xs[r % n_inputs], xs[r % n_inputs], out)
         torch.cuda.synchronize()
         if r < 5:
             continue
@@ -71,11 +72,14 @@ def main():
     ap.add_argument("--runs", type=int, default=200)
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--sweep-ring", default="", help="comma list of ring slot counts to compare")
+    ap.add_argument("--hot", action="store_true", help="one layer copy and one input: weights stay in L2")
     a = ap.parse_args()
     sweep = [int(v) for v in a.sweep_ring.split(",") if v] or [a.ring_slots]
     for rs in sweep:
-        rows, total, used = timeline(a.workload, a.copies, a.runs, rs)
-        print(f"# {a.workload}: ring slots {used}, median first-entry -> last-exit {total:.2f} us")
+        rows, total, used = timeline(a.workload, 1 if a.hot else a.copies, a.runs, rs,
+                                     n_inputs=1 if a.hot else 64)
+        print(f"# {a.workload}{' (hot: weights in L2)' if a.hot else ''}: ring slots {used}, "
+              f"median first-entry -> last-exit {total:.2f} us")
         print(f"{'event':>16} {'median':>8} {'p10':>8} {'p90':>8} {'max':>8}")
         for name, med, p10, p90, mx in rows:
             print(f"{name:>16} {med:8.2f} {p10:8.2f} {p90:8.2f} {mx:8.2f}")
