@@ -61,11 +61,25 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// [lo, hi) share of n items for CTA c of g.
-__device__ __forceinline__ void split_range(long long n, int c, int g, long long& lo, long long& hi) {
-  lo = n * c / g;
-  hi = n * (c + 1) / g;
+// [lo, hi) share of n items for CTA c of g (n * g < 2^32 for every phase).
+__device__ __forceinline__ void split_range(int n, int c, int g, int& lo, int& hi) {
+  lo = (int)((unsigned)n * (unsigned)c / (unsigned)g);
+  hi = (int)((unsigned)n * (unsigned)(c + 1) / (unsigned)g);
 }
+
+// Position in the shared-memory ring: stage number, its slot and the slot's
+// mbarrier phase parity, advanced without divisions.
+struct Ring {
+  int seq = 0, slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int nslots) {
+    ++seq;
+    if (++slot == nslots) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
@@ -128,9 +142,8 @@ struct Ctx {
   // ahead of its slot; an mbarrier parity only tells adjacent phases apart. The
   // producer therefore records which stage owns a slot before arming it, and the
   // parity wait starts only once `seq` owns the slot.
-  __device__ bool wait_full(long long seq) const {
-    const int slot = (int)(seq % p.nslots);
-    for (uint32_t spin = 0; slot_seq[slot] != (int)seq; ++spin) {
+  __device__ bool wait_full(const Ring& r) const {
+    for (uint32_t spin = 0; slot_seq[r.slot] != r.seq; ++spin) {
       __nanosleep(64);  // leave the issue slots to the warps doing arithmetic
       if ((spin & 15) == 15) {
         if (aborted()) return false;
@@ -140,16 +153,13 @@ struct Ctx {
         }
       }
     }
-    return wait_bar(full0 + 8u * slot, (uint32_t)((seq / p.nslots) & 1), SITE_RING_FULL);
+    return wait_bar(full0 + 8u * r.slot, r.phase, SITE_RING_FULL);
   }
-  // Producer side: bounded wait for the slot of stage `seq` to be free.
-  __device__ bool wait_empty(long long seq) const {
-    const int slot = (int)(seq % p.nslots);
-    return wait_bar(empty0 + 8u * slot, (uint32_t)(((seq / p.nslots) & 1) ^ 1), SITE_RING_EMPTY);
+  // Producer side: bounded wait for the slot of stage `r` to be free.
+  __device__ bool wait_empty(const Ring& r) const {
+    return wait_bar(empty0 + 8u * r.slot, r.phase ^ 1u, SITE_RING_EMPTY);
   }
-  __device__ void release(long long seq, uint32_t count) const {
-    mbar_arrive(empty0 + 8u * (uint32_t)(seq % p.nslots), count);
-  }
+  __device__ void release(const Ring& r, uint32_t count) const { mbar_arrive(empty0 + 8u * r.slot, count); }
 };
 
 // Routing tables in shared memory.
@@ -180,21 +190,38 @@ struct Route {
 // --------------------------------------------------------------------------
 // Items of the gate/up phases are (slot u, row j) pairs flattened as u * I + j;
 // a stage holds up to q consecutive items of one slot (expert). Router items are
-// row pairs; a stage holds up to qr of them (I = 0: no slot boundaries).
-__device__ __forceinline__ long long stage_end(long long a, long long hi, int q, int I) {
-  long long b = a + q;
-  if (I > 0) {
-    const long long bound = (a / I + 1) * I;
-    b = b < bound ? b : bound;
+// row pairs; a stage holds up to qr of them (no slot boundaries). Item t of the
+// CTA's range [lo, hi) goes to consumer warp (t - lo) % kNC.
+struct ItemWalk {
+  int a, hi, u, j, r;  // next item, end, its slot and row, (a - lo) % kNC
+  int q, I;            // items per stage, rows per slot (0: no boundaries)
+  __device__ __forceinline__ ItemWalk(int lo, int hi_, int q_, int I_) : a(lo), hi(hi_), r(0), q(q_), I(I_) {
+    u = I_ > 0 ? lo / I_ : 0;
+    j = I_ > 0 ? lo - u * I_ : lo;
   }
-  return b < hi ? b : hi;
-}
-
-// This warp's item in stage [a, b) of a range starting at lo (item t goes to
-// warp (t - lo) % kNC); b or later when the warp has none.
-__device__ __forceinline__ long long warp_item(long long a, long long lo, int warp) {
-  return a + ((warp - (int)((a - lo) % kNC)) + kNC) % kNC;
-}
+  __device__ __forceinline__ bool more() const { return a < hi; }
+  // items in the current stage
+  __device__ __forceinline__ int count() const {
+    int n = min(q, hi - a);
+    if (I > 0) n = min(n, I - j);
+    return n;
+  }
+  // offset of warp w's item in the current stage (>= count() when it has none)
+  __device__ __forceinline__ int offset(int w) const {
+    const int d = w - r;
+    return d < 0 ? d + kNC : d;
+  }
+  __device__ __forceinline__ void advance(int n) {
+    a += n;
+    j += n;
+    if (I > 0 && j == I) {
+      j = 0;
+      ++u;
+    }
+    r += n;
+    if (r >= kNC) r -= kNC;
+  }
+};
 
 // --------------------------------------------------------------------------
 // consumer: x rows (arrive by bulk copy; optionally RMS-normalised in place)
@@ -407,93 +434,82 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
   }
 }
 
-// Router stages: up to qr consecutive row pairs per stage; item t of the CTA's
-// range goes to consumer warp (t - lo) % kNC. Writes tagged logits.
+enum ItemKind : int { ITEM_ROUTER = 0, ITEM_SHARED = 1, ITEM_ROUTED = 2 };
+
+// One phase of row-pair items (router rows, shared gate/up rows or routed
+// gate/up rows): each consumer warp takes its items of every stage, computes
+// the dot products against x and publishes tagged results. Returns the ring
+// position after the phase. Not inlined: the three phases share this code.
 template <int FMT, int MAXM>
-__device__ void consume_router(const Ctx& c, const XRegs<FMT, MAXM>& xr, long long& seq) {
+__device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring) {
   const Params& p = c.p;
-  long long lo, hi;
-  split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
+  const bool router = kind == ITEM_ROUTER;
+  const int n = router ? p.E / 2 : (kind == ITEM_SHARED ? p.S * p.I : c.misc[MISC_NROUTED] * p.I);
+  int lo, hi;
+  split_range(n, blockIdx.x, p.grid, lo, hi);
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
-  const uint32_t mask = (1u << p.M) - 1u;
   const uint32_t ep = c.epoch();
-  for (long long a = lo; a < hi; ++seq) {
-    const long long b = stage_end(a, hi, p.qr, 0);
-    const long long t = warp_item(a, lo, c.warp);
-    if (t < b && !c.aborted() && c.wait_full(seq)) {
-      const uint8_t* st = c.slot_ptr((int)(seq % p.nslots)) + (size_t)(t - a) * p.rpair_bytes;
+  const int slot0 = kind == ITEM_ROUTED ? p.S : 0;
+  XRegs<FMT, MAXM> xr;
+  load_xregs<FMT, MAXM>(c, xr);
+  for (ItemWalk w(lo, hi, router ? p.qr : p.q, router ? 0 : p.I); w.more(); ring.next(p.nslots)) {
+    const int nq = w.count();
+    const int iq = w.offset(c.warp);
+    if (iq < nq && !c.aborted() && c.wait_full(ring)) {
+      const uint8_t* st = c.slot_ptr(ring.slot);
       PairAcc<MAXM> acc;
-      pair_dot_bf16<MAXM, FMT == FMT_BF16>(reinterpret_cast<const uint4*>(st),
-                                           reinterpret_cast<const uint4*>(st + 2 * p.H), p.H / 8, xr.b,
-                                           xs, mask, c.lane, acc);
-      if (!(p.test_flags & TEST_SKIP_LOGITS)) {
+      if (router) {
+        const uint32_t mask = (1u << p.M) - 1u;
+        const uint8_t* rp = st + (size_t)iq * p.rpair_bytes;
+        pair_dot_bf16<MAXM, FMT == FMT_BF16>(reinterpret_cast<const uint4*>(rp),
+                                             reinterpret_cast<const uint4*>(rp + 2 * p.H), p.H / 8, xr.b, xs,
+                                             mask, c.lane, acc);
+        const int t = w.a + iq;
+        if (!(p.test_flags & TEST_SKIP_LOGITS)) {
+#pragma unroll
+          for (int m = 0; m < MAXM; ++m) {
+            if (c.lane == m && m < p.M) {
+              st_tagged(&p.logits[(size_t)m * p.E + 2 * t], ep, acc.g[m]);
+              st_tagged(&p.logits[(size_t)m * p.E + 2 * t + 1], ep, acc.u[m]);
+            }
+          }
+        }
+      } else {
+        const int slot = w.u + slot0;
+        const int j = w.j + iq;
+        const uint32_t mask = kind == ITEM_SHARED ? (1u << p.M) - 1u : rt.slot_mask[slot];
+        float gsg = 1.0f, gsu = 1.0f;
+        if (FMT == FMT_BF16) {
+          pair_dot_bf16<MAXM, true>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
+                                    reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
+                                    p.nchunk_h, xr.b, xs, mask, c.lane, acc);
+        } else {
+          const uint8_t* scb = st + (size_t)2 * nq * p.row13;
+          pair_dot_fp4<MAXM>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
+                             reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
+                             reinterpret_cast<const uint16_t*>(scb + (size_t)iq * p.sc13),
+                             reinterpret_cast<const uint16_t*>(scb + (size_t)(nq + iq) * p.sc13), p.nchunk_h,
+                             xr.h, xs, p.H, mask, c.lane, acc);
+          const int e = kind == ITEM_SHARED ? -1 - slot : rt.slot_e[slot];
+          const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
+          gsg = gs[0];
+          gsu = gs[1];
+        }
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
-          if (c.lane == m && m < p.M) {
-            st_tagged(&p.logits[(size_t)m * p.E + 2 * t], ep, acc.g[m]);
-            st_tagged(&p.logits[(size_t)m * p.E + 2 * t + 1], ep, acc.u[m]);
+          if (c.lane == m && (mask >> m & 1u)) {
+            float h = silu_f32(acc.g[m] * gsg) * (acc.u[m] * gsu);
+            if (kind == ITEM_ROUTED) h *= rt.slot_w[slot * p.maxm + m];
+            st_tagged(&p.hbuf[((size_t)slot * p.maxm + m) * p.I + j], ep, h);
           }
         }
       }
       __syncwarp();
-      if (c.lane == 0) c.release(seq, t == a ? (uint32_t)(kNC - (b - a) + 1) : 1u);
+      if (c.lane == 0) c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
     }
-    a = b;
+    w.advance(nq);
   }
-}
-
-// Gate/up stages. `shared_phase`: items are (shared s, j), weight 1; otherwise
-// (routed union slot u, j) with the row's routing weight folded into h.
-template <int FMT, int MAXM>
-__device__ void consume_pairs(const Ctx& c, const Route& rt, const XRegs<FMT, MAXM>& xr,
-                              bool shared_phase, long long& seq) {
-  const Params& p = c.p;
-  const long long n = shared_phase ? (long long)p.S * p.I : (long long)c.misc[MISC_NROUTED] * p.I;
-  long long lo, hi;
-  split_range(n, blockIdx.x, p.grid, lo, hi);
-  const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
-  const uint32_t ep = c.epoch();
-  const int slot0 = shared_phase ? 0 : p.S;
-  for (long long a = lo; a < hi; ++seq) {
-    const long long b = stage_end(a, hi, p.q, p.I);
-    const long long t = warp_item(a, lo, c.warp);
-    if (t < b && !c.aborted() && c.wait_full(seq)) {
-      const int nq = (int)(b - a), iq = (int)(t - a);
-      const int slot = (int)(t / p.I) + slot0;
-      const int j = (int)(t % p.I);
-      const uint32_t mask = shared_phase ? (1u << p.M) - 1u : rt.slot_mask[slot];
-      const uint8_t* st = c.slot_ptr((int)(seq % p.nslots));
-      PairAcc<MAXM> acc;
-      float gsg = 1.0f, gsu = 1.0f;
-      if (FMT == FMT_BF16) {
-        pair_dot_bf16<MAXM, true>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
-                                  reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
-                                  p.nchunk_h, xr.b, xs, mask, c.lane, acc);
-      } else {
-        const uint8_t* scb = st + (size_t)2 * nq * p.row13;
-        pair_dot_fp4<MAXM>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
-                           reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
-                           reinterpret_cast<const uint16_t*>(scb + (size_t)iq * p.sc13),
-                           reinterpret_cast<const uint16_t*>(scb + (size_t)(nq + iq) * p.sc13), p.nchunk_h,
-                           xr.h, xs, p.H, mask, c.lane, acc);
-        const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
-        const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
-        gsg = gs[0];
-        gsu = gs[1];
-      }
-#pragma unroll
-      for (int m = 0; m < MAXM; ++m) {
-        if (c.lane == m && (mask >> m & 1u)) {
-          float h = silu_f32(acc.g[m] * gsg) * (acc.u[m] * gsu);
-          if (!shared_phase) h *= rt.slot_w[slot * p.maxm + m];
-          st_tagged(&p.hbuf[((size_t)slot * p.maxm + m) * p.I + j], ep, h);
-        }
-      }
-      __syncwarp();
-      if (c.lane == 0) c.release(seq, t == a ? (uint32_t)(kNC - nq + 1) : 1u);
-    }
-    a = b;
-  }
+  return ring;
 }
 
 // --------------------------------------------------------------------------
@@ -650,10 +666,7 @@ static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bo
 // consumer phase D
 // --------------------------------------------------------------------------
 __device__ __forceinline__ void cta_rows(const Params& p, int& r_lo, int& r_hi) {
-  long long lo, hi;
-  split_range(p.H, blockIdx.x, p.grid, lo, hi);
-  r_lo = (int)lo;
-  r_hi = (int)hi;
+  split_range(p.H, blockIdx.x, p.grid, r_lo, r_hi);
 }
 
 // Wait until every CTA has its copy of x (only needed when the output
@@ -738,7 +751,7 @@ static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float
 }
 
 template <int FMT, int MAXM>
-__device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, long long& seq) {
+__device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, Ring ring) {
   const Params& p = c.p;
   int r_lo, r_hi;
   cta_rows(p, r_lo, r_hi);
@@ -770,11 +783,11 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, l
       if (!c.aborted()) stage_h(c, rt, hs, sl0, sl1);
       bar_sync(kBarConsumers, kNC * 32);
       if (rb == 0 && sl0 == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
-      for (int sl = sl0; sl < sl1; ++sl, ++seq) {
+      for (int sl = sl0; sl < sl1; ++sl, ring.next(p.nslots)) {
         const uint32_t mask = rt.slot_mask[sl];
-        const bool got = !c.aborted() && c.wait_full(seq);
+        const bool got = !c.aborted() && c.wait_full(ring);
         if (got && active) {
-          const uint8_t* st = c.slot_ptr((int)(seq % p.nslots));
+          const uint8_t* st = c.slot_ptr(ring.slot);
           float gsc = 1.0f;
           if (FMT == FMT_NVFP4) {
             const int e = rt.slot_e[sl];
@@ -832,7 +845,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, l
           }
         }
         __syncwarp();
-        if (got && c.lane == 0) c.release(seq, 1);
+        if (got && c.lane == 0) c.release(ring, 1);
       }
       sl0 = sl1;
     }
@@ -900,18 +913,18 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, l
 struct Producer {
   const Ctx& c;
   uint64_t pol;
-  long long issued = 0;  // stages whose copies were issued
+  Ring ring;            // next stage to issue
+  int issued = 0;       // stages whose copies were issued
   __device__ Producer(const Ctx& cc) : c(cc) { pol = policy_evict_first(); }
 
   // Claims the next stage's slot and announces its bytes. False on abort.
-  __device__ bool begin(long long seq, uint32_t bytes, uint32_t& dst, uint32_t& bar) {
-    if (c.aborted() || !c.wait_empty(seq)) return false;
-    const int slot = (int)(seq % c.p.nslots);
-    dst = smem_u32(c.slot_ptr(slot));
-    bar = c.full0 + 8u * slot;
-    c.slot_seq[slot] = (int)seq;  // before arming: see Ctx::wait_full
+  __device__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar) {
+    if (c.aborted() || !c.wait_empty(ring)) return false;
+    dst = smem_u32(c.slot_ptr(ring.slot));
+    bar = c.full0 + 8u * ring.slot;
+    c.slot_seq[ring.slot] = ring.seq;  // before arming: see Ctx::wait_full
     mbar_arrive_expect_tx(bar, bytes);
-    issued = seq + 1;
+    issued = ring.seq + 1;
     return true;
   }
 
@@ -923,72 +936,68 @@ struct Producer {
     bulk_g2s(smem_u32(c.sm + p.off_x), p.x, bytes, c.xbar, pol);
   }
 
-  __device__ void router(long long& seq) {
+  __device__ void router() {
     const Params& p = c.p;
-    long long lo, hi;
+    int lo, hi;
     split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
-    for (long long a = lo; a < hi; ++seq) {
-      const long long b = stage_end(a, hi, p.qr, 0);
-      const uint32_t bytes = (uint32_t)((b - a) * p.rpair_bytes);
+    for (ItemWalk w(lo, hi, p.qr, 0); w.more(); ring.next(p.nslots)) {
+      const int nq = w.count();
+      const uint32_t bytes = (uint32_t)nq * p.rpair_bytes;
       uint32_t dst, bar;
-      if (!begin(seq, bytes, dst, bar)) return;
-      bulk_g2s(dst, p.router_w + (size_t)a * p.rpair_bytes, bytes, bar, pol);
-      a = b;
+      if (!begin(bytes, dst, bar)) return;
+      bulk_g2s(dst, p.router_w + (size_t)w.a * p.rpair_bytes, bytes, bar, pol);
+      w.advance(nq);
     }
   }
 
   // Gate/up stages: consecutive rows of one expert as a gate block and an up
   // block (plus the two scale blocks for NVFP4).
-  __device__ void pairs(bool shared_phase, const Route& rt, long long& seq) {
+  __device__ void pairs(bool shared_phase, const Route& rt) {
     const Params& p = c.p;
-    const long long n = shared_phase ? (long long)p.S * p.I : (long long)c.misc[MISC_NROUTED] * p.I;
-    long long lo, hi;
+    const int n = shared_phase ? p.S * p.I : c.misc[MISC_NROUTED] * p.I;
+    int lo, hi;
     split_range(n, blockIdx.x, p.grid, lo, hi);
-    for (long long a = lo; a < hi; ++seq) {
-      const long long b = stage_end(a, hi, p.q, p.I);
-      const int nq = (int)(b - a);
-      const int slot = (int)(a / p.I) + (shared_phase ? 0 : p.S);
-      const int j = (int)(a % p.I);
+    for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(p.nslots)) {
+      const int nq = w.count();
+      const int slot = w.u + (shared_phase ? 0 : p.S);
       uint32_t dst, bar;
-      if (!begin(seq, (uint32_t)nq * p.pair_bytes, dst, bar)) return;
+      if (!begin((uint32_t)nq * p.pair_bytes, dst, bar)) return;
       const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
-      const uint8_t* w = e >= 0 ? p.w13 : p.sh_w13;
+      const uint8_t* wt = e >= 0 ? p.w13 : p.sh_w13;
       const uint8_t* ws = e >= 0 ? p.w13_s : p.sh_w13_s;
       const size_t ex = (size_t)(e >= 0 ? e : -1 - e);
-      const size_t rg = ex * 2 * p.I + j, ru = rg + p.I;  // first gate row, first up row
+      const size_t rg = ex * 2 * p.I + w.j, ru = rg + p.I;  // first gate row, first up row
       const uint32_t cb = (uint32_t)nq * p.row13;
-      bulk_g2s(dst, w + rg * p.row13, cb, bar, pol);
-      bulk_g2s(dst + cb, w + ru * p.row13, cb, bar, pol);
+      bulk_g2s(dst, wt + rg * p.row13, cb, bar, pol);
+      bulk_g2s(dst + cb, wt + ru * p.row13, cb, bar, pol);
       if (p.sc13) {
         const uint32_t sb = (uint32_t)nq * p.sc13;
         bulk_g2s(dst + 2 * cb, ws + rg * p.sc13, sb, bar, pol);
         bulk_g2s(dst + 2 * cb + sb, ws + ru * p.sc13, sb, bar, pol);
       }
-      a = b;
+      w.advance(nq);
     }
   }
 
   // Down stages (row block rb, union slot sl) for sl in [sl_lo, sl_hi).
-  __device__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi, long long& seq) {
+  __device__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi) {
     const Params& p = c.p;
     int r_lo, r_hi;
     cta_rows(p, r_lo, r_hi);
     const int rb_lo = r_lo + rb * p.d_rows_stage;
     const int nr = min(p.d_rows_stage, r_hi - rb_lo);
-    for (int sl = sl_lo; sl < sl_hi; ++sl, ++seq) {
+    for (int sl = sl_lo; sl < sl_hi; ++sl) {
       const int e = sl < p.S ? -1 - sl : rt.slot_e[sl];
-      const uint8_t* w = e >= 0 ? p.w2 : p.sh_w2;
+      const uint8_t* wt = e >= 0 ? p.w2 : p.sh_w2;
       const uint8_t* ws = e >= 0 ? p.w2_s : p.sh_w2_s;
       const size_t ex = (size_t)(e >= 0 ? e : -1 - e);
       const size_t row0 = ex * p.H + rb_lo;
       const uint32_t cb = (uint32_t)nr * p.row2, sb = (uint32_t)nr * p.sc2;
       uint32_t dst, bar;
-      if (!begin(seq, cb + sb, dst, bar)) {
-        seq = seq + (sl_hi - sl);
-        return;
-      }
-      bulk_g2s(dst, w + row0 * p.row2, cb, bar, pol);
+      if (!begin(cb + sb, dst, bar)) return;
+      bulk_g2s(dst, wt + row0 * p.row2, cb, bar, pol);
       if (sb) bulk_g2s(dst + (uint32_t)p.d_rows_stage * p.row2, ws + row0 * p.sc2, sb, bar, pol);
+      ring.next(p.nslots);
     }
   }
 
@@ -1011,12 +1020,13 @@ struct Producer {
     }
   }
 
-  // Before exit: wait (bounded) for this CTA's copies still in flight.
+  // Before exit: wait (bounded) for this CTA's copies still in flight: the last
+  // nslots issued stages, each the newest use of its slot.
   __device__ void drain() {
     const Params& p = c.p;
-    const long long first = issued > p.nslots ? issued - p.nslots : 0;
+    const int first = issued > p.nslots ? issued - p.nslots : 0;
     const uint64_t t = global_ns();
-    for (long long q = first; q < issued; ++q) {
+    for (int q = first; q < issued; ++q) {
       const uint32_t bar = c.full0 + 8u * (uint32_t)(q % p.nslots);
       const uint32_t par = (uint32_t)((q / p.nslots) & 1);
       while (!mbar_try_wait(bar, par)) {
@@ -1064,14 +1074,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
   if (c.warp == kNC) {
     // ------------------------------------------------------------ producer
     Producer pr(c);
-    long long seq = 0;
     if (c.lane == 0) {
       c.stamp(ST_START);
       if (PHASES == PH_ALL) {
         pr.x_rows();
         x_issued = true;
       }
-      if (PHASES & PH_R) pr.router(seq);
+      if (PHASES & PH_R) pr.router();
       if (kChain && kNeedX) {
         pdl_wait();  // x may be the previous kernel's output
         if (!c.aborted()) {
@@ -1080,12 +1089,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
       }
       if (PHASES & PH_R) {
-        pr.pairs(true, rt, seq);
+        pr.pairs(true, rt);
         c.stamp(ST_P_R_ISSUED);
         if (PHASES & PH_D) pr.prefetch_shared_down();
       } else if (PHASES == PH_D) {
         // The shared experts' down rows of the first row block need no routing.
-        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, seq);
+        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S);
       }
     }
     if (kRoute) {
@@ -1095,13 +1104,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     if (c.lane == 0) {
       c.stamp(ST_P_ROUTE);
       if (PHASES & PH_U) {
-        pr.pairs(false, rt, seq);
+        pr.pairs(false, rt);
         c.stamp(ST_P_U_ISSUED);
       }
       if (PHASES & PH_D) {
         const int nsl = p.S + c.misc[MISC_NROUTED];
         const int first = PHASES == PH_D ? p.S : 0;  // the chain issued these before routing
-        for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl, seq);
+        for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl);
         c.stamp(ST_P_D_ISSUED);
       }
       if (c.aborted()) pr.drain();
@@ -1122,12 +1131,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     if (c.tid == 0) c.stamp(ST_X_LOADED);
     if (PHASES == PH_ALL && p.out_aliases_x && c.tid == 0)
       st_tagged(p.xflags + blockIdx.x, c.epoch(), 0.0f);
-    long long seq = 0;
+    Ring ring;
     if (PHASES & PH_R) {
-      XRegs<FMT, MAXM> xr;
-      load_xregs<FMT, MAXM>(c, xr);
-      consume_router<FMT, MAXM>(c, xr, seq);
-      consume_pairs<FMT, MAXM>(c, rt, xr, true, seq);
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTER, ring);
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring);
       if (c.tid == 0) c.stamp(ST_R_DONE);
     }
     if (kRoute) {
@@ -1136,12 +1143,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       if (c.tid == 0) c.stamp(ST_ROUTED);
     }
     if (PHASES & PH_U) {
-      XRegs<FMT, MAXM> xr;
-      load_xregs<FMT, MAXM>(c, xr);
-      consume_pairs<FMT, MAXM>(c, rt, xr, false, seq);
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTED, ring);
       if (c.tid == 0) c.stamp(ST_U_DONE);
     }
-    if (PHASES & PH_D) consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, seq);
+    if (PHASES & PH_D) consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, ring);
     if (c.tid == 0) c.stamp(ST_D_DONE);
   }
   __syncthreads();
