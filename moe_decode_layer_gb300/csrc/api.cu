@@ -266,6 +266,8 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   const size_t o_logits = take(maxm * E * 8);
   const size_t o_h = take((size_t)p.nslot_max * maxm * I * 8);
   const size_t o_xf = take((size_t)p.grid * 8);
+  const size_t o_rf = take((size_t)p.grid * 8);
+  const size_t o_uf = take((size_t)p.grid * 8);
   const size_t tag_end = off;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
@@ -308,6 +310,8 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
   p.hbuf = reinterpret_cast<unsigned long long*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
+  p.rflags = reinterpret_cast<unsigned long long*>(base + o_rf);
+  p.uflags = reinterpret_cast<unsigned long long*>(base + o_uf);
   h->stage_x = reinterpret_cast<uint16_t*>(base + o_sx);
   h->stage_r = reinterpret_cast<uint16_t*>(base + o_sr);
   h->stage_out = reinterpret_cast<uint16_t*>(base + o_so);

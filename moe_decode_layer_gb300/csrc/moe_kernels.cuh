@@ -89,6 +89,9 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
+struct Ctx;
+static __device__ __noinline__ bool wait_flags(const Ctx& c, const unsigned long long* flags, uint32_t site);
+
 struct Ctx {
   const Params& p;
   uint8_t* sm;
@@ -539,7 +542,7 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
       }
     }
     if (!__any_sync(kFull, bad)) break;
-    __nanosleep(32);
+    __nanosleep(64);
     bool stop = c.aborted();
     if (!stop && (++spins & 63) == 0 && c.peer_failed()) stop = true;
     if (!stop && c.expired()) {
@@ -553,6 +556,7 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
       break;
     }
   }
+  if (m == 0 && c.lane == 0) c.stamp(ST_LOGITS);
   // lane-local best as (key << 32 | (PM - 1 - i)): larger key, then lower index
   auto best = [&]() {
     unsigned long long v[PM];
@@ -584,6 +588,7 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
       lb = best();
     }
   }
+  if (m == 0 && c.lane == 0) c.stamp(ST_TOPK);
   const float v0 = __shfl_sync(kFull, my_v, 0);
   const float ex = c.lane < p.K ? expf(my_v - v0) : 0.0f;
   float sum = ex;
@@ -604,6 +609,10 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
 
 static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
   const Params& p = c.p;
+  // Every CTA's "router logits stored" flag first: one word per CTA instead of
+  // re-reading all logits while they are still being produced.
+  if (!c.aborted()) wait_flags(c, p.rflags, SITE_FLAGS);
+  bar_sync(kBarConsumers, kNC * 32);
   if (c.warp < p.M) {
     if (p.E <= 16 * 32)
       topk_row<16>(c, rt, c.warp, write_topk);
@@ -667,6 +676,29 @@ static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bo
 // --------------------------------------------------------------------------
 __device__ __forceinline__ void cta_rows(const Params& p, int& r_lo, int& r_hi) {
   split_range(p.H, blockIdx.x, p.grid, r_lo, r_hi);
+}
+
+// Waits (bounded, with back-off) until every CTA's tagged flag carries the
+// current run's tag. Each consumer thread polls at most a few flags. The flags
+// are only a cheap readiness hint: the data they announce is still read with
+// its own tag check.
+static __device__ __noinline__ bool wait_flags(const Ctx& c, const unsigned long long* flags, uint32_t site) {
+  const Params& p = c.p;
+  const uint32_t ep = c.epoch();
+  uint32_t spins = 0;
+  for (int i = c.tid; i < p.grid; i += kNC * 32) {
+    while ((uint32_t)(ld_relaxed_u64(flags + i) >> 32) != ep) {
+      __nanosleep(128);
+      if ((++spins & 15) == 0) {
+        if (c.aborted() || c.peer_failed()) return false;
+        if (c.expired()) {
+          c.fail(site);
+          return false;
+        }
+      }
+    }
+  }
+  return true;
 }
 
 // Wait until every CTA has its copy of x (only needed when the output
@@ -766,6 +798,11 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, R
   float* red = reinterpret_cast<float*>(c.sm + p.off_red);
   constexpr int CH_EL = FMT == FMT_BF16 ? 8 : 32;  // elements per chunk
   bool first_batch = true;
+  if (nrb > 0) {
+    if (!c.aborted()) wait_flags(c, p.uflags, SITE_FLAGS);
+    bar_sync(kBarConsumers, kNC * 32);
+    if (c.tid == 0) c.stamp(ST_U_FLAGS);
+  }
   for (int rb = 0; rb < nrb; ++rb) {
     const int rb_lo = r_lo + rb * drs;
     const int nr = min(drs, r_hi - rb_lo);
@@ -1134,17 +1171,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     Ring ring;
     if (PHASES & PH_R) {
       ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTER, ring);
-      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring);
-      if (c.tid == 0) c.stamp(ST_R_DONE);
+      bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
+      if (c.tid == 0) st_tagged(p.rflags + blockIdx.x, c.epoch(), 0.0f);
     }
     if (kRoute) {
       route_rows(c, rt, (PHASES & PH_U) != 0);
       bar_arrive(kBarRoute, kThreads);
       if (c.tid == 0) c.stamp(ST_ROUTED);
     }
+    if (PHASES & PH_R) {
+      // shared experts' gate/up stages were issued before routing
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring);
+      if (c.tid == 0) c.stamp(ST_R_DONE);
+    }
     if (PHASES & PH_U) {
       ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTED, ring);
       if (c.tid == 0) c.stamp(ST_U_DONE);
+    }
+    if (PHASES & (PH_R | PH_U)) {
+      bar_sync(kBarConsumers, kNC * 32);  // this CTA's h rows are all stored
+      if (c.tid == 0) st_tagged(p.uflags + blockIdx.x, c.epoch(), 0.0f);
     }
     if (PHASES & PH_D) consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, ring);
     if (c.tid == 0) c.stamp(ST_D_DONE);

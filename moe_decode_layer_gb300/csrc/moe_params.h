@@ -29,7 +29,8 @@ enum WaitSite : uint32_t {
   SITE_LOGITS = 3,
   SITE_HIDDEN = 4,
   SITE_XFLAGS = 5,
-  SITE_DRAIN = 6
+  SITE_DRAIN = 6,
+  SITE_FLAGS = 7
 };
 // Test flags.
 enum TestFlag : int { TEST_SKIP_LOGITS = 1 };
@@ -47,6 +48,9 @@ enum Stamp : int {
   ST_P_ROUTE = 9,     // producer: routing received
   ST_P_U_ISSUED = 10, // producer: last routed gate/up stage issued
   ST_P_D_ISSUED = 11, // producer: last down stage issued
+  ST_LOGITS = 12,     // all router logits seen (routing warp 0)
+  ST_TOPK = 13,       // top-k of row 0 done
+  ST_U_FLAGS = 14,    // every CTA's gate/up results published
   kStampSlots = 16
 };
 
@@ -83,6 +87,8 @@ struct Params {
   unsigned long long* logits;  // [maxm][E] tagged
   unsigned long long* hbuf;    // [nslot_max][maxm][I] tagged
   unsigned long long* xflags;  // [grid] tagged: this CTA has read x
+  unsigned long long* rflags;  // [grid] tagged: this CTA's router logits are stored
+  unsigned long long* uflags;  // [grid] tagged: this CTA's gate/up results are stored
   uint32_t* ctrl;              // CTRL_WORDS
   int out_aliases_x;
   // planned layout
