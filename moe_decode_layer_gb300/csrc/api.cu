@@ -133,7 +133,23 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   if (hs_pairs < maxm) hs_pairs = maxm;
   p.hs_pairs = hs_pairs;
   p.off_hs = (int)fixed;
-  p.off_ring = (int)round_up(fixed + (size_t)hs_pairs * per_pair, 128);
+  // routing scratch shares the h staging area (routing is over before any h is staged)
+  size_t ro = fixed;
+  auto rtake = [&](size_t bytes, size_t align) {
+    ro = round_up(ro, align);
+    const size_t at = ro;
+    ro += bytes;
+    return static_cast<int>(at);
+  };
+  p.off_lg = rtake((size_t)maxm * E * 4, 16);
+  p.off_cand = rtake((size_t)maxm * moe::kCandMax * 8, 8);
+  p.off_lmax = rtake((size_t)maxm * 32 * 8, 8);
+  p.off_thr = rtake((size_t)maxm * 8, 8);
+  p.off_ccount = rtake((size_t)maxm * 4, 4);
+  p.off_wtmp = rtake((size_t)maxm * 16 * 4, 4);
+  p.off_wpc = rtake(32 * 4, 4);
+  const size_t area = std::max(ro, fixed + (size_t)hs_pairs * per_pair);
+  p.off_ring = (int)round_up(area, 128);
   const long long ring_budget = (long long)smem_optin - 1024 - p.off_ring;
   const long long ns = ring_budget > 0 ? ring_budget / (long long)slot : 0;
   if (ns < 2) return MOE_ERR_UNSUPPORTED;
@@ -263,11 +279,10 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
     return at;
   };
   const size_t o_ctrl = take(moe::CTRL_WORDS * 4);
-  const size_t o_logits = take(maxm * E * 8);
+  const size_t o_logits = take(moe::kLogitRep * maxm * E * 8);
   const size_t o_h = take((size_t)p.nslot_max * maxm * I * 8);
   const size_t o_xf = take((size_t)p.grid * 8);
-  const size_t o_rf = take((size_t)p.grid * 8);
-  const size_t o_uf = take((size_t)p.grid * 8);
+
   const size_t tag_end = off;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
@@ -310,8 +325,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
   p.hbuf = reinterpret_cast<unsigned long long*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
-  p.rflags = reinterpret_cast<unsigned long long*>(base + o_rf);
-  p.uflags = reinterpret_cast<unsigned long long*>(base + o_uf);
+
   h->stage_x = reinterpret_cast<uint16_t*>(base + o_sx);
   h->stage_r = reinterpret_cast<uint16_t*>(base + o_sr);
   h->stage_out = reinterpret_cast<uint16_t*>(base + o_so);

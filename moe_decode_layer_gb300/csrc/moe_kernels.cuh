@@ -89,9 +89,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
-struct Ctx;
-static __device__ __noinline__ bool wait_flags(const Ctx& c, const unsigned long long* flags, uint32_t site);
-
 struct Ctx {
   const Params& p;
   uint8_t* sm;
@@ -99,6 +96,7 @@ struct Ctx {
   volatile int* slot_seq;  // [nslots] ring stage that currently owns each slot
   uint32_t full0, empty0, xbar;
   uint64_t t0;
+  long long c0;
   int tid, warp, lane;
 
   __device__ Ctx(const Params& pp, uint8_t* base) : p(pp), sm(base) {
@@ -108,6 +106,7 @@ struct Ctx {
     empty0 = smem_u32(sm + p.off_empty);
     xbar = smem_u32(sm + p.off_xbar);
     t0 = global_ns();
+    c0 = clock64();
     tid = threadIdx.x;
     warp = tid >> 5;
     lane = tid & 31;
@@ -126,6 +125,9 @@ struct Ctx {
   // Phase timestamp (one plain store; off unless the handle has a stamp buffer).
   __device__ void stamp(int ev) const {
     if (p.stamps) p.stamps[(size_t)blockIdx.x * kStampSlots + ev] = global_ns();
+  }
+  __device__ void count(int ev, unsigned long long v) const {
+    if (p.stamps) atomicAdd(&p.stamps[(size_t)blockIdx.x * kStampSlots + ev], v);
   }
 
   // Bounded wait on an mbarrier phase. False on abort / timeout.
@@ -187,6 +189,30 @@ struct Route {
         slot_w(reinterpret_cast<float*>(sm + p.off_slot_w)),
         pair_base(reinterpret_cast<int*>(sm + p.off_pair_base)) {}
 };
+
+// Hand-off counters: after storing its share of a phase's results, every CTA
+// adds one to a 64-bit counter; readers wait (one thread per CTA, bounded, with
+// back-off) until it reaches the grid size. The count is only a cheap readiness
+// hint -- one word polled per CTA instead of every result -- and the results are
+// still read with their own tag check. The last CTA of a run resets the counters.
+__device__ __forceinline__ void count_done(const Params& p, int word) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p.ctrl + word) : "memory");
+}
+static __device__ __noinline__ bool wait_count(const Ctx& c, int word, uint32_t site) {
+  const Params& p = c.p;
+  const unsigned long long* cnt = reinterpret_cast<const unsigned long long*>(p.ctrl + word);
+  for (uint32_t spin = 0; ld_relaxed_u64(cnt) < (unsigned long long)p.grid; ++spin) {
+    __nanosleep(100);
+    if ((spin & 15) == 15) {
+      if (c.aborted() || c.peer_failed()) return false;
+      if (c.expired()) {
+        c.fail(site);
+        return false;
+      }
+    }
+  }
+  return true;
+}
 
 // --------------------------------------------------------------------------
 // stage schedule: the same walk on the producer and the consumer side
@@ -459,6 +485,7 @@ __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int ki
     const int nq = w.count();
     const int iq = w.offset(c.warp);
     if (iq < nq && !c.aborted() && c.wait_full(ring)) {
+      if (c.warp == 0 && c.lane == 0 && w.a == lo) c.stamp(kind == ITEM_ROUTER ? ST_ROUTER_DATA : ST_U_DATA);
       const uint8_t* st = c.slot_ptr(ring.slot);
       PairAcc<MAXM> acc;
       if (router) {
@@ -472,8 +499,12 @@ __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int ki
 #pragma unroll
           for (int m = 0; m < MAXM; ++m) {
             if (c.lane == m && m < p.M) {
-              st_tagged(&p.logits[(size_t)m * p.E + 2 * t], ep, acc.g[m]);
-              st_tagged(&p.logits[(size_t)m * p.E + 2 * t + 1], ep, acc.u[m]);
+#pragma unroll
+              for (int r = 0; r < kLogitRep; ++r) {
+                unsigned long long* dst = p.logits + ((size_t)r * p.maxm + m) * p.E + 2 * t;
+                st_tagged(dst, ep, acc.g[m]);
+                st_tagged(dst + 1, ep, acc.u[m]);
+              }
             }
           }
         }
@@ -518,177 +549,36 @@ __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int ki
 // --------------------------------------------------------------------------
 // consumer phase T: top-k per row and the expert union
 // --------------------------------------------------------------------------
-// Row m's top-k on warp m: lane l holds the logits of experts [l*P, l*P+P) as
-// order-preserving keys; each round takes the warp-wide max (ties: lowest lane,
-// then lowest index, i.e. the lower expert id) and the winning lane rescans.
-template <int PM>
-__device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
-  const Params& p = c.p;
-  const uint32_t ep = c.epoch();
-  const int P = (p.E + 31) / 32;
-  const int base = c.lane * P;
-  const unsigned long long* row = p.logits + (size_t)m * p.E;
-  uint32_t key[PM];
-  uint64_t spins = 0;
-  for (;;) {
-    uint32_t bad = 0;
-#pragma unroll
-    for (int i = 0; i < PM; ++i) {
-      key[i] = 0;
-      if (i < P && base + i < p.E) {
-        const unsigned long long v = ld_relaxed_u64(row + base + i);
-        bad |= (uint32_t)(v >> 32) != ep;
-        key[i] = f32_order_key(__uint_as_float((uint32_t)v));
-      }
-    }
-    if (!__any_sync(kFull, bad)) break;
-    __nanosleep(64);
-    bool stop = c.aborted();
-    if (!stop && (++spins & 63) == 0 && c.peer_failed()) stop = true;
-    if (!stop && c.expired()) {
-      if (c.lane == 0) c.fail(SITE_LOGITS);
-      stop = true;
-    }
-    if (__any_sync(kFull, stop)) {
-      if (c.lane == 0) *reinterpret_cast<volatile int*>(c.misc + MISC_ABORT) = 1;
-#pragma unroll
-      for (int i = 0; i < PM; ++i) key[i] = (i < P && base + i < p.E) ? 1u : 0u;  // any valid ids
-      break;
-    }
-  }
-  if (m == 0 && c.lane == 0) c.stamp(ST_LOGITS);
-  // lane-local best as (key << 32 | (PM - 1 - i)): larger key, then lower index
-  auto best = [&]() {
-    unsigned long long v[PM];
-#pragma unroll
-    for (int i = 0; i < PM; ++i) v[i] = ((unsigned long long)key[i] << 32) | (unsigned)(PM - 1 - i);
-#pragma unroll
-    for (int w = PM / 2; w; w >>= 1)
-#pragma unroll
-      for (int i = 0; i < w; ++i) v[i] = v[i] > v[i + w] ? v[i] : v[i + w];
-    return v[0];
-  };
-  unsigned long long lb = best();
-  int my_e = 0;
-  float my_v = 0.0f;
-  for (int j = 0; j < p.K; ++j) {
-    const uint32_t lmax = (uint32_t)(lb >> 32);
-    const uint32_t gmax = warp_max_u32(lmax);
-    const int winner = __ffs(__ballot_sync(kFull, lmax == gmax)) - 1;
-    const int lidx = PM - 1 - (int)(lb & 0xffffffffu);
-    const int e = __shfl_sync(kFull, base + lidx, winner);
-    if (c.lane == j) {
-      my_e = e;
-      my_v = order_key_f32(gmax);
-    }
-    if (c.lane == winner) {
-#pragma unroll
-      for (int i = 0; i < PM; ++i)
-        if (i == lidx) key[i] = 0;
-      lb = best();
-    }
-  }
-  if (m == 0 && c.lane == 0) c.stamp(ST_TOPK);
-  const float v0 = __shfl_sync(kFull, my_v, 0);
-  const float ex = c.lane < p.K ? expf(my_v - v0) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-  if (c.lane < p.K) {
-    const float w = ex / sum;
-    rt.sel_e[m * p.K + c.lane] = my_e;
-    rt.sel_w[m * p.K + c.lane] = w;
-    atomicOr(&rt.emask[my_e], 1u << m);
-    atomicOr(&rt.bitmap[my_e >> 5], 1u << (my_e & 31));
-    if (write_topk && blockIdx.x == 0) {
-      if (p.topk_idx) p.topk_idx[m * p.K + c.lane] = my_e;
-      if (p.topk_w) p.topk_w[m * p.K + c.lane] = w;
-    }
-  }
-}
-
-static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
-  const Params& p = c.p;
-  // Every CTA's "router logits stored" flag first: one word per CTA instead of
-  // re-reading all logits while they are still being produced.
-  if (!c.aborted()) wait_flags(c, p.rflags, SITE_FLAGS);
-  bar_sync(kBarConsumers, kNC * 32);
-  if (c.warp < p.M) {
-    if (p.E <= 16 * 32)
-      topk_row<16>(c, rt, c.warp, write_topk);
-    else
-      topk_row<32>(c, rt, c.warp, write_topk);
-  }
-  bar_sync(kBarConsumers, kNC * 32);
-  if (c.warp == 0) {
-    // Union slots S.. in ascending expert id: popcount prefix over the bitmap.
-    const int words = (p.E + 31) / 32;
-    const uint32_t w = c.lane < words ? rt.bitmap[c.lane] : 0u;
-    const int cnt = __popc(w);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(kFull, incl, o);
-      if (c.lane >= o) incl += v;
-    }
-    int s = p.S + incl - cnt;
-    for (uint32_t bits = w; bits; bits &= bits - 1) {
-      const int e = c.lane * 32 + __ffs(bits) - 1;
-      rt.slot_of[e] = s;
-      rt.slot_e[s] = e;
-      rt.slot_mask[s] = rt.emask[e];
-      ++s;
-    }
-    const int n_routed = __shfl_sync(kFull, incl, 31);
-    for (int t = c.lane; t < p.S; t += 32) {
-      rt.slot_e[t] = -1 - t;
-      rt.slot_mask[t] = (1u << p.M) - 1u;
-      for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
-    }
-    __syncwarp();
-    for (int t = c.lane; t < p.M * p.K; t += 32)
-      rt.slot_w[rt.slot_of[rt.sel_e[t]] * p.maxm + t / p.K] = rt.sel_w[t] * p.routed_scale;
-    // (slot, row) pair index of each slot: prefix of the row-mask popcounts
-    const int nsl = p.S + n_routed;
-    int carry = 0;
-    for (int s0 = 0; s0 < nsl; s0 += 32) {
-      const int sl = s0 + c.lane;
-      const int pc = sl < nsl ? __popc(rt.slot_mask[sl]) : 0;
-      int in = pc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(kFull, in, o);
-        if (c.lane >= o) in += v;
-      }
-      if (sl < nsl) rt.pair_base[sl] = carry + in - pc;
-      carry += __shfl_sync(kFull, in, 31);
-    }
-    if (c.lane == 0) {
-      rt.pair_base[nsl] = carry;
-      c.misc[MISC_NROUTED] = n_routed;
-    }
-  }
-  bar_sync(kBarConsumers, kNC * 32);
-}
-
-// --------------------------------------------------------------------------
-// consumer phase D
-// --------------------------------------------------------------------------
-__device__ __forceinline__ void cta_rows(const Params& p, int& r_lo, int& r_hi) {
-  split_range(p.H, blockIdx.x, p.grid, r_lo, r_hi);
-}
-
-// Waits (bounded, with back-off) until every CTA's tagged flag carries the
-// current run's tag. Each consumer thread polls at most a few flags. The flags
-// are only a cheap readiness hint: the data they announce is still read with
-// its own tag check.
-static __device__ __noinline__ bool wait_flags(const Ctx& c, const unsigned long long* flags, uint32_t site) {
-  const Params& p = c.p;
+// Copies n 16-byte units of tagged words (two fp32 values each) from src to dst
+// in shared memory: every consumer thread keeps kStageBatch loads in flight and
+// re-polls only the units whose tag is not current yet. False on abort / timeout.
+static __device__ __noinline__ bool stage_tagged(const Ctx& c, const unsigned long long* src, float* dst, int n,
+                                                 uint32_t site) {
   const uint32_t ep = c.epoch();
   uint32_t spins = 0;
-  for (int i = c.tid; i < p.grid; i += kNC * 32) {
-    while ((uint32_t)(ld_relaxed_u64(flags + i) >> 32) != ep) {
-      __nanosleep(128);
+  for (int base = c.tid; base < n; base += kNC * 32 * kStageBatch) {
+    uint32_t pending = 0;
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k)
+      if (base + k * kNC * 32 < n) pending |= 1u << k;
+    while (pending) {
+      unsigned long long v0[kStageBatch], v1[kStageBatch];
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        v0[k] = v1[k] = 0;
+        if (pending >> k & 1u) ld_tagged2(src + 2 * (base + k * kNC * 32), v0[k], v1[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        if ((pending >> k & 1u) && (uint32_t)(v0[k] >> 32) == ep && (uint32_t)(v1[k] >> 32) == ep) {
+          const int u = base + k * kNC * 32;
+          dst[2 * u] = __uint_as_float((uint32_t)v0[k]);
+          dst[2 * u + 1] = __uint_as_float((uint32_t)v1[k]);
+          pending &= ~(1u << k);
+        }
+      }
+      if (!pending) break;
+      __nanosleep(64);
       if ((++spins & 15) == 0) {
         if (c.aborted() || c.peer_failed()) return false;
         if (c.expired()) {
@@ -699,6 +589,197 @@ static __device__ __noinline__ bool wait_flags(const Ctx& c, const unsigned long
     }
   }
   return true;
+}
+
+// Packed key of expert e with logit v: (order-preserving bits << 32) | ~e, so
+// the larger logit wins and equal logits go to the lower expert id. 0 = none.
+__device__ __forceinline__ unsigned long long pack_key(float v, int e) {
+  return ((unsigned long long)f32_order_key(v) << 32) | (uint32_t)(0xffffffffu - (uint32_t)e);
+}
+__device__ __forceinline__ int key_expert(unsigned long long k) { return (int)(0xffffffffu - (uint32_t)k); }
+__device__ __forceinline__ float key_value(unsigned long long k) { return order_key_f32((uint32_t)(k >> 32)); }
+
+// Row m's top-k on warp m, from the logits staged in shared memory. Lane l
+// holds experts [l*P, l*P+P). The K-th largest of the 32 lane maxima bounds the
+// K-th largest logit from below (those K lane maxima are K distinct logits), so
+// every selected expert is at or above it; the few candidates at or above it
+// are ranked in parallel. With many exact ties the candidates can exceed
+// kCandMax; then K rounds of a warp-wide max select instead.
+template <int PM>
+__device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
+  const Params& p = c.p;
+  const float* lg = reinterpret_cast<const float*>(c.sm + p.off_lg) + (size_t)m * p.E;
+  unsigned long long* lmax = reinterpret_cast<unsigned long long*>(c.sm + p.off_lmax) + m * 32;
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + m * kCandMax;
+  unsigned long long* thr = reinterpret_cast<unsigned long long*>(c.sm + p.off_thr) + m;
+  int* ccount = reinterpret_cast<int*>(c.sm + p.off_ccount) + m;
+  float* wtmp = reinterpret_cast<float*>(c.sm + p.off_wtmp) + m * 16;
+  const int P = (p.E + 31) / 32;
+  const int base = c.lane * P;
+  unsigned long long key[PM];
+  unsigned long long best = 0;
+#pragma unroll
+  for (int i = 0; i < PM; ++i) {
+    key[i] = 0;
+    if (i < P && base + i < p.E) key[i] = pack_key(lg[base + i], base + i);
+    best = key[i] > best ? key[i] : best;
+  }
+  lmax[c.lane] = best;
+  if (c.lane == 0) *ccount = 0;
+  __syncwarp();
+  int r = 0;
+  for (int j = 0; j < 32; ++j) r += lmax[j] > best;
+  if (r == p.K - 1) *thr = best;
+  __syncwarp();
+  const unsigned long long t = *thr;
+#pragma unroll
+  for (int i = 0; i < PM; ++i) {
+    if (key[i] != 0 && key[i] >= t) {
+      const int pos = atomicAdd(ccount, 1);
+      if (pos < kCandMax) cand[pos] = key[i];
+    }
+  }
+  __syncwarp();
+  const int C = *ccount;
+  int* sel_e = rt.sel_e + m * p.K;
+  float* sel_v = rt.sel_w + m * p.K;  // logits first, weights after
+  if (C <= kCandMax) {
+    for (int ci = c.lane; ci < C; ci += 32) {
+      const unsigned long long v = cand[ci];
+      int rank = 0;
+      for (int j = 0; j < C; ++j) rank += cand[j] > v;
+      if (rank < p.K) {
+        sel_e[rank] = key_expert(v);
+        sel_v[rank] = key_value(v);
+      }
+    }
+  } else {
+    unsigned long long lb = best;
+    for (int j = 0; j < p.K; ++j) {
+      const uint32_t hi = (uint32_t)(lb >> 32);
+      const uint32_t ghi = warp_max_u32(hi);
+      const uint32_t lo = hi == ghi ? (uint32_t)lb : 0u;
+      const uint32_t glo = warp_max_u32(lo);  // ~e: the lowest expert id among the max
+      if (hi == ghi && (uint32_t)lb == glo) {
+        sel_e[j] = key_expert(lb);
+        sel_v[j] = key_value(lb);
+#pragma unroll
+        for (int i = 0; i < PM; ++i)
+          if (key[i] == lb) key[i] = 0;
+        lb = 0;
+#pragma unroll
+        for (int i = 0; i < PM; ++i) lb = key[i] > lb ? key[i] : lb;
+      }
+      __syncwarp();
+    }
+  }
+  __syncwarp();
+  // renormalised softmax over the selection, the sum in a fixed order
+  if (c.lane < p.K) wtmp[c.lane] = expf(sel_v[c.lane] - sel_v[0]);
+  __syncwarp();
+  if (c.lane < p.K) {
+    float sum = 0.0f;
+    for (int j = 0; j < p.K; ++j) sum += wtmp[j];
+    const float w = wtmp[c.lane] / sum;
+    const int e = sel_e[c.lane];
+    atomicOr(&rt.emask[e], 1u << m);
+    atomicOr(&rt.bitmap[e >> 5], 1u << (e & 31));
+    if (write_topk && blockIdx.x == 0) {
+      if (p.topk_idx) p.topk_idx[m * p.K + c.lane] = e;
+      if (p.topk_w) p.topk_w[m * p.K + c.lane] = w;
+    }
+    __syncwarp((1u << p.K) - 1u);
+    sel_v[c.lane] = w;
+  }
+}
+
+// The union of chosen experts on warp 0: slots S.. in ascending expert id from
+// per-word popcounts of the bitmap (prefix read back from shared memory), the
+// combine weights, and the (slot, row) pair index of every slot.
+__device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
+  const Params& p = c.p;
+  int* wpc = reinterpret_cast<int*>(c.sm + p.off_wpc);
+  const int words = (p.E + 31) / 32;
+  const uint32_t w = c.lane < words ? rt.bitmap[c.lane] : 0u;
+  wpc[c.lane] = __popc(w);
+  __syncwarp();
+  int before = 0, total = 0;
+  for (int j = 0; j < 32; ++j) {
+    const int v = wpc[j];
+    before += j < c.lane ? v : 0;
+    total += v;
+  }
+  int s = p.S + before;
+  for (uint32_t bits = w; bits; bits &= bits - 1) {
+    const int e = c.lane * 32 + __ffs(bits) - 1;
+    rt.slot_of[e] = s;
+    rt.slot_e[s] = e;
+    rt.slot_mask[s] = rt.emask[e];
+    ++s;
+  }
+  for (int t = c.lane; t < p.S; t += 32) {
+    rt.slot_e[t] = -1 - t;
+    rt.slot_mask[t] = (1u << p.M) - 1u;
+    for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
+  }
+  __syncwarp();
+  for (int t = c.lane; t < p.M * p.K; t += 32)
+    rt.slot_w[rt.slot_of[rt.sel_e[t]] * p.maxm + t / p.K] = rt.sel_w[t] * p.routed_scale;
+  const int nsl = p.S + total;
+  int carry = 0;
+  for (int s0 = 0; s0 < nsl; s0 += 32) {
+    const int sl = s0 + c.lane;
+    __syncwarp();
+    wpc[c.lane] = sl < nsl ? __popc(rt.slot_mask[sl]) : 0;
+    __syncwarp();
+    int pre = 0, sum = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int v = wpc[j];
+      pre += j < c.lane ? v : 0;
+      sum += v;
+    }
+    if (sl < nsl) rt.pair_base[sl] = carry + pre;
+    carry += sum;
+  }
+  if (c.lane == 0) {
+    rt.pair_base[nsl] = carry;
+    c.misc[MISC_NROUTED] = total;
+  }
+}
+
+static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
+  const Params& p = c.p;
+  // every CTA's router logits stored (count), before reading any of them
+  if (c.tid == 0) {
+    if (!c.aborted()) wait_count(c, CTRL_RCOUNT, SITE_FLAGS);
+    c.stamp(ST_RCOUNT);
+  }
+  bar_sync(kBarConsumers, kNC * 32);
+  // this CTA's replica of the logits into shared memory (coalesced, tag-checked)
+  float* lg = reinterpret_cast<float*>(c.sm + p.off_lg);
+  const unsigned long long* src = p.logits + (size_t)(blockIdx.x % kLogitRep) * p.maxm * p.E;
+  bool ok = !c.aborted() && stage_tagged(c, src, lg, p.M * p.E / 2, SITE_LOGITS);
+  if (!ok)  // keep going on well-defined data: outputs are void after a timeout
+    for (int i = c.tid; i < p.M * p.E; i += kNC * 32) lg[i] = 0.0f;
+  bar_sync(kBarConsumers, kNC * 32);
+  if (c.tid == 0) c.stamp(ST_LOGITS);
+  if (c.warp < p.M) {
+    if (p.E <= 16 * 32)
+      topk_row<16>(c, rt, c.warp, write_topk);
+    else
+      topk_row<32>(c, rt, c.warp, write_topk);
+  }
+  bar_sync(kBarConsumers, kNC * 32);
+  if (c.tid == 0) c.stamp(ST_TOPK);
+  if (c.warp == 0) union_warp(c, rt);
+  bar_sync(kBarConsumers, kNC * 32);
+}
+
+// --------------------------------------------------------------------------
+// consumer phase D
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void cta_rows(const Params& p, int& r_lo, int& r_hi) {
+  split_range(p.H, blockIdx.x, p.grid, r_lo, r_hi);
 }
 
 // Wait until every CTA has its copy of x (only needed when the output
@@ -756,6 +837,7 @@ static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float
       }
     }
     while (pending) {
+      if (c.tid == 0) c.count(ST_H_ROUNDS, 1);
       unsigned long long v0[kStageBatch], v1[kStageBatch];
 #pragma unroll
       for (int k = 0; k < kStageBatch; ++k) {
@@ -782,8 +864,9 @@ static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float
   return true;
 }
 
+// wait_u: the gate/up results come from this same kernel (single-kernel schedule)
 template <int FMT, int MAXM>
-__device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, Ring ring) {
+__device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, bool wait_u, Ring ring) {
   const Params& p = c.p;
   int r_lo, r_hi;
   cta_rows(p, r_lo, r_hi);
@@ -798,10 +881,12 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, R
   float* red = reinterpret_cast<float*>(c.sm + p.off_red);
   constexpr int CH_EL = FMT == FMT_BF16 ? 8 : 32;  // elements per chunk
   bool first_batch = true;
-  if (nrb > 0) {
-    if (!c.aborted()) wait_flags(c, p.uflags, SITE_FLAGS);
+  if (nrb > 0 && wait_u) {
+    if (c.tid == 0) {
+      if (!c.aborted()) wait_count(c, CTRL_UCOUNT, SITE_FLAGS);
+      c.stamp(ST_U_FLAGS);
+    }
     bar_sync(kBarConsumers, kNC * 32);
-    if (c.tid == 0) c.stamp(ST_U_FLAGS);
   }
   for (int rb = 0; rb < nrb; ++rb) {
     const int rb_lo = r_lo + rb * drs;
@@ -982,7 +1067,13 @@ struct Producer {
       const uint32_t bytes = (uint32_t)nq * p.rpair_bytes;
       uint32_t dst, bar;
       if (!begin(bytes, dst, bar)) return;
-      bulk_g2s(dst, p.router_w + (size_t)w.a * p.rpair_bytes, bytes, bar, pol);
+      // several smaller copies: each bulk copy streams at a fraction of the SM's
+      // bandwidth, and the router rows are on the critical path
+      const uint8_t* src = p.router_w + (size_t)w.a * p.rpair_bytes;
+      for (uint32_t o = 0; o < bytes; o += kRouterCopy) {
+        const uint32_t nb = min((uint32_t)kRouterCopy, bytes - o);
+        bulk_g2s(dst + o, src + o, nb, bar, pol);
+      }
       w.advance(nq);
     }
   }
@@ -1172,7 +1263,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     if (PHASES & PH_R) {
       ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTER, ring);
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
-      if (c.tid == 0) st_tagged(p.rflags + blockIdx.x, c.epoch(), 0.0f);
+      if (c.tid == 0) {
+        count_done(p, CTRL_RCOUNT);
+        c.stamp(ST_RFLAG);
+      }
     }
     if (kRoute) {
       route_rows(c, rt, (PHASES & PH_U) != 0);
@@ -1188,18 +1282,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTED, ring);
       if (c.tid == 0) c.stamp(ST_U_DONE);
     }
-    if (PHASES & (PH_R | PH_U)) {
+    if (PHASES & PH_U) {
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's h rows are all stored
-      if (c.tid == 0) st_tagged(p.uflags + blockIdx.x, c.epoch(), 0.0f);
+      if (c.tid == 0) count_done(p, CTRL_UCOUNT);
     }
-    if (PHASES & PH_D) consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, ring);
-    if (c.tid == 0) c.stamp(ST_D_DONE);
+    if (PHASES & PH_D)
+      consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, PHASES == PH_ALL, ring);
+    if (c.tid == 0) {
+      c.stamp(ST_D_DONE);
+      if (p.stamps) {
+        p.stamps[(size_t)blockIdx.x * kStampSlots + ST_CLOCK_MHZ] =
+            (unsigned long long)(clock64() - c.c0) * 1000ull / (global_ns() - c.t0 + 1);
+      }
+    }
   }
   __syncthreads();
   if (kLast && c.tid == 0) {
     const uint32_t prev = atomicAdd(&p.ctrl[CTRL_EXIT], 1u);
     if (prev == gridDim.x - 1) {
       p.ctrl[CTRL_EXIT] = 0u;
+      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
+      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_UCOUNT) = 0ull;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;
       p.ctrl[CTRL_EPOCH] = e;

@@ -12,6 +12,9 @@ constexpr int kCplBf16 = 16;             // 16-byte x chunks per lane kept in re
 constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVFP4 (H <= 4096)
 constexpr int kStageTarget = 32768;      // ring slot size aimed for (bytes)
 constexpr int kMinSlots = 4;             // ring slots kept before shrinking the h staging area
+constexpr int kLogitRep = 4;             // copies of the router logits (spreads the all-CTA read)
+constexpr int kCandMax = 64;             // top-k candidates ranked in parallel per row
+constexpr int kRouterCopy = 4096;        // bytes per bulk copy of router rows (more copies in flight)
 
 enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
 
@@ -20,7 +23,10 @@ enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
 enum Phase : int { PH_R = 1, PH_U = 2, PH_D = 4, PH_ALL = 7 };
 
 // Control words at the start of the handle's scratch.
-enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3, CTRL_WORDS = 64 };
+// CTRL_RCOUNT / CTRL_UCOUNT (64-bit, 8-byte aligned word index): CTAs whose router
+// logits / gate-up results of the current run are stored; reset by the last CTA.
+enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3, CTRL_RCOUNT = 4,
+                  CTRL_UCOUNT = 6, CTRL_WORDS = 64 };
 // Device status bits and the wait that gave up first.
 enum DevErr : uint32_t { DEV_ERR_TIMEOUT = 1u };
 enum WaitSite : uint32_t {
@@ -50,8 +56,15 @@ enum Stamp : int {
   ST_P_D_ISSUED = 11, // producer: last down stage issued
   ST_LOGITS = 12,     // all router logits seen (routing warp 0)
   ST_TOPK = 13,       // top-k of row 0 done
-  ST_U_FLAGS = 14,    // every CTA's gate/up results published
-  kStampSlots = 16
+  ST_U_FLAGS = 14,    // the gate/up-done count reached the grid size
+  ST_ROUTER_DATA = 15,// warp 0's first router stage landed
+  ST_RFLAG = 16,      // this CTA counted its router logits as stored
+  ST_U_DATA = 17,     // warp 0's first routed gate/up stage landed
+  ST_RCOUNT = 18,     // the router-done count reached the grid size
+  ST_H_ROUNDS = 20,   // (count, not a time) poll rounds of the h staging
+  ST_LOGIT_ROUNDS = 21,  // (count) poll rounds of the logits
+  ST_CLOCK_MHZ = 23,  // (value) SM clock cycles per microsecond over the kernel
+  kStampSlots = 24
 };
 
 // Shared-memory words kept in the misc block.
@@ -84,11 +97,9 @@ struct Params {
   int32_t* topk_idx;
   float* topk_w;
   // scratch (device, owned by the handle)
-  unsigned long long* logits;  // [maxm][E] tagged
+  unsigned long long* logits;  // [kLogitRep][maxm][E] tagged
   unsigned long long* hbuf;    // [nslot_max][maxm][I] tagged
   unsigned long long* xflags;  // [grid] tagged: this CTA has read x
-  unsigned long long* rflags;  // [grid] tagged: this CTA's router logits are stored
-  unsigned long long* uflags;  // [grid] tagged: this CTA's gate/up results are stored
   uint32_t* ctrl;              // CTRL_WORDS
   int out_aliases_x;
   // planned layout
@@ -109,6 +120,7 @@ struct Params {
   // shared-memory offsets from the aligned base
   int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
   int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;
+  int off_lg, off_cand, off_lmax, off_ccount, off_thr, off_wtmp, off_wpc;  // routing scratch (in the hs area)
   int off_red, off_misc, off_ring;
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;

@@ -28,14 +28,16 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
     layers = [synth.make_layer(shape, seed=2000 + i, device="cuda") for i in range(copies)]
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=sched) for i in range(copies)]
     grid = mods[0].info(_lib.MOE_INFO_GRID)
-    stamps = torch.zeros((grid, 16), dtype=torch.int64, device="cuda")
+    stamps = torch.zeros((grid, _lib.STAMP_SLOTS), dtype=torch.int64, device="cuda")
     for md in mods:
         if ring_slots:
             md.set_option(_lib.MOE_OPT_RING_SLOTS, min(ring_slots, md.info(_lib.MOE_INFO_RING_SLOTS)))
     xs = [synth.hidden_rows(m, shape.hidden, seed=70_000 + j, rho=wl["rho"]).cuda() for j in range(n_inputs)]
     out = torch.empty_like(xs[0])
     per_event = {k: [] for k in _lib.STAMP_NAMES}
+    per_count = {k: [] for k in _lib.STAMP_COUNTS}
     totals = []
+    derived = {}
     for r in range(runs + 5):
         md = mods[r % copies]
         md.set_option(_lib.MOE_OPT_STAMPS, stamps.data_ptr() if r >= 5 else 0)
@@ -52,6 +54,15 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
                 if v:
                     per_event[k].append((v - t0) / 1000.0)
         totals.append((int(st[:, 6].max()) - t0) / 1000.0)
+        # per-run derived: the last CTA to publish its router flag vs the first
+        # CTA to see all logits
+        rf = [v for v in st[:, 16].tolist() if v]
+        ls = [v for v in st[:, 12].tolist() if v]
+        if rf and ls:
+            derived.setdefault("last_rcount_add", []).append((max(rf) - t0) / 1000.0)
+            derived.setdefault("first_logits_seen", []).append((min(ls) - t0) / 1000.0)
+        for k in _lib.STAMP_COUNTS:
+            per_count[k].extend(v for v in st[:, k].tolist() if v)
     for md in mods:
         md.set_option(_lib.MOE_OPT_STAMPS, 0)
         assert md.status() == _lib.MOE_OK
@@ -62,6 +73,14 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
             continue
         q = lambda f: v[min(len(v) - 1, int(f * len(v)))]  # noqa: E731
         rows.append((name, statistics.median(v), q(0.1), q(0.9), v[-1]))
+    for k, name in _lib.STAMP_COUNTS.items():
+        v = sorted(per_count[k])
+        if v:
+            q = lambda f: v[min(len(v) - 1, int(f * len(v)))]  # noqa: E731
+            rows.append((name, statistics.median(v), q(0.1), q(0.9), v[-1]))
+    for name, v in derived.items():
+        v = sorted(v)
+        rows.append(("run:" + name, statistics.median(v), v[len(v) // 10], v[(9 * len(v)) // 10], v[-1]))
     return rows, statistics.median(totals), mods[0].info(_lib.MOE_OPT_RING_SLOTS)
 
 
