@@ -191,6 +191,38 @@ enum {
 moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value);
 moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value);
 
+/*
+ * moe_decode_run_static -- the same layer step without a handle, allocating
+ * nothing. The pages have no counterpart; this is a convenience of the library.
+ *
+ * For callers that cannot allocate device memory: code hosted by a framework
+ * that owns all device memory and forbids allocations after start-up, code on a
+ * latency-critical thread that must not take cudaMalloc's implicit device
+ * synchronisation or driver locks, or callers that cannot keep a handle alive
+ * between calls. The caller still passes the weights, inputs and outputs
+ * (device pointers, same meaning and layout as for moe_decode_create and
+ * moe_decode_run; cfg->sched is ignored: the single-kernel schedule runs).
+ *
+ * Scratch: a file-scope device array of MOE_DECODE_STATIC_SCRATCH_BYTES that
+ * every GPU loading the library holds until exit. Configs whose scratch
+ * (control words, 4 copies of the M x E logits and S + min(E, M*k) expert rows
+ * of M x I intermediate values as 8-byte words, one flag per SM) exceeds it
+ * return MOE_ERR_UNSUPPORTED before any device work. The first call on a device
+ * sets the array up (resolves its device address and fills it, a blocking
+ * memset); make that first call before any CUDA stream capture. Every call
+ * shares the array and it keeps the last call's contents; calls that overlap on
+ * the GPU (from different streams or threads, on one device) race, so issue
+ * them one after another.
+ *
+ * Blocking: the call waits for the step on `stream` and returns its device
+ * status (MOE_OK or MOE_ERR_DEVICE_TIMEOUT), as moe_decode_run_host does.
+ * Never calls cudaMalloc, cudaFree or any allocating library routine.
+ */
+#define MOE_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+moe_status moe_decode_run_static(const moe_decode_config* cfg, const moe_decode_weights* w, const void* x,
+                                 const void* residual, void* out, int32_t m_rows, int32_t* topk_idx,
+                                 float* topk_w, moe_stream_t stream);
+
 /* Frees the handle's scratch (waits for the device first). NULL is a no-op. */
 moe_status moe_decode_destroy(moe_decode_handle* h);
 

@@ -46,8 +46,10 @@ MOE_INFO_RING_SLOTS = 19
 MOE_INFO_SLOT_BYTES = 20
 MOE_INFO_KERNELS_PER_RUN = 21
 MOE_INFO_SCRATCH_BYTES = 22
+STATIC_SCRATCH_BYTES = 8 << 20
 
 EXPORTS = ("moe_decode_config_check", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",
+           "moe_decode_run_static",
            "moe_decode_get_status", "moe_decode_set_option", "moe_decode_get_info",
            "moe_decode_destroy", "moe_decode_status_string", "moe_decode_abi_version")
 
@@ -95,6 +97,8 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
                                           ctypes.POINTER(vp)]
         lib.moe_decode_run.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
         lib.moe_decode_run_host.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
+        lib.moe_decode_run_static.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, vp, i32,
+                                              vp, vp, vp]
         lib.moe_decode_get_status.argtypes = [vp, vp]
         lib.moe_decode_set_option.argtypes = [vp, i32, i64]
         lib.moe_decode_get_info.argtypes = [vp, i32, ctypes.POINTER(i64)]

@@ -9,6 +9,7 @@
 #include <new>
 
 #include "../../include/moe_decode.h"
+#include "internal.h"
 #include "kernel_table.h"
 #include "moe_params.h"
 
@@ -221,6 +222,31 @@ moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace moe {
+moe_status check_config_host(const moe_decode_config* cfg) { return check_config(cfg); }
+moe_status check_weights_host(const moe_decode_config& cfg, const moe_decode_weights* w) {
+  return check_weights(cfg, w);
+}
+moe_status plan_host(const moe_decode_config& cfg, int sms, int smem_optin, Params& p) {
+  return plan(cfg, sms, smem_optin, p);
+}
+void bind_weights_host(const moe_decode_weights& w, Params& p) {
+  p.router_w = static_cast<const uint8_t*>(w.router_w);
+  p.w13 = static_cast<const uint8_t*>(w.w13);
+  p.w2 = static_cast<const uint8_t*>(w.w2);
+  p.w13_s = static_cast<const uint8_t*>(w.w13_scale);
+  p.w2_s = static_cast<const uint8_t*>(w.w2_scale);
+  p.w13_gs = w.w13_gscale;
+  p.w2_gs = w.w2_gscale;
+  p.sh_w13 = static_cast<const uint8_t*>(w.sh_w13);
+  p.sh_w2 = static_cast<const uint8_t*>(w.sh_w2);
+  p.sh_w13_s = static_cast<const uint8_t*>(w.sh_w13_scale);
+  p.sh_w2_s = static_cast<const uint8_t*>(w.sh_w2_scale);
+  p.sh_w13_gs = w.sh_w13_gscale;
+  p.sh_w2_gs = w.sh_w2_gscale;
+}
+}  // namespace moe
 
 extern "C" {
 

@@ -1,0 +1,135 @@
+// moe_decode_run_static: the layer step for callers that cannot allocate device
+// memory. Its scratch lives in a fixed-size array of device memory defined
+// below at file scope, so the call needs no handle and allocates nothing.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/moe_decode.h"
+#include "internal.h"
+#include "kernel_table.h"
+#include "moe_params.h"
+
+namespace {
+
+// Control words, router logits, h rows and per-CTA flags of one call. Every GPU
+// that loads the library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_DECODE_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kCtrlBytes = 256;  // moe::CTRL_WORDS 32-bit words, padded
+std::mutex g_setup_mu;
+void* g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch per device
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Once per device, with that device current: the array's device address (the
+// name g_static_scratch in host code is only a stand-in, not that address),
+// control words zeroed and every tagged word set to a tag no run ever uses.
+moe_status setup_device(int dev, unsigned char** out) {
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    unsigned char* b = static_cast<unsigned char*>(p);
+    if (cudaMemset(b, 0, kCtrlBytes) != cudaSuccess ||
+        cudaMemset(b + kCtrlBytes, 0xff, MOE_DECODE_STATIC_SCRATCH_BYTES - kCtrlBytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const moe_decode_weights* w,
+                                            const void* x, const void* residual, void* out, int32_t m_rows,
+                                            int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  moe_status st = moe::check_config_host(cfg);
+  if (st != MOE_OK) return st;
+  if (!x || !residual || !out || m_rows < 1 || m_rows > cfg->max_rows) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  int dev = 0, sms = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe::Params p;
+  if ((st = moe::plan_host(*cfg, sms, optin, p)) != MOE_OK) return st;
+  // scratch layout inside the static array; larger configs are rejected
+  const size_t maxm = cfg->max_rows, E = cfg->num_experts, I = cfg->inter;
+  const size_t o_logits = kCtrlBytes;
+  const size_t o_h = o_logits + round256((size_t)moe::kLogitRep * maxm * E * 8);
+  const size_t o_xf = o_h + round256((size_t)p.nslot_max * maxm * I * 8);
+  const size_t need = o_xf + round256((size_t)p.grid * 8);
+  if (need > MOE_DECODE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+  if ((st = moe::check_weights_host(*cfg, w)) != MOE_OK) return st;
+  unsigned char* base = nullptr;
+  if ((st = setup_device(dev, &base)) != MOE_OK) return st;
+
+  moe::bind_weights_host(*w, p);
+  p.ctrl = reinterpret_cast<uint32_t*>(base);
+  p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
+  p.hbuf = reinterpret_cast<unsigned long long*>(base + o_h);
+  p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
+  p.M = m_rows;
+  p.x = static_cast<const uint16_t*>(x);
+  p.resid = static_cast<const uint16_t*>(residual);
+  p.out = static_cast<uint16_t*>(out);
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  const size_t bytes = (size_t)m_rows * p.H * 2;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
+  p.out_aliases_x = (xa < oa + bytes && oa < xa + bytes) ? 1 : 0;
+
+  const int maxm_t = m_rows == 1 ? 1 : 8;
+  const void* kernel = p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, moe::PH_ALL)
+                                               : moe::kernel_nvfp4(maxm_t, moe::PH_ALL);
+  if (!kernel) return MOE_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // a status left by an earlier call must not stop this one
+  if (cudaMemsetAsync(p.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(p.grid);
+  lc.blockDim = dim3(moe::kThreads);
+  lc.dynamicSmemBytes = p.smem_bytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&lc, kernel, args) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  // wait for the step and report its device status (the status word lives in
+  // the shared array too, so it is read and cleared here)
+  uint32_t status = 0;
+  if (cudaMemcpyAsync(&status, p.ctrl + moe::CTRL_STATUS, sizeof(status), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (status != 0) {
+    if (cudaMemsetAsync(p.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_ERR_DEVICE_TIMEOUT;
+  }
+  return MOE_OK;
+}
