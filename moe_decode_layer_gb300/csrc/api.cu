@@ -143,12 +143,12 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
     return static_cast<int>(at);
   };
   p.off_lg = rtake((size_t)maxm * E * 4, 16);
-  p.off_cand = rtake((size_t)maxm * moe::kCandMax * 8, 8);
-  p.off_lmax = rtake((size_t)maxm * 32 * 8, 8);
+  p.off_cand = rtake((size_t)maxm * moe::kCandMax * 8, 16);
+  p.off_lmax = rtake((size_t)maxm * 32 * 4, 16);
   p.off_thr = rtake((size_t)maxm * 8, 8);
   p.off_ccount = rtake((size_t)maxm * 4, 4);
-  p.off_wtmp = rtake((size_t)maxm * 16 * 4, 4);
-  p.off_wpc = rtake(32 * 4, 4);
+  p.off_wtmp = rtake((size_t)maxm * 16 * 4, 16);
+  p.off_wpc = rtake(32 * 4, 16);
   const size_t area = std::max(ro, fixed + (size_t)hs_pairs * per_pair);
   p.off_ring = (int)round_up(area, 128);
   const long long ring_budget = (long long)smem_optin - 1024 - p.off_ring;
@@ -158,7 +158,8 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
   p.d_rows_stage = drs;
   p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
-  p.qr = std::max(1, std::min(moe::kNC, p.slot_bytes / p.rpair_bytes));
+  // router stages: at most kNC / 2 row pairs, so every row gets at least one warp
+  p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
   p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
   p.timeout_ns = kDefaultTimeoutNs;
   return MOE_OK;

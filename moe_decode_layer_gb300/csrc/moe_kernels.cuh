@@ -463,6 +463,62 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
   }
 }
 
+// Router stages: the router logits are on the critical path of every CTA (all
+// of them wait for all logits), so the CTA's few router rows are each split
+// over several consumer warps along H; the partial sums meet in shared memory.
+template <int MAXM>
+__device__ __noinline__ Ring consume_router(const Ctx& c, Ring ring) {
+  const Params& p = c.p;
+  int lo, hi;
+  split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
+  const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
+  float* part = reinterpret_cast<float*>(c.sm + p.off_red);  // [kNC][8]
+  const uint32_t ep = c.epoch();
+  const int nch = p.H / 8;
+  for (ItemWalk w(lo, hi, p.qr, 0); w.more(); ring.next(p.nslots)) {
+    const int nq = w.count();
+    const int nrow = 2 * nq;  // <= kNC: the planner keeps qr <= kNC / 2
+    const int ws = kNC / nrow;
+    const int row = c.warp / ws, seg = c.warp % ws;
+    float acc[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) acc[m] = 0.0f;
+    if (row < nrow && !c.aborted() && c.wait_full(ring)) {
+      const uint4* wr = reinterpret_cast<const uint4*>(c.slot_ptr(ring.slot) + (size_t)row * 2 * p.H);
+      const int c0 = seg * nch / ws, c1 = (seg + 1) * nch / ws;
+      for (int ch = c0 + c.lane; ch < c1; ch += 32) {
+        const uint4 wv = wr[ch];
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+          if (m < p.M) dot8_bf16(acc[m], wv, xs[m * nch + ch]);
+      }
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m)
+#pragma unroll
+        for (int o = 16; o; o >>= 1) acc[m] += __shfl_xor_sync(kFull, acc[m], o);
+      if (c.lane == 0)
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) part[c.warp * 8 + m] = acc[m];
+    }
+    bar_sync(kBarConsumers, kNC * 32);  // every partial sum of the stage is in `part`
+    if (c.lane == 0) c.release(ring, 1);
+    for (int t = c.tid; t < nrow * p.M; t += kNC * 32) {
+      const int r = t / p.M, m = t % p.M;
+      float v = 0.0f;
+      for (int s = 0; s < ws; ++s) v += part[(r * ws + s) * 8 + m];
+      if (!(p.test_flags & TEST_SKIP_LOGITS)) {
+        const int e = 2 * w.a + r;
+#pragma unroll
+        for (int rep = 0; rep < kLogitRep; ++rep)
+          st_tagged(p.logits + ((size_t)rep * p.maxm + m) * p.E + e, ep, v);
+      }
+    }
+    bar_sync(kBarConsumers, kNC * 32);  // `part` is free again
+    w.advance(nq);
+  }
+  return ring;
+}
+
 enum ItemKind : int { ITEM_ROUTER = 0, ITEM_SHARED = 1, ITEM_ROUTED = 2 };
 
 // One phase of row-pair items (router rows, shared gate/up rows or routed
@@ -600,43 +656,56 @@ __device__ __forceinline__ int key_expert(unsigned long long k) { return (int)(0
 __device__ __forceinline__ float key_value(unsigned long long k) { return order_key_f32((uint32_t)(k >> 32)); }
 
 // Row m's top-k on warp m, from the logits staged in shared memory. Lane l
-// holds experts [l*P, l*P+P). The K-th largest of the 32 lane maxima bounds the
-// K-th largest logit from below (those K lane maxima are K distinct logits), so
-// every selected expert is at or above it; the few candidates at or above it
-// are ranked in parallel. With many exact ties the candidates can exceed
-// kCandMax; then K rounds of a warp-wide max select instead.
+// holds experts 32 i + l. The K-th largest of the 32 lane maxima (by value, with
+// multiplicity) bounds the K-th largest logit from below -- those K lane maxima
+// are K distinct logits -- so every selected expert has a logit at or above it;
+// the few candidates at or above it are ranked in parallel on exact keys (ties:
+// the lower expert id). With many exact ties the candidates can exceed kCandMax;
+// then K rounds of a warp-wide max select instead.
 template <int PM>
 __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
   const Params& p = c.p;
   const float* lg = reinterpret_cast<const float*>(c.sm + p.off_lg) + (size_t)m * p.E;
-  unsigned long long* lmax = reinterpret_cast<unsigned long long*>(c.sm + p.off_lmax) + m * 32;
+  uint32_t* lmax = reinterpret_cast<uint32_t*>(c.sm + p.off_lmax) + m * 32;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + m * kCandMax;
-  unsigned long long* thr = reinterpret_cast<unsigned long long*>(c.sm + p.off_thr) + m;
+  uint32_t* thr = reinterpret_cast<uint32_t*>(c.sm + p.off_thr) + m * 2;
   int* ccount = reinterpret_cast<int*>(c.sm + p.off_ccount) + m;
   float* wtmp = reinterpret_cast<float*>(c.sm + p.off_wtmp) + m * 16;
-  const int P = (p.E + 31) / 32;
-  const int base = c.lane * P;
-  unsigned long long key[PM];
-  unsigned long long best = 0;
+  const int lane = c.lane;
+  uint32_t key[PM];
+  uint32_t best = 0;
 #pragma unroll
   for (int i = 0; i < PM; ++i) {
-    key[i] = 0;
-    if (i < P && base + i < p.E) key[i] = pack_key(lg[base + i], base + i);
+    const int e = 32 * i + lane;
+    key[i] = e < p.E ? f32_order_key(lg[e]) : 0u;
     best = key[i] > best ? key[i] : best;
   }
-  lmax[c.lane] = best;
-  if (c.lane == 0) *ccount = 0;
+  lmax[lane] = best;
+  if (lane == 0) *ccount = 0;
   __syncwarp();
-  int r = 0;
-  for (int j = 0; j < 32; ++j) r += lmax[j] > best;
-  if (r == p.K - 1) *thr = best;
-  __syncwarp();
-  const unsigned long long t = *thr;
+  int gt = 0, ge = 0;
+  const uint4* l4 = reinterpret_cast<const uint4*>(lmax);
 #pragma unroll
-  for (int i = 0; i < PM; ++i) {
-    if (key[i] != 0 && key[i] >= t) {
-      const int pos = atomicAdd(ccount, 1);
-      if (pos < kCandMax) cand[pos] = key[i];
+  for (int j = 0; j < 8; ++j) {
+    const uint4 q = l4[j];
+    gt += (q.x > best) + (q.y > best) + (q.z > best) + (q.w > best);
+    ge += (q.x >= best) + (q.y >= best) + (q.z >= best) + (q.w >= best);
+  }
+  if (gt <= p.K - 1 && ge >= p.K) *thr = best;  // the K-th largest lane max (ties write the same value)
+  __syncwarp();
+  const uint32_t t = *thr;
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < PM; ++i) cnt += key[i] != 0u && key[i] >= t;
+  if (cnt) {
+    int o = atomicAdd(ccount, cnt);
+#pragma unroll
+    for (int i = 0; i < PM; ++i) {
+      if (key[i] != 0u && key[i] >= t) {
+        const int e = 32 * i + lane;
+        if (o < kCandMax) cand[o] = ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)e);
+        ++o;
+      }
     }
   }
   __syncwarp();
@@ -644,17 +713,30 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
   int* sel_e = rt.sel_e + m * p.K;
   float* sel_v = rt.sel_w + m * p.K;  // logits first, weights after
   if (C <= kCandMax) {
-    for (int ci = c.lane; ci < C; ci += 32) {
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
+    for (int ci = lane; ci < C; ci += 32) {
       const unsigned long long v = cand[ci];
-      int rank = 0;
-      for (int j = 0; j < C; ++j) rank += cand[j] > v;
+      int r0 = 0, r1 = 0;
+      for (int j = 0; 2 * j < C; ++j) {
+        const ulonglong2 q = c2[j];
+        r0 += q.x > v;
+        r1 += (2 * j + 1 < C) && q.y > v;
+      }
+      const int rank = r0 + r1;
       if (rank < p.K) {
         sel_e[rank] = key_expert(v);
         sel_v[rank] = key_value(v);
       }
     }
   } else {
-    unsigned long long lb = best;
+    unsigned long long kk[PM];
+    unsigned long long lb = 0;
+#pragma unroll
+    for (int i = 0; i < PM; ++i) {
+      const int e = 32 * i + lane;
+      kk[i] = key[i] ? ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)e) : 0ull;
+      lb = kk[i] > lb ? kk[i] : lb;
+    }
     for (int j = 0; j < p.K; ++j) {
       const uint32_t hi = (uint32_t)(lb >> 32);
       const uint32_t ghi = warp_max_u32(hi);
@@ -665,31 +747,31 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
         sel_v[j] = key_value(lb);
 #pragma unroll
         for (int i = 0; i < PM; ++i)
-          if (key[i] == lb) key[i] = 0;
+          if (kk[i] == lb) kk[i] = 0;
         lb = 0;
 #pragma unroll
-        for (int i = 0; i < PM; ++i) lb = key[i] > lb ? key[i] : lb;
+        for (int i = 0; i < PM; ++i) lb = kk[i] > lb ? kk[i] : lb;
       }
       __syncwarp();
     }
   }
   __syncwarp();
   // renormalised softmax over the selection, the sum in a fixed order
-  if (c.lane < p.K) wtmp[c.lane] = expf(sel_v[c.lane] - sel_v[0]);
+  if (lane < p.K) wtmp[lane] = expf(sel_v[lane] - sel_v[0]);
   __syncwarp();
-  if (c.lane < p.K) {
+  if (lane < p.K) {
     float sum = 0.0f;
     for (int j = 0; j < p.K; ++j) sum += wtmp[j];
-    const float w = wtmp[c.lane] / sum;
-    const int e = sel_e[c.lane];
+    const float w = wtmp[lane] / sum;
+    const int e = sel_e[lane];
     atomicOr(&rt.emask[e], 1u << m);
     atomicOr(&rt.bitmap[e >> 5], 1u << (e & 31));
     if (write_topk && blockIdx.x == 0) {
-      if (p.topk_idx) p.topk_idx[m * p.K + c.lane] = e;
-      if (p.topk_w) p.topk_w[m * p.K + c.lane] = w;
+      if (p.topk_idx) p.topk_idx[m * p.K + lane] = e;
+      if (p.topk_w) p.topk_w[m * p.K + lane] = w;
     }
     __syncwarp((1u << p.K) - 1u);
-    sel_v[c.lane] = w;
+    sel_v[lane] = w;
   }
 }
 
@@ -704,10 +786,14 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
   wpc[c.lane] = __popc(w);
   __syncwarp();
   int before = 0, total = 0;
-  for (int j = 0; j < 32; ++j) {
-    const int v = wpc[j];
-    before += j < c.lane ? v : 0;
-    total += v;
+  const int4* w4 = reinterpret_cast<const int4*>(wpc);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int4 v = w4[j];
+    const int b0 = 4 * j;
+    before += (b0 < c.lane ? v.x : 0) + (b0 + 1 < c.lane ? v.y : 0) + (b0 + 2 < c.lane ? v.z : 0) +
+              (b0 + 3 < c.lane ? v.w : 0);
+    total += (v.x + v.y) + (v.z + v.w);
   }
   int s = p.S + before;
   for (uint32_t bits = w; bits; bits &= bits - 1) {
@@ -733,10 +819,13 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
     wpc[c.lane] = sl < nsl ? __popc(rt.slot_mask[sl]) : 0;
     __syncwarp();
     int pre = 0, sum = 0;
-    for (int j = 0; j < 32; ++j) {
-      const int v = wpc[j];
-      pre += j < c.lane ? v : 0;
-      sum += v;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int4 v = w4[j];
+      const int b0 = 4 * j;
+      pre += (b0 < c.lane ? v.x : 0) + (b0 + 1 < c.lane ? v.y : 0) + (b0 + 2 < c.lane ? v.z : 0) +
+             (b0 + 3 < c.lane ? v.w : 0);
+      sum += (v.x + v.y) + (v.z + v.w);
     }
     if (sl < nsl) rt.pair_base[sl] = carry + pre;
     carry += sum;
@@ -1261,7 +1350,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       st_tagged(p.xflags + blockIdx.x, c.epoch(), 0.0f);
     Ring ring;
     if (PHASES & PH_R) {
-      ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTER, ring);
+      ring = consume_router<MAXM>(c, ring);
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
       if (c.tid == 0) {
         count_done(p, CTRL_RCOUNT);
