@@ -205,8 +205,8 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
  *
  * Scratch: a file-scope device array of MOE_DECODE_STATIC_SCRATCH_BYTES that
  * every GPU loading the library holds until exit. Configs whose scratch
- * (control words, 4 copies of the M x E logits and S + min(E, M*k) expert rows
- * of M x I intermediate values as 8-byte words, one flag per SM) exceeds it
+ * (control words, 4 copies of the M x E logits and 4 copies of S + min(E, M*k)
+ * expert rows of M x I intermediate values as 8-byte words, one flag per SM) exceeds it
  * return MOE_ERR_UNSUPPORTED before any device work. The first call on a device
  * sets the array up (resolves its device address and fills it, a blocking
  * memset); make that first call before any CUDA stream capture. Every call

@@ -111,6 +111,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.off_slot_mask = take((size_t)p.nslot_max * 4, 4);
   p.off_slot_w = take((size_t)p.nslot_max * maxm * 4, 4);
   p.off_pair_base = take((size_t)(p.nslot_max + 1) * 4, 4);
+  p.off_pair_sr = take((size_t)p.npair_max * 4, 4);
   p.off_red = take((size_t)moe::kNC * moe::kRpgMax * 8 * 4, 16);
   p.off_misc = take(moe::MISC_WORDS * 4, 16);
   const size_t fixed = round_up(off, 128);
@@ -307,7 +308,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   };
   const size_t o_ctrl = take(moe::CTRL_WORDS * 4);
   const size_t o_logits = take(moe::kLogitRep * maxm * E * 8);
-  const size_t o_h = take((size_t)p.nslot_max * maxm * I * 8);
+  const size_t o_h = take((size_t)moe::kHRep * p.nslot_max * maxm * I * 8);
   const size_t o_xf = take((size_t)p.grid * 8);
 
   const size_t tag_end = off;

@@ -590,7 +590,10 @@ __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int ki
           if (c.lane == m && (mask >> m & 1u)) {
             float h = silu_f32(acc.g[m] * gsg) * (acc.u[m] * gsu);
             if (kind == ITEM_ROUTED) h *= rt.slot_w[slot * p.maxm + m];
-            st_tagged(&p.hbuf[((size_t)slot * p.maxm + m) * p.I + j], ep, h);
+            const size_t at = ((size_t)slot * p.maxm + m) * p.I + j;
+            const size_t rep_stride = (size_t)p.nslot_max * p.maxm * p.I;
+#pragma unroll
+            for (int r = 0; r < kHRep; ++r) st_tagged(p.hbuf + r * rep_stride + at, ep, h);
           }
         }
       }
@@ -827,7 +830,13 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
              (b0 + 3 < c.lane ? v.w : 0);
       sum += (v.x + v.y) + (v.z + v.w);
     }
-    if (sl < nsl) rt.pair_base[sl] = carry + pre;
+    if (sl < nsl) {
+      rt.pair_base[sl] = carry + pre;
+      // (slot << 4 | row) of each of this slot's pairs, rows ascending
+      int* psr = reinterpret_cast<int*>(c.sm + p.off_pair_sr);
+      int q = carry + pre;
+      for (uint32_t msk = rt.slot_mask[sl]; msk; msk &= msk - 1) psr[q++] = (sl << 4) | (__ffs(msk) - 1);
+    }
     carry += sum;
   }
   if (c.lane == 0) {
@@ -901,6 +910,9 @@ static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float
   const int p0 = rt.pair_base[sl0];
   const int half = p.I / 2;
   const int n = (rt.pair_base[sl1] - p0) * half;  // 16-byte units
+  const int* psr = reinterpret_cast<const int*>(c.sm + p.off_pair_sr);
+  const unsigned long long* hrep =
+      p.hbuf + (size_t)(blockIdx.x % kHRep) * p.nslot_max * p.maxm * p.I;  // this CTA's copy
   uint64_t spins = 0;
   for (int base = c.tid; base < n; base += kNC * 32 * kStageBatch) {
     uint32_t pending = 0;
@@ -909,19 +921,13 @@ static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float
 #pragma unroll
     for (int k = 0; k < kStageBatch; ++k) {
       const int u = base + k * kNC * 32;
-      src[k] = p.hbuf;
+      src[k] = hrep;
       dst[k] = hs;
       if (u < n) {
-        const int pr = p0 + u / half, kk = 2 * (u % half);
-        // pair pr -> (slot, row): the slot whose pair range holds pr, then the
-        // row of that slot's mask with this rank
-        int sl = sl0;
-        while (rt.pair_base[sl + 1] <= pr) ++sl;
-        uint32_t msk = rt.slot_mask[sl];
-        for (int r = pr - rt.pair_base[sl]; r > 0; --r) msk &= msk - 1;
-        const int m = __ffs(msk) - 1;
-        src[k] = p.hbuf + ((size_t)sl * p.maxm + m) * p.I + kk;
-        dst[k] = hs + (size_t)(pr - p0) * p.I + kk;
+        const int pr = u / half, kk = 2 * (u - pr * half);
+        const int sr = psr[p0 + pr];
+        src[k] = hrep + ((size_t)(sr >> 4) * p.maxm + (sr & 15)) * p.I + kk;
+        dst[k] = hs + (size_t)pr * p.I + kk;
         pending |= 1u << k;
       }
     }

@@ -13,6 +13,7 @@ constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVF
 constexpr int kStageTarget = 32768;      // ring slot size aimed for (bytes)
 constexpr int kMinSlots = 4;             // ring slots kept before shrinking the h staging area
 constexpr int kLogitRep = 4;             // copies of the router logits (spreads the all-CTA read)
+constexpr int kHRep = 4;                 // copies of the h rows (spreads the all-CTA read)
 constexpr int kCandMax = 64;             // top-k candidates ranked in parallel per row
 constexpr int kRouterCopy = 4096;        // bytes per bulk copy of router rows (more copies in flight)
 
@@ -98,7 +99,7 @@ struct Params {
   float* topk_w;
   // scratch (device, owned by the handle)
   unsigned long long* logits;  // [kLogitRep][maxm][E] tagged
-  unsigned long long* hbuf;    // [nslot_max][maxm][I] tagged
+  unsigned long long* hbuf;    // [kHRep][nslot_max][maxm][I] tagged
   unsigned long long* xflags;  // [grid] tagged: this CTA has read x
   uint32_t* ctrl;              // CTRL_WORDS
   int out_aliases_x;
@@ -121,6 +122,7 @@ struct Params {
   int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
   int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;
   int off_lg, off_cand, off_lmax, off_ccount, off_thr, off_wtmp, off_wpc;  // routing scratch (in the hs area)
+  int off_pair_sr;   // [npair_max] (slot << 4 | row) of each (slot, row) pair
   int off_red, off_misc, off_ring;
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;

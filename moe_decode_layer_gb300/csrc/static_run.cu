@@ -73,7 +73,7 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   const size_t maxm = cfg->max_rows, E = cfg->num_experts, I = cfg->inter;
   const size_t o_logits = kCtrlBytes;
   const size_t o_h = o_logits + round256((size_t)moe::kLogitRep * maxm * E * 8);
-  const size_t o_xf = o_h + round256((size_t)p.nslot_max * maxm * I * 8);
+  const size_t o_xf = o_h + round256((size_t)moe::kHRep * p.nslot_max * maxm * I * 8);
   const size_t need = o_xf + round256((size_t)p.grid * 8);
   if (need > MOE_DECODE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
   if ((st = moe::check_weights_host(*cfg, w)) != MOE_OK) return st;
