@@ -294,64 +294,95 @@ static __device__ __noinline__ void prepare_x(const Ctx& c) {
 // consumer: dot products of one row pair with the token rows in `mask`.
 // Results are warp-reduced (butterfly), so every lane holds all sums.
 // --------------------------------------------------------------------------
-template <int MAXM>
-struct PairAcc {
-  float g[MAXM];
-  float u[MAXM];
+// Sums of one (gate row, up row) item for one x row, held by one lane after
+// the warp reduction: lane k holds the k-th row of the item's row mask (m = -1
+// on lanes without a row).
+struct RowSums {
+  int m;
+  float g, u;
 };
 
-template <int MAXM>
-__device__ __forceinline__ void warp_reduce_pair(PairAcc<MAXM>& a, uint32_t mask) {
+__device__ __forceinline__ void warp_sum2(float& g, float& u) {
 #pragma unroll
-  for (int m = 0; m < MAXM; ++m) {
-    if (mask >> m & 1u) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        a.g[m] += __shfl_xor_sync(kFull, a.g[m], o);
-        a.u[m] += __shfl_xor_sync(kFull, a.u[m], o);
-      }
-    }
+  for (int o = 16; o; o >>= 1) {
+    g += __shfl_xor_sync(kFull, g, o);
+    u += __shfl_xor_sync(kFull, u, o);
   }
 }
 
-// bf16 rows a, b against x. XREG (MAXM == 1 only): the lane's x chunks in
-// registers; otherwise x rows from shared memory. Two partial sums per row
-// (even / odd chunk) shorten the dependent FMA chain.
-template <int MAXM, bool XREG>
-__device__ __forceinline__ void pair_dot_bf16(const uint4* wa, const uint4* wb, int nch, const uint4* xr,
-                                              const uint4* xs, uint32_t mask, int lane, PairAcc<MAXM>& a) {
-  if (MAXM == 1 && XREG) {
-    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+// bf16 rows a, b against one x row held in the lane's registers (xr: chunks
+// lane, lane + 32, ...). Two partial sums per row (even / odd chunk) shorten
+// the dependent FMA chain.
+__device__ __forceinline__ RowSums dot_one_bf16(const uint4* wa, const uint4* wb, int nch, const uint4* xr,
+                                                int lane) {
+  float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < kCplBf16; i += 2) {
-      const int ch0 = lane + 32 * i, ch1 = ch0 + 32;
-      if (ch0 < nch) {
-        dot8_bf16(g0, wa[ch0], xr[i]);
-        dot8_bf16(u0, wb[ch0], xr[i]);
-      }
-      if (ch1 < nch) {
-        dot8_bf16(g1, wa[ch1], xr[i + 1]);
-        dot8_bf16(u1, wb[ch1], xr[i + 1]);
-      }
+  for (int i = 0; i < kCplBf16; i += 2) {
+    const int ch0 = lane + 32 * i, ch1 = ch0 + 32;
+    if (ch0 < nch) {
+      dot8_bf16(g0, wa[ch0], xr[i]);
+      dot8_bf16(u0, wb[ch0], xr[i]);
     }
-    a.g[0] = g0 + g1;
-    a.u[0] = u0 + u1;
-  } else {
+    if (ch1 < nch) {
+      dot8_bf16(g1, wa[ch1], xr[i + 1]);
+      dot8_bf16(u1, wb[ch1], xr[i + 1]);
+    }
+  }
+  RowSums r{0, g0 + g1, u0 + u1};
+  warp_sum2(r.g, r.u);
+  if (lane != 0) r.m = -1;
+  return r;
+}
+
+// bf16 rows a, b against the N x rows of `mask` (N = popcount), x rows in
+// shared memory. Only the rows that chose the expert are computed; two chunks
+// per step give each row four independent FMA chains.
+template <int N>
+__device__ __forceinline__ RowSums dot_rows_bf16(const uint4* wa, const uint4* wb, int nch, const uint4* xs,
+                                                 uint32_t mask, int lane) {
+  int rows[N];
+  const uint4* xp[N];
+  uint32_t msk = mask;
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m) a.g[m] = a.u[m] = 0.0f;
-    for (int ch = lane; ch < nch; ch += 32) {
-      const uint4 va = wa[ch], vb = wb[ch];
+  for (int k = 0; k < N; ++k) {
+    rows[k] = __ffs(msk) - 1;
+    msk &= msk - 1;
+    xp[k] = xs + rows[k] * nch;
+  }
+  float g0[N], g1[N], u0[N], u1[N];
 #pragma unroll
-      for (int m = 0; m < MAXM; ++m) {
-        if (mask >> m & 1u) {
-          const uint4 xv = xs[m * nch + ch];
-          dot8_bf16(a.g[m], va, xv);
-          dot8_bf16(a.u[m], vb, xv);
-        }
+  for (int k = 0; k < N; ++k) g0[k] = g1[k] = u0[k] = u1[k] = 0.0f;
+  int ch = lane;
+  if (N <= 4) {  // two chunks per step while the registers allow it
+    for (; ch + 32 < nch; ch += 64) {  // nch is a multiple of 32: the trip count is warp-uniform
+      const uint4 a0 = wa[ch], b0 = wb[ch], a1 = wa[ch + 32], b1 = wb[ch + 32];
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const uint4 x0 = xp[k][ch], x1 = xp[k][ch + 32];
+        dot8_bf16(g0[k], a0, x0);
+        dot8_bf16(u0[k], b0, x0);
+        dot8_bf16(g1[k], a1, x1);
+        dot8_bf16(u1[k], b1, x1);
       }
     }
   }
-  warp_reduce_pair<MAXM>(a, mask);
+  for (; ch < nch; ch += 32) {
+    const uint4 a0 = wa[ch], b0 = wb[ch];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const uint4 x0 = xp[k][ch];
+      dot8_bf16(g0[k], a0, x0);
+      dot8_bf16(u0[k], b0, x0);
+    }
+  }
+  RowSums r{-1, 0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    float g = g0[k] + g1[k], u = u0[k] + u1[k];
+    warp_sum2(g, u);
+    if (lane == k) r = RowSums{rows[k], g, u};
+  }
+  return r;
 }
 
 // One NVFP4 chunk: 32 e2m1 codes (16 bytes) in two 16-element blocks with their
@@ -391,42 +422,110 @@ __device__ __forceinline__ void bf16x8_to_f16x8(const uint4 v, uint32_t* o) {
   }
 }
 
-// NVFP4 rows a, b (codes qa, qb; scales sa, sb). xr: lane's x chunks as fp16
-// (MAXM == 1, 16 words per chunk); xs: bf16 x rows (MAXM > 1).
-template <int MAXM>
-__device__ __forceinline__ void pair_dot_fp4(const uint4* qa, const uint4* qb, const uint16_t* sa,
-                                             const uint16_t* sb, int nch, const uint32_t* xr,
-                                             const uint4* xs, int H, uint32_t mask, int lane,
-                                             PairAcc<MAXM>& a) {
+// NVFP4 rows a, b (codes qa, qb; scales sa, sb) against one x row held in the
+// lane's registers as fp16 (16 words per 32-element chunk).
+__device__ __forceinline__ RowSums dot_one_fp4(const uint4* qa, const uint4* qb, const uint16_t* sa,
+                                               const uint16_t* sb, int nch, const uint32_t* xr, int lane) {
+  RowSums r{0, 0.0f, 0.0f};
 #pragma unroll
-  for (int m = 0; m < MAXM; ++m) a.g[m] = a.u[m] = 0.0f;
-  if (MAXM == 1) {
+  for (int i = 0; i < kCplFp4; ++i) {
+    const int ch = lane + 32 * i;
+    if (ch < nch) {
+      dot32_fp4(r.g, qa[ch], sa[ch], xr + 16 * i);
+      dot32_fp4(r.u, qb[ch], sb[ch], xr + 16 * i);
+    }
+  }
+  warp_sum2(r.g, r.u);
+  if (lane != 0) r.m = -1;
+  return r;
+}
+
+// NVFP4 rows a, b against the N bf16 x rows of `mask` in shared memory.
+template <int N>
+__device__ __forceinline__ RowSums dot_rows_fp4(const uint4* qa, const uint4* qb, const uint16_t* sa,
+                                                const uint16_t* sb, int nch, const uint4* xs, int H,
+                                                uint32_t mask, int lane) {
+  int rows[N];
+  const uint4* xp[N];
+  uint32_t msk = mask;
 #pragma unroll
-    for (int i = 0; i < kCplFp4; ++i) {
-      const int ch = lane + 32 * i;
-      if (ch < nch) {
-        dot32_fp4(a.g[0], qa[ch], sa[ch], xr + 16 * i);
-        dot32_fp4(a.u[0], qb[ch], sb[ch], xr + 16 * i);
+  for (int k = 0; k < N; ++k) {
+    rows[k] = __ffs(msk) - 1;
+    msk &= msk - 1;
+    xp[k] = xs + (size_t)rows[k] * (H / 8);
+  }
+  float g[N], u[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) g[k] = u[k] = 0.0f;
+  for (int ch = lane; ch < nch; ch += 32) {
+    const uint4 va = qa[ch], vb = qb[ch];
+    const uint32_t s_a = sa[ch], s_b = sb[ch];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      uint32_t xh[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(xp[k][ch * 4 + q], xh + 4 * q);
+      dot32_fp4(g[k], va, s_a, xh);
+      dot32_fp4(u[k], vb, s_b, xh);
+    }
+  }
+  RowSums r{-1, 0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    warp_sum2(g[k], u[k]);
+    if (lane == k) r = RowSums{rows[k], g[k], u[k]};
+  }
+  return r;
+}
+
+// The item's gate/up sums: the register path for single-row kernels, else the
+// N-row path for the item's row count.
+template <int FMT, int MAXM>
+__device__ __forceinline__ RowSums item_dot(const uint8_t* st, int iq, int nq, const Params& p,
+                                            const uint4* xb, const uint32_t* xh, const uint4* xs, uint32_t mask,
+                                            int lane) {
+  if (FMT == FMT_BF16) {
+    const uint4* wa = reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13);
+    const uint4* wb = reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13);
+    const int nch = p.nchunk_h;
+    if constexpr (MAXM == 1) {
+      return dot_one_bf16(wa, wb, nch, xb, lane);
+    } else {
+      switch (__popc(mask)) {
+        case 1: return dot_rows_bf16<1>(wa, wb, nch, xs, mask, lane);
+        case 2: return dot_rows_bf16<2>(wa, wb, nch, xs, mask, lane);
+        case 3: return dot_rows_bf16<3>(wa, wb, nch, xs, mask, lane);
+        case 4: return dot_rows_bf16<4>(wa, wb, nch, xs, mask, lane);
+        case 5: return dot_rows_bf16<5>(wa, wb, nch, xs, mask, lane);
+        case 6: return dot_rows_bf16<6>(wa, wb, nch, xs, mask, lane);
+        case 7: return dot_rows_bf16<7>(wa, wb, nch, xs, mask, lane);
+        case 8: return dot_rows_bf16<8>(wa, wb, nch, xs, mask, lane);
+        default: return RowSums{-1, 0.0f, 0.0f};
       }
     }
   } else {
-    for (int ch = lane; ch < nch; ch += 32) {
-      const uint4 va = qa[ch], vb = qb[ch];
-      const uint32_t s_a = sa[ch], s_b = sb[ch];
-#pragma unroll
-      for (int m = 0; m < MAXM; ++m) {
-        if (mask >> m & 1u) {
-          uint32_t xh[16];
-          const uint4* xrow = xs + (size_t)m * (H / 8) + ch * 4;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(xrow[q], xh + 4 * q);
-          dot32_fp4(a.g[m], va, s_a, xh);
-          dot32_fp4(a.u[m], vb, s_b, xh);
-        }
+    const uint4* qa = reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13);
+    const uint4* qb = reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13);
+    const uint8_t* scb = st + (size_t)2 * nq * p.row13;
+    const uint16_t* sa = reinterpret_cast<const uint16_t*>(scb + (size_t)iq * p.sc13);
+    const uint16_t* sb = reinterpret_cast<const uint16_t*>(scb + (size_t)(nq + iq) * p.sc13);
+    const int nch = p.nchunk_h;
+    if constexpr (MAXM == 1) {
+      return dot_one_fp4(qa, qb, sa, sb, nch, xh, lane);
+    } else {
+      switch (__popc(mask)) {
+        case 1: return dot_rows_fp4<1>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 2: return dot_rows_fp4<2>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 3: return dot_rows_fp4<3>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 4: return dot_rows_fp4<4>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 5: return dot_rows_fp4<5>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 6: return dot_rows_fp4<6>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 7: return dot_rows_fp4<7>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        case 8: return dot_rows_fp4<8>(qa, qb, sa, sb, nch, xs, p.H, mask, lane);
+        default: return RowSums{-1, 0.0f, 0.0f};
       }
     }
   }
-  warp_reduce_pair<MAXM>(a, mask);
 }
 
 // --------------------------------------------------------------------------
@@ -519,83 +618,47 @@ __device__ __noinline__ Ring consume_router(const Ctx& c, Ring ring) {
   return ring;
 }
 
-enum ItemKind : int { ITEM_ROUTER = 0, ITEM_SHARED = 1, ITEM_ROUTED = 2 };
+enum ItemKind : int { ITEM_SHARED = 1, ITEM_ROUTED = 2 };
 
-// One phase of row-pair items (router rows, shared gate/up rows or routed
-// gate/up rows): each consumer warp takes its items of every stage, computes
-// the dot products against x and publishes tagged results. Returns the ring
-// position after the phase. Not inlined: the three phases share this code.
+// One phase of gate/up items (shared experts' or routed experts' row pairs):
+// each consumer warp takes its items of every stage, computes the dot products
+// against the rows of x that chose the expert and publishes tagged h values.
+// Returns the ring position after the phase. Not inlined: both phases share it.
 template <int FMT, int MAXM>
 __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring) {
   const Params& p = c.p;
-  const bool router = kind == ITEM_ROUTER;
-  const int n = router ? p.E / 2 : (kind == ITEM_SHARED ? p.S * p.I : c.misc[MISC_NROUTED] * p.I);
+  const int n = kind == ITEM_SHARED ? p.S * p.I : c.misc[MISC_NROUTED] * p.I;
   int lo, hi;
   split_range(n, blockIdx.x, p.grid, lo, hi);
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
   const uint32_t ep = c.epoch();
   const int slot0 = kind == ITEM_ROUTED ? p.S : 0;
+  const size_t rep_stride = (size_t)p.nslot_max * p.maxm * p.I;
   XRegs<FMT, MAXM> xr;
   load_xregs<FMT, MAXM>(c, xr);
-  for (ItemWalk w(lo, hi, router ? p.qr : p.q, router ? 0 : p.I); w.more(); ring.next(p.nslots)) {
+  for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(p.nslots)) {
     const int nq = w.count();
     const int iq = w.offset(c.warp);
     if (iq < nq && !c.aborted() && c.wait_full(ring)) {
-      if (c.warp == 0 && c.lane == 0 && w.a == lo) c.stamp(kind == ITEM_ROUTER ? ST_ROUTER_DATA : ST_U_DATA);
+      if (c.warp == 0 && c.lane == 0 && w.a == lo) c.stamp(ST_U_DATA);
       const uint8_t* st = c.slot_ptr(ring.slot);
-      PairAcc<MAXM> acc;
-      if (router) {
-        const uint32_t mask = (1u << p.M) - 1u;
-        const uint8_t* rp = st + (size_t)iq * p.rpair_bytes;
-        pair_dot_bf16<MAXM, FMT == FMT_BF16>(reinterpret_cast<const uint4*>(rp),
-                                             reinterpret_cast<const uint4*>(rp + 2 * p.H), p.H / 8, xr.b, xs,
-                                             mask, c.lane, acc);
-        const int t = w.a + iq;
-        if (!(p.test_flags & TEST_SKIP_LOGITS)) {
+      const int slot = w.u + slot0;
+      const int j = w.j + iq;
+      const uint32_t mask = kind == ITEM_SHARED ? (1u << p.M) - 1u : rt.slot_mask[slot];
+      const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane);
+      float gsg = 1.0f, gsu = 1.0f;
+      if (FMT == FMT_NVFP4) {
+        const int e = kind == ITEM_SHARED ? -1 - slot : rt.slot_e[slot];
+        const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
+        gsg = gs[0];
+        gsu = gs[1];
+      }
+      if (rs.m >= 0) {
+        float h = silu_f32(rs.g * gsg) * (rs.u * gsu);
+        if (kind == ITEM_ROUTED) h *= rt.slot_w[slot * p.maxm + rs.m];
+        const size_t at = ((size_t)slot * p.maxm + rs.m) * p.I + j;
 #pragma unroll
-          for (int m = 0; m < MAXM; ++m) {
-            if (c.lane == m && m < p.M) {
-#pragma unroll
-              for (int r = 0; r < kLogitRep; ++r) {
-                unsigned long long* dst = p.logits + ((size_t)r * p.maxm + m) * p.E + 2 * t;
-                st_tagged(dst, ep, acc.g[m]);
-                st_tagged(dst + 1, ep, acc.u[m]);
-              }
-            }
-          }
-        }
-      } else {
-        const int slot = w.u + slot0;
-        const int j = w.j + iq;
-        const uint32_t mask = kind == ITEM_SHARED ? (1u << p.M) - 1u : rt.slot_mask[slot];
-        float gsg = 1.0f, gsu = 1.0f;
-        if (FMT == FMT_BF16) {
-          pair_dot_bf16<MAXM, true>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
-                                    reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
-                                    p.nchunk_h, xr.b, xs, mask, c.lane, acc);
-        } else {
-          const uint8_t* scb = st + (size_t)2 * nq * p.row13;
-          pair_dot_fp4<MAXM>(reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13),
-                             reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13),
-                             reinterpret_cast<const uint16_t*>(scb + (size_t)iq * p.sc13),
-                             reinterpret_cast<const uint16_t*>(scb + (size_t)(nq + iq) * p.sc13), p.nchunk_h,
-                             xr.h, xs, p.H, mask, c.lane, acc);
-          const int e = kind == ITEM_SHARED ? -1 - slot : rt.slot_e[slot];
-          const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
-          gsg = gs[0];
-          gsu = gs[1];
-        }
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-          if (c.lane == m && (mask >> m & 1u)) {
-            float h = silu_f32(acc.g[m] * gsg) * (acc.u[m] * gsu);
-            if (kind == ITEM_ROUTED) h *= rt.slot_w[slot * p.maxm + m];
-            const size_t at = ((size_t)slot * p.maxm + m) * p.I + j;
-            const size_t rep_stride = (size_t)p.nslot_max * p.maxm * p.I;
-#pragma unroll
-            for (int r = 0; r < kHRep; ++r) st_tagged(p.hbuf + r * rep_stride + at, ep, h);
-          }
-        }
+        for (int r = 0; r < kHRep; ++r) st_tagged(p.hbuf + r * rep_stride + at, ep, h);
       }
       __syncwarp();
       if (c.lane == 0) c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
