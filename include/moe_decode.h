@@ -205,8 +205,9 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
  *
  * Scratch: a file-scope device array of MOE_DECODE_STATIC_SCRATCH_BYTES that
  * every GPU loading the library holds until exit. Configs whose scratch
- * (control words, 4 copies of the M x E logits and 4 copies of S + min(E, M*k)
- * expert rows of M x I intermediate values as 8-byte words, one flag per SM) exceeds it
+ * (control words, 4 copies of the M x E logits as 8-byte words, 4 copies of the
+ * I fp32 intermediate values of each of the S*M + k*M (expert, row) pairs, one
+ * flag per SM) exceeds it
  * return MOE_ERR_UNSUPPORTED before any device work. The first call on a device
  * sets the array up (resolves its device address and fills it, a blocking
  * memset); make that first call before any CUDA stream capture. Every call
@@ -218,7 +219,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
  * status (MOE_OK or MOE_ERR_DEVICE_TIMEOUT), as moe_decode_run_host does.
  * Never calls cudaMalloc, cudaFree or any allocating library routine.
  */
-#define MOE_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+#define MOE_DECODE_STATIC_SCRATCH_BYTES (4u << 20)
 moe_status moe_decode_run_static(const moe_decode_config* cfg, const moe_decode_weights* w, const void* x,
                                  const void* residual, void* out, int32_t m_rows, int32_t* topk_idx,
                                  float* topk_w, moe_stream_t stream);

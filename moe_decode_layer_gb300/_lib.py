@@ -37,7 +37,7 @@ STAMP_NAMES = {0: "start", 1: "x_loaded", 2: "R_done", 3: "routed", 4: "U_done",
                6: "D_done", 8: "prod_R_issued", 9: "prod_route", 10: "prod_U_issued",
                11: "prod_D_issued", 12: "logits_seen", 13: "topk_row0", 14: "ucount_full",
                15: "router_data", 16: "rcount_add", 17: "U_first_data", 18: "rcount_full"}
-STAMP_COUNTS = {20: "h_poll_rounds(tid0)", 21: "logit_poll_rounds", 23: "sm_clock_mhz"}
+STAMP_COUNTS = {7: "D_hwait_us(t0)", 21: "logit_poll_rounds", 22: "D_wait_us(warp0)", 23: "sm_clock_mhz"}
 STAMP_SLOTS = 24
 MOE_INFO_GRID = 16
 MOE_INFO_THREADS = 17
@@ -46,7 +46,7 @@ MOE_INFO_RING_SLOTS = 19
 MOE_INFO_SLOT_BYTES = 20
 MOE_INFO_KERNELS_PER_RUN = 21
 MOE_INFO_SCRATCH_BYTES = 22
-STATIC_SCRATCH_BYTES = 8 << 20
+STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTS = ("moe_decode_config_check", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",
            "moe_decode_run_static",

@@ -100,6 +100,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.off_full = take(moe::kMaxSlots * 8, 8);
   p.off_empty = take(moe::kMaxSlots * 8, 8);
   p.off_xbar = take(8, 8);
+  p.off_hbar = take(16, 8);
   p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
   p.off_x = take((size_t)maxm * H * 2, 128);
   p.off_sel_e = take((size_t)maxm * K * 4, 4);
@@ -120,9 +121,12 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   // gate/up pair and one down stage of this CTA's rows
   const int rows_per_cta = (H + p.grid - 1) / p.grid;
   int drs = std::min(rows_per_cta, moe::kRpgMax * p.ng);
+  // a slot holds a whole number of gate/up pairs (about kStageTarget bytes), so
+  // that no slot space is left unused in the gate/up phases
+  const size_t q0 = std::max<size_t>(1, std::min<size_t>(moe::kNC, moe::kStageTarget / p.pair_bytes));
   size_t slot = 0;
   for (;;) {
-    slot = round_up(std::max({(size_t)moe::kStageTarget, (size_t)p.rpair_bytes, (size_t)p.pair_bytes,
+    slot = round_up(std::max({q0 * p.pair_bytes, (size_t)p.rpair_bytes, (size_t)p.pair_bytes,
                               (size_t)drs * (p.row2 + p.sc2)}), 128);
     if ((long long)(moe::kMinSlots * slot) <= avail - (long long)maxm * I * 4 || drs == 1) break;
     drs = (drs + 1) / 2;
@@ -134,6 +138,9 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   int hs_pairs = (int)std::min<long long>(p.npair_max, hs_room > 0 ? hs_room / (long long)per_pair : 0);
   if (hs_pairs < maxm) hs_pairs = maxm;
   p.hs_pairs = hs_pairs;
+  // all pairs at once; else two buffers (one batch lands while the other is in
+  // use) when each holds a full slot's rows; else one buffer
+  p.hs_nbuf = (hs_pairs < p.npair_max && hs_pairs >= 2 * maxm) ? 2 : 1;
   p.off_hs = (int)fixed;
   // routing scratch shares the h staging area (routing is over before any h is staged)
   size_t ro = fixed;
@@ -157,6 +164,10 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   if (ns < 2) return MOE_ERR_UNSUPPORTED;
   p.slot_bytes = (int)slot;
   p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
+  // the h area is idle from the end of routing until the down phase: the routed
+  // gate/up stages also use the slots that fit there
+  p.off_xslot = (int)fixed;
+  p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   p.d_rows_stage = drs;
   p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
   // router stages: at most kNC / 2 row pairs, so every row gets at least one warp
@@ -308,7 +319,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   };
   const size_t o_ctrl = take(moe::CTRL_WORDS * 4);
   const size_t o_logits = take(moe::kLogitRep * maxm * E * 8);
-  const size_t o_h = take((size_t)moe::kHRep * p.nslot_max * maxm * I * 8);
+  const size_t o_h = take((size_t)moe::kHRep * p.npair_max * I * 4);
   const size_t o_xf = take((size_t)p.grid * 8);
 
   const size_t tag_end = off;
@@ -351,7 +362,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   p.sh_w2_gs = w->sh_w2_gscale;
   p.ctrl = reinterpret_cast<uint32_t*>(base + o_ctrl);
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
-  p.hbuf = reinterpret_cast<unsigned long long*>(base + o_h);
+  p.hbuf = reinterpret_cast<float*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
 
   h->stage_x = reinterpret_cast<uint16_t*>(base + o_sx);

@@ -27,12 +27,20 @@
 //      bf16(residual + sum) with one rounding (blog section "PDL: ...": the combine
 //      is an fp32 sum with a single final cast).
 //
-// Hand-offs between CTAs carry no fence and no flag: every value is stored as a
+// Router logits pass between CTAs without a fence or a flag: every value is a
 // 64-bit word (run tag << 32 | fp32 bits) and readers poll until the tag equals
 // the current run's tag ("Muse Spark Open Ultrafast", section "Megakernel
 // internals", part 3: a GPU-scope fence with bulk loads in flight costs
 // microseconds, so the data carries its own readiness). The tag is a per-handle
-// counter that the last CTA of a run advances, so buffers are never reset.
+// counter that the last CTA of a run advances, so buffers are never reset. The
+// h values (I floats per (expert, row) pair, in pair order, four copies) are
+// released once per CTA by a fence and a count; after the count reaches the grid
+// size each CTA fetches its batches of pairs with one bulk copy each, the next
+// batch landing while the current one is in use.
+//
+// All device functions are inlined into the kernel: parameters are then read
+// from the kernel's parameter space and the helper objects stay in registers
+// (through a reference in a separate function both would be memory loads).
 //
 // Every wait (mbarrier, tagged poll) is bounded by the handle's wait limit; on
 // expiry the CTA records DEV_ERR_TIMEOUT in the status word, stops issuing
@@ -69,15 +77,20 @@ __device__ __forceinline__ void split_range(int n, int c, int g, int& lo, int& h
 
 // Position in the shared-memory ring: stage number, its slot and the slot's
 // mbarrier phase parity, advanced without divisions.
+// The slot count may differ between phases (the routed gate/up stages also use
+// the extra slots), so each slot keeps its own use parity.
 struct Ring {
   int seq = 0, slot = 0;
-  uint32_t phase = 0;
+  uint64_t par = 0;  // bit s: parity of slot s's current use
+  __device__ __forceinline__ uint32_t phase() const { return (uint32_t)(par >> slot) & 1u; }
   __device__ __forceinline__ void next(int nslots) {
     ++seq;
-    if (++slot == nslots) {
-      slot = 0;
-      phase ^= 1u;
-    }
+    par ^= 1ull << slot;
+    if (++slot >= nslots) slot = 0;
+  }
+  // Entering a phase with fewer slots: the next stage must be one of them.
+  __device__ __forceinline__ void fit(int nslots) {
+    if (slot >= nslots) slot = 0;
   }
 };
 
@@ -117,11 +130,16 @@ struct Ctx {
     atomicOr(&p.ctrl[CTRL_STATUS], DEV_ERR_TIMEOUT);
     atomicCAS(&p.ctrl[CTRL_WHERE], 0u, site);
   }
+  // Stop this CTA's waits without a status of its own (another CTA set one).
+  __device__ void abort_local() const { *reinterpret_cast<volatile int*>(misc + MISC_ABORT) = 1; }
   __device__ bool expired() const { return global_ns() - t0 > p.timeout_ns; }
   // Another CTA gave up: stop waiting on data it will never publish.
   __device__ bool peer_failed() const { return ld_relaxed_u32(&p.ctrl[CTRL_STATUS]) != 0; }
   __device__ uint32_t epoch() const { return static_cast<uint32_t>(misc[MISC_EPOCH]); }
-  __device__ uint8_t* slot_ptr(int slot) const { return sm + p.off_ring + (size_t)slot * p.slot_bytes; }
+  __device__ uint8_t* slot_ptr(int slot) const {
+    return slot < p.nslots ? sm + p.off_ring + (size_t)slot * p.slot_bytes
+                           : sm + p.off_xslot + (size_t)(slot - p.nslots) * p.slot_bytes;
+  }
   // Phase timestamp (one plain store; off unless the handle has a stamp buffer).
   __device__ void stamp(int ev) const {
     if (p.stamps) p.stamps[(size_t)blockIdx.x * kStampSlots + ev] = global_ns();
@@ -158,11 +176,11 @@ struct Ctx {
         }
       }
     }
-    return wait_bar(full0 + 8u * r.slot, r.phase, SITE_RING_FULL);
+    return wait_bar(full0 + 8u * r.slot, r.phase(), SITE_RING_FULL);
   }
   // Producer side: bounded wait for the slot of stage `r` to be free.
   __device__ bool wait_empty(const Ring& r) const {
-    return wait_bar(empty0 + 8u * r.slot, r.phase ^ 1u, SITE_RING_EMPTY);
+    return wait_bar(empty0 + 8u * r.slot, r.phase() ^ 1u, SITE_RING_EMPTY);
   }
   __device__ void release(const Ring& r, uint32_t count) const { mbar_arrive(empty0 + 8u * r.slot, count); }
 };
@@ -198,7 +216,7 @@ struct Route {
 __device__ __forceinline__ void count_done(const Params& p, int word) {
   asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p.ctrl + word) : "memory");
 }
-static __device__ __noinline__ bool wait_count(const Ctx& c, int word, uint32_t site) {
+static __device__ __forceinline__ bool wait_count(const Ctx& c, int word, uint32_t site) {
   const Params& p = c.p;
   const unsigned long long* cnt = reinterpret_cast<const unsigned long long*>(p.ctrl + word);
   for (uint32_t spin = 0; ld_relaxed_u64(cnt) < (unsigned long long)p.grid; ++spin) {
@@ -255,7 +273,7 @@ struct ItemWalk {
 // --------------------------------------------------------------------------
 // consumer: x rows (arrive by bulk copy; optionally RMS-normalised in place)
 // --------------------------------------------------------------------------
-static __device__ __noinline__ void prepare_x(const Ctx& c) {
+static __device__ __forceinline__ void prepare_x(const Ctx& c) {
   const Params& p = c.p;
   if (!c.wait_bar(c.xbar, 0, SITE_RING_FULL)) return;
   if (!p.pre_rmsnorm) return;
@@ -412,16 +430,6 @@ __device__ __forceinline__ void dot32_fp4(float& acc, const uint4 q, uint32_t sc
   acc = fmaf(s1, part[1], acc);
 }
 
-// bf16 x chunk (8 values) -> 4 fp16x2 words (exact for |x| in the fp16 range).
-__device__ __forceinline__ void bf16x8_to_f16x8(const uint4 v, uint32_t* o) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __half2 h = __floats2half2_rn(bf16lo(w[q]), bf16hi(w[q]));
-    o[q] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-}
-
 // NVFP4 rows a, b (codes qa, qb; scales sa, sb) against one x row held in the
 // lane's registers as fp16 (16 words per 32-element chunk).
 __device__ __forceinline__ RowSums dot_one_fp4(const uint4* qa, const uint4* qb, const uint16_t* sa,
@@ -440,7 +448,7 @@ __device__ __forceinline__ RowSums dot_one_fp4(const uint4* qa, const uint4* qb,
   return r;
 }
 
-// NVFP4 rows a, b against the N bf16 x rows of `mask` in shared memory.
+// NVFP4 rows a, b against the N fp16 x rows of `mask` in shared memory.
 template <int N>
 __device__ __forceinline__ RowSums dot_rows_fp4(const uint4* qa, const uint4* qb, const uint16_t* sa,
                                                 const uint16_t* sb, int nch, const uint4* xs, int H,
@@ -464,7 +472,13 @@ __device__ __forceinline__ RowSums dot_rows_fp4(const uint4* qa, const uint4* qb
     for (int k = 0; k < N; ++k) {
       uint32_t xh[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(xp[k][ch * 4 + q], xh + 4 * q);
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = xp[k][ch * 4 + q];
+        xh[4 * q] = v.x;
+        xh[4 * q + 1] = v.y;
+        xh[4 * q + 2] = v.z;
+        xh[4 * q + 3] = v.w;
+      }
       dot32_fp4(g[k], va, s_a, xh);
       dot32_fp4(u[k], vb, s_b, xh);
     }
@@ -550,15 +564,33 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
       const int ch = c.lane + 32 * i;
       xr.b[i] = ch < nch8 ? xs[ch] : make_uint4(0, 0, 0, 0);
     }
-  } else {
+  } else {  // x rows are fp16 by now
 #pragma unroll
     for (int i = 0; i < kCplFp4; ++i) {
       const int ch = c.lane + 32 * i;  // 32-element chunk
       if (ch < p.H / 32) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(xs[ch * 4 + q], &xr.h[16 * i + 4 * q]);
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = xs[ch * 4 + q];
+          xr.h[16 * i + 4 * q] = v.x;
+          xr.h[16 * i + 4 * q + 1] = v.y;
+          xr.h[16 * i + 4 * q + 2] = v.z;
+          xr.h[16 * i + 4 * q + 3] = v.w;
+        }
       }
     }
+  }
+}
+
+// NVFP4 experts multiply e2m1 codes (exact in fp16) with fp16 activations:
+// once the bf16 router no longer needs them, the CTA's x rows are converted in
+// place (exact for values inside the fp16 range).
+static __device__ __forceinline__ void x_to_f16(const Ctx& c) {
+  uint32_t* xw = reinterpret_cast<uint32_t*>(c.sm + c.p.off_x);
+  for (int i = c.tid; i < c.p.M * c.p.H / 2; i += kNC * 32) {
+    const uint32_t v = xw[i];
+    const __half2 h = __floats2half2_rn(bf16lo(v), bf16hi(v));
+    xw[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
 }
 
@@ -566,7 +598,7 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
 // of them wait for all logits), so the CTA's few router rows are each split
 // over several consumer warps along H; the partial sums meet in shared memory.
 template <int MAXM>
-__device__ __noinline__ Ring consume_router(const Ctx& c, Ring ring) {
+__device__ __forceinline__ Ring consume_router(const Ctx& c, Ring ring) {
   const Params& p = c.p;
   int lo, hi;
   split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
@@ -574,6 +606,7 @@ __device__ __noinline__ Ring consume_router(const Ctx& c, Ring ring) {
   float* part = reinterpret_cast<float*>(c.sm + p.off_red);  // [kNC][8]
   const uint32_t ep = c.epoch();
   const int nch = p.H / 8;
+  ring.fit(p.nslots);
   for (ItemWalk w(lo, hi, p.qr, 0); w.more(); ring.next(p.nslots)) {
     const int nq = w.count();
     const int nrow = 2 * nq;  // <= kNC: the planner keeps qr <= kNC / 2
@@ -623,20 +656,21 @@ enum ItemKind : int { ITEM_SHARED = 1, ITEM_ROUTED = 2 };
 // One phase of gate/up items (shared experts' or routed experts' row pairs):
 // each consumer warp takes its items of every stage, computes the dot products
 // against the rows of x that chose the expert and publishes tagged h values.
-// Returns the ring position after the phase. Not inlined: both phases share it.
+// Returns the ring position after the phase.
 template <int FMT, int MAXM>
-__device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring) {
+__device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring) {
   const Params& p = c.p;
   const int n = kind == ITEM_SHARED ? p.S * p.I : c.misc[MISC_NROUTED] * p.I;
   int lo, hi;
   split_range(n, blockIdx.x, p.grid, lo, hi);
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
-  const uint32_t ep = c.epoch();
   const int slot0 = kind == ITEM_ROUTED ? p.S : 0;
-  const size_t rep_stride = (size_t)p.nslot_max * p.maxm * p.I;
+  const size_t rep_stride = (size_t)p.npair_max * p.I;
   XRegs<FMT, MAXM> xr;
   load_xregs<FMT, MAXM>(c, xr);
-  for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(p.nslots)) {
+  const int nsl_ring = kind == ITEM_ROUTED ? p.nslots + p.nslots_x : p.nslots;
+  ring.fit(nsl_ring);
+  for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(nsl_ring)) {
     const int nq = w.count();
     const int iq = w.offset(c.warp);
     if (iq < nq && !c.aborted() && c.wait_full(ring)) {
@@ -646,19 +680,25 @@ __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int ki
       const int j = w.j + iq;
       const uint32_t mask = kind == ITEM_SHARED ? (1u << p.M) - 1u : rt.slot_mask[slot];
       const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane);
-      float gsg = 1.0f, gsu = 1.0f;
+      float gsg = 1.0f, gsu = 1.0f, gs2 = 1.0f;
       if (FMT == FMT_NVFP4) {
         const int e = kind == ITEM_SHARED ? -1 - slot : rt.slot_e[slot];
         const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
         gsg = gs[0];
         gsu = gs[1];
+        gs2 = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];  // the down weights' tensor scale, applied once here
       }
       if (rs.m >= 0) {
         float h = silu_f32(rs.g * gsg) * (rs.u * gsu);
         if (kind == ITEM_ROUTED) h *= rt.slot_w[slot * p.maxm + rs.m];
-        const size_t at = ((size_t)slot * p.maxm + rs.m) * p.I + j;
+        if (FMT == FMT_NVFP4) h *= gs2;
+        // pair index: a shared slot holds every row (pairs s * M + m); a routed
+        // slot's rows follow its pair base in ascending order
+        const int pair = kind == ITEM_SHARED ? slot * p.M + rs.m
+                                             : rt.pair_base[slot] + __popc(mask & ((1u << rs.m) - 1u));
+        const size_t at = (size_t)pair * p.I + j;
 #pragma unroll
-        for (int r = 0; r < kHRep; ++r) st_tagged(p.hbuf + r * rep_stride + at, ep, h);
+        for (int r = 0; r < kHRep; ++r) p.hbuf[r * rep_stride + at] = h;
       }
       __syncwarp();
       if (c.lane == 0) c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
@@ -674,7 +714,7 @@ __device__ __noinline__ Ring consume_items(const Ctx& c, const Route& rt, int ki
 // Copies n 16-byte units of tagged words (two fp32 values each) from src to dst
 // in shared memory: every consumer thread keeps kStageBatch loads in flight and
 // re-polls only the units whose tag is not current yet. False on abort / timeout.
-static __device__ __noinline__ bool stage_tagged(const Ctx& c, const unsigned long long* src, float* dst, int n,
+static __device__ __forceinline__ bool stage_tagged(const Ctx& c, const unsigned long long* src, float* dst, int n,
                                                  uint32_t site) {
   const uint32_t ep = c.epoch();
   uint32_t spins = 0;
@@ -908,7 +948,7 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
   }
 }
 
-static __device__ __noinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
+static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
   const Params& p = c.p;
   // every CTA's router logits stored (count), before reading any of them
   if (c.tid == 0) {
@@ -945,7 +985,7 @@ __device__ __forceinline__ void cta_rows(const Params& p, int& r_lo, int& r_hi) 
 
 // Wait until every CTA has its copy of x (only needed when the output
 // overwrites x in the single-kernel schedule).
-static __device__ __noinline__ bool wait_xflags(const Ctx& c) {
+static __device__ __forceinline__ bool wait_xflags(const Ctx& c) {
   const Params& p = c.p;
   const uint32_t ep = c.epoch();
   uint64_t spins = 0;
@@ -963,63 +1003,26 @@ static __device__ __noinline__ bool wait_xflags(const Ctx& c) {
   return true;
 }
 
-// Copies the h rows of slots [sl0, sl1) (tagged, produced by all CTAs) into hs
-// in (slot, row) pair order, kStageBatch 16-byte loads in flight per thread,
-// re-polling only the words whose tag is not current yet. False on abort /
-// timeout.
-static __device__ __noinline__ bool stage_h(const Ctx& c, const Route& rt, float* hs, int sl0, int sl1) {
+// Down-phase batches: slots [sl0, sl1) whose (expert, row) pairs fit one h
+// buffer of `cap` pairs.
+__device__ __forceinline__ int batch_end(const Route& rt, int sl0, int nsl, int cap) {
+  int sl1 = sl0 + 1;
+  while (sl1 < nsl && rt.pair_base[sl1 + 1] - rt.pair_base[sl0] <= cap) ++sl1;
+  return sl1;
+}
+
+// The h values of the pairs of slots [sl0, sl1) -- contiguous in pair order --
+// from this CTA's copy of the h buffer into shared h buffer b: one bulk copy
+// counted on the buffer's mbarrier. Thread 0 only.
+__device__ __forceinline__ void issue_h(const Ctx& c, const Route& rt, int sl0, int sl1, int b, int cap) {
   const Params& p = c.p;
-  const uint32_t ep = c.epoch();
   const int p0 = rt.pair_base[sl0];
-  const int half = p.I / 2;
-  const int n = (rt.pair_base[sl1] - p0) * half;  // 16-byte units
-  const int* psr = reinterpret_cast<const int*>(c.sm + p.off_pair_sr);
-  const unsigned long long* hrep =
-      p.hbuf + (size_t)(blockIdx.x % kHRep) * p.nslot_max * p.maxm * p.I;  // this CTA's copy
-  uint64_t spins = 0;
-  for (int base = c.tid; base < n; base += kNC * 32 * kStageBatch) {
-    uint32_t pending = 0;
-    const unsigned long long* src[kStageBatch];
-    float* dst[kStageBatch];
-#pragma unroll
-    for (int k = 0; k < kStageBatch; ++k) {
-      const int u = base + k * kNC * 32;
-      src[k] = hrep;
-      dst[k] = hs;
-      if (u < n) {
-        const int pr = u / half, kk = 2 * (u - pr * half);
-        const int sr = psr[p0 + pr];
-        src[k] = hrep + ((size_t)(sr >> 4) * p.maxm + (sr & 15)) * p.I + kk;
-        dst[k] = hs + (size_t)pr * p.I + kk;
-        pending |= 1u << k;
-      }
-    }
-    while (pending) {
-      if (c.tid == 0) c.count(ST_H_ROUNDS, 1);
-      unsigned long long v0[kStageBatch], v1[kStageBatch];
-#pragma unroll
-      for (int k = 0; k < kStageBatch; ++k) {
-        v0[k] = v1[k] = 0;
-        if (pending >> k & 1u) ld_tagged2(src[k], v0[k], v1[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < kStageBatch; ++k) {
-        if ((pending >> k & 1u) && (uint32_t)(v0[k] >> 32) == ep && (uint32_t)(v1[k] >> 32) == ep) {
-          dst[k][0] = __uint_as_float((uint32_t)v0[k]);
-          dst[k][1] = __uint_as_float((uint32_t)v1[k]);
-          pending &= ~(1u << k);
-        }
-      }
-      if (!pending) break;
-      __nanosleep(32);
-      if (c.aborted() || ((++spins & 63) == 0 && c.peer_failed())) return false;
-      if (c.expired()) {
-        c.fail(SITE_HIDDEN);
-        return false;
-      }
-    }
-  }
-  return true;
+  const uint32_t bytes = (uint32_t)(rt.pair_base[sl1] - p0) * (uint32_t)p.I * 4u;
+  const float* src = p.hbuf + ((size_t)(blockIdx.x % kHRep) * p.npair_max + p0) * p.I;
+  float* dst = reinterpret_cast<float*>(c.sm + p.off_hs) + (size_t)b * cap * p.I;
+  const uint32_t bar = smem_u32(c.sm + p.off_hbar) + 8u * b;
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_g2s_plain(smem_u32(dst), src, bytes, bar);
 }
 
 // wait_u: the gate/up results come from this same kernel (single-kernel schedule)
@@ -1035,17 +1038,41 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
   const int g = ctid / p.tg;   // thread group
   const int ch = ctid % p.tg;  // 16-byte code chunk of a down row
   const bool active = g < p.ng;
-  float* hs = reinterpret_cast<float*>(c.sm + p.off_hs);
+  const float* hs0 = reinterpret_cast<const float*>(c.sm + p.off_hs);
   float* red = reinterpret_cast<float*>(c.sm + p.off_red);
+  const uint32_t hbar0 = smem_u32(c.sm + p.off_hbar);
+  const int nbuf = p.hs_nbuf, cap = p.hs_pairs / nbuf;
   constexpr int CH_EL = FMT == FMT_BF16 ? 8 : 32;  // elements per chunk
-  bool first_batch = true;
-  if (nrb > 0 && wait_u) {
-    if (c.tid == 0) {
-      if (!c.aborted()) wait_count(c, CTRL_UCOUNT, SITE_FLAGS);
-      c.stamp(ST_U_FLAGS);
+  // Thread 0 keeps the next nbuf batches of h in flight: batch uses run over
+  // (row block, batch) in order; use u goes to buffer u % nbuf.
+  int a_rb = 0, a_sl = 0, issued = 0, landed = 0;
+  auto issue_next = [&]() {
+    const int sl1 = batch_end(rt, a_sl, nsl, cap);
+    issue_h(c, rt, a_sl, sl1, issued % nbuf, cap);
+    ++issued;
+    a_sl = sl1;
+    if (a_sl >= nsl) {
+      a_sl = 0;
+      ++a_rb;
     }
+  };
+  if (nrb > 0) {
+    fence_proxy_async_shared();  // generic accesses to the h area (routing scratch) before the copies into it
     bar_sync(kBarConsumers, kNC * 32);
+    if (c.tid == 0) {
+      bool ok = !c.aborted();
+      if (ok && wait_u) {
+        ok = wait_count(c, CTRL_UCOUNT, SITE_FLAGS);
+        if (!ok) c.abort_local();
+      }
+      c.stamp(ST_U_FLAGS);
+      __threadfence();             // acquire every CTA's h stores ...
+      fence_proxy_async_global();  // ... for the bulk copies that read them
+      for (int b = 0; ok && b < nbuf && a_rb < nrb; ++b) issue_next();
+    }
   }
+  int used = 0;
+  ring.fit(p.nslots);
   for (int rb = 0; rb < nrb; ++rb) {
     const int rb_lo = r_lo + rb * drs;
     const int nr = min(drs, r_hi - rb_lo);
@@ -1055,24 +1082,21 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
 #pragma unroll
       for (int m = 0; m < MAXM; ++m) acc[ri][m] = 0.0f;
     for (int sl0 = 0; sl0 < nsl;) {
-      // the batch of slots whose h rows fit in hs at once
-      int sl1 = sl0 + 1;
-      while (sl1 < nsl && rt.pair_base[sl1 + 1] - rt.pair_base[sl0] <= p.hs_pairs) ++sl1;
-      if (!first_batch) bar_sync(kBarConsumers, kNC * 32);  // hs is free again
-      first_batch = false;
-      if (!c.aborted()) stage_h(c, rt, hs, sl0, sl1);
-      bar_sync(kBarConsumers, kNC * 32);
+      const int sl1 = batch_end(rt, sl0, nsl, cap);
+      const int b = used % nbuf;
+      const uint64_t th = p.stamps ? global_ns() : 0;
+      const bool have = !c.aborted() && c.wait_bar(hbar0 + 8u * b, (uint32_t)(used / nbuf) & 1u, SITE_HIDDEN);
+      if (p.stamps && c.tid == 0) c.count(ST_D_HWAIT_NS, global_ns() - th);
+      if (have && c.tid == 0) landed = used + 1;
+      const float* hs = hs0 + (size_t)b * cap * p.I;
       if (rb == 0 && sl0 == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
       for (int sl = sl0; sl < sl1; ++sl, ring.next(p.nslots)) {
         const uint32_t mask = rt.slot_mask[sl];
+        const uint64_t tw = p.stamps ? global_ns() : 0;
         const bool got = !c.aborted() && c.wait_full(ring);
-        if (got && active) {
+        if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, global_ns() - tw);
+        if (got && have && active) {
           const uint8_t* st = c.slot_ptr(ring.slot);
-          float gsc = 1.0f;
-          if (FMT == FMT_NVFP4) {
-            const int e = rt.slot_e[sl];
-            gsc = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];
-          }
           int hp = rt.pair_base[sl] - rt.pair_base[sl0];
 #pragma unroll
           for (int m = 0; m < MAXM; ++m) {
@@ -1083,10 +1107,10 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
 #pragma unroll
             for (int q = 0; q < CH_EL / 4; ++q) {
               const float4 f = hq[q];
-              hv[4 * q] = f.x * gsc;
-              hv[4 * q + 1] = f.y * gsc;
-              hv[4 * q + 2] = f.z * gsc;
-              hv[4 * q + 3] = f.w * gsc;
+              hv[4 * q] = f.x;
+              hv[4 * q + 1] = f.y;
+              hv[4 * q + 2] = f.z;
+              hv[4 * q + 3] = f.w;
             }
 #pragma unroll
             for (int ri = 0; ri < kRpgMax; ++ri) {
@@ -1127,6 +1151,9 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         __syncwarp();
         if (got && c.lane == 0) c.release(ring, 1);
       }
+      bar_sync(kBarConsumers, kNC * 32);  // h buffer b is free again
+      if (c.tid == 0 && !c.aborted() && a_rb < nrb) issue_next();
+      ++used;
       sl0 = sl1;
     }
     // Reduce each row's partial sums over the group's threads and write out.
@@ -1185,6 +1212,14 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
       bar_sync(kBarConsumers, kNC * 32);
     }
   }
+  // after an abort: h batches issued but not seen landing must land before exit
+  if (c.tid == 0) {
+    const uint64_t t = global_ns();
+    for (int u = landed; u < issued; ++u) {
+      while (!mbar_try_wait(hbar0 + 8u * (u % nbuf), (uint32_t)(u / nbuf) & 1u) && global_ns() - t < p.timeout_ns) {
+      }
+    }
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -1194,7 +1229,7 @@ struct Producer {
   const Ctx& c;
   uint64_t pol;
   Ring ring;            // next stage to issue
-  int issued = 0;       // stages whose copies were issued
+  uint64_t used = 0;    // slots that received copies
   __device__ Producer(const Ctx& cc) : c(cc) { pol = policy_evict_first(); }
 
   // Claims the next stage's slot and announces its bytes. False on abort.
@@ -1204,7 +1239,7 @@ struct Producer {
     bar = c.full0 + 8u * ring.slot;
     c.slot_seq[ring.slot] = ring.seq;  // before arming: see Ctx::wait_full
     mbar_arrive_expect_tx(bar, bytes);
-    issued = ring.seq + 1;
+    used |= 1ull << ring.slot;
     return true;
   }
 
@@ -1220,6 +1255,7 @@ struct Producer {
     const Params& p = c.p;
     int lo, hi;
     split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
+    ring.fit(p.nslots);
     for (ItemWalk w(lo, hi, p.qr, 0); w.more(); ring.next(p.nslots)) {
       const int nq = w.count();
       const uint32_t bytes = (uint32_t)nq * p.rpair_bytes;
@@ -1243,7 +1279,9 @@ struct Producer {
     const int n = shared_phase ? p.S * p.I : c.misc[MISC_NROUTED] * p.I;
     int lo, hi;
     split_range(n, blockIdx.x, p.grid, lo, hi);
-    for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(p.nslots)) {
+    const int nsl_ring = shared_phase ? p.nslots : p.nslots + p.nslots_x;
+    ring.fit(nsl_ring);
+    for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(nsl_ring)) {
       const int nq = w.count();
       const int slot = w.u + (shared_phase ? 0 : p.S);
       uint32_t dst, bar;
@@ -1272,6 +1310,7 @@ struct Producer {
     cta_rows(p, r_lo, r_hi);
     const int rb_lo = r_lo + rb * p.d_rows_stage;
     const int nr = min(p.d_rows_stage, r_hi - rb_lo);
+    ring.fit(p.nslots);
     for (int sl = sl_lo; sl < sl_hi; ++sl) {
       const int e = sl < p.S ? -1 - sl : rt.slot_e[sl];
       const uint8_t* wt = e >= 0 ? p.w2 : p.sh_w2;
@@ -1306,15 +1345,15 @@ struct Producer {
     }
   }
 
-  // Before exit: wait (bounded) for this CTA's copies still in flight: the last
-  // nslots issued stages, each the newest use of its slot.
+  // Before exit: wait (bounded) for this CTA's copies still in flight: the
+  // newest use of every slot that received copies.
   __device__ void drain() {
     const Params& p = c.p;
-    const int first = issued > p.nslots ? issued - p.nslots : 0;
     const uint64_t t = global_ns();
-    for (int q = first; q < issued; ++q) {
-      const uint32_t bar = c.full0 + 8u * (uint32_t)(q % p.nslots);
-      const uint32_t par = (uint32_t)((q / p.nslots) & 1);
+    for (uint64_t u = used; u; u &= u - 1) {
+      const int s = __ffsll((long long)u) - 1;
+      const uint32_t bar = c.full0 + 8u * (uint32_t)s;
+      const uint32_t par = (uint32_t)((ring.par >> s) & 1u) ^ 1u;  // the parity of its last use
       while (!mbar_try_wait(bar, par)) {
         if (global_ns() - t > p.timeout_ns) {
           c.fail(SITE_DRAIN);
@@ -1342,12 +1381,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
 
   if (kChain) pdl_launch_dependents();
   if (c.tid == 0) {
-    for (int i = 0; i < p.nslots; ++i) {
+    for (int i = 0; i < p.nslots + p.nslots_x; ++i) {
       mbar_init(c.full0 + 8u * i, 1);
       mbar_init(c.empty0 + 8u * i, kNC);
       c.slot_seq[i] = -1;
     }
     mbar_init(c.xbar, 1);
+    mbar_init(smem_u32(sm + p.off_hbar), 1);
+    mbar_init(smem_u32(sm + p.off_hbar) + 8u, 1);
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;
     c.misc[MISC_NROUTED] = 0;
@@ -1431,18 +1472,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       bar_arrive(kBarRoute, kThreads);
       if (c.tid == 0) c.stamp(ST_ROUTED);
     }
+    if (FMT == FMT_NVFP4 && kNeedX) {  // the router is done with the bf16 x rows
+      x_to_f16(c);
+      bar_sync(kBarConsumers, kNC * 32);
+    }
     if (PHASES & PH_R) {
       // shared experts' gate/up stages were issued before routing
       ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring);
+      fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
       if (c.tid == 0) c.stamp(ST_R_DONE);
     }
     if (PHASES & PH_U) {
       ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTED, ring);
+      fence_proxy_async_global();
       if (c.tid == 0) c.stamp(ST_U_DONE);
     }
     if (PHASES & PH_U) {
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's h rows are all stored
-      if (c.tid == 0) count_done(p, CTRL_UCOUNT);
+      if (c.tid == 0) {
+        __threadfence();  // release them with the count
+        count_done(p, CTRL_UCOUNT);
+      }
     }
     if (PHASES & PH_D)
       consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, PHASES == PH_ALL, ring);

@@ -62,8 +62,9 @@ enum Stamp : int {
   ST_RFLAG = 16,      // this CTA counted its router logits as stored
   ST_U_DATA = 17,     // warp 0's first routed gate/up stage landed
   ST_RCOUNT = 18,     // the router-done count reached the grid size
-  ST_H_ROUNDS = 20,   // (count, not a time) poll rounds of the h staging
+  ST_D_HWAIT_NS = 7,     // (sum, thread 0) ns waiting for h batches in the down phase
   ST_LOGIT_ROUNDS = 21,  // (count) poll rounds of the logits
+  ST_D_WAIT_NS = 22,     // (sum, warp 0) ns down-phase warp 0 waited for its stages
   ST_CLOCK_MHZ = 23,  // (value) SM clock cycles per microsecond over the kernel
   kStampSlots = 24
 };
@@ -99,7 +100,7 @@ struct Params {
   float* topk_w;
   // scratch (device, owned by the handle)
   unsigned long long* logits;  // [kLogitRep][maxm][E] tagged
-  unsigned long long* hbuf;    // [kHRep][nslot_max][maxm][I] tagged
+  float* hbuf;                 // [kHRep][npair_max][I]: h of each (expert, row) pair, pair order
   unsigned long long* xflags;  // [grid] tagged: this CTA has read x
   uint32_t* ctrl;              // CTRL_WORDS
   int out_aliases_x;
@@ -117,8 +118,12 @@ struct Params {
   int grid;
   int nslot_max;     // S + min(E, maxm * K)
   int npair_max;     // S * maxm + maxm * K: (expert, row) pairs with an h row
-  int hs_pairs;      // h rows the down phase stages in shared memory at once
+  int hs_pairs;      // h rows (pairs) the down phase holds in shared memory
+  int hs_nbuf;       // 1: one batch buffer of hs_pairs; 2: two of hs_pairs / 2 (next batch in flight)
   // shared-memory offsets from the aligned base
+  int off_hbar;      // [2] mbarriers of the h batch buffers
+  int nslots_x;      // extra ring slots for the routed gate/up stages, in the h area
+  int off_xslot;     // first extra slot (slots nslots .. nslots + nslots_x - 1)
   int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
   int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;
   int off_lg, off_cand, off_lmax, off_ccount, off_thr, off_wtmp, off_wpc;  // routing scratch (in the hs area)

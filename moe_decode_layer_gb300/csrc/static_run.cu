@@ -73,7 +73,7 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   const size_t maxm = cfg->max_rows, E = cfg->num_experts, I = cfg->inter;
   const size_t o_logits = kCtrlBytes;
   const size_t o_h = o_logits + round256((size_t)moe::kLogitRep * maxm * E * 8);
-  const size_t o_xf = o_h + round256((size_t)moe::kHRep * p.nslot_max * maxm * I * 8);
+  const size_t o_xf = o_h + round256((size_t)moe::kHRep * p.npair_max * I * 4);
   const size_t need = o_xf + round256((size_t)p.grid * 8);
   if (need > MOE_DECODE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
   if ((st = moe::check_weights_host(*cfg, w)) != MOE_OK) return st;
@@ -83,7 +83,7 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   moe::bind_weights_host(*w, p);
   p.ctrl = reinterpret_cast<uint32_t*>(base);
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
-  p.hbuf = reinterpret_cast<unsigned long long*>(base + o_h);
+  p.hbuf = reinterpret_cast<float*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
   p.M = m_rows;
   p.x = static_cast<const uint16_t*>(x);

@@ -61,8 +61,9 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
         if rf and ls:
             derived.setdefault("last_rcount_add", []).append((max(rf) - t0) / 1000.0)
             derived.setdefault("first_logits_seen", []).append((min(ls) - t0) / 1000.0)
-        for k in _lib.STAMP_COUNTS:
-            per_count[k].extend(v for v in st[:, k].tolist() if v)
+        for k, name in _lib.STAMP_COUNTS.items():
+            scale = 1e-3 if "_us" in name else 1.0  # ns sums shown in microseconds
+            per_count[k].extend(v * scale for v in st[:, k].tolist() if v)
     for md in mods:
         md.set_option(_lib.MOE_OPT_STAMPS, 0)
         assert md.status() == _lib.MOE_OK

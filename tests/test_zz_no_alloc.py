@@ -79,7 +79,8 @@ def test_static_entry_rejects_oversized_scratch():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = _lib.load()
-    # 8 rows x (16 + 1) x 1024 ... : the expert rows alone need far more than the array
+    # 8 rows x (16 routed + 1 shared) experts x 3072 fp32 h values in 4 copies: 6.7 MB,
+    # more than the array holds; the layout itself fits in shared memory
     big = _lib.Config(hidden=1024, inter=3072, num_experts=1024, top_k=16, num_shared=1, max_rows=8,
                       wdtype=0, score=0, routed_scale=1.0, pre_rmsnorm=0, rms_eps=1e-6, sched=0)
     w = _lib.Weights()
