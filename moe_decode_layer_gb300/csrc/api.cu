@@ -120,7 +120,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   // ring slot: one stage of ~kStageTarget bytes, at least one router pair, one
   // gate/up pair and one down stage of this CTA's rows
   const int rows_per_cta = (H + p.grid - 1) / p.grid;
-  int drs = std::min(rows_per_cta, moe::kRpgMax * p.ng);
+  int drs = std::min(rows_per_cta, moe::rows_per_group(p.fmt) * p.ng);
   // a slot holds a whole number of gate/up pairs (about kStageTarget bytes), so
   // that no slot space is left unused in the gate/up phases
   const size_t q0 = std::max<size_t>(1, std::min<size_t>(moe::kNC, moe::kStageTarget / p.pair_bytes));
@@ -166,6 +166,10 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
   // the h area is idle from the end of routing until the down phase: the routed
   // gate/up stages also use the slots that fit there
+  // routed gate/up items are split by cost: streaming the pair plus the FMA work
+  // of each row that chose the expert (measured on GB300: an extra row adds ~1/8
+  // of a bf16 item's time and ~1/3 of an NVFP4 item's)
+  p.item_base = p.fmt == moe::FMT_BF16 ? 8 : 2;
   p.off_xslot = (int)fixed;
   p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   p.d_rows_stage = drs;

@@ -660,9 +660,13 @@ enum ItemKind : int { ITEM_SHARED = 1, ITEM_ROUTED = 2 };
 template <int FMT, int MAXM>
 __device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring) {
   const Params& p = c.p;
-  const int n = kind == ITEM_SHARED ? p.S * p.I : c.misc[MISC_NROUTED] * p.I;
   int lo, hi;
-  split_range(n, blockIdx.x, p.grid, lo, hi);
+  if (kind == ITEM_SHARED) {
+    split_range(p.S * p.I, blockIdx.x, p.grid, lo, hi);
+  } else {
+    lo = c.misc[MISC_ULO];
+    hi = c.misc[MISC_UHI];
+  }
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
   const int slot0 = kind == ITEM_ROUTED ? p.S : 0;
   const size_t rep_stride = (size_t)p.npair_max * p.I;
@@ -696,7 +700,11 @@ __device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int
         // slot's rows follow its pair base in ascending order
         const int pair = kind == ITEM_SHARED ? slot * p.M + rs.m
                                              : rt.pair_base[slot] + __popc(mask & ((1u << rs.m) - 1u));
-        const size_t at = (size_t)pair * p.I + j;
+        // NVFP4: within a pair the values are interleaved for the down phase's
+        // 32-element chunks (element e of chunk c at (e / 4) * 4 * tg + 4 * c + e % 4),
+        // so each 16-byte read of a warp is contiguous; bf16 keeps the natural order
+        size_t at = (size_t)pair * p.I + j;
+        if (FMT == FMT_NVFP4) at = (size_t)pair * p.I + (size_t)((j % 32) >> 2) * (4 * p.tg) + 4 * (j / 32) + (j & 3);
 #pragma unroll
         for (int r = 0; r < kHRep; ++r) p.hbuf[r * rep_stride + at] = h;
       }
@@ -946,6 +954,30 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
     rt.pair_base[nsl] = carry;
     c.misc[MISC_NROUTED] = total;
   }
+  __syncwarp();
+  // This CTA's routed gate/up items [lo, hi) of the slot-major item sequence,
+  // balanced by cost: an item of a slot chosen by N rows costs item_base + N
+  // (its bytes plus the FMA work of its rows). The cost up to routed slot u is
+  // I * (item_base * u + pairs before it); the boundary at cost t is the first
+  // item that starts at or after t, so adjacent CTAs' ranges meet exactly.
+  if (c.lane == 0) {
+    const int* pb = rt.pair_base + p.S;
+    const uint32_t I = (uint32_t)p.I, base = (uint32_t)p.item_base;
+    auto cum = [&](int u) { return I * (base * (uint32_t)u + (uint32_t)(pb[u] - pb[0])); };
+    auto item_at = [&](uint32_t t) {
+      int lo = 0, hi = total;  // largest u in [0, total] with cum(u) <= t
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum(mid) <= t) lo = mid; else hi = mid - 1;
+      }
+      if (lo == total) return total * p.I;
+      const uint32_t w = base + (uint32_t)(pb[lo + 1] - pb[lo]);
+      return lo * p.I + (int)((t - cum(lo) + w - 1) / w);
+    };
+    const uint32_t tot = cum(total);  // <= 2^23: the products below stay in 32 bits
+    c.misc[MISC_ULO] = item_at(tot * blockIdx.x / (uint32_t)p.grid);
+    c.misc[MISC_UHI] = item_at(tot * (blockIdx.x + 1) / (uint32_t)p.grid);
+  }
 }
 
 static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
@@ -1042,7 +1074,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
   float* red = reinterpret_cast<float*>(c.sm + p.off_red);
   const uint32_t hbar0 = smem_u32(c.sm + p.off_hbar);
   const int nbuf = p.hs_nbuf, cap = p.hs_pairs / nbuf;
-  constexpr int CH_EL = FMT == FMT_BF16 ? 8 : 32;  // elements per chunk
+  constexpr int RPG = rows_per_group(FMT);  // rows per thread group and stage
   // Thread 0 keeps the next nbuf batches of h in flight: batch uses run over
   // (row block, batch) in order; use u goes to buffer u % nbuf.
   int a_rb = 0, a_sl = 0, issued = 0, landed = 0;
@@ -1076,9 +1108,9 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
   for (int rb = 0; rb < nrb; ++rb) {
     const int rb_lo = r_lo + rb * drs;
     const int nr = min(drs, r_hi - rb_lo);
-    float acc[kRpgMax][MAXM];
+    float acc[RPG][MAXM];
 #pragma unroll
-    for (int ri = 0; ri < kRpgMax; ++ri)
+    for (int ri = 0; ri < RPG; ++ri)
 #pragma unroll
       for (int m = 0; m < MAXM; ++m) acc[ri][m] = 0.0f;
     for (int sl0 = 0; sl0 < nsl;) {
@@ -1101,47 +1133,54 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
 #pragma unroll
           for (int m = 0; m < MAXM; ++m) {
             if (!(mask >> m & 1u)) continue;
-            float hv[CH_EL];
-            const float4* hq = reinterpret_cast<const float4*>(hs + (size_t)hp * p.I + ch * CH_EL);
+            const float* hrow = hs + (size_t)hp * p.I;
             ++hp;
+            if (FMT == FMT_BF16) {
+              const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
+              const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
+              const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int q = 0; q < CH_EL / 4; ++q) {
-              const float4 f = hq[q];
-              hv[4 * q] = f.x;
-              hv[4 * q + 1] = f.y;
-              hv[4 * q + 2] = f.z;
-              hv[4 * q + 3] = f.w;
-            }
-#pragma unroll
-            for (int ri = 0; ri < kRpgMax; ++ri) {
-              const int r = g + ri * p.ng;
-              if (r < nr) {
-                if (FMT == FMT_BF16) {
+              for (int ri = 0; ri < RPG; ++ri) {
+                const int r = g + ri * p.ng;
+                if (r < nr) {
                   const uint4 w = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
                   dot8_bf16_f32(acc[ri][m], w, hv);
-                } else {
-                  const uint4 qv = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
-                  const uint32_t sc = reinterpret_cast<const uint16_t*>(
-                      st + (size_t)drs * p.row2 + (size_t)r * p.sc2)[ch];
-                  const uint32_t sf = e4m3x2_to_f16x2(sc);
-                  const float s[2] = {__half2float(__ushort_as_half((unsigned short)(sf & 0xffffu))),
-                                      __half2float(__ushort_as_half((unsigned short)(sf >> 16)))};
-                  const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                }
+              }
+            } else {
+              // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
 #pragma unroll
-                  for (int blk = 0; blk < 2; ++blk) {
+              for (int blk = 0; blk < 2; ++blk) {
+                float hv[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float4 f = *reinterpret_cast<const float4*>(hrow + 4 * ch + (blk * 4 + q) * 4 * p.tg);
+                  hv[4 * q] = f.x;
+                  hv[4 * q + 1] = f.y;
+                  hv[4 * q + 2] = f.z;
+                  hv[4 * q + 3] = f.w;
+                }
+#pragma unroll
+                for (int ri = 0; ri < RPG; ++ri) {
+                  const int r = g + ri * p.ng;
+                  if (r < nr) {
+                    const uint2 qv = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2 + 16 * ch)[blk];
+                    const uint32_t sb = st[(size_t)drs * p.row2 + (size_t)r * p.sc2 + 2 * ch + blk];
+                    const float sv = __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2(sb) & 0xffffu)));
+                    const uint32_t qw[2] = {qv.x, qv.y};
                     float part = 0.0f;
 #pragma unroll
                     for (int wi = 0; wi < 2; ++wi) {
 #pragma unroll
                       for (int by = 0; by < 4; ++by) {
-                        const uint32_t wv = e2m1x2_to_f16x2((qw[blk * 2 + wi] >> (8 * by)) & 0xffu);
-                        const int e0 = blk * 16 + wi * 8 + by * 2;
+                        const uint32_t wv = e2m1x2_to_f16x2((qw[wi] >> (8 * by)) & 0xffu);
+                        const int e0 = wi * 8 + by * 2;
                         const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
                         part = fmaf(__low2float(wh), hv[e0], part);
                         part = fmaf(__high2float(wh), hv[e0 + 1], part);
                       }
                     }
-                    acc[ri][m] = fmaf(s[blk], part, acc[ri][m]);
+                    acc[ri][m] = fmaf(sv, part, acc[ri][m]);
                   }
                 }
               }
@@ -1164,13 +1203,13 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
     const bool write = !c.aborted();
     if (p.tg <= 32) {
 #pragma unroll
-      for (int ri = 0; ri < kRpgMax; ++ri)
+      for (int ri = 0; ri < RPG; ++ri)
 #pragma unroll
         for (int m = 0; m < MAXM; ++m)
           for (int o = p.tg >> 1; o; o >>= 1) acc[ri][m] += __shfl_xor_sync(kFull, acc[ri][m], o);
       if (write && active && ch == 0) {
 #pragma unroll
-        for (int ri = 0; ri < kRpgMax; ++ri) {
+        for (int ri = 0; ri < RPG; ++ri) {
           const int r = g + ri * p.ng;
           if (r < nr) {
             const int row = rb_lo + r;
@@ -1186,23 +1225,23 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
       }
     } else {
 #pragma unroll
-      for (int ri = 0; ri < kRpgMax; ++ri)
+      for (int ri = 0; ri < RPG; ++ri)
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
           float v = acc[ri][m];
 #pragma unroll
           for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-          if (c.lane == 0) red[(c.warp * kRpgMax + ri) * MAXM + m] = v;
+          if (c.lane == 0) red[(c.warp * RPG + ri) * MAXM + m] = v;
         }
       bar_sync(kBarConsumers, kNC * 32);
       const int wpg = p.tg / 32;
       if (write && active && ch < 32) {  // first warp of each group writes
-        for (int q = c.lane; q < kRpgMax * MAXM; q += 32) {
+        for (int q = c.lane; q < RPG * MAXM; q += 32) {
           const int ri = q / MAXM, m = q % MAXM;
           const int r = g + ri * p.ng;
           if (r < nr && m < p.M) {
             float y = 0.0f;
-            for (int w = 0; w < wpg; ++w) y += red[((g * wpg + w) * kRpgMax + ri) * MAXM + m];
+            for (int w = 0; w < wpg; ++w) y += red[((g * wpg + w) * RPG + ri) * MAXM + m];
             const int row = rb_lo + r;
             const float rv = __uint_as_float((uint32_t)p.resid[(size_t)m * p.H + row] << 16);
             p.out[(size_t)m * p.H + row] = f32_to_bf16_bits(rv + y);
@@ -1276,9 +1315,13 @@ struct Producer {
   // block (plus the two scale blocks for NVFP4).
   __device__ void pairs(bool shared_phase, const Route& rt) {
     const Params& p = c.p;
-    const int n = shared_phase ? p.S * p.I : c.misc[MISC_NROUTED] * p.I;
     int lo, hi;
-    split_range(n, blockIdx.x, p.grid, lo, hi);
+    if (shared_phase) {
+      split_range(p.S * p.I, blockIdx.x, p.grid, lo, hi);
+    } else {
+      lo = c.misc[MISC_ULO];
+      hi = c.misc[MISC_UHI];
+    }
     const int nsl_ring = shared_phase ? p.nslots : p.nslots + p.nslots_x;
     ring.fit(nsl_ring);
     for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(nsl_ring)) {

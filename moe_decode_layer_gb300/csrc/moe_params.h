@@ -6,7 +6,9 @@ namespace moe {
 
 constexpr int kNC = 12;                  // consumer warps per CTA
 constexpr int kThreads = (kNC + 1) * 32; // + one producer warp
-constexpr int kRpgMax = 6;               // down-projection rows per thread group per stage
+constexpr int kRpgMax = 6;               // down-projection rows per thread group per stage (at most)
+constexpr int kRpgFp4 = 3;               // NVFP4: its 32-element chunks leave more groups, so fewer rows each
+__host__ __device__ constexpr int rows_per_group(int fmt) { return fmt == 0 ? kRpgMax : kRpgFp4; }
 constexpr int kMaxSlots = 64;            // ring slots (upper bound for the barrier arrays)
 constexpr int kCplBf16 = 16;             // 16-byte x chunks per lane kept in registers (H <= 4096)
 constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVFP4 (H <= 4096)
@@ -70,7 +72,8 @@ enum Stamp : int {
 };
 
 // Shared-memory words kept in the misc block.
-enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_WTOT = 8, MISC_WORDS = 32 };
+enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_ULO = 3, MISC_UHI = 4, MISC_WTOT = 8,
+                  MISC_WORDS = 32 };
 
 struct Params {
   // shapes
@@ -122,6 +125,7 @@ struct Params {
   int hs_nbuf;       // 1: one batch buffer of hs_pairs; 2: two of hs_pairs / 2 (next batch in flight)
   // shared-memory offsets from the aligned base
   int off_hbar;      // [2] mbarriers of the h batch buffers
+  int item_base;     // cost of a routed gate/up item with N rows: item_base + N
   int nslots_x;      // extra ring slots for the routed gate/up stages, in the h area
   int off_xslot;     // first extra slot (slots nslots .. nslots + nslots_x - 1)
   int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
