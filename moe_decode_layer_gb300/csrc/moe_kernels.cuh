@@ -980,6 +980,44 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
   }
 }
 
+// The union for a single token row on warp 0: the K selected experts in
+// ascending id become slots S.., one pair each; the same tables as union_warp
+// builds, from K lanes and K shuffles instead of bitmap and pair prefixes.
+__device__ __forceinline__ void union_one_row(const Ctx& c, const Route& rt) {
+  const Params& p = c.p;
+  const int K = p.K, S = p.S, lane = c.lane;
+  int* psr = reinterpret_cast<int*>(c.sm + p.off_pair_sr);
+  const int e = lane < K ? rt.sel_e[lane] : 0x7fffffff;
+  const float w = lane < K ? rt.sel_w[lane] : 0.0f;
+  int rank = 0;
+  for (int j = 0; j < K; ++j) rank += __shfl_sync(kFull, e, j) < e;
+  if (lane < K) {
+    const int sl = S + rank;
+    rt.slot_of[e] = sl;
+    rt.slot_e[sl] = e;
+    rt.slot_mask[sl] = 1u;
+    rt.slot_w[sl * p.maxm] = w * p.routed_scale;
+    rt.pair_base[sl] = sl;  // shared slots hold one pair each, so slot and pair index agree
+    psr[sl] = sl << 4;
+  }
+  for (int t = lane; t < S; t += 32) {
+    rt.slot_e[t] = -1 - t;
+    rt.slot_mask[t] = 1u;
+    for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
+    rt.pair_base[t] = t;
+    psr[t] = t << 4;
+  }
+  if (lane == 0) {
+    rt.pair_base[S + K] = S + K;
+    c.misc[MISC_NROUTED] = K;
+    // every routed item has one row: the cost split is the plain split
+    int lo, hi;
+    split_range(K * p.I, blockIdx.x, p.grid, lo, hi);
+    c.misc[MISC_ULO] = lo;
+    c.misc[MISC_UHI] = hi;
+  }
+}
+
 static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
   const Params& p = c.p;
   // every CTA's router logits stored (count), before reading any of them
@@ -1004,7 +1042,12 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
   }
   bar_sync(kBarConsumers, kNC * 32);
   if (c.tid == 0) c.stamp(ST_TOPK);
-  if (c.warp == 0) union_warp(c, rt);
+  if (c.warp == 0) {
+    if (p.M == 1)
+      union_one_row(c, rt);
+    else
+      union_warp(c, rt);
+  }
   bar_sync(kBarConsumers, kNC * 32);
 }
 
@@ -1195,6 +1238,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
       ++used;
       sl0 = sl1;
     }
+    if (rb == nrb - 1 && c.tid == 0) c.stamp(ST_D_SUMMED);
     // Reduce each row's partial sums over the group's threads and write out.
     if (check_xflags && rb == 0) {
       if (!c.aborted()) wait_xflags(c);

@@ -53,6 +53,7 @@ enum Stamp : int {
   ST_U_DONE = 4,      // routed gate/up stages consumed (warp 0 view)
   ST_D_FIRST = 5,     // first down stage's inputs staged
   ST_D_DONE = 6,      // outputs written
+  ST_D_SUMMED = 19,   // down sums of the last row block complete (before the output reduction)
   ST_P_R_ISSUED = 8,  // producer: last router / shared stage issued
   ST_P_ROUTE = 9,     // producer: routing received
   ST_P_U_ISSUED = 10, // producer: last routed gate/up stage issued
