@@ -1563,16 +1563,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       x_to_f16(c);
       bar_sync(kBarConsumers, kNC * 32);
     }
-    if (PHASES & PH_R) {
-      // shared experts' gate/up stages were issued before routing
-      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring);
-      fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
-      if (c.tid == 0) c.stamp(ST_R_DONE);
-    }
-    if (PHASES & PH_U) {
-      ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTED, ring);
-      fence_proxy_async_global();
-      if (c.tid == 0) c.stamp(ST_U_DONE);
+    // gate/up items: the shared experts' (their stages were issued before
+    // routing), then the routed experts'; one loop so that the code exists once
+    constexpr int kKind0 = (PHASES & PH_R) ? ITEM_SHARED : ITEM_ROUTED;
+    constexpr int kKind1 = (PHASES & PH_U) ? ITEM_ROUTED : ITEM_SHARED;
+    if (PHASES & (PH_R | PH_U)) {
+#pragma unroll 1
+      for (int kind = kKind0; kind <= kKind1; ++kind) {
+        ring = consume_items<FMT, MAXM>(c, rt, kind, ring);
+        fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
+        if (c.tid == 0) c.stamp(kind == ITEM_SHARED ? ST_R_DONE : ST_U_DONE);
+      }
     }
     if (PHASES & PH_U) {
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's h rows are all stored
