@@ -1079,10 +1079,11 @@ static __device__ __forceinline__ bool wait_xflags(const Ctx& c) {
 }
 
 // Down-phase batches: slots [sl0, sl1) whose (expert, row) pairs fit one h
-// buffer of `cap` pairs.
-__device__ __forceinline__ int batch_end(const Route& rt, int sl0, int nsl, int cap) {
+// buffer of `cap` pairs. With S >= 0 the first S (shared) slots form batches of
+// their own (their h is complete long before the routed experts').
+__device__ __forceinline__ int batch_end(const Route& rt, int sl0, int nsl, int cap, int S) {
   int sl1 = sl0 + 1;
-  while (sl1 < nsl && rt.pair_base[sl1 + 1] - rt.pair_base[sl0] <= cap) ++sl1;
+  while (sl1 < nsl && sl1 != S && rt.pair_base[sl1 + 1] - rt.pair_base[sl0] <= cap) ++sl1;
   return sl1;
 }
 
@@ -1118,33 +1119,45 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
   const uint32_t hbar0 = smem_u32(c.sm + p.off_hbar);
   const int nbuf = p.hs_nbuf, cap = p.hs_pairs / nbuf;
   constexpr int RPG = rows_per_group(FMT);  // rows per thread group and stage
-  // Thread 0 keeps the next nbuf batches of h in flight: batch uses run over
-  // (row block, batch) in order; use u goes to buffer u % nbuf.
+  // Thread 0 keeps up to nbuf batches of h in flight: batch uses run over
+  // (row block, batch) in order; use u goes to buffer u % nbuf and may be issued
+  // once use u - nbuf is done. With two buffers (the pairs do not all fit at
+  // once) and wait_u, a batch of shared slots waits only for every CTA's shared
+  // h (SCOUNT): the shared experts' down stages run while the last gate/up items
+  // finish elsewhere. Every other batch waits for all h (UCOUNT).
+  const int split = (wait_u && nbuf == 2) ? p.S : -1;
   int a_rb = 0, a_sl = 0, issued = 0, landed = 0;
-  auto issue_next = [&]() {
-    const int sl1 = batch_end(rt, a_sl, nsl, cap);
-    issue_h(c, rt, a_sl, sl1, issued % nbuf, cap);
-    ++issued;
-    a_sl = sl1;
-    if (a_sl >= nsl) {
-      a_sl = 0;
-      ++a_rb;
+  bool s_ok = !wait_u, u_ok = !wait_u;
+  auto issue_ready = [&](int limit, bool may_wait) {  // thread 0
+    while (issued < limit && a_rb < nrb && !c.aborted()) {
+      const bool routed = a_sl >= split;
+      bool& ok = routed ? u_ok : s_ok;
+      if (!ok) {
+        if (!may_wait) return;
+        if (!wait_count(c, routed ? CTRL_UCOUNT : CTRL_SCOUNT, SITE_FLAGS)) {
+          c.abort_local();
+          return;
+        }
+        if (routed) c.stamp(ST_U_FLAGS);
+        __threadfence();             // acquire every CTA's h stores ...
+        fence_proxy_async_global();  // ... for the bulk copies that read them
+        ok = true;
+      }
+      const int sl1 = batch_end(rt, a_sl, nsl, cap, split);
+      issue_h(c, rt, a_sl, sl1, issued % nbuf, cap);
+      ++issued;
+      a_sl = sl1;
+      if (a_sl >= nsl) {
+        a_sl = 0;
+        ++a_rb;
+      }
     }
   };
   if (nrb > 0) {
     fence_proxy_async_shared();  // generic accesses to the h area (routing scratch) before the copies into it
     bar_sync(kBarConsumers, kNC * 32);
-    if (c.tid == 0) {
-      bool ok = !c.aborted();
-      if (ok && wait_u) {
-        ok = wait_count(c, CTRL_UCOUNT, SITE_FLAGS);
-        if (!ok) c.abort_local();
-      }
-      c.stamp(ST_U_FLAGS);
-      __threadfence();             // acquire every CTA's h stores ...
-      fence_proxy_async_global();  // ... for the bulk copies that read them
-      for (int b = 0; ok && b < nbuf && a_rb < nrb; ++b) issue_next();
-    }
+    if (c.tid == 0) issue_ready(1, true);           // the first batch, waiting as needed
+    if (c.tid == 0) issue_ready(nbuf, split <= 0);  // more without waiting for the routed h
   }
   int used = 0;
   ring.fit(p.nslots);
@@ -1157,8 +1170,9 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
 #pragma unroll
       for (int m = 0; m < MAXM; ++m) acc[ri][m] = 0.0f;
     for (int sl0 = 0; sl0 < nsl;) {
-      const int sl1 = batch_end(rt, sl0, nsl, cap);
+      const int sl1 = batch_end(rt, sl0, nsl, cap, split);
       const int b = used % nbuf;
+      if (c.tid == 0) issue_ready(used + nbuf, true);  // this batch if it was held back, and the next
       const uint64_t th = p.stamps ? global_ns() : 0;
       const bool have = !c.aborted() && c.wait_bar(hbar0 + 8u * b, (uint32_t)(used / nbuf) & 1u, SITE_HIDDEN);
       if (p.stamps && c.tid == 0) c.count(ST_D_HWAIT_NS, global_ns() - th);
@@ -1234,7 +1248,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         if (got && c.lane == 0) c.release(ring, 1);
       }
       bar_sync(kBarConsumers, kNC * 32);  // h buffer b is free again
-      if (c.tid == 0 && !c.aborted() && a_rb < nrb) issue_next();
+      if (c.tid == 0) issue_ready(used + 1 + nbuf, false);
       ++used;
       sl0 = sl1;
     }
@@ -1573,6 +1587,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         ring = consume_items<FMT, MAXM>(c, rt, kind, ring);
         fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
         if (c.tid == 0) c.stamp(kind == ITEM_SHARED ? ST_R_DONE : ST_U_DONE);
+        if (PHASES == PH_ALL && kind == ITEM_SHARED && p.S > 0 && p.hs_nbuf == 2) {
+          bar_sync(kBarConsumers, kNC * 32);  // this CTA's shared h rows are all stored
+          if (c.tid == 0) {
+            __threadfence();  // release them with the count
+            count_done(p, CTRL_SCOUNT);
+          }
+        }
       }
     }
     if (PHASES & PH_U) {
@@ -1599,6 +1620,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       p.ctrl[CTRL_EXIT] = 0u;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_UCOUNT) = 0ull;
+      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_SCOUNT) = 0ull;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;
       p.ctrl[CTRL_EPOCH] = e;

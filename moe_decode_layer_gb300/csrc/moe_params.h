@@ -26,10 +26,11 @@ enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
 enum Phase : int { PH_R = 1, PH_U = 2, PH_D = 4, PH_ALL = 7 };
 
 // Control words at the start of the handle's scratch.
-// CTRL_RCOUNT / CTRL_UCOUNT (64-bit, 8-byte aligned word index): CTAs whose router
-// logits / gate-up results of the current run are stored; reset by the last CTA.
+// CTRL_RCOUNT / CTRL_UCOUNT / CTRL_SCOUNT (64-bit, 8-byte aligned word index): CTAs
+// whose router logits / gate-up results / shared experts' gate-up results of the
+// current run are stored; reset by the last CTA.
 enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3, CTRL_RCOUNT = 4,
-                  CTRL_UCOUNT = 6, CTRL_WORDS = 64 };
+                  CTRL_UCOUNT = 6, CTRL_SCOUNT = 8, CTRL_WORDS = 64 };
 // Device status bits and the wait that gave up first.
 enum DevErr : uint32_t { DEV_ERR_TIMEOUT = 1u };
 enum WaitSite : uint32_t {
