@@ -167,9 +167,9 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   // the h area is idle from the end of routing until the down phase: the routed
   // gate/up stages also use the slots that fit there
   // routed gate/up items are split by cost: streaming the pair plus the FMA work
-  // of each row that chose the expert (measured on GB300: an extra row adds ~1/8
-  // of a bf16 item's time and ~1/3 of an NVFP4 item's)
-  p.item_base = p.fmt == moe::FMT_BF16 ? 8 : 2;
+  // of each row that chose the expert (fitted on GB300 per-CTA phase times: an
+  // extra row adds ~1/6 of a bf16 item's time and about one NVFP4 item's)
+  p.item_base = p.fmt == moe::FMT_BF16 ? 6 : 1;
   p.off_xslot = (int)fixed;
   p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   p.d_rows_stage = drs;
