@@ -779,7 +779,7 @@ __device__ __forceinline__ float key_value(unsigned long long k) { return order_
 template <int PM>
 __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
   const Params& p = c.p;
-  const float* lg = reinterpret_cast<const float*>(c.sm + p.off_lg) + (size_t)m * p.E;
+  float* lg = reinterpret_cast<float*>(c.sm + p.off_lg) + (size_t)m * p.E;
   uint32_t* lmax = reinterpret_cast<uint32_t*>(c.sm + p.off_lmax) + m * 32;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + m * kCandMax;
   uint32_t* thr = reinterpret_cast<uint32_t*>(c.sm + p.off_thr) + m * 2;
@@ -886,97 +886,89 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
     }
     __syncwarp((1u << p.K) - 1u);
     sel_v[lane] = w;
+    lg[e] = w;  // the union reads the combine weight of (row m, expert e) here
   }
 }
 
-// The union of chosen experts on warp 0: slots S.. in ascending expert id from
-// per-word popcounts of the bitmap (prefix read back from shared memory), the
-// combine weights, and the (slot, row) pair index of every slot.
+// The union of chosen experts on warp 0, in one pass over the bitmap: lane l
+// owns word l (experts 32 l ..); one warp scan of (pairs, experts) per word
+// gives every slot (ascending expert id, after the S shared slots) and its pair
+// base; each lane then writes its slots' tables, combine weights (left by the
+// top-k in the logits array) and (slot, row) pairs, and counts how many slot
+// starts lie at or below the CTA's cost boundaries for the gate/up split.
 __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
   const Params& p = c.p;
-  int* wpc = reinterpret_cast<int*>(c.sm + p.off_wpc);
+  const int lane = c.lane, S = p.S, M = p.M;
   const int words = (p.E + 31) / 32;
-  const uint32_t w = c.lane < words ? rt.bitmap[c.lane] : 0u;
-  wpc[c.lane] = __popc(w);
-  __syncwarp();
-  int before = 0, total = 0;
-  const int4* w4 = reinterpret_cast<const int4*>(wpc);
+  const float* wgt = reinterpret_cast<const float*>(c.sm + p.off_lg);  // [M][E]: weights of the selected
+  int* psr = reinterpret_cast<int*>(c.sm + p.off_pair_sr);
+  const uint32_t w = lane < words ? rt.bitmap[lane] : 0u;
+  int npairs = 0;
+  for (uint32_t b = w; b; b &= b - 1) npairs += __popc(rt.emask[lane * 32 + __ffs(b) - 1]);
+  // exclusive warp scan of (pairs << 16 | experts)
+  const uint32_t v = ((uint32_t)npairs << 16) | (uint32_t)__popc(w);
+  uint32_t inc = v;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int4 v = w4[j];
-    const int b0 = 4 * j;
-    before += (b0 < c.lane ? v.x : 0) + (b0 + 1 < c.lane ? v.y : 0) + (b0 + 2 < c.lane ? v.z : 0) +
-              (b0 + 3 < c.lane ? v.w : 0);
-    total += (v.x + v.y) + (v.z + v.w);
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += y;
   }
-  int s = p.S + before;
-  for (uint32_t bits = w; bits; bits &= bits - 1) {
-    const int e = c.lane * 32 + __ffs(bits) - 1;
-    rt.slot_of[e] = s;
-    rt.slot_e[s] = e;
-    rt.slot_mask[s] = rt.emask[e];
-    ++s;
+  const uint32_t exc = inc - v, all = __shfl_sync(kFull, inc, 31);
+  const int total = (int)(all & 0xffffu), tpairs = (int)(all >> 16);
+  // the cost split: cum(u) = I * (item_base * u + pairs before routed slot u)
+  const uint32_t I = (uint32_t)p.I, base = (uint32_t)p.item_base;
+  const uint32_t tcost = I * (base * (uint32_t)total + (uint32_t)tpairs);  // <= 2^23
+  const uint32_t t0 = tcost * blockIdx.x / (uint32_t)p.grid, t1 = tcost * (blockIdx.x + 1) / (uint32_t)p.grid;
+  int n0 = 0, n1 = 0;
+  int u = (int)(exc & 0xffffu), q = (int)(exc >> 16);  // routed slot index and pairs before it
+  for (uint32_t b = w; b; b &= b - 1) {
+    const int e = lane * 32 + __ffs(b) - 1;
+    const uint32_t msk = rt.emask[e];
+    const int sl = S + u;
+    const uint32_t cu = I * (base * (uint32_t)u + (uint32_t)q);
+    n0 += cu <= t0;
+    n1 += cu <= t1;
+    rt.slot_of[e] = sl;
+    rt.slot_e[sl] = e;
+    rt.slot_mask[sl] = msk;
+    rt.pair_base[sl] = S * M + q;
+    for (uint32_t mm = msk; mm; mm &= mm - 1) {
+      const int m = __ffs(mm) - 1;
+      rt.slot_w[sl * p.maxm + m] = wgt[m * p.E + e] * p.routed_scale;
+      psr[S * M + q] = (sl << 4) | m;
+      ++q;
+    }
+    ++u;
   }
-  for (int t = c.lane; t < p.S; t += 32) {
+  for (int t = lane; t < S; t += 32) {
     rt.slot_e[t] = -1 - t;
-    rt.slot_mask[t] = (1u << p.M) - 1u;
+    rt.slot_mask[t] = (1u << M) - 1u;
+    rt.pair_base[t] = t * M;
     for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
+    for (int m = 0; m < M; ++m) psr[t * M + m] = (t << 4) | m;
   }
-  __syncwarp();
-  for (int t = c.lane; t < p.M * p.K; t += 32)
-    rt.slot_w[rt.slot_of[rt.sel_e[t]] * p.maxm + t / p.K] = rt.sel_w[t] * p.routed_scale;
-  const int nsl = p.S + total;
-  int carry = 0;
-  for (int s0 = 0; s0 < nsl; s0 += 32) {
-    const int sl = s0 + c.lane;
-    __syncwarp();
-    wpc[c.lane] = sl < nsl ? __popc(rt.slot_mask[sl]) : 0;
-    __syncwarp();
-    int pre = 0, sum = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int4 v = w4[j];
-      const int b0 = 4 * j;
-      pre += (b0 < c.lane ? v.x : 0) + (b0 + 1 < c.lane ? v.y : 0) + (b0 + 2 < c.lane ? v.z : 0) +
-             (b0 + 3 < c.lane ? v.w : 0);
-      sum += (v.x + v.y) + (v.z + v.w);
-    }
-    if (sl < nsl) {
-      rt.pair_base[sl] = carry + pre;
-      // (slot << 4 | row) of each of this slot's pairs, rows ascending
-      int* psr = reinterpret_cast<int*>(c.sm + p.off_pair_sr);
-      int q = carry + pre;
-      for (uint32_t msk = rt.slot_mask[sl]; msk; msk &= msk - 1) psr[q++] = (sl << 4) | (__ffs(msk) - 1);
-    }
-    carry += sum;
-  }
-  if (c.lane == 0) {
-    rt.pair_base[nsl] = carry;
+  if (lane == 0) {
+    rt.pair_base[S + total] = S * M + tpairs;
     c.misc[MISC_NROUTED] = total;
+    n0 += tcost <= t0;  // the end of the sequence, u = total
+    n1 += tcost <= t1;
   }
-  __syncwarp();
-  // This CTA's routed gate/up items [lo, hi) of the slot-major item sequence,
-  // balanced by cost: an item of a slot chosen by N rows costs item_base + N
-  // (its bytes plus the FMA work of its rows). The cost up to routed slot u is
-  // I * (item_base * u + pairs before it); the boundary at cost t is the first
-  // item that starts at or after t, so adjacent CTAs' ranges meet exactly.
-  if (c.lane == 0) {
-    const int* pb = rt.pair_base + p.S;
-    const uint32_t I = (uint32_t)p.I, base = (uint32_t)p.item_base;
-    auto cum = [&](int u) { return I * (base * (uint32_t)u + (uint32_t)(pb[u] - pb[0])); };
-    auto item_at = [&](uint32_t t) {
-      int lo = 0, hi = total;  // largest u in [0, total] with cum(u) <= t
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cum(mid) <= t) lo = mid; else hi = mid - 1;
-      }
-      if (lo == total) return total * p.I;
-      const uint32_t w = base + (uint32_t)(pb[lo + 1] - pb[lo]);
-      return lo * p.I + (int)((t - cum(lo) + w - 1) / w);
-    };
-    const uint32_t tot = cum(total);  // <= 2^23: the products below stay in 32 bits
-    c.misc[MISC_ULO] = item_at(tot * blockIdx.x / (uint32_t)p.grid);
-    c.misc[MISC_UHI] = item_at(tot * (blockIdx.x + 1) / (uint32_t)p.grid);
+  const int u0 = (int)__reduce_add_sync(kFull, (uint32_t)n0) - 1;
+  const int u1 = (int)__reduce_add_sync(kFull, (uint32_t)n1) - 1;
+  // each boundary: the first item at or after its cost, found by the lane that owns its slot
+  u = (int)(exc & 0xffffu);
+  q = (int)(exc >> 16);
+  for (uint32_t b = w; b; b &= b - 1) {
+    const int n = __popc(rt.emask[lane * 32 + __ffs(b) - 1]);
+    const uint32_t cu = I * (base * (uint32_t)u + (uint32_t)q), wu = base + (uint32_t)n;
+    if (u == u0) c.misc[MISC_ULO] = u * p.I + (int)((t0 - cu + wu - 1) / wu);
+    if (u == u1) c.misc[MISC_UHI] = u * p.I + (int)((t1 - cu + wu - 1) / wu);
+    q += n;
+    ++u;
+  }
+  if (lane == 0) {
+    if (u0 >= total) c.misc[MISC_ULO] = total * p.I;
+    if (u1 >= total) c.misc[MISC_UHI] = total * p.I;
   }
 }
 
