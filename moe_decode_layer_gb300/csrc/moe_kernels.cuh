@@ -783,8 +783,6 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
   uint32_t* lmax = reinterpret_cast<uint32_t*>(c.sm + p.off_lmax) + m * 32;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + m * kCandMax;
   uint32_t* thr = reinterpret_cast<uint32_t*>(c.sm + p.off_thr) + m * 2;
-  int* ccount = reinterpret_cast<int*>(c.sm + p.off_ccount) + m;
-  float* wtmp = reinterpret_cast<float*>(c.sm + p.off_wtmp) + m * 16;
   const int lane = c.lane;
   uint32_t key[PM];
   uint32_t best = 0;
@@ -795,7 +793,6 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
     best = key[i] > best ? key[i] : best;
   }
   lmax[lane] = best;
-  if (lane == 0) *ccount = 0;
   __syncwarp();
   int gt = 0, ge = 0;
   const uint4* l4 = reinterpret_cast<const uint4*>(lmax);
@@ -811,8 +808,16 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
   int cnt = 0;
 #pragma unroll
   for (int i = 0; i < PM; ++i) cnt += key[i] != 0u && key[i] >= t;
+  // candidate positions: exclusive warp scan of the lanes' counts
+  int o = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(kFull, o, d);
+    if (lane >= d) o += y;
+  }
+  const int C = __shfl_sync(kFull, o, 31);
+  o -= cnt;
   if (cnt) {
-    int o = atomicAdd(ccount, cnt);
 #pragma unroll
     for (int i = 0; i < PM; ++i) {
       if (key[i] != 0u && key[i] >= t) {
@@ -823,7 +828,6 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
     }
   }
   __syncwarp();
-  const int C = *ccount;
   int* sel_e = rt.sel_e + m * p.K;
   float* sel_v = rt.sel_w + m * p.K;  // logits first, weights after
   if (C <= kCandMax) {
@@ -870,13 +874,15 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
     }
   }
   __syncwarp();
-  // renormalised softmax over the selection, the sum in a fixed order
-  if (lane < p.K) wtmp[lane] = expf(sel_v[lane] - sel_v[0]);
-  __syncwarp();
+  // renormalised softmax over the selection (a butterfly sum: a fixed order)
+  const float v = lane < p.K ? sel_v[lane] : 0.0f;
+  const float v0 = __shfl_sync(kFull, v, 0);  // every lane takes part in the shuffle
+  const float ex = lane < p.K ? expf(v - v0) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int d = 16; d; d >>= 1) sum += __shfl_xor_sync(kFull, sum, d);
   if (lane < p.K) {
-    float sum = 0.0f;
-    for (int j = 0; j < p.K; ++j) sum += wtmp[j];
-    const float w = wtmp[lane] / sum;
+    const float w = ex / sum;
     const int e = sel_e[lane];
     atomicOr(&rt.emask[e], 1u << m);
     atomicOr(&rt.bitmap[e >> 5], 1u << (e & 31));
