@@ -100,6 +100,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.off_full = take(moe::kMaxSlots * 8, 8);
   p.off_empty = take(moe::kMaxSlots * 8, 8);
   p.off_xbar = take(8, 8);
+  p.off_xfree = take(8, 8);
   p.off_hbar = take(16, 8);
   p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
   p.off_x = take((size_t)maxm * H * 2, 128);
@@ -171,6 +172,9 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   // extra row adds ~1/6 of a bf16 item's time and about one NVFP4 item's)
   p.item_base = p.fmt == moe::FMT_BF16 ? 6 : 1;
   p.off_xslot = (int)fixed;
+  // the x rows are dead once the gate/up items are done: their area holds one
+  // more down-phase slot when it is large enough
+  p.nslots_d = ((size_t)maxm * H * 2 >= slot && p.nslots < moe::kMaxSlots) ? 1 : 0;
   p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   p.d_rows_stage = drs;
   p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));

@@ -136,8 +136,11 @@ struct Ctx {
   // Another CTA gave up: stop waiting on data it will never publish.
   __device__ bool peer_failed() const { return ld_relaxed_u32(&p.ctrl[CTRL_STATUS]) != 0; }
   __device__ uint32_t epoch() const { return static_cast<uint32_t>(misc[MISC_EPOCH]); }
-  __device__ uint8_t* slot_ptr(int slot) const {
+  // Slots past nslots: in the gate/up phase extra slots in the h area, in the
+  // down phase (d) the x area.
+  __device__ uint8_t* slot_ptr(int slot, bool d = false) const {
     return slot < p.nslots ? sm + p.off_ring + (size_t)slot * p.slot_bytes
+           : d             ? sm + p.off_x
                            : sm + p.off_xslot + (size_t)(slot - p.nslots) * p.slot_bytes;
   }
   // Phase timestamp (one plain store; off unless the handle has a stamp buffer).
@@ -1100,8 +1103,9 @@ __device__ __forceinline__ void issue_h(const Ctx& c, const Route& rt, int sl0, 
 }
 
 // wait_u: the gate/up results come from this same kernel (single-kernel schedule)
+// nd: down-phase slots in the x area (0 or 1)
 template <int FMT, int MAXM>
-__device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, bool wait_u, Ring ring) {
+__device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, bool wait_u, Ring ring, int nd) {
   const Params& p = c.p;
   int r_lo, r_hi;
   cta_rows(p, r_lo, r_hi);
@@ -1158,7 +1162,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
     if (c.tid == 0) issue_ready(nbuf, split <= 0);  // more without waiting for the routed h
   }
   int used = 0;
-  ring.fit(p.nslots);
+  ring.fit(p.nslots + nd);
   for (int rb = 0; rb < nrb; ++rb) {
     const int rb_lo = r_lo + rb * drs;
     const int nr = min(drs, r_hi - rb_lo);
@@ -1177,13 +1181,13 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
       if (have && c.tid == 0) landed = used + 1;
       const float* hs = hs0 + (size_t)b * cap * p.I;
       if (rb == 0 && sl0 == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
-      for (int sl = sl0; sl < sl1; ++sl, ring.next(p.nslots)) {
+      for (int sl = sl0; sl < sl1; ++sl, ring.next(p.nslots + nd)) {
         const uint32_t mask = rt.slot_mask[sl];
         const uint64_t tw = p.stamps ? global_ns() : 0;
         const bool got = !c.aborted() && c.wait_full(ring);
         if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, global_ns() - tw);
         if (got && have && active) {
-          const uint8_t* st = c.slot_ptr(ring.slot);
+          const uint8_t* st = c.slot_ptr(ring.slot, true);
           int hp = rt.pair_base[sl] - rt.pair_base[sl0];
 #pragma unroll
           for (int m = 0; m < MAXM; ++m) {
@@ -1328,9 +1332,14 @@ struct Producer {
   __device__ Producer(const Ctx& cc) : c(cc) { pol = policy_evict_first(); }
 
   // Claims the next stage's slot and announces its bytes. False on abort.
-  __device__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar) {
+  bool x_free = false;  // the consumers are done with x (down-phase slot in the x area)
+  __device__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar, bool d = false) {
     if (c.aborted() || !c.wait_empty(ring)) return false;
-    dst = smem_u32(c.slot_ptr(ring.slot));
+    if (d && ring.slot >= c.p.nslots && !x_free) {
+      if (!c.wait_bar(smem_u32(c.sm + c.p.off_xfree), 0, SITE_RING_EMPTY)) return false;
+      x_free = true;
+    }
+    dst = smem_u32(c.slot_ptr(ring.slot, d));
     bar = c.full0 + 8u * ring.slot;
     c.slot_seq[ring.slot] = ring.seq;  // before arming: see Ctx::wait_full
     mbar_arrive_expect_tx(bar, bytes);
@@ -1403,13 +1412,14 @@ struct Producer {
   }
 
   // Down stages (row block rb, union slot sl) for sl in [sl_lo, sl_hi).
-  __device__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi) {
+  // nd: down-phase slots in the x area (0 or 1)
+  __device__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi, int nd) {
     const Params& p = c.p;
     int r_lo, r_hi;
     cta_rows(p, r_lo, r_hi);
     const int rb_lo = r_lo + rb * p.d_rows_stage;
     const int nr = min(p.d_rows_stage, r_hi - rb_lo);
-    ring.fit(p.nslots);
+    ring.fit(p.nslots + nd);
     for (int sl = sl_lo; sl < sl_hi; ++sl) {
       const int e = sl < p.S ? -1 - sl : rt.slot_e[sl];
       const uint8_t* wt = e >= 0 ? p.w2 : p.sh_w2;
@@ -1418,10 +1428,10 @@ struct Producer {
       const size_t row0 = ex * p.H + rb_lo;
       const uint32_t cb = (uint32_t)nr * p.row2, sb = (uint32_t)nr * p.sc2;
       uint32_t dst, bar;
-      if (!begin(cb + sb, dst, bar)) return;
+      if (!begin(cb + sb, dst, bar, true)) return;
       bulk_g2s(dst, wt + row0 * p.row2, cb, bar, pol);
       if (sb) bulk_g2s(dst + (uint32_t)p.d_rows_stage * p.row2, ws + row0 * p.sc2, sb, bar, pol);
-      ring.next(p.nslots);
+      ring.next(p.nslots + nd);
     }
   }
 
@@ -1480,12 +1490,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
 
   if (kChain) pdl_launch_dependents();
   if (c.tid == 0) {
-    for (int i = 0; i < p.nslots + p.nslots_x; ++i) {
+    for (int i = 0; i < p.nslots + max(p.nslots_x, p.nslots_d); ++i) {
       mbar_init(c.full0 + 8u * i, 1);
       mbar_init(c.empty0 + 8u * i, kNC);
       c.slot_seq[i] = -1;
     }
     mbar_init(c.xbar, 1);
+    mbar_init(smem_u32(sm + p.off_xfree), 1);
     mbar_init(smem_u32(sm + p.off_hbar), 1);
     mbar_init(smem_u32(sm + p.off_hbar) + 8u, 1);
     mbar_init_fence();
@@ -1520,7 +1531,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         if (PHASES & PH_D) pr.prefetch_shared_down();
       } else if (PHASES == PH_D) {
         // The shared experts' down rows of the first row block need no routing.
-        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S);
+        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, 0);
       }
     }
     if (kRoute) {
@@ -1536,7 +1547,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       if (PHASES & PH_D) {
         const int nsl = p.S + c.misc[MISC_NROUTED];
         const int first = PHASES == PH_D ? p.S : 0;  // the chain issued these before routing
-        for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl);
+        const int nd = PHASES == PH_ALL ? p.nslots_d : 0;
+        for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl, nd);
         c.stamp(ST_P_D_ISSUED);
       }
       if (c.aborted()) pr.drain();
@@ -1599,10 +1611,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       if (c.tid == 0) {
         __threadfence();  // release them with the count
         count_done(p, CTRL_UCOUNT);
+        if (PHASES == PH_ALL) mbar_arrive(smem_u32(sm + p.off_xfree), 1);  // x is dead: its area may take a down stage
       }
     }
     if (PHASES & PH_D)
-      consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, PHASES == PH_ALL, ring);
+      consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, PHASES == PH_ALL, ring,
+                              PHASES == PH_ALL ? p.nslots_d : 0);
     if (c.tid == 0) {
       c.stamp(ST_D_DONE);
       if (p.stamps) {

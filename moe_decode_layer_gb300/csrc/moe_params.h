@@ -130,6 +130,8 @@ struct Params {
   int item_base;     // cost of a routed gate/up item with N rows: item_base + N
   int nslots_x;      // extra ring slots for the routed gate/up stages, in the h area
   int off_xslot;     // first extra slot (slots nslots .. nslots + nslots_x - 1)
+  int nslots_d;      // 1: in the down phase slot nslots lies in the x area (x is dead by then)
+  int off_xfree;     // mbarrier: the consumers are done with x (single-kernel schedule)
   int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
   int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;
   int off_lg, off_cand, off_lmax, off_ccount, off_thr, off_wtmp, off_wpc;  // routing scratch (in the hs area)
