@@ -1079,6 +1079,26 @@ static __device__ __forceinline__ bool wait_xflags(const Ctx& c) {
   return true;
 }
 
+// Per-slot h readiness (every pair fits the h area): this CTA adds the number of
+// its gate/up items of each slot to that slot's count; a slot's h is complete
+// when its count reaches I. Thread 0, after the CTA's h stores and a fence.
+__device__ __forceinline__ void count_slots(const Ctx& c) {
+  const Params& p = c.p;
+  auto add = [&](int slot0, int lo, int hi) {
+    for (int u = lo / p.I; lo < hi; ++u) {
+      const int end = min(hi, (u + 1) * p.I);
+      asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p.ctrl + CTRL_SLOTCNT + slot0 + u),
+                   "r"((uint32_t)(end - lo))
+                   : "memory");
+      lo = end;
+    }
+  };
+  int slo, shi;
+  split_range(p.S * p.I, blockIdx.x, p.grid, slo, shi);
+  add(0, slo, shi);
+  add(p.S, c.misc[MISC_ULO], c.misc[MISC_UHI]);
+}
+
 // Down-phase batches: slots [sl0, sl1) whose (expert, row) pairs fit one h
 // buffer of `cap` pairs. With S >= 0 the first S (shared) slots form batches of
 // their own (their h is complete long before the routed experts').
@@ -1155,7 +1175,10 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
       }
     }
   };
-  if (nrb > 0) {
+  // per-slot mode: one producer lane fetches each slot's h as soon as it is
+  // complete (fetch_h_per_slot); all pairs stay in the h area for every row block
+  const bool per_slot = wait_u && p.hs_perslot;
+  if (nrb > 0 && !per_slot) {
     fence_proxy_async_shared();  // generic accesses to the h area (routing scratch) before the copies into it
     bar_sync(kBarConsumers, kNC * 32);
     if (c.tid == 0) issue_ready(1, true);           // the first batch, waiting as needed
@@ -1174,15 +1197,23 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
     for (int sl0 = 0; sl0 < nsl;) {
       const int sl1 = batch_end(rt, sl0, nsl, cap, split);
       const int b = used % nbuf;
-      if (c.tid == 0) issue_ready(used + nbuf, true);  // this batch if it was held back, and the next
-      const uint64_t th = p.stamps ? global_ns() : 0;
-      const bool have = !c.aborted() && c.wait_bar(hbar0 + 8u * b, (uint32_t)(used / nbuf) & 1u, SITE_HIDDEN);
-      if (p.stamps && c.tid == 0) c.count(ST_D_HWAIT_NS, global_ns() - th);
-      if (have && c.tid == 0) landed = used + 1;
+      bool have = true;
+      if (!per_slot) {
+        if (c.tid == 0) issue_ready(used + nbuf, true);  // this batch if it was held back, and the next
+        const uint64_t th = p.stamps ? global_ns() : 0;
+        have = !c.aborted() && c.wait_bar(hbar0 + 8u * b, (uint32_t)(used / nbuf) & 1u, SITE_HIDDEN);
+        if (p.stamps && c.tid == 0) c.count(ST_D_HWAIT_NS, global_ns() - th);
+        if (have && c.tid == 0) landed = used + 1;
+      }
       const float* hs = hs0 + (size_t)b * cap * p.I;
       if (rb == 0 && sl0 == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
       for (int sl = sl0; sl < sl1; ++sl, ring.next(p.nslots + nd)) {
         const uint32_t mask = rt.slot_mask[sl];
+        if (per_slot && rb == 0) {  // this slot's h (once: it stays for later row blocks)
+          const uint64_t th = p.stamps ? global_ns() : 0;
+          have = !c.aborted() && c.wait_bar(c.full0 + 8u * (kHSlotBar + sl), 0, SITE_HIDDEN);
+          if (p.stamps && c.tid == 0) c.count(ST_D_HWAIT_NS, global_ns() - th);
+        }
         const uint64_t tw = p.stamps ? global_ns() : 0;
         const bool got = !c.aborted() && c.wait_full(ring);
         if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, global_ns() - tw);
@@ -1249,8 +1280,10 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         __syncwarp();
         if (got && c.lane == 0) c.release(ring, 1);
       }
-      bar_sync(kBarConsumers, kNC * 32);  // h buffer b is free again
-      if (c.tid == 0) issue_ready(used + 1 + nbuf, false);
+      if (!per_slot) {
+        bar_sync(kBarConsumers, kNC * 32);  // h buffer b is free again
+        if (c.tid == 0) issue_ready(used + 1 + nbuf, false);
+      }
       ++used;
       sl0 = sl1;
     }
@@ -1332,9 +1365,76 @@ struct Producer {
   __device__ Producer(const Ctx& cc) : c(cc) { pol = policy_evict_first(); }
 
   // Claims the next stage's slot and announces its bytes. False on abort.
-  bool x_free = false;  // the consumers are done with x (down-phase slot in the x area)
+  bool x_free = false;  // the consumers are done with x and the h area (down-phase slot in the x area)
+
+  // Per-slot h fetches (single-kernel schedule, every pair fits the h area):
+  // while it issues the down stages, the producer copies each slot's h values --
+  // in pair order -- into the h area as soon as the slot's count is complete and
+  // this CTA is done with the h area, counted on the slot's own mbarrier.
+  const Route* h_rt = nullptr;  // set: fetches active
+  int h_next = 0, h_nsl = 0;
+  __device__ bool test_x_free() {
+    if (!x_free && mbar_test_wait(smem_u32(c.sm + c.p.off_xfree), 0)) x_free = true;
+    return x_free;
+  }
+  __device__ void poll_h() {
+    const Params& p = c.p;
+    if (!h_rt || h_next >= h_nsl || !test_x_free()) return;
+    const float* rep = p.hbuf + (size_t)(blockIdx.x % kHRep) * p.npair_max * p.I;
+    float* hs = reinterpret_cast<float*>(c.sm + p.off_hs);
+    while (h_next < h_nsl && ld_relaxed_u32(p.ctrl + CTRL_SLOTCNT + h_next) >= (uint32_t)p.I) {
+      __threadfence();             // acquire the slot's h stores ...
+      fence_proxy_async_global();  // ... for the bulk copy that reads them
+      const int p0 = h_rt->pair_base[h_next];
+      const uint32_t bytes = (uint32_t)(h_rt->pair_base[h_next + 1] - p0) * (uint32_t)p.I * 4u;
+      const uint32_t bar = c.full0 + 8u * (kHSlotBar + h_next);
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s_plain(smem_u32(hs + (size_t)p0 * p.I), rep + (size_t)p0 * p.I, bytes, bar);
+      ++h_next;
+    }
+  }
+  // Bounded: the remaining fetches once every down stage is issued.
+  __device__ void finish_h() {
+    uint32_t spins = 0;
+    while (h_rt && h_next < h_nsl && !c.aborted()) {
+      poll_h();
+      if (h_next >= h_nsl) break;
+      __nanosleep(64);
+      if ((++spins & 15) == 0) {
+        if (c.peer_failed()) return;
+        if (c.expired()) {
+          c.fail(SITE_HIDDEN);
+          return;
+        }
+      }
+    }
+  }
+  // After an abort: the fetches issued must land before exit.
+  __device__ void drain_h() const {
+    const uint64_t t = global_ns();
+    for (int sl = 0; sl < h_next; ++sl)
+      while (!mbar_try_wait(c.full0 + 8u * (kHSlotBar + sl), 0) && global_ns() - t < c.p.timeout_ns) {
+      }
+  }
+
   __device__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar, bool d = false) {
-    if (c.aborted() || !c.wait_empty(ring)) return false;
+    if (c.aborted()) return false;
+    if (h_rt) {  // poll the h fetches while the slot is busy
+      uint32_t spins = 0;
+      // wake on the slot's release or after 200 ns to poll the h counts
+      while (!mbar_try_wait_ns(c.empty0 + 8u * ring.slot, ring.phase() ^ 1u, 200u)) {
+        poll_h();
+        if ((++spins & 15) == 0) {
+          if (c.aborted()) return false;
+          if (c.expired()) {
+            c.fail(SITE_RING_EMPTY);
+            return false;
+          }
+        }
+      }
+    } else if (!c.wait_empty(ring)) {
+      return false;
+    }
     if (d && ring.slot >= c.p.nslots && !x_free) {
       if (!c.wait_bar(smem_u32(c.sm + c.p.off_xfree), 0, SITE_RING_EMPTY)) return false;
       x_free = true;
@@ -1497,6 +1597,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     }
     mbar_init(c.xbar, 1);
     mbar_init(smem_u32(sm + p.off_xfree), 1);
+    if (PHASES == PH_ALL && p.hs_perslot)
+      for (int i = 0; i < p.nslot_max; ++i) mbar_init(c.full0 + 8u * (kHSlotBar + i), 1);
     mbar_init(smem_u32(sm + p.off_hbar), 1);
     mbar_init(smem_u32(sm + p.off_hbar) + 8u, 1);
     mbar_init_fence();
@@ -1548,10 +1650,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         const int nsl = p.S + c.misc[MISC_NROUTED];
         const int first = PHASES == PH_D ? p.S : 0;  // the chain issued these before routing
         const int nd = PHASES == PH_ALL ? p.nslots_d : 0;
+        if (PHASES == PH_ALL && p.hs_perslot) {
+          pr.h_rt = &rt;
+          pr.h_nsl = nsl;
+        }
         for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl, nd);
+        pr.finish_h();
         c.stamp(ST_P_D_ISSUED);
       }
-      if (c.aborted()) pr.drain();
+      if (c.aborted()) {
+        pr.drain();
+        pr.drain_h();
+      }
       // the x copy may still be in flight if the consumers gave up before it landed
       if (x_issued && c.aborted()) {
         const uint64_t t = global_ns();
@@ -1607,11 +1717,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       }
     }
     if (PHASES & PH_U) {
+      // the h area takes bulk copies from here on (per-slot h fetches)
+      if (PHASES == PH_ALL && p.hs_perslot) fence_proxy_async_shared();
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's h rows are all stored
       if (c.tid == 0) {
-        __threadfence();  // release them with the count
+        __threadfence();  // release them with the count(s)
         count_done(p, CTRL_UCOUNT);
-        if (PHASES == PH_ALL) mbar_arrive(smem_u32(sm + p.off_xfree), 1);  // x is dead: its area may take a down stage
+        if (PHASES == PH_ALL && p.hs_perslot) count_slots(c);
+        if (PHASES == PH_ALL) mbar_arrive(smem_u32(sm + p.off_xfree), 1);  // x and the h area are free
       }
     }
     if (PHASES & PH_D)
@@ -1633,6 +1746,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_UCOUNT) = 0ull;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_SCOUNT) = 0ull;
+      if (PHASES == PH_ALL && p.hs_perslot)
+        for (int i = 0; i < p.nslot_max; ++i) p.ctrl[CTRL_SLOTCNT + i] = 0u;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;
       p.ctrl[CTRL_EPOCH] = e;

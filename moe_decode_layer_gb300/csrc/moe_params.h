@@ -30,7 +30,10 @@ enum Phase : int { PH_R = 1, PH_U = 2, PH_D = 4, PH_ALL = 7 };
 // whose router logits / gate-up results / shared experts' gate-up results of the
 // current run are stored; reset by the last CTA.
 enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3, CTRL_RCOUNT = 4,
-                  CTRL_UCOUNT = 6, CTRL_SCOUNT = 8, CTRL_WORDS = 64 };
+                  CTRL_UCOUNT = 6, CTRL_SCOUNT = 8, CTRL_SLOTCNT = 16, CTRL_WORDS = 176 };
+// CTRL_SLOTCNT + s: gate/up items of union slot s whose h is stored (all CTAs of
+// the run; complete at I). Used when every pair's h fits the h area at once.
+constexpr int kHSlotBar = 32;  // per-slot h mbarriers: full-barrier entries kHSlotBar + s (s < 32)
 // Device status bits and the wait that gave up first.
 enum DevErr : uint32_t { DEV_ERR_TIMEOUT = 1u };
 enum WaitSite : uint32_t {
@@ -131,6 +134,8 @@ struct Params {
   int nslots_x;      // extra ring slots for the routed gate/up stages, in the h area
   int off_xslot;     // first extra slot (slots nslots .. nslots + nslots_x - 1)
   int nslots_d;      // 1: in the down phase slot nslots lies in the x area (x is dead by then)
+  int hs_perslot;    // 1: all pairs fit the h area; the single-kernel schedule fetches each slot's h
+                     // as soon as that slot's items are done (per-slot counts and mbarriers)
   int off_xfree;     // mbarrier: the consumers are done with x (single-kernel schedule)
   int off_full, off_empty, off_xbar, off_slot_seq, off_x, off_hs, off_sel_e, off_sel_w;
   int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;

@@ -18,9 +18,11 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_scratch[MOE_DECODE_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kCtrlBytes = 256;  // moe::CTRL_WORDS 32-bit words, padded
+constexpr size_t kCtrlBytes = 1024;  // moe::CTRL_WORDS 32-bit words, padded
 std::mutex g_setup_mu;
 void* g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch per device
+
+static_assert(kCtrlBytes >= moe::CTRL_WORDS * 4, "control words exceed their area");
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
