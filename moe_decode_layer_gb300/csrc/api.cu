@@ -175,14 +175,15 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   // the x rows are dead once the gate/up items are done: their area holds one
   // more down-phase slot when it is large enough
   p.nslots_d = ((size_t)maxm * H * 2 >= slot && p.nslots < moe::kMaxSlots) ? 1 : 0;
+  p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   // per-slot h fetches: measured faster for NVFP4 (its gate/up phase ends less
-  // evenly across CTAs), not for bf16, which keeps one fetch after all h is stored
+  // evenly across CTAs), not for bf16, which keeps one fetch after all h is stored.
+  // Their mbarriers follow every ring slot's full barrier.
   p.hs_perslot = (p.fmt == moe::FMT_NVFP4 && p.hs_nbuf == 1 && hs_pairs >= p.npair_max &&
                   p.nslot_max <= moe::kMaxSlots - moe::kHSlotBar &&
                   p.nslots + std::max(p.nslots_x, p.nslots_d) <= moe::kHSlotBar)
                      ? 1
                      : 0;
-  p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   p.d_rows_stage = drs;
   p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
   // router stages: at most kNC / 2 row pairs, so every row gets at least one warp

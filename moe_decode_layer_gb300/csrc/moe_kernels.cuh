@@ -1229,14 +1229,17 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
               const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
               const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
               const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+              // every row of the group, branch-free: rows past the block repeat
+              // the last one (their sums are never written), so all loads issue
+              // before the arithmetic
+              uint4 wv[RPG];
 #pragma unroll
               for (int ri = 0; ri < RPG; ++ri) {
-                const int r = g + ri * p.ng;
-                if (r < nr) {
-                  const uint4 w = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
-                  dot8_bf16_f32(acc[ri][m], w, hv);
-                }
+                const int r = min(g + ri * p.ng, nr - 1);
+                wv[ri] = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
               }
+#pragma unroll
+              for (int ri = 0; ri < RPG; ++ri) dot8_bf16_f32(acc[ri][m], wv[ri], hv);
             } else {
               // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
 #pragma unroll
