@@ -458,7 +458,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--workload", default="ling_m1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sched", default="persistent", choices=["persistent", "pdl_chain", "chain"])
+    ap.add_argument("--sched", default="persistent", choices=["persistent", "phased", "interleaved", "pdl_chain", "chain"])
     ap.add_argument("--copies", type=int, default=8, help="distinct layer copies (single-layer workloads)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--ring-slots", type=int, default=0, help="cap on shared-memory ring slots (0 = planned)")

@@ -178,8 +178,15 @@ enum {
                                   so every wait on them runs into the limit          */
   MOE_OPT_RING_SLOTS = 4,      /* shared-memory ring slots used, 2 .. the planned count */
   MOE_OPT_STAMPS = 5,          /* device pointer (as int64) to a uint64 buffer of
-                                  MOE_INFO_GRID x 16 words, or 0: each CTA stores the
+                                  MOE_INFO_GRID x 24 words, or 0: each CTA stores the
                                   %globaltimer ns at its phase boundaries (profiling)  */
+  MOE_OPT_INTERLEAVE = 6,      /* MOE_SCHED_PERSISTENT runs with the slot-interleaved
+                                  kernel (gate/up items and down stages alternate
+                                  slot by slot) when its layout fits and: 1 (default)
+                                  for bf16 weights and one token row, where it
+                                  measured faster; 2 always; 0 never (the phase-
+                                  ordered kernel). get_info: the mode, 0 when the
+                                  interleaved layout does not fit.                   */
   MOE_INFO_GRID = 16,          /* CTAs per kernel                                   */
   MOE_INFO_THREADS = 17,       /* threads per CTA                                   */
   MOE_INFO_SMEM = 18,          /* dynamic shared memory per CTA, bytes              */

@@ -33,6 +33,7 @@ MOE_OPT_WAIT_TIMEOUT_NS = 2
 MOE_OPT_TEST_FLAGS = 3
 MOE_OPT_RING_SLOTS = 4
 MOE_OPT_STAMPS = 5
+MOE_OPT_INTERLEAVE = 6
 STAMP_NAMES = {0: "start", 1: "x_loaded", 2: "R_done", 3: "routed", 4: "U_done", 5: "D_first",
                6: "D_done", 8: "prod_R_issued", 9: "prod_route", 10: "prod_U_issued",
                11: "prod_D_issued", 12: "logits_seen", 13: "topk_row0", 14: "ucount_full",

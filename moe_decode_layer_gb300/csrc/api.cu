@@ -18,9 +18,13 @@ using moe::Params;
 struct moe_decode_handle {
   moe_decode_config cfg;
   Params base;       // everything but the per-run pointers and M
+  Params ilv;        // the same for the slot-interleaved single kernel (when has_ilv)
+  bool has_ilv = false;
+  int ilv_mode = 1;  // MOE_OPT_INTERLEAVE
   int device = 0;
   int sched = MOE_SCHED_PERSISTENT;
   int max_slots = 0;  // ring slots the planned shared memory holds
+  int max_slots_ilv = 0;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   uint16_t* stage_x = nullptr;  // run_host staging
@@ -66,7 +70,10 @@ moe_status check_config(const moe_decode_config* c) {
 
 // Plans the per-CTA layout for a device with `sms` SMs and `smem_optin` bytes
 // of opt-in shared memory per block.
-moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) {
+// ilv: the layout of the slot-interleaved single kernel (every output row of a
+// CTA in one down stage, whose ring slot also holds the slot's h rows; no h
+// staging area). MOE_ERR_UNSUPPORTED when that layout does not fit.
+moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, bool ilv) {
   std::memset(&p, 0, sizeof(p));
   const int H = c.hidden, I = c.inter, E = c.num_experts, K = c.top_k, S = c.num_shared;
   const int maxm = c.max_rows;
@@ -116,20 +123,28 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.off_pair_sr = take((size_t)p.npair_max * 4, 4);
   p.off_red = take((size_t)moe::kNC * moe::kRpgMax * 8 * 4, 16);
   p.off_misc = take(moe::MISC_WORDS * 4, 16);
+  p.off_ucnt = take(moe::ILV_WORDS * 4, 16);
+  p.off_dslot = take((size_t)p.nslot_max * 4, 4);
   const size_t fixed = round_up(off, 128);
   const long long avail = (long long)smem_optin - 1024 - (long long)fixed;
   // ring slot: one stage of ~kStageTarget bytes, at least one router pair, one
   // gate/up pair and one down stage of this CTA's rows
   const int rows_per_cta = (H + p.grid - 1) / p.grid;
   int drs = std::min(rows_per_cta, moe::rows_per_group(p.fmt) * p.ng);
+  if (ilv) {
+    // every output row of the CTA in one down stage, then the slot's h rows
+    // (at most maxm pairs); the counters hold every union slot
+    if (drs < rows_per_cta || p.nslot_max > moe::CTRL_WORDS - moe::CTRL_SLOTCNT) return MOE_ERR_UNSUPPORTED;
+    p.d_hoff = (int)round_up((size_t)drs * (p.row2 + p.sc2), 16);
+  }
   // a slot holds a whole number of gate/up pairs (about kStageTarget bytes), so
   // that no slot space is left unused in the gate/up phases
   const size_t q0 = std::max<size_t>(1, std::min<size_t>(moe::kNC, moe::kStageTarget / p.pair_bytes));
   size_t slot = 0;
   for (;;) {
-    slot = round_up(std::max({q0 * p.pair_bytes, (size_t)p.rpair_bytes, (size_t)p.pair_bytes,
-                              (size_t)drs * (p.row2 + p.sc2)}), 128);
-    if ((long long)(moe::kMinSlots * slot) <= avail - (long long)maxm * I * 4 || drs == 1) break;
+    const size_t dstage = ilv ? (size_t)p.d_hoff + (size_t)maxm * I * 4 : (size_t)drs * (p.row2 + p.sc2);
+    slot = round_up(std::max({q0 * p.pair_bytes, (size_t)p.rpair_bytes, (size_t)p.pair_bytes, dstage}), 128);
+    if (ilv || (long long)(moe::kMinSlots * slot) <= avail - (long long)maxm * I * 4 || drs == 1) break;
     drs = (drs + 1) / 2;
   }
   // h staging area: all (expert, row) pairs when they fit next to kMinSlots ring
@@ -138,10 +153,11 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   long long hs_room = avail - (long long)(moe::kMinSlots * slot);
   int hs_pairs = (int)std::min<long long>(p.npair_max, hs_room > 0 ? hs_room / (long long)per_pair : 0);
   if (hs_pairs < maxm) hs_pairs = maxm;
+  if (ilv) hs_pairs = 0;  // h rows travel in the down stages
   p.hs_pairs = hs_pairs;
   // all pairs at once; else two buffers (one batch lands while the other is in
   // use) when each holds a full slot's rows; else one buffer
-  p.hs_nbuf = (hs_pairs < p.npair_max && hs_pairs >= 2 * maxm) ? 2 : 1;
+  p.hs_nbuf = (!ilv && hs_pairs < p.npair_max && hs_pairs >= 2 * maxm) ? 2 : 1;
   p.off_hs = (int)fixed;
   // routing scratch shares the h staging area (routing is over before any h is staged)
   size_t ro = fixed;
@@ -162,7 +178,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.off_ring = (int)round_up(area, 128);
   const long long ring_budget = (long long)smem_optin - 1024 - p.off_ring;
   const long long ns = ring_budget > 0 ? ring_budget / (long long)slot : 0;
-  if (ns < 2) return MOE_ERR_UNSUPPORTED;
+  if (ns < (ilv ? 3 : 2)) return MOE_ERR_UNSUPPORTED;
   p.slot_bytes = (int)slot;
   p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
   // the h area is idle from the end of routing until the down phase: the routed
@@ -174,12 +190,12 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   p.off_xslot = (int)fixed;
   // the x rows are dead once the gate/up items are done: their area holds one
   // more down-phase slot when it is large enough
-  p.nslots_d = ((size_t)maxm * H * 2 >= slot && p.nslots < moe::kMaxSlots) ? 1 : 0;
-  p.nslots_x = (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
+  p.nslots_d = (!ilv && (size_t)maxm * H * 2 >= slot && p.nslots < moe::kMaxSlots) ? 1 : 0;
+  p.nslots_x = ilv ? 0 : (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   // per-slot h fetches: measured faster for NVFP4 (its gate/up phase ends less
   // evenly across CTAs), not for bf16, which keeps one fetch after all h is stored.
   // Their mbarriers follow every ring slot's full barrier.
-  p.hs_perslot = (p.fmt == moe::FMT_NVFP4 && p.hs_nbuf == 1 && hs_pairs >= p.npair_max &&
+  p.hs_perslot = (!ilv && p.fmt == moe::FMT_NVFP4 && p.hs_nbuf == 1 && hs_pairs >= p.npair_max &&
                   p.nslot_max <= moe::kMaxSlots - moe::kHSlotBar &&
                   p.nslots + std::max(p.nslots_x, p.nslots_d) <= moe::kHSlotBar)
                      ? 1
@@ -189,6 +205,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p) 
   // router stages: at most kNC / 2 row pairs, so every row gets at least one warp
   p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
   p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
+  p.ilv_lag = 4;
   p.timeout_ns = kDefaultTimeoutNs;
   return MOE_OK;
 }
@@ -218,11 +235,43 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Weight and scratch pointers of `from` into `to` (two layouts of one handle).
+void bind_pointers(const Params& from, Params& to) {
+  to.router_w = from.router_w;
+  to.w13 = from.w13;
+  to.w13_s = from.w13_s;
+  to.w13_gs = from.w13_gs;
+  to.w2 = from.w2;
+  to.w2_s = from.w2_s;
+  to.w2_gs = from.w2_gs;
+  to.sh_w13 = from.sh_w13;
+  to.sh_w13_s = from.sh_w13_s;
+  to.sh_w13_gs = from.sh_w13_gs;
+  to.sh_w2 = from.sh_w2;
+  to.sh_w2_s = from.sh_w2_s;
+  to.sh_w2_gs = from.sh_w2_gs;
+  to.logits = from.logits;
+  to.hbuf = from.hbuf;
+  to.xflags = from.xflags;
+  to.ctrl = from.ctrl;
+}
+
+// Whether a persistent run of m rows takes the slot-interleaved kernel: always
+// when forced (mode 2), else where it measured faster on GB300 -- bf16 weights,
+// one token row (mode 1).
+bool interleaved(const moe_decode_handle* h, int m) {
+  if (h->sched != MOE_SCHED_PERSISTENT || !h->has_ilv) return false;
+  return h->ilv_mode == 2 || (h->ilv_mode == 1 && h->base.fmt == moe::FMT_BF16 && m == 1);
+}
+// The layout a run of m rows uses.
+const Params& active_params(const moe_decode_handle* h, int m) { return interleaved(h, m) ? h->ilv : h->base; }
+
 moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
   const int maxm_t = p.M == 1 ? 1 : 8;
+  const bool ilv = interleaved(h, p.M);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(moe::kThreads);
+  cfg.blockDim = dim3(ilv ? moe::kThreadsIlv : moe::kThreads);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -232,7 +281,8 @@ moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelExC(&cfg, kernel_for(p, maxm_t, moe::PH_ALL), args) != cudaSuccess)
+    if (cudaLaunchKernelExC(&cfg, kernel_for(p, maxm_t, ilv ? moe::PH_ILV : moe::PH_ALL), args) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
@@ -257,8 +307,8 @@ moe_status check_config_host(const moe_decode_config* cfg) { return check_config
 moe_status check_weights_host(const moe_decode_config& cfg, const moe_decode_weights* w) {
   return check_weights(cfg, w);
 }
-moe_status plan_host(const moe_decode_config& cfg, int sms, int smem_optin, Params& p) {
-  return plan(cfg, sms, smem_optin, p);
+moe_status plan_host(const moe_decode_config& cfg, int sms, int smem_optin, Params& p, bool ilv) {
+  return plan(cfg, sms, smem_optin, p, ilv);
 }
 void bind_weights_host(const moe_decode_weights& w, Params& p) {
   p.router_w = static_cast<const uint8_t*>(w.router_w);
@@ -307,8 +357,9 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
-  Params p;
-  if ((st = plan(*cfg, sms, optin, p)) != MOE_OK) return st;
+  Params p, pi;
+  if ((st = plan(*cfg, sms, optin, p, false)) != MOE_OK) return st;
+  const bool has_ilv = plan(*cfg, sms, optin, pi, true) == MOE_OK;
   // Every kernel this handle may launch gets the shared-memory size, and one
   // CTA of the single-kernel schedule must fit on every SM.
   const int phases[4] = {moe::PH_ALL, moe::PH_R, moe::PH_U, moe::PH_D};
@@ -320,6 +371,14 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
         return MOE_ERR_CUDA;
       int blocks = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, moe::kThreads, p.smem_bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (blocks < 1) return MOE_ERR_UNSUPPORTED;
+    }
+    if (has_ilv) {
+      const void* k = kernel_for(pi, mt, moe::PH_ILV);
+      int blocks = 0;
+      if (!k || cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pi.smem_bytes) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, moe::kThreadsIlv, pi.smem_bytes) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (blocks < 1) return MOE_ERR_UNSUPPORTED;
     }
@@ -388,6 +447,13 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->stage_w = reinterpret_cast<float*>(base + o_sw);
   h->base = p;
   h->max_slots = p.nslots;
+  h->has_ilv = has_ilv;
+  if (has_ilv) {
+    // the interleaved layout, with the same weights and scratch
+    bind_pointers(p, pi);
+    h->ilv = pi;
+    h->max_slots_ilv = pi.nslots;
+  }
   *out = h;
   return MOE_OK;
 }
@@ -399,7 +465,7 @@ moe_status moe_decode_run(moe_decode_handle* h, const void* x, const void* resid
   if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
     return MOE_ERR_INVALID_ARG;
-  Params p = h->base;
+  Params p = active_params(h, m_rows);
   p.M = m_rows;
   p.x = static_cast<const uint16_t*>(x);
   p.resid = static_cast<const uint16_t*>(residual);
@@ -460,19 +526,24 @@ moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t v
       return MOE_OK;
     case MOE_OPT_WAIT_TIMEOUT_NS:
       if (value <= 0) return MOE_ERR_INVALID_ARG;
-      h->base.timeout_ns = (unsigned long long)value;
+      h->base.timeout_ns = h->ilv.timeout_ns = (unsigned long long)value;
       return MOE_OK;
     case MOE_OPT_TEST_FLAGS:
       if (value < 0 || value > moe::TEST_SKIP_LOGITS) return MOE_ERR_INVALID_ARG;
-      h->base.test_flags = (int)value;
+      h->base.test_flags = h->ilv.test_flags = (int)value;
       return MOE_OK;
     case MOE_OPT_RING_SLOTS:
-      if (value < 2 || value > h->max_slots) return MOE_ERR_INVALID_ARG;
-      h->base.nslots = (int)value;
+      if (value < 2 || value > std::max(h->max_slots, h->max_slots_ilv)) return MOE_ERR_INVALID_ARG;
+      h->base.nslots = std::min((int)value, h->max_slots);
+      h->ilv.nslots = std::min((int)value, h->max_slots_ilv);
       return MOE_OK;
     case MOE_OPT_STAMPS:
       if (value & 7) return MOE_ERR_INVALID_ARG;
-      h->base.stamps = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+      h->base.stamps = h->ilv.stamps = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+      return MOE_OK;
+    case MOE_OPT_INTERLEAVE:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      h->ilv_mode = (int)value;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -484,13 +555,14 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_OPT_SCHED: *value = h->sched; return MOE_OK;
     case MOE_OPT_WAIT_TIMEOUT_NS: *value = (int64_t)h->base.timeout_ns; return MOE_OK;
     case MOE_OPT_TEST_FLAGS: *value = h->base.test_flags; return MOE_OK;
-    case MOE_OPT_RING_SLOTS: *value = h->base.nslots; return MOE_OK;
+    case MOE_OPT_RING_SLOTS: *value = active_params(h, 1).nslots; return MOE_OK;
     case MOE_OPT_STAMPS: *value = (int64_t)reinterpret_cast<uintptr_t>(h->base.stamps); return MOE_OK;
+    case MOE_OPT_INTERLEAVE: *value = h->has_ilv ? h->ilv_mode : 0; return MOE_OK;
     case MOE_INFO_GRID: *value = h->base.grid; return MOE_OK;
-    case MOE_INFO_THREADS: *value = moe::kThreads; return MOE_OK;
-    case MOE_INFO_SMEM: *value = h->base.smem_bytes; return MOE_OK;
-    case MOE_INFO_RING_SLOTS: *value = h->base.nslots; return MOE_OK;
-    case MOE_INFO_SLOT_BYTES: *value = h->base.slot_bytes; return MOE_OK;
+    case MOE_INFO_THREADS: *value = interleaved(h, 1) ? moe::kThreadsIlv : moe::kThreads; return MOE_OK;
+    case MOE_INFO_SMEM: *value = active_params(h, 1).smem_bytes; return MOE_OK;
+    case MOE_INFO_RING_SLOTS: *value = active_params(h, 1).nslots; return MOE_OK;
+    case MOE_INFO_SLOT_BYTES: *value = active_params(h, 1).slot_bytes; return MOE_OK;
     case MOE_INFO_KERNELS_PER_RUN: *value = h->sched == MOE_SCHED_PERSISTENT ? 1 : 3; return MOE_OK;
     case MOE_INFO_SCRATCH_BYTES: *value = (int64_t)h->scratch_bytes; return MOE_OK;
   }

@@ -11,6 +11,7 @@ static const void* pick(int phases) {
     case PH_R: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_R>);
     case PH_U: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_U>);
     case PH_D: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_NVFP4, MAXM, PH_D>);
+    case PH_ILV: return reinterpret_cast<const void*>(&moe_ilv_kernel<FMT_NVFP4, MAXM>);
     default: return nullptr;
   }
 }

@@ -75,6 +75,15 @@ __device__ __forceinline__ void split_range(int n, int c, int g, int& lo, int& h
   hi = (int)((unsigned)n * (unsigned)(c + 1) / (unsigned)g);
 }
 
+// Slot-interleaved schedule: the gate/up rows [lo, hi) of union slot s that
+// this CTA computes. Each slot's I rows are split over all CTAs; the map from
+// CTA to row block rotates from slot to slot, so the CTAs given one row more
+// differ between slots.
+__device__ __forceinline__ void ilv_rows(const Params& p, int s, int& lo, int& hi) {
+  const int c = (int)((blockIdx.x + (unsigned)s * (unsigned)kIlvRot) % (unsigned)p.grid);
+  split_range(p.I, c, p.grid, lo, hi);
+}
+
 // Position in the shared-memory ring: stage number, its slot and the slot's
 // mbarrier phase parity, advanced without divisions.
 // The slot count may differ between phases (the routed gate/up stages also use
@@ -654,6 +663,51 @@ __device__ __forceinline__ Ring consume_router(const Ctx& c, Ring ring) {
   return ring;
 }
 
+// The items of one gate/up stage that fall to this warp: dot products against
+// the x rows that chose the expert, SwiGLU and the combine weight, h stored in
+// pair order (four copies); the slot is handed back for the absent warps too.
+template <int FMT, int MAXM>
+__device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const ItemWalk& w, const Ring& ring,
+                                           int slot, bool shared, const XRegs<FMT, MAXM>& xr, const uint4* xs,
+                                           bool first) {
+  const Params& p = c.p;
+  const size_t rep_stride = (size_t)p.npair_max * p.I;
+  const int nq = w.count();
+  const int iq = w.offset(c.warp);
+  if (iq < nq && !c.aborted() && c.wait_full(ring)) {
+    if (c.warp == 0 && c.lane == 0 && first) c.stamp(ST_U_DATA);
+    const uint8_t* st = c.slot_ptr(ring.slot);
+    const int j = w.j + iq;
+    const uint32_t mask = shared ? (1u << p.M) - 1u : rt.slot_mask[slot];
+    const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane);
+    float gsg = 1.0f, gsu = 1.0f, gs2 = 1.0f;
+    if (FMT == FMT_NVFP4) {
+      const int e = shared ? -1 - slot : rt.slot_e[slot];
+      const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
+      gsg = gs[0];
+      gsu = gs[1];
+      gs2 = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];  // the down weights' tensor scale, applied once here
+    }
+    if (rs.m >= 0) {
+      float h = silu_f32(rs.g * gsg) * (rs.u * gsu);
+      if (!shared) h *= rt.slot_w[slot * p.maxm + rs.m];
+      if (FMT == FMT_NVFP4) h *= gs2;
+      // pair index: a shared slot holds every row (pairs s * M + m); a routed
+      // slot's rows follow its pair base in ascending order
+      const int pair = shared ? slot * p.M + rs.m : rt.pair_base[slot] + __popc(mask & ((1u << rs.m) - 1u));
+      // NVFP4: within a pair the values are interleaved for the down phase's
+      // 32-element chunks (element e of chunk c at (e / 4) * 4 * tg + 4 * c + e % 4),
+      // so each 16-byte read of a warp is contiguous; bf16 keeps the natural order
+      size_t at = (size_t)pair * p.I + j;
+      if (FMT == FMT_NVFP4) at = (size_t)pair * p.I + (size_t)((j % 32) >> 2) * (4 * p.tg) + 4 * (j / 32) + (j & 3);
+#pragma unroll
+      for (int r = 0; r < kHRep; ++r) p.hbuf[r * rep_stride + at] = h;
+    }
+    __syncwarp();
+    if (c.lane == 0) c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
+  }
+}
+
 enum ItemKind : int { ITEM_SHARED = 1, ITEM_ROUTED = 2 };
 
 // One phase of gate/up items (shared experts' or routed experts' row pairs):
@@ -672,49 +726,13 @@ __device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int
   }
   const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
   const int slot0 = kind == ITEM_ROUTED ? p.S : 0;
-  const size_t rep_stride = (size_t)p.npair_max * p.I;
   XRegs<FMT, MAXM> xr;
   load_xregs<FMT, MAXM>(c, xr);
   const int nsl_ring = kind == ITEM_ROUTED ? p.nslots + p.nslots_x : p.nslots;
   ring.fit(nsl_ring);
   for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(nsl_ring)) {
-    const int nq = w.count();
-    const int iq = w.offset(c.warp);
-    if (iq < nq && !c.aborted() && c.wait_full(ring)) {
-      if (c.warp == 0 && c.lane == 0 && w.a == lo) c.stamp(ST_U_DATA);
-      const uint8_t* st = c.slot_ptr(ring.slot);
-      const int slot = w.u + slot0;
-      const int j = w.j + iq;
-      const uint32_t mask = kind == ITEM_SHARED ? (1u << p.M) - 1u : rt.slot_mask[slot];
-      const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane);
-      float gsg = 1.0f, gsu = 1.0f, gs2 = 1.0f;
-      if (FMT == FMT_NVFP4) {
-        const int e = kind == ITEM_SHARED ? -1 - slot : rt.slot_e[slot];
-        const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
-        gsg = gs[0];
-        gsu = gs[1];
-        gs2 = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];  // the down weights' tensor scale, applied once here
-      }
-      if (rs.m >= 0) {
-        float h = silu_f32(rs.g * gsg) * (rs.u * gsu);
-        if (kind == ITEM_ROUTED) h *= rt.slot_w[slot * p.maxm + rs.m];
-        if (FMT == FMT_NVFP4) h *= gs2;
-        // pair index: a shared slot holds every row (pairs s * M + m); a routed
-        // slot's rows follow its pair base in ascending order
-        const int pair = kind == ITEM_SHARED ? slot * p.M + rs.m
-                                             : rt.pair_base[slot] + __popc(mask & ((1u << rs.m) - 1u));
-        // NVFP4: within a pair the values are interleaved for the down phase's
-        // 32-element chunks (element e of chunk c at (e / 4) * 4 * tg + 4 * c + e % 4),
-        // so each 16-byte read of a warp is contiguous; bf16 keeps the natural order
-        size_t at = (size_t)pair * p.I + j;
-        if (FMT == FMT_NVFP4) at = (size_t)pair * p.I + (size_t)((j % 32) >> 2) * (4 * p.tg) + 4 * (j / 32) + (j & 3);
-#pragma unroll
-        for (int r = 0; r < kHRep; ++r) p.hbuf[r * rep_stride + at] = h;
-      }
-      __syncwarp();
-      if (c.lane == 0) c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
-    }
-    w.advance(nq);
+    item_stage<FMT, MAXM>(c, rt, w, ring, w.u + slot0, kind == ITEM_SHARED, xr, xs, w.a == lo);
+    w.advance(w.count());
   }
   return ring;
 }
@@ -1122,6 +1140,136 @@ __device__ __forceinline__ void issue_h(const Ctx& c, const Route& rt, int sl0, 
   bulk_g2s_plain(smem_u32(dst), src, bytes, bar);
 }
 
+// One down stage: this thread's rows of the CTA's output block (group g, 16-byte
+// code chunk ch) against the h rows of the slot's pairs (hs, in pair order),
+// accumulated in fp32 over the slots.
+template <int FMT, int MAXM>
+__device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, const float* hs, uint32_t mask,
+                                           float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch, int nr) {
+  constexpr int RPG = rows_per_group(FMT);
+  const int drs = p.d_rows_stage;
+  int hp = 0;
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    if (!(mask >> m & 1u)) continue;
+    const float* hrow = hs + (size_t)hp * p.I;
+    ++hp;
+    if (FMT == FMT_BF16) {
+      const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
+      const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
+      const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      // every row of the group, branch-free: rows past the block repeat
+      // the last one (their sums are never written), so all loads issue
+      // before the arithmetic
+      uint4 wv[RPG];
+#pragma unroll
+      for (int ri = 0; ri < RPG; ++ri) {
+        const int r = min(g + ri * p.ng, nr - 1);
+        wv[ri] = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
+      }
+#pragma unroll
+      for (int ri = 0; ri < RPG; ++ri) dot8_bf16_f32(acc[ri][m], wv[ri], hv);
+    } else {
+      // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        float hv[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = *reinterpret_cast<const float4*>(hrow + 4 * ch + (blk * 4 + q) * 4 * p.tg);
+          hv[4 * q] = f.x;
+          hv[4 * q + 1] = f.y;
+          hv[4 * q + 2] = f.z;
+          hv[4 * q + 3] = f.w;
+        }
+#pragma unroll
+        for (int ri = 0; ri < RPG; ++ri) {
+          const int r = g + ri * p.ng;
+          if (r < nr) {
+            const uint2 qv = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2 + 16 * ch)[blk];
+            const uint32_t sb = st[(size_t)drs * p.row2 + (size_t)r * p.sc2 + 2 * ch + blk];
+            const float sv = __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2(sb) & 0xffffu)));
+            const uint32_t qw[2] = {qv.x, qv.y};
+            float part = 0.0f;
+#pragma unroll
+            for (int wi = 0; wi < 2; ++wi) {
+#pragma unroll
+              for (int by = 0; by < 4; ++by) {
+                const uint32_t wv = e2m1x2_to_f16x2((qw[wi] >> (8 * by)) & 0xffu);
+                const int e0 = wi * 8 + by * 2;
+                const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
+                part = fmaf(__low2float(wh), hv[e0], part);
+                part = fmaf(__high2float(wh), hv[e0 + 1], part);
+              }
+            }
+            acc[ri][m] = fmaf(sv, part, acc[ri][m]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Sums of each output row over the group's threads, plus the residual, rounded
+// once to bf16 and stored (rows rb_lo + r, r < nr).
+template <int FMT, int MAXM>
+__device__ __forceinline__ void write_rows(const Ctx& c, float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch,
+                                           bool active, int nr, int rb_lo) {
+  const Params& p = c.p;
+  constexpr int RPG = rows_per_group(FMT);
+  float* red = reinterpret_cast<float*>(c.sm + p.off_red);
+  const bool write = !c.aborted();
+  if (p.tg <= 32) {
+#pragma unroll
+    for (int ri = 0; ri < RPG; ++ri)
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m)
+        for (int o = p.tg >> 1; o; o >>= 1) acc[ri][m] += __shfl_xor_sync(kFull, acc[ri][m], o);
+    if (write && active && ch == 0) {
+#pragma unroll
+      for (int ri = 0; ri < RPG; ++ri) {
+        const int r = g + ri * p.ng;
+        if (r < nr) {
+          const int row = rb_lo + r;
+#pragma unroll
+          for (int m = 0; m < MAXM; ++m) {
+            if (m < p.M) {
+              const float rv = __uint_as_float((uint32_t)p.resid[(size_t)m * p.H + row] << 16);
+              p.out[(size_t)m * p.H + row] = f32_to_bf16_bits(rv + acc[ri][m]);
+            }
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int ri = 0; ri < RPG; ++ri)
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m) {
+        float v = acc[ri][m];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+        if (c.lane == 0) red[(c.warp * RPG + ri) * MAXM + m] = v;
+      }
+    bar_sync(kBarConsumers, kNC * 32);
+    const int wpg = p.tg / 32;
+    if (write && active && ch < 32) {  // first warp of each group writes
+      for (int q = c.lane; q < RPG * MAXM; q += 32) {
+        const int ri = q / MAXM, m = q % MAXM;
+        const int r = g + ri * p.ng;
+        if (r < nr && m < p.M) {
+          float y = 0.0f;
+          for (int w = 0; w < wpg; ++w) y += red[((g * wpg + w) * RPG + ri) * MAXM + m];
+          const int row = rb_lo + r;
+          const float rv = __uint_as_float((uint32_t)p.resid[(size_t)m * p.H + row] << 16);
+          p.out[(size_t)m * p.H + row] = f32_to_bf16_bits(rv + y);
+        }
+      }
+    }
+    bar_sync(kBarConsumers, kNC * 32);
+  }
+}
+
 // wait_u: the gate/up results come from this same kernel (single-kernel schedule)
 // nd: down-phase slots in the x area (0 or 1)
 template <int FMT, int MAXM>
@@ -1217,69 +1365,9 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         const uint64_t tw = p.stamps ? global_ns() : 0;
         const bool got = !c.aborted() && c.wait_full(ring);
         if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, global_ns() - tw);
-        if (got && have && active) {
-          const uint8_t* st = c.slot_ptr(ring.slot, true);
-          int hp = rt.pair_base[sl] - rt.pair_base[sl0];
-#pragma unroll
-          for (int m = 0; m < MAXM; ++m) {
-            if (!(mask >> m & 1u)) continue;
-            const float* hrow = hs + (size_t)hp * p.I;
-            ++hp;
-            if (FMT == FMT_BF16) {
-              const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
-              const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
-              const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-              // every row of the group, branch-free: rows past the block repeat
-              // the last one (their sums are never written), so all loads issue
-              // before the arithmetic
-              uint4 wv[RPG];
-#pragma unroll
-              for (int ri = 0; ri < RPG; ++ri) {
-                const int r = min(g + ri * p.ng, nr - 1);
-                wv[ri] = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
-              }
-#pragma unroll
-              for (int ri = 0; ri < RPG; ++ri) dot8_bf16_f32(acc[ri][m], wv[ri], hv);
-            } else {
-              // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
-#pragma unroll
-              for (int blk = 0; blk < 2; ++blk) {
-                float hv[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const float4 f = *reinterpret_cast<const float4*>(hrow + 4 * ch + (blk * 4 + q) * 4 * p.tg);
-                  hv[4 * q] = f.x;
-                  hv[4 * q + 1] = f.y;
-                  hv[4 * q + 2] = f.z;
-                  hv[4 * q + 3] = f.w;
-                }
-#pragma unroll
-                for (int ri = 0; ri < RPG; ++ri) {
-                  const int r = g + ri * p.ng;
-                  if (r < nr) {
-                    const uint2 qv = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2 + 16 * ch)[blk];
-                    const uint32_t sb = st[(size_t)drs * p.row2 + (size_t)r * p.sc2 + 2 * ch + blk];
-                    const float sv = __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2(sb) & 0xffffu)));
-                    const uint32_t qw[2] = {qv.x, qv.y};
-                    float part = 0.0f;
-#pragma unroll
-                    for (int wi = 0; wi < 2; ++wi) {
-#pragma unroll
-                      for (int by = 0; by < 4; ++by) {
-                        const uint32_t wv = e2m1x2_to_f16x2((qw[wi] >> (8 * by)) & 0xffu);
-                        const int e0 = wi * 8 + by * 2;
-                        const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
-                        part = fmaf(__low2float(wh), hv[e0], part);
-                        part = fmaf(__high2float(wh), hv[e0 + 1], part);
-                      }
-                    }
-                    acc[ri][m] = fmaf(sv, part, acc[ri][m]);
-                  }
-                }
-              }
-            }
-          }
-        }
+        if (got && have && active)
+          down_stage<FMT, MAXM>(p, c.slot_ptr(ring.slot, true), hs + (size_t)(rt.pair_base[sl] - rt.pair_base[sl0]) * p.I,
+                                mask, acc, g, ch, nr);
         __syncwarp();
         if (got && c.lane == 0) c.release(ring, 1);
       }
@@ -1296,56 +1384,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
       if (!c.aborted()) wait_xflags(c);
       bar_sync(kBarConsumers, kNC * 32);
     }
-    const bool write = !c.aborted();
-    if (p.tg <= 32) {
-#pragma unroll
-      for (int ri = 0; ri < RPG; ++ri)
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m)
-          for (int o = p.tg >> 1; o; o >>= 1) acc[ri][m] += __shfl_xor_sync(kFull, acc[ri][m], o);
-      if (write && active && ch == 0) {
-#pragma unroll
-        for (int ri = 0; ri < RPG; ++ri) {
-          const int r = g + ri * p.ng;
-          if (r < nr) {
-            const int row = rb_lo + r;
-#pragma unroll
-            for (int m = 0; m < MAXM; ++m) {
-              if (m < p.M) {
-                const float rv = __uint_as_float((uint32_t)p.resid[(size_t)m * p.H + row] << 16);
-                p.out[(size_t)m * p.H + row] = f32_to_bf16_bits(rv + acc[ri][m]);
-              }
-            }
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int ri = 0; ri < RPG; ++ri)
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-          float v = acc[ri][m];
-#pragma unroll
-          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-          if (c.lane == 0) red[(c.warp * RPG + ri) * MAXM + m] = v;
-        }
-      bar_sync(kBarConsumers, kNC * 32);
-      const int wpg = p.tg / 32;
-      if (write && active && ch < 32) {  // first warp of each group writes
-        for (int q = c.lane; q < RPG * MAXM; q += 32) {
-          const int ri = q / MAXM, m = q % MAXM;
-          const int r = g + ri * p.ng;
-          if (r < nr && m < p.M) {
-            float y = 0.0f;
-            for (int w = 0; w < wpg; ++w) y += red[((g * wpg + w) * RPG + ri) * MAXM + m];
-            const int row = rb_lo + r;
-            const float rv = __uint_as_float((uint32_t)p.resid[(size_t)m * p.H + row] << 16);
-            p.out[(size_t)m * p.H + row] = f32_to_bf16_bits(rv + y);
-          }
-        }
-      }
-      bar_sync(kBarConsumers, kNC * 32);
-    }
+    write_rows<FMT, MAXM>(c, acc, g, ch, active, nr, rb_lo);
   }
   // after an abort: h batches issued but not seen landing must land before exit
   if (c.tid == 0) {
@@ -1420,6 +1459,47 @@ struct Producer {
       }
   }
 
+  // Slot-interleaved schedule: a down stage carries the h rows of its slot
+  // behind the weights. The producer copies the weights when it issues the
+  // stage; the hand-off warp adds the h rows (counted on the same full barrier)
+  // once every CTA has counted the slot's gate/up items as stored.
+  // Gate/up stages of union slot s: this CTA's block of the slot's rows.
+  __device__ void ilv_pairs(const Route& rt, int s) {
+    const Params& p = c.p;
+    int lo, hi;
+    ilv_rows(p, s, lo, hi);
+    const int e = s < p.S ? -1 - s : rt.slot_e[s];
+    for (ItemWalk w(s * p.I + lo, s * p.I + hi, p.q, p.I); w.more(); ring.next(p.nslots)) {
+      const int nq = w.count();
+      uint32_t dst, bar;
+      if (!begin((uint32_t)nq * p.pair_bytes, dst, bar)) return;
+      copy_pairs(e, w.j, nq, dst, bar);
+      w.advance(nq);
+    }
+  }
+  // The down stage of union slot s: this CTA's output rows of the expert's down
+  // matrix now; the hand-off warp adds the slot's h rows later.
+  __device__ void ilv_down(const Route& rt, int s) {
+    const Params& p = c.p;
+    int r_lo, r_hi;
+    cta_rows(p, r_lo, r_hi);
+    const int nr = r_hi - r_lo;
+    const int e = s < p.S ? -1 - s : rt.slot_e[s];
+    const uint8_t* wt = e >= 0 ? p.w2 : p.sh_w2;
+    const uint8_t* ws = e >= 0 ? p.w2_s : p.sh_w2_s;
+    const size_t row0 = (size_t)(e >= 0 ? e : -1 - e) * p.H + r_lo;
+    const uint32_t cb = (uint32_t)nr * p.row2, sb = (uint32_t)nr * p.sc2;
+    const uint32_t hb = (uint32_t)(rt.pair_base[s + 1] - rt.pair_base[s]) * (uint32_t)p.I * 4u;
+    uint32_t dst, bar;
+    if (!begin(cb + sb + hb, dst, bar)) return;
+    bulk_g2s(dst, wt + row0 * p.row2, cb, bar, pol);
+    if (sb) bulk_g2s(dst + (uint32_t)p.d_rows_stage * p.row2, ws + row0 * p.sc2, sb, bar, pol);
+    reinterpret_cast<volatile int*>(c.sm + p.off_dslot)[s] = ring.slot;
+    __threadfence_block();  // the barrier's byte count and the slot before the count of issued stages
+    reinterpret_cast<volatile int*>(c.sm + p.off_ucnt)[ILV_DISSUED] = s + 1;
+    ring.next(p.nslots);
+  }
+
   __device__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar, bool d = false) {
     if (c.aborted()) return false;
     if (h_rt) {  // poll the h fetches while the slot is busy
@@ -1479,6 +1559,24 @@ struct Producer {
     }
   }
 
+  // Rows j .. j + nq - 1 of expert e (shared expert -1 - e when e < 0) as a
+  // gate block and an up block (plus the two scale blocks for NVFP4).
+  __device__ void copy_pairs(int e, int j, int nq, uint32_t dst, uint32_t bar) const {
+    const Params& p = c.p;
+    const uint8_t* wt = e >= 0 ? p.w13 : p.sh_w13;
+    const uint8_t* ws = e >= 0 ? p.w13_s : p.sh_w13_s;
+    const size_t ex = (size_t)(e >= 0 ? e : -1 - e);
+    const size_t rg = ex * 2 * p.I + j, ru = rg + p.I;  // first gate row, first up row
+    const uint32_t cb = (uint32_t)nq * p.row13;
+    bulk_g2s(dst, wt + rg * p.row13, cb, bar, pol);
+    bulk_g2s(dst + cb, wt + ru * p.row13, cb, bar, pol);
+    if (p.sc13) {
+      const uint32_t sb = (uint32_t)nq * p.sc13;
+      bulk_g2s(dst + 2 * cb, ws + rg * p.sc13, sb, bar, pol);
+      bulk_g2s(dst + 2 * cb + sb, ws + ru * p.sc13, sb, bar, pol);
+    }
+  }
+
   // Gate/up stages: consecutive rows of one expert as a gate block and an up
   // block (plus the two scale blocks for NVFP4).
   __device__ void pairs(bool shared_phase, const Route& rt) {
@@ -1497,19 +1595,7 @@ struct Producer {
       const int slot = w.u + (shared_phase ? 0 : p.S);
       uint32_t dst, bar;
       if (!begin((uint32_t)nq * p.pair_bytes, dst, bar)) return;
-      const int e = shared_phase ? -1 - slot : rt.slot_e[slot];
-      const uint8_t* wt = e >= 0 ? p.w13 : p.sh_w13;
-      const uint8_t* ws = e >= 0 ? p.w13_s : p.sh_w13_s;
-      const size_t ex = (size_t)(e >= 0 ? e : -1 - e);
-      const size_t rg = ex * 2 * p.I + w.j, ru = rg + p.I;  // first gate row, first up row
-      const uint32_t cb = (uint32_t)nq * p.row13;
-      bulk_g2s(dst, wt + rg * p.row13, cb, bar, pol);
-      bulk_g2s(dst + cb, wt + ru * p.row13, cb, bar, pol);
-      if (p.sc13) {
-        const uint32_t sb = (uint32_t)nq * p.sc13;
-        bulk_g2s(dst + 2 * cb, ws + rg * p.sc13, sb, bar, pol);
-        bulk_g2s(dst + 2 * cb + sb, ws + ru * p.sc13, sb, bar, pol);
-      }
+      copy_pairs(shared_phase ? -1 - slot : rt.slot_e[slot], w.j, nq, dst, bar);
       w.advance(nq);
     }
   }
@@ -1751,6 +1837,275 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_SCOUNT) = 0ull;
       if (PHASES == PH_ALL && p.hs_perslot)
         for (int i = 0; i < p.nslot_max; ++i) p.ctrl[CTRL_SLOTCNT + i] = 0u;
+      uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
+      if (e == 0xffffffffu) e = 0u;
+      p.ctrl[CTRL_EPOCH] = e;
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// the slot-interleaved single kernel
+// --------------------------------------------------------------------------
+// Gate/up items of union slot s (this CTA's row block), then the warp's arrival
+// on the slot's counter in shared memory (a CTA-scope release of its h stores).
+template <int FMT, int MAXM>
+__device__ __forceinline__ Ring ilv_items(const Ctx& c, const Route& rt, int s, Ring ring, int& rot) {
+  const Params& p = c.p;
+  int lo, hi;
+  ilv_rows(p, s, lo, hi);
+  if (hi > lo) {
+    const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
+    XRegs<FMT, MAXM> xr;
+    load_xregs<FMT, MAXM>(c, xr);
+    ItemWalk w(s * p.I + lo, s * p.I + hi, p.q, p.I);
+    w.r = rot;  // the warp rotation carries over between slots
+    for (; w.more(); ring.next(p.nslots)) {
+      item_stage<FMT, MAXM>(c, rt, w, ring, s, s < p.S, xr, xs, false);
+      w.advance(w.count());
+    }
+    rot = w.r;
+    fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
+  }
+  // arrival (every warp, every slot, with or without items): the hand-off warp
+  // counts the slot done when all kNC warps have arrived
+  __syncwarp();
+  if (c.lane == 0) {
+    __threadfence_block();
+    atomicAdd(reinterpret_cast<int*>(c.sm + p.off_ucnt) + (s & (kIlvCnt - 1)), 1);
+  }
+  return ring;
+}
+
+// The down stage of union slot s: the CTA's output rows of the expert's down
+// matrix against the slot's h rows, both in the stage's ring slot.
+template <int FMT, int MAXM>
+__device__ __forceinline__ Ring ilv_down(const Ctx& c, const Route& rt, int s, Ring ring,
+                                         float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch, bool active,
+                                         int nr) {
+  const Params& p = c.p;
+  const bool got = !c.aborted() && c.wait_full(ring);
+  if (got && active) {
+    const uint8_t* st = c.slot_ptr(ring.slot);
+    down_stage<FMT, MAXM>(p, st, reinterpret_cast<const float*>(st + p.d_hoff), rt.slot_mask[s], acc, g, ch, nr);
+  }
+  __syncwarp();
+  if (got && c.lane == 0) c.release(ring, 1);
+  ring.next(p.nslots);
+  return ring;
+}
+
+// The h rows of slot s into its down stage's ring slot (hand-off warp, lane 0).
+__device__ __forceinline__ void ilv_fetch(const Ctx& c, const Route& rt, int s) {
+  const Params& p = c.p;
+  const int rs = reinterpret_cast<const volatile int*>(c.sm + p.off_dslot)[s];
+  const int p0 = rt.pair_base[s];
+  const uint32_t bytes = (uint32_t)(rt.pair_base[s + 1] - p0) * (uint32_t)p.I * 4u;
+  const float* src = p.hbuf + ((size_t)(blockIdx.x % kHRep) * p.npair_max + p0) * p.I;
+  fence_proxy_async_global();  // the acquired h stores before the bulk copy that reads them
+  bulk_g2s_plain(smem_u32(c.slot_ptr(rs) + p.d_hoff), src, bytes, c.full0 + 8u * (uint32_t)rs);
+}
+
+// Two hand-off warps keep GPU-scope fences and L2 polls away from the consumer
+// warps and the producer. The publisher (lane 0) counts this CTA's gate/up
+// items of a slot as stored once every consumer warp has arrived, with one fence
+// for all slots found complete.
+__device__ __forceinline__ void ilv_publish(const Ctx& c) {
+  const Params& p = c.p;
+  volatile int* w = reinterpret_cast<volatile int*>(c.sm + p.off_ucnt);
+  const int nsl = p.S + c.misc[MISC_NROUTED];
+  uint32_t spins = 0;
+  for (int pub = 0; pub < nsl;) {
+    int np = pub;
+    while (np < nsl && w[np & (kIlvCnt - 1)] >= kNC * (np / kIlvCnt + 1)) ++np;
+    if (np > pub) {
+      __threadfence();  // acquires the warps' h stores (through the counters) and releases them
+      for (; pub < np; ++pub) {
+        int lo, hi;
+        ilv_rows(p, pub, lo, hi);
+        if (hi > lo) red_add_u32(p.ctrl + CTRL_SLOTCNT + pub, (uint32_t)(hi - lo));
+      }
+      continue;
+    }
+    __nanosleep(32);
+    // the consumers arrive even after an abort; bounded all the same
+    if ((++spins & 63) == 0 && global_ns() - c.t0 > 2 * p.timeout_ns) {
+      c.fail(SITE_HIDDEN);
+      return;
+    }
+  }
+}
+
+// The fetcher (lane 0) copies the h rows of each issued down stage once every
+// CTA has counted the slot. After an abort it copies the remaining h parts
+// anyway, so that every armed full barrier completes.
+__device__ __forceinline__ void ilv_fetcher(const Ctx& c, const Route& rt) {
+  const Params& p = c.p;
+  volatile int* w = reinterpret_cast<volatile int*>(c.sm + p.off_ucnt);
+  int hn = 0;
+  uint32_t spins = 0;
+  bool failed = false;
+  for (;;) {
+    const int di = w[ILV_DISSUED];
+    __threadfence_block();  // the issued stages' slots after their count
+    const bool ab = c.aborted();
+    bool progress = false;
+    while (hn < di && (ab || ld_acquire_u32(p.ctrl + CTRL_SLOTCNT + hn) >= (uint32_t)p.I)) {
+      ilv_fetch(c, rt, hn++);
+      progress = true;
+    }
+    if (w[ILV_PDONE] && hn == w[ILV_DISSUED]) break;
+    if (!progress) {
+      __nanosleep(32);
+      if ((++spins & 15) == 0) {
+        if (!ab && c.peer_failed()) c.abort_local();  // another CTA gave up: stop waiting on it
+        if (c.expired()) {
+          if (!failed) c.fail(SITE_HIDDEN);
+          failed = true;
+          if (global_ns() - c.t0 > 2 * p.timeout_ns) break;  // bounded even if the others stall
+        }
+      }
+    }
+  }
+}
+
+// One kernel for the whole step, phases overlapped slot by slot: router rows
+// and the shared experts' gate/up rows, routing, then for t = S, S + 1, ...:
+// the gate/up items of slot t and every down stage of a slot s with
+// s + lag <= t. A down stage needs the h rows of its slot from every CTA; the
+// lag leaves the slot's count time to complete while later gate/up stages stream.
+template <int FMT, int MAXM>
+__global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctx c(p, sm);
+  Route rt(p, sm);
+  if (c.tid == 0) {
+    for (int i = 0; i < p.nslots; ++i) {
+      mbar_init(c.full0 + 8u * i, 1);
+      mbar_init(c.empty0 + 8u * i, kNC);
+      c.slot_seq[i] = -1;
+    }
+    mbar_init(c.xbar, 1);
+    mbar_init_fence();
+    c.misc[MISC_ABORT] = 0;
+    c.misc[MISC_NROUTED] = 0;
+  }
+  if (c.tid < ILV_WORDS) reinterpret_cast<int*>(sm + p.off_ucnt)[c.tid] = 0;
+  for (int e = c.tid; e < p.E; e += kThreadsIlv) rt.emask[e] = 0u;
+  for (int e = c.tid; e < (p.E + 31) / 32; e += kThreadsIlv) rt.bitmap[e] = 0u;
+  __syncthreads();
+
+  int r_lo, r_hi;
+  cta_rows(p, r_lo, r_hi);
+  const int nr = r_hi - r_lo;  // every output row of the CTA in one down stage (planned)
+  if (c.warp > kNC) {
+    // ------------------------------------------------------------ hand-off warps
+    __syncwarp();
+    bar_sync(kBarRoute, kThreadsIlv);
+    if (c.lane == 0) {
+      if (c.warp == kNC + 1)
+        ilv_publish(c);
+      else
+        ilv_fetcher(c, rt);
+    }
+    __syncwarp();
+  } else if (c.warp == kNC) {
+    // ------------------------------------------------------------ producer
+    Producer pr(c);
+    if (c.lane == 0) {
+      c.stamp(ST_START);
+      pr.x_rows();
+      pr.router();
+      for (int s = 0; s < p.S; ++s) pr.ilv_pairs(rt, s);
+      c.stamp(ST_P_R_ISSUED);
+      pr.prefetch_shared_down();
+    }
+    __syncwarp();
+    bar_sync(kBarRoute, kThreadsIlv);
+    if (c.lane == 0) {
+      c.stamp(ST_P_ROUTE);
+      const int nsl = p.S + c.misc[MISC_NROUTED];
+      int dnext = 0;
+      for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
+        if (t < nsl) pr.ilv_pairs(rt, t);
+        while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t) pr.ilv_down(rt, dnext++);
+      }
+      c.stamp(ST_P_D_ISSUED);
+      __threadfence_block();
+      reinterpret_cast<volatile int*>(sm + p.off_ucnt)[ILV_PDONE] = 1;
+      if (c.aborted()) {
+        pr.drain();  // the hand-off warp completes the h parts of armed down stages
+        // the x copy may still be in flight if the consumers gave up before it landed
+        const uint64_t t = global_ns();
+        while (!mbar_try_wait(c.xbar, 0) && global_ns() - t < p.timeout_ns) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers
+    if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
+    prepare_x(c);
+    bar_sync(kBarConsumers, kNC * 32);
+    if (c.tid == 0) c.stamp(ST_X_LOADED);
+    if (p.out_aliases_x && c.tid == 0) st_tagged(p.xflags + blockIdx.x, c.epoch(), 0.0f);
+    Ring ring;
+    ring = consume_router<MAXM>(c, ring);
+    bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
+    if (c.tid == 0) {
+      count_done(p, CTRL_RCOUNT);
+      c.stamp(ST_RFLAG);
+    }
+    route_rows(c, rt, true);
+    bar_arrive(kBarRoute, kThreadsIlv);
+    if (c.tid == 0) c.stamp(ST_ROUTED);
+    if (FMT == FMT_NVFP4) {  // the router is done with the bf16 x rows
+      x_to_f16(c);
+      bar_sync(kBarConsumers, kNC * 32);
+    }
+    constexpr int RPG = rows_per_group(FMT);
+    const int g = c.tid / p.tg, ch = c.tid % p.tg;
+    const bool active = g < p.ng;
+    float acc[RPG][MAXM];
+#pragma unroll
+    for (int ri = 0; ri < RPG; ++ri)
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m) acc[ri][m] = 0.0f;
+    const int nsl = p.S + c.misc[MISC_NROUTED];
+    int rot = 0, dnext = 0;
+#pragma unroll 1
+    for (int s = 0; s < p.S; ++s) ring = ilv_items<FMT, MAXM>(c, rt, s, ring, rot);
+    if (c.tid == 0) c.stamp(ST_R_DONE);
+#pragma unroll 1
+    for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
+      if (t < nsl) ring = ilv_items<FMT, MAXM>(c, rt, t, ring, rot);
+      while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t)
+        ring = ilv_down<FMT, MAXM>(c, rt, dnext++, ring, acc, g, ch, active, nr);
+    }
+    if (c.tid == 0) c.stamp(ST_D_SUMMED);
+    if (nr > 0) {
+      if (p.out_aliases_x) {
+        if (!c.aborted()) wait_xflags(c);
+        bar_sync(kBarConsumers, kNC * 32);
+      }
+      write_rows<FMT, MAXM>(c, acc, g, ch, active, nr, r_lo);
+    }
+    if (c.tid == 0) {
+      c.stamp(ST_D_DONE);
+      if (p.stamps) {
+        p.stamps[(size_t)blockIdx.x * kStampSlots + ST_CLOCK_MHZ] =
+            (unsigned long long)(clock64() - c.c0) * 1000ull / (global_ns() - c.t0 + 1);
+      }
+    }
+  }
+  __syncthreads();
+  if (c.tid == 0) {
+    const uint32_t prev = atomicAdd(&p.ctrl[CTRL_EXIT], 1u);
+    if (prev == gridDim.x - 1) {
+      p.ctrl[CTRL_EXIT] = 0u;
+      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
+      for (int i = 0; i < p.nslot_max; ++i) p.ctrl[CTRL_SLOTCNT + i] = 0u;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;
       p.ctrl[CTRL_EPOCH] = e;

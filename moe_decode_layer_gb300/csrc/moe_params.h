@@ -6,6 +6,7 @@ namespace moe {
 
 constexpr int kNC = 12;                  // consumer warps per CTA
 constexpr int kThreads = (kNC + 1) * 32; // + one producer warp
+constexpr int kThreadsIlv = kThreads + 64;  // slot-interleaved kernel: + two hand-off warps
 constexpr int kRpgMax = 6;               // down-projection rows per thread group per stage (at most)
 constexpr int kRpgFp4 = 3;               // NVFP4: its 32-element chunks leave more groups, so fewer rows each
 __host__ __device__ constexpr int rows_per_group(int fmt) { return fmt == 0 ? kRpgMax : kRpgFp4; }
@@ -24,6 +25,15 @@ enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
 // Phases a kernel runs: router + shared gate/up (R), routed gate/up (U),
 // down + combine + residual (D).
 enum Phase : int { PH_R = 1, PH_U = 2, PH_D = 4, PH_ALL = 7 };
+// Kernel selector (not a phase set): the single kernel with the slot-interleaved
+// schedule -- each CTA computes a block of rows of every union slot's gate/up
+// items, and the down stage of slot s follows the gate/up items of slot s + lag.
+constexpr int PH_ILV = 8;
+constexpr int kIlvRot = 37;  // per slot, the CTA -> row-block map rotates by this many CTAs
+constexpr int kIlvCnt = 8;   // per-CTA arrival counters of the interleaved schedule (slot s uses s % 8)
+// Interleaved-schedule words in shared memory (off_ucnt): the arrival counters,
+// then the down stages issued and the producer's done flag.
+enum IlvWord : int { ILV_DISSUED = kIlvCnt, ILV_PDONE = kIlvCnt + 1, ILV_WORDS = kIlvCnt + 4 };
 
 // Control words at the start of the handle's scratch.
 // CTRL_RCOUNT / CTRL_UCOUNT / CTRL_SCOUNT (64-bit, 8-byte aligned word index): CTAs
@@ -141,6 +151,12 @@ struct Params {
   int off_emask, off_bitmap, off_slot_of, off_slot_e, off_slot_mask, off_slot_w, off_pair_base;
   int off_lg, off_cand, off_lmax, off_ccount, off_thr, off_wtmp, off_wpc;  // routing scratch (in the hs area)
   int off_pair_sr;   // [npair_max] (slot << 4 | row) of each (slot, row) pair
+  // slot-interleaved schedule
+  int ilv_lag;       // the down stage of slot s follows the gate/up items of slot s + ilv_lag
+  int d_hoff;        // byte offset of the h rows inside a down stage's ring slot
+  int off_ucnt;      // [ILV_WORDS]: consumer warps done with a slot's gate/up items (cumulative
+                     // per counter), down stages issued, producer done
+  int off_dslot;     // [nslot_max] ring slot of each slot's down stage (producer)
   int off_red, off_misc, off_ring;
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;

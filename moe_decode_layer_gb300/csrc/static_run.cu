@@ -70,7 +70,10 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   moe::Params p;
-  if ((st = moe::plan_host(*cfg, sms, optin, p)) != MOE_OK) return st;
+  // the slot-interleaved kernel where it measured faster (bf16 weights, one token
+  // row) and its layout fits, else the phase-ordered one
+  const bool ilv = cfg->wdtype == MOE_W_BF16 && m_rows == 1 && moe::plan_host(*cfg, sms, optin, p, true) == MOE_OK;
+  if (!ilv && (st = moe::plan_host(*cfg, sms, optin, p, false)) != MOE_OK) return st;
   // scratch layout inside the static array; larger configs are rejected
   const size_t maxm = cfg->max_rows, E = cfg->num_experts, I = cfg->inter;
   const size_t o_logits = kCtrlBytes;
@@ -98,8 +101,8 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   p.out_aliases_x = (xa < oa + bytes && oa < xa + bytes) ? 1 : 0;
 
   const int maxm_t = m_rows == 1 ? 1 : 8;
-  const void* kernel = p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, moe::PH_ALL)
-                                               : moe::kernel_nvfp4(maxm_t, moe::PH_ALL);
+  const int which = ilv ? moe::PH_ILV : moe::PH_ALL;
+  const void* kernel = p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, which) : moe::kernel_nvfp4(maxm_t, which);
   if (!kernel) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -108,7 +111,7 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   if (cudaMemsetAsync(p.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(p.grid);
-  lc.blockDim = dim3(moe::kThreads);
+  lc.blockDim = dim3(ilv ? moe::kThreadsIlv : moe::kThreads);
   lc.dynamicSmemBytes = p.smem_bytes;
   lc.stream = s;
   cudaLaunchAttribute attr[1];

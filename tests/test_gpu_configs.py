@@ -40,7 +40,7 @@ def fp4layer():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("sched", ["persistent", "pdl_chain"])
+@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "pdl_chain"])
 @pytest.mark.parametrize("m", [1, 6])
 def test_nvfp4_layer(fp4layer, sched, m):
     shape = synth.MUSE_NVFP4

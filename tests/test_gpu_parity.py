@@ -19,7 +19,7 @@ from tests import helpers
 
 pytestmark = pytest.mark.gpu
 
-SCHEDS = ["persistent", "pdl_chain", "chain"]
+SCHEDS = ["persistent", "phased", "interleaved", "pdl_chain", "chain"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -178,7 +178,8 @@ def test_shapes(cfg, m):
             ref, _, _ = helpers.oracle_layer(shape, layer, x, x)
             helpers.assert_close(out, ref)
         outs.append(out)
-    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
 
 
 # ----------------------------------------------------------------------------- Ling-shaped layer
@@ -191,13 +192,25 @@ def test_ling_m1(ling, sched):
     _check(synth.LING, ling, x, out, idx, w)
 
 
-@pytest.mark.parametrize("sched", ["persistent", "pdl_chain"])
+@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "pdl_chain"])
 def test_ling_m6_correlated(ling, sched):
     x = helpers.hidden_with_margin(ling["router_w"], 6, synth.LING.top_k, seed=1, rho=0.5)
     _, out, idx, w = _run(synth.LING, ling, x, sched=sched)
     _check(synth.LING, ling, x, out, idx, w)
     distinct = len(set(idx.flatten().tolist()))
     assert 8 <= distinct <= 48
+
+
+def test_ling_interleave_modes(ling):
+    """The Ling-shaped layer fits the slot-interleaved layout at M = 1 and M = 6:
+    the default mode (1) uses it for single-row runs, "interleaved" forces it (2),
+    "phased" switches it off (0)."""
+    for m in (1, 6):
+        assert MoEDecodeLayer(synth.LING, ling, m).info(_lib.MOE_OPT_INTERLEAVE) == 1
+        assert MoEDecodeLayer(synth.LING, ling, m, sched="interleaved").info(_lib.MOE_OPT_INTERLEAVE) == 2
+        assert MoEDecodeLayer(synth.LING, ling, m, sched="phased").info(_lib.MOE_OPT_INTERLEAVE) == 0
+    assert MoEDecodeLayer(synth.LING, ling, 1).info(_lib.MOE_INFO_THREADS) == 480
+    assert MoEDecodeLayer(synth.LING, ling, 1, sched="phased").info(_lib.MOE_INFO_THREADS) == 416
 
 
 def test_ling_moe_part_alone(ling):
