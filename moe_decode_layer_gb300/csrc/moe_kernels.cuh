@@ -58,6 +58,7 @@ namespace moe {
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kBarConsumers = 1;  // named barrier: the kNC consumer warps
 constexpr int kBarRoute = 2;      // named barrier: consumers -> producer, routing ready
+constexpr int kBarRouting = 3;    // named barrier: the routing warps (interleaved kernel)
 constexpr int kStageBatch = 8;    // tagged words in flight per thread when staging h
 
 // --------------------------------------------------------------------------
@@ -83,6 +84,14 @@ __device__ __forceinline__ void ilv_rows(const Params& p, int s, int& lo, int& h
   const int c = (int)((blockIdx.x + (unsigned)s * (unsigned)kIlvRot) % (unsigned)p.grid);
   split_range(p.I, c, p.grid, lo, hi);
 }
+// Interleaved schedule: consumer warps 0 .. ilv_nrw - 1 route; the others
+// compute the shared experts' gate/up items meanwhile, in stages of at most
+// ilv_sq pairs (one item per warp and stage).
+__device__ __forceinline__ int ilv_nrw(const Params& p) { return max(p.M, 2); }
+__device__ __forceinline__ int ilv_sq(const Params& p) { return min(p.q, kNC - ilv_nrw(p)); }
+// Threads meeting at the routing-ready barrier: the routing warps, the producer
+// and the two hand-off warps.
+__device__ __forceinline__ int ilv_route_threads(const Params& p) { return (ilv_nrw(p) + 3) * 32; }
 
 // Position in the shared-memory ring: stage number, its slot and the slot's
 // mbarrier phase parity, advanced without divisions.
@@ -252,8 +261,9 @@ static __device__ __forceinline__ bool wait_count(const Ctx& c, int word, uint32
 // row pairs; a stage holds up to qr of them (no slot boundaries). Item t of the
 // CTA's range [lo, hi) goes to consumer warp (t - lo) % kNC.
 struct ItemWalk {
-  int a, hi, u, j, r;  // next item, end, its slot and row, (a - lo) % kNC
+  int a, hi, u, j, r;  // next item, end, its slot and row, (a - lo) % nw
   int q, I;            // items per stage, rows per slot (0: no boundaries)
+  int w0 = 0, nw = kNC;  // the warps that take items: w0 .. w0 + nw - 1 (q <= nw)
   __device__ __forceinline__ ItemWalk(int lo, int hi_, int q_, int I_) : a(lo), hi(hi_), r(0), q(q_), I(I_) {
     u = I_ > 0 ? lo / I_ : 0;
     j = I_ > 0 ? lo - u * I_ : lo;
@@ -267,8 +277,9 @@ struct ItemWalk {
   }
   // offset of warp w's item in the current stage (>= count() when it has none)
   __device__ __forceinline__ int offset(int w) const {
-    const int d = w - r;
-    return d < 0 ? d + kNC : d;
+    if (w < w0 || w >= w0 + nw) return kNC;
+    const int d = w - w0 - r;
+    return d < 0 ? d + nw : d;
   }
   __device__ __forceinline__ void advance(int n) {
     a += n;
@@ -278,7 +289,7 @@ struct ItemWalk {
       ++u;
     }
     r += n;
-    if (r >= kNC) r -= kNC;
+    if (r >= nw) r -= nw;
   }
 };
 
@@ -741,28 +752,29 @@ __device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int
 // consumer phase T: top-k per row and the expert union
 // --------------------------------------------------------------------------
 // Copies n 16-byte units of tagged words (two fp32 values each) from src to dst
-// in shared memory: every consumer thread keeps kStageBatch loads in flight and
-// re-polls only the units whose tag is not current yet. False on abort / timeout.
+// in shared memory: each of the nthr calling threads keeps kStageBatch loads in
+// flight and re-polls only the units whose tag is not current yet. False on
+// abort / timeout.
 static __device__ __forceinline__ bool stage_tagged(const Ctx& c, const unsigned long long* src, float* dst, int n,
-                                                 uint32_t site) {
+                                                 uint32_t site, int nthr) {
   const uint32_t ep = c.epoch();
   uint32_t spins = 0;
-  for (int base = c.tid; base < n; base += kNC * 32 * kStageBatch) {
+  for (int base = c.tid; base < n; base += nthr * kStageBatch) {
     uint32_t pending = 0;
 #pragma unroll
     for (int k = 0; k < kStageBatch; ++k)
-      if (base + k * kNC * 32 < n) pending |= 1u << k;
+      if (base + k * nthr < n) pending |= 1u << k;
     while (pending) {
       unsigned long long v0[kStageBatch], v1[kStageBatch];
 #pragma unroll
       for (int k = 0; k < kStageBatch; ++k) {
         v0[k] = v1[k] = 0;
-        if (pending >> k & 1u) ld_tagged2(src + 2 * (base + k * kNC * 32), v0[k], v1[k]);
+        if (pending >> k & 1u) ld_tagged2(src + 2 * (base + k * nthr), v0[k], v1[k]);
       }
 #pragma unroll
       for (int k = 0; k < kStageBatch; ++k) {
         if ((pending >> k & 1u) && (uint32_t)(v0[k] >> 32) == ep && (uint32_t)(v1[k] >> 32) == ep) {
-          const int u = base + k * kNC * 32;
+          const int u = base + k * nthr;
           dst[2 * u] = __uint_as_float((uint32_t)v0[k]);
           dst[2 * u + 1] = __uint_as_float((uint32_t)v1[k]);
           pending &= ~(1u << k);
@@ -1037,21 +1049,24 @@ __device__ __forceinline__ void union_one_row(const Ctx& c, const Route& rt) {
   }
 }
 
-static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk) {
+// nthr threads (the first nthr / 32 consumer warps, at least p.M) route; they
+// meet at named barrier `bar`.
+static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk,
+                                                  int nthr = kNC * 32, int bar = kBarConsumers) {
   const Params& p = c.p;
   // every CTA's router logits stored (count), before reading any of them
   if (c.tid == 0) {
     if (!c.aborted()) wait_count(c, CTRL_RCOUNT, SITE_FLAGS);
     c.stamp(ST_RCOUNT);
   }
-  bar_sync(kBarConsumers, kNC * 32);
+  bar_sync(bar, nthr);
   // this CTA's replica of the logits into shared memory (coalesced, tag-checked)
   float* lg = reinterpret_cast<float*>(c.sm + p.off_lg);
   const unsigned long long* src = p.logits + (size_t)(blockIdx.x % kLogitRep) * p.maxm * p.E;
-  bool ok = !c.aborted() && stage_tagged(c, src, lg, p.M * p.E / 2, SITE_LOGITS);
+  bool ok = !c.aborted() && stage_tagged(c, src, lg, p.M * p.E / 2, SITE_LOGITS, nthr);
   if (!ok)  // keep going on well-defined data: outputs are void after a timeout
-    for (int i = c.tid; i < p.M * p.E; i += kNC * 32) lg[i] = 0.0f;
-  bar_sync(kBarConsumers, kNC * 32);
+    for (int i = c.tid; i < p.M * p.E; i += nthr) lg[i] = 0.0f;
+  bar_sync(bar, nthr);
   if (c.tid == 0) c.stamp(ST_LOGITS);
   if (c.warp < p.M) {
     if (p.E <= 16 * 32)
@@ -1059,7 +1074,7 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
     else
       topk_row<32>(c, rt, c.warp, write_topk);
   }
-  bar_sync(kBarConsumers, kNC * 32);
+  bar_sync(bar, nthr);
   if (c.tid == 0) c.stamp(ST_TOPK);
   if (c.warp == 0) {
     if (p.M == 1)
@@ -1067,7 +1082,7 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
     else
       union_warp(c, rt);
   }
-  bar_sync(kBarConsumers, kNC * 32);
+  bar_sync(bar, nthr);
 }
 
 // --------------------------------------------------------------------------
@@ -1464,12 +1479,12 @@ struct Producer {
   // stage; the hand-off warp adds the h rows (counted on the same full barrier)
   // once every CTA has counted the slot's gate/up items as stored.
   // Gate/up stages of union slot s: this CTA's block of the slot's rows.
-  __device__ void ilv_pairs(const Route& rt, int s) {
+  __device__ void ilv_pairs(const Route& rt, int s, int q) {
     const Params& p = c.p;
     int lo, hi;
     ilv_rows(p, s, lo, hi);
     const int e = s < p.S ? -1 - s : rt.slot_e[s];
-    for (ItemWalk w(s * p.I + lo, s * p.I + hi, p.q, p.I); w.more(); ring.next(p.nslots)) {
+    for (ItemWalk w(s * p.I + lo, s * p.I + hi, q, p.I); w.more(); ring.next(p.nslots)) {
       const int nq = w.count();
       uint32_t dst, bar;
       if (!begin((uint32_t)nq * p.pair_bytes, dst, bar)) return;
@@ -1850,7 +1865,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
 // Gate/up items of union slot s (this CTA's row block), then the warp's arrival
 // on the slot's counter in shared memory (a CTA-scope release of its h stores).
 template <int FMT, int MAXM>
-__device__ __forceinline__ Ring ilv_items(const Ctx& c, const Route& rt, int s, Ring ring, int& rot) {
+__device__ __forceinline__ Ring ilv_items(const Ctx& c, const Route& rt, int s, Ring ring, int& rot, int w0, int nw,
+                                          int q) {
   const Params& p = c.p;
   int lo, hi;
   ilv_rows(p, s, lo, hi);
@@ -1858,7 +1874,9 @@ __device__ __forceinline__ Ring ilv_items(const Ctx& c, const Route& rt, int s, 
     const uint4* xs = reinterpret_cast<const uint4*>(c.sm + p.off_x);
     XRegs<FMT, MAXM> xr;
     load_xregs<FMT, MAXM>(c, xr);
-    ItemWalk w(s * p.I + lo, s * p.I + hi, p.q, p.I);
+    ItemWalk w(s * p.I + lo, s * p.I + hi, q, p.I);
+    w.w0 = w0;
+    w.nw = nw;
     w.r = rot;  // the warp rotation carries over between slots
     for (; w.more(); ring.next(p.nslots)) {
       item_stage<FMT, MAXM>(c, rt, w, ring, s, s < p.S, xr, xs, false);
@@ -2002,7 +2020,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
   if (c.warp > kNC) {
     // ------------------------------------------------------------ hand-off warps
     __syncwarp();
-    bar_sync(kBarRoute, kThreadsIlv);
+    bar_sync(kBarRoute, ilv_route_threads(p));
     if (c.lane == 0) {
       if (c.warp == kNC + 1)
         ilv_publish(c);
@@ -2017,18 +2035,18 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
       c.stamp(ST_START);
       pr.x_rows();
       pr.router();
-      for (int s = 0; s < p.S; ++s) pr.ilv_pairs(rt, s);
+      for (int s = 0; s < p.S; ++s) pr.ilv_pairs(rt, s, ilv_sq(p));
       c.stamp(ST_P_R_ISSUED);
       pr.prefetch_shared_down();
     }
     __syncwarp();
-    bar_sync(kBarRoute, kThreadsIlv);
+    bar_sync(kBarRoute, ilv_route_threads(p));
     if (c.lane == 0) {
       c.stamp(ST_P_ROUTE);
       const int nsl = p.S + c.misc[MISC_NROUTED];
       int dnext = 0;
       for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
-        if (t < nsl) pr.ilv_pairs(rt, t);
+        if (t < nsl) pr.ilv_pairs(rt, t, p.q);
         while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t) pr.ilv_down(rt, dnext++);
       }
       c.stamp(ST_P_D_ISSUED);
@@ -2057,12 +2075,15 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
       count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
-    route_rows(c, rt, true);
-    bar_arrive(kBarRoute, kThreadsIlv);
-    if (c.tid == 0) c.stamp(ST_ROUTED);
     if (FMT == FMT_NVFP4) {  // the router is done with the bf16 x rows
       x_to_f16(c);
       bar_sync(kBarConsumers, kNC * 32);
+    }
+    const int nrw = ilv_nrw(p);
+    if (c.warp < nrw) {
+      route_rows(c, rt, true, nrw * 32, kBarRouting);
+      bar_arrive(kBarRoute, ilv_route_threads(p));
+      if (c.tid == 0) c.stamp(ST_ROUTED);
     }
     constexpr int RPG = rows_per_group(FMT);
     const int g = c.tid / p.tg, ch = c.tid % p.tg;
@@ -2072,14 +2093,18 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     for (int ri = 0; ri < RPG; ++ri)
 #pragma unroll
       for (int m = 0; m < MAXM; ++m) acc[ri][m] = 0.0f;
-    const int nsl = p.S + c.misc[MISC_NROUTED];
     int rot = 0, dnext = 0;
+    // the shared experts' items: the non-routing warps compute them while routing
+    // runs; the routing warps walk the same stages (without items) afterwards
 #pragma unroll 1
-    for (int s = 0; s < p.S; ++s) ring = ilv_items<FMT, MAXM>(c, rt, s, ring, rot);
+    for (int s = 0; s < p.S; ++s) ring = ilv_items<FMT, MAXM>(c, rt, s, ring, rot, nrw, kNC - nrw, ilv_sq(p));
+    bar_sync(kBarConsumers, kNC * 32);  // the routing tables, for every warp
     if (c.tid == 0) c.stamp(ST_R_DONE);
+    const int nsl = p.S + c.misc[MISC_NROUTED];
+    rot = 0;
 #pragma unroll 1
     for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
-      if (t < nsl) ring = ilv_items<FMT, MAXM>(c, rt, t, ring, rot);
+      if (t < nsl) ring = ilv_items<FMT, MAXM>(c, rt, t, ring, rot, 0, kNC, p.q);
       while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t)
         ring = ilv_down<FMT, MAXM>(c, rt, dnext++, ring, acc, g, ch, active, nr);
     }
