@@ -266,7 +266,10 @@ def run_ours(args, rank, world, dist):
 
     kernels_per_run = mods[0].info(_lib.MOE_INFO_KERNELS_PER_RUN)
     peak, peak_kind = measured_peak()
-    kernel_name = "moe_layer_kernel" if args.sched == "persistent" else "moe_layer_kernel_chain"
+    if mods[0].info(_lib.MOE_INFO_INTERLEAVED_ROWS) >> (m - 1) & 1:
+        kernel_name = "moe_ilv_kernel"
+    else:
+        kernel_name = "moe_layer_kernel" if args.sched in ("persistent", "phased", "interleaved") else "moe_layer_kernel_chain"
     traffic, digest = traffic_record(kernel_name, args.workload)
     ms_step = elapsed_ms / K
     gbs = bytes_total / (elapsed_ms * 1e-3) / 1e9

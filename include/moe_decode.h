@@ -193,7 +193,10 @@ enum {
   MOE_INFO_RING_SLOTS = 19,    /* shared-memory weight ring: slots                  */
   MOE_INFO_SLOT_BYTES = 20,    /*                            bytes per slot         */
   MOE_INFO_KERNELS_PER_RUN = 21,
-  MOE_INFO_SCRATCH_BYTES = 22
+  MOE_INFO_SCRATCH_BYTES = 22,
+  MOE_INFO_INTERLEAVED_ROWS = 23 /* bit m-1 set: a run of m rows under the current
+                                    schedule and MOE_OPT_INTERLEAVE takes the
+                                    slot-interleaved kernel                        */
 };
 moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value);
 moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value);

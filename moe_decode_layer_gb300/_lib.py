@@ -48,6 +48,7 @@ MOE_INFO_RING_SLOTS = 19
 MOE_INFO_SLOT_BYTES = 20
 MOE_INFO_KERNELS_PER_RUN = 21
 MOE_INFO_SCRATCH_BYTES = 22
+MOE_INFO_INTERLEAVED_ROWS = 23
 STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTS = ("moe_decode_config_check", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",

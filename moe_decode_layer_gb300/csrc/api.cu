@@ -565,6 +565,13 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_INFO_SLOT_BYTES: *value = active_params(h, 1).slot_bytes; return MOE_OK;
     case MOE_INFO_KERNELS_PER_RUN: *value = h->sched == MOE_SCHED_PERSISTENT ? 1 : 3; return MOE_OK;
     case MOE_INFO_SCRATCH_BYTES: *value = (int64_t)h->scratch_bytes; return MOE_OK;
+    case MOE_INFO_INTERLEAVED_ROWS: {
+      int64_t mask = 0;
+      for (int m = 1; m <= h->cfg.max_rows; ++m)
+        if (interleaved(h, m)) mask |= int64_t(1) << (m - 1);
+      *value = mask;
+      return MOE_OK;
+    }
   }
   return MOE_ERR_INVALID_ARG;
 }

@@ -209,6 +209,9 @@ def test_ling_interleave_modes(ling):
         assert MoEDecodeLayer(synth.LING, ling, m).info(_lib.MOE_OPT_INTERLEAVE) == 1
         assert MoEDecodeLayer(synth.LING, ling, m, sched="interleaved").info(_lib.MOE_OPT_INTERLEAVE) == 2
         assert MoEDecodeLayer(synth.LING, ling, m, sched="phased").info(_lib.MOE_OPT_INTERLEAVE) == 0
+    assert MoEDecodeLayer(synth.LING, ling, 6).info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0b1
+    assert MoEDecodeLayer(synth.LING, ling, 6, sched="interleaved").info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0b111111
+    assert MoEDecodeLayer(synth.LING, ling, 6, sched="phased").info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0
     assert MoEDecodeLayer(synth.LING, ling, 1).info(_lib.MOE_INFO_THREADS) == 480
     assert MoEDecodeLayer(synth.LING, ling, 1, sched="phased").info(_lib.MOE_INFO_THREADS) == 416
 
