@@ -33,10 +33,18 @@
 // internals", part 3: a GPU-scope fence with bulk loads in flight costs
 // microseconds, so the data carries its own readiness). The tag is a per-handle
 // counter that the last CTA of a run advances, so buffers are never reset. The
-// h values (I floats per (expert, row) pair, in pair order, four copies) are
-// released once per CTA by a fence and a count; after the count reaches the grid
-// size each CTA fetches its batches of pairs with one bulk copy each, the next
-// batch landing while the current one is in use.
+// h values (I floats per (expert, row) pair, in pair order, four copies) go
+// through global memory too:
+//   - moe_layer_kernel (phases in order, and the three-kernel chain): each CTA
+//     releases its h once by a fence and a count; after the count reaches the
+//     grid size each CTA fetches its batches of pairs with one bulk copy each,
+//     the next batch landing while the current one is in use.
+//   - moe_ilv_kernel (slot-interleaved): each CTA computes a block of rows of
+//     every union slot; per slot, a hand-off warp fences once and counts the
+//     CTA's items, and another copies the slot's h rows behind the down weights
+//     of that slot's down stage once every CTA has counted it. The down stage of
+//     slot s follows the gate/up items of slot s + lag, so gate/up and down
+//     weights stream as one sequence and no CTA waits for all gate/up results.
 //
 // All device functions are inlined into the kernel: parameters are then read
 // from the kernel's parameter space and the helper objects stay in registers
