@@ -205,7 +205,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   // router stages: at most kNC / 2 row pairs, so every row gets at least one warp
   p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
   p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
-  p.ilv_lag = 4;
+  p.ilv_lag = 5;
   p.timeout_ns = kDefaultTimeoutNs;
   return MOE_OK;
 }
