@@ -128,11 +128,42 @@ typedef struct moe_decode_handle moe_decode_handle;
 moe_status moe_decode_config_check(const moe_decode_config* cfg);
 
 /*
+ * The launch layout create would plan for cfg on a device with `sms` SMs and
+ * `smem_optin` bytes of opt-in shared memory per block, computed on the host
+ * (no CUDA call). `interleaved` = 1 asks for the slot-interleaved single kernel's
+ * layout (MOE_ERR_UNSUPPORTED when it does not fit), 0 for the phase-ordered
+ * kernels'. All fields in bytes or counts; filled only on MOE_OK.
+ */
+typedef struct moe_decode_plan_info {
+  int32_t smem_bytes;        /* dynamic shared memory per CTA (incl. alignment slack)   */
+  int32_t ring_slots;        /* weight ring slots                                         */
+  int32_t slot_bytes;        /* bytes per slot                                            */
+  int32_t extra_slots;       /* gate/up ring slots carved from the idle h area             */
+  int32_t down_slot_in_x;    /* 1: one more down-phase slot in the x area                  */
+  int32_t pairs_per_stage;   /* gate/up row pairs per stage                                */
+  int32_t router_pairs_per_stage;
+  int32_t down_rows_per_stage;
+  int32_t h_pairs;           /* (expert, row) h rows staged in shared memory at once       */
+  int32_t h_buffers;         /* 1 or 2 h batch buffers                                    */
+  int32_t h_per_slot;        /* 1: per-slot h fetches (phase-ordered, NVFP4)               */
+  int32_t slots_max;         /* union slots at most: shared + min(E, max_rows * k)         */
+  int32_t pairs_max;         /* (expert, row) pairs at most                                */
+  int32_t lag;               /* interleaved: down stage of slot s after the gate/up of s+lag */
+  int32_t down_h_offset;     /* interleaved: h rows' offset in a down stage's slot        */
+  int32_t threads;           /* threads per CTA                                           */
+} moe_decode_plan_info;
+moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t smem_optin, int32_t interleaved,
+                           moe_decode_plan_info* out);
+
+/*
  * Builds a handle for the current CUDA device: validates cfg and the weight
  * pointers, allocates the handle's device scratch (control words, tagged
  * logits and intermediate activations, host-call staging buffers) and plans the
  * launch shape from the device's SM count and shared memory. Copies nothing and
  * repacks no weight. On error *out is NULL and nothing stays allocated.
+ * MOE_ERR_UNSUPPORTED also when cfg passes moe_decode_config_check but its layout
+ * does not fit the device's shared memory (the largest H x I at max_rows 6..8;
+ * moe_decode_plan tells in advance).
  */
 moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weights* w,
                              moe_decode_handle** out);

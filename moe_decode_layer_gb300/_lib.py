@@ -51,7 +51,7 @@ MOE_INFO_SCRATCH_BYTES = 22
 MOE_INFO_INTERLEAVED_ROWS = 23
 STATIC_SCRATCH_BYTES = 4 << 20
 
-EXPORTS = ("moe_decode_config_check", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",
+EXPORTS = ("moe_decode_config_check", "moe_decode_plan", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",
            "moe_decode_run_static",
            "moe_decode_get_status", "moe_decode_set_option", "moe_decode_get_info",
            "moe_decode_destroy", "moe_decode_status_string", "moe_decode_abi_version")
@@ -70,6 +70,13 @@ class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router_w", "w13", "w2", "w13_scale", "w2_scale", "w13_gscale", "w2_gscale",
         "sh_w13", "sh_w2", "sh_w13_scale", "sh_w2_scale", "sh_w13_gscale", "sh_w2_gscale")]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "smem_bytes", "ring_slots", "slot_bytes", "extra_slots", "down_slot_in_x", "pairs_per_stage",
+        "router_pairs_per_stage", "down_rows_per_stage", "h_pairs", "h_buffers", "h_per_slot", "slots_max",
+        "pairs_max", "lag", "down_h_offset", "threads")]
 
 
 class MoEDecodeError(RuntimeError):
@@ -96,6 +103,7 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         lib = ctypes.CDLL(_build.LIB)
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         lib.moe_decode_config_check.argtypes = [ctypes.POINTER(Config)]
+        lib.moe_decode_plan.argtypes = [ctypes.POINTER(Config), i32, i32, i32, ctypes.POINTER(PlanInfo)]
         lib.moe_decode_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights),
                                           ctypes.POINTER(vp)]
         lib.moe_decode_run.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]

@@ -345,6 +345,32 @@ const char* moe_decode_status_string(moe_status s) {
 
 moe_status moe_decode_config_check(const moe_decode_config* cfg) { return check_config(cfg); }
 
+moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t smem_optin, int32_t interleaved,
+                           moe_decode_plan_info* out) {
+  if (!out || sms <= 0 || smem_optin <= 0 || interleaved < 0 || interleaved > 1) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  Params p;
+  if ((st = plan(*cfg, sms, smem_optin, p, interleaved != 0)) != MOE_OK) return st;
+  out->smem_bytes = p.smem_bytes;
+  out->ring_slots = p.nslots;
+  out->slot_bytes = p.slot_bytes;
+  out->extra_slots = p.nslots_x;
+  out->down_slot_in_x = p.nslots_d;
+  out->pairs_per_stage = p.q;
+  out->router_pairs_per_stage = p.qr;
+  out->down_rows_per_stage = p.d_rows_stage;
+  out->h_pairs = p.hs_pairs;
+  out->h_buffers = p.hs_nbuf;
+  out->h_per_slot = p.hs_perslot;
+  out->slots_max = p.nslot_max;
+  out->pairs_max = p.npair_max;
+  out->lag = interleaved ? p.ilv_lag : 0;
+  out->down_h_offset = interleaved ? p.d_hoff : 0;
+  out->threads = interleaved ? moe::kThreadsIlv : moe::kThreads;
+  return MOE_OK;
+}
+
 moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weights* w,
                              moe_decode_handle** out) {
   if (!out) return MOE_ERR_INVALID_ARG;

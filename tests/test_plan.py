@@ -1,0 +1,116 @@
+"""Launch planning on the host (no GPU): for a sweep of supported configs and device
+sizes, the planned shared-memory layout of both single-kernel schedules fits the device,
+every stage fits its ring slot, and the barrier and counter index ranges stay inside their
+arrays. moe_decode_plan is the library's own planner, called through the C ABI."""
+
+import ctypes
+import itertools
+
+import pytest
+
+from moe_decode_layer_gb300 import _lib
+
+K_MAX_SLOTS = 64        # full / empty barrier arrays
+K_HSLOT_BAR = 32        # per-slot h barriers start at this full-barrier index
+K_SLOT_COUNTERS = 160   # per-slot counters in the control words
+K_NC = 12               # consumer warps
+
+
+def _cfg(h, i, e, k, s, m, fp4):
+    return _lib.Config(hidden=h, inter=i, num_experts=e, top_k=k, num_shared=s, max_rows=m,
+                       wdtype=_lib.MOE_W_NVFP4 if fp4 else _lib.MOE_W_BF16, score=0, routed_scale=1.0,
+                       pre_rmsnorm=0, rms_eps=1e-6, sched=0)
+
+
+def _plan(lib, cfg, sms, optin, ilv):
+    info = _lib.PlanInfo()
+    st = lib.moe_decode_plan(ctypes.byref(cfg), sms, optin, ilv, ctypes.byref(info))
+    return st, info
+
+
+def _sweep():
+    for fp4, h, i, e, k, s, m in itertools.product(
+            (False, True), (256, 1024, 2560, 4096), (64, 128, 256, 768, 1024, 3072), (16, 64, 512, 1024),
+            (1, 2, 8, 16), (0, 1, 4), (1, 6, 8)):
+        if k > e:
+            continue
+        yield fp4, h, i, e, k, s, m
+
+
+@pytest.mark.parametrize("sms,optin", [(152, 232448), (148, 232448), (132, 232448), (152, 166912)])
+def test_planned_layouts_fit(sms, optin):
+    lib = _lib.load()
+    n_checked = n_ilv = n_unfit = 0
+    for fp4, h, i, e, k, s, m in _sweep():
+        cfg = _cfg(h, i, e, k, s, m, fp4)
+        if lib.moe_decode_config_check(ctypes.byref(cfg)) != _lib.MOE_OK:
+            continue
+        pair = 2 * (h // 2 + h // 16) if fp4 else 4 * h
+        down_row = (i // 2 + i // 16) if fp4 else 2 * i
+        for ilv in (0, 1):
+            st, p = _plan(lib, cfg, sms, optin, ilv)
+            if st != _lib.MOE_OK:
+                assert st == _lib.MOE_ERR_UNSUPPORTED, (cfg, ilv, st)
+                if not ilv:
+                    # on a GB300 only the largest rows at many token rows outgrow the
+                    # shared memory (with less shared memory, more do)
+                    if optin >= 232448:
+                        assert m >= 6 and h * i >= 2560 * 3072, (h, i, e, k, s, m, fp4, sms, optin)
+                    else:
+                        assert m >= 6, (h, i, e, k, s, m, fp4, sms, optin)
+                    n_unfit += 1
+                continue
+            what = f"{'nvfp4' if fp4 else 'bf16'} H={h} I={i} E={e} k={k} S={s} M={m} ilv={ilv} sms={sms}"
+            assert p.smem_bytes <= optin, what
+            assert p.slot_bytes % 128 == 0, what
+            assert p.ring_slots >= (3 if ilv else 2), what
+            assert p.ring_slots + max(p.extra_slots, p.down_slot_in_x) <= K_MAX_SLOTS, what
+            assert 1 <= p.pairs_per_stage <= K_NC and p.pairs_per_stage * pair <= p.slot_bytes, what
+            assert 1 <= p.router_pairs_per_stage <= K_NC // 2, what
+            assert p.router_pairs_per_stage * 4 * h <= p.slot_bytes, what
+            assert p.slots_max == s + min(e, m * k) and p.pairs_max == s * m + m * k, what
+            if p.h_per_slot:
+                assert p.ring_slots + max(p.extra_slots, p.down_slot_in_x) <= K_HSLOT_BAR, what
+                assert p.slots_max <= K_MAX_SLOTS - K_HSLOT_BAR, what
+            if ilv:
+                n_ilv += 1
+                rows = -(-h // sms)
+                assert p.down_rows_per_stage == rows, what
+                assert p.down_h_offset % 16 == 0 and p.down_h_offset >= rows * down_row, what
+                assert p.down_h_offset + m * i * 4 <= p.slot_bytes, what
+                assert p.slots_max <= K_SLOT_COUNTERS and p.lag >= 1 and p.threads == 480, what
+                assert p.h_pairs == 0 and p.extra_slots == 0 and p.down_slot_in_x == 0, what
+            else:
+                assert p.down_rows_per_stage * down_row <= p.slot_bytes, what
+                assert p.h_buffers in (1, 2) and p.h_pairs >= m, what
+                if p.h_buffers == 2:
+                    assert p.h_pairs < p.pairs_max, what
+                assert p.threads == 416, what
+            n_checked += 1
+    assert n_checked > 500 and n_ilv > 100 and n_unfit < n_checked // 10
+
+
+def test_plan_of_the_benchmarked_layers():
+    """The Ling-shaped layer on 152 SMs: both single-kernel layouts fit, with the
+    numbers the kernels were measured with."""
+    lib = _lib.load()
+    for m in (1, 6):
+        cfg = _cfg(2560, 768, 512, 8, 1, m, False)
+        st, p = _plan(lib, cfg, 152, 232448, 0)
+        assert st == _lib.MOE_OK and p.slot_bytes == 30720 and p.pairs_per_stage == 3
+        assert p.down_rows_per_stage == 17
+        st, q = _plan(lib, cfg, 152, 232448, 1)
+        assert st == _lib.MOE_OK and q.lag == 5 and q.down_rows_per_stage == 17
+    st, p = _plan(lib, _cfg(2560, 768, 512, 8, 1, 1, False), 152, 232448, 0)
+    assert p.ring_slots == 6 and p.h_pairs == 9 and p.h_buffers == 1
+
+
+def test_plan_rejects_bad_arguments():
+    lib = _lib.load()
+    cfg = _cfg(2560, 768, 512, 8, 1, 1, False)
+    info = _lib.PlanInfo()
+    assert lib.moe_decode_plan(ctypes.byref(cfg), 0, 232448, 0, ctypes.byref(info)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_plan(ctypes.byref(cfg), 152, 232448, 2, ctypes.byref(info)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_plan(ctypes.byref(cfg), 152, 232448, 0, None) == _lib.MOE_ERR_INVALID_ARG
+    bad = _cfg(2560, 776, 512, 8, 1, 1, False)  # 97 threads per down group
+    assert lib.moe_decode_plan(ctypes.byref(bad), 152, 232448, 0, ctypes.byref(info)) == _lib.MOE_ERR_UNSUPPORTED
