@@ -48,13 +48,14 @@ def _run_static(lib, cfg, w, x, m, k):
     return out, idx, wt
 
 
-@pytest.mark.parametrize("case", ["tiny_m2", "ling_e64_m6", "nvfp4_small_m3"])
+@pytest.mark.parametrize("case", ["tiny_m2", "ling_e64_m1", "ling_e64_m6", "nvfp4_small_m3"])
 def test_static_entry_matches_handle_entry(case):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = _lib.load()
     shape, m = {
         "tiny_m2": (synth.TINY, 2),
+        "ling_e64_m1": (synth.LING_E64, 1),  # bf16, one row: the slot-interleaved kernel
         "ling_e64_m6": (synth.LING_E64, 6),
         "nvfp4_small_m3": (synth.LayerShape(hidden=512, inter=256, num_experts=32, top_k=4, num_shared=1,
                                             wdtype="nvfp4"), 3),
