@@ -95,13 +95,46 @@ def topk_renorm(logits_row: np.ndarray, k: int):
     return idx.astype(np.int64), e / e.sum()
 
 
-def route(x: np.ndarray, router_w: np.ndarray, k: int):
+SCORE_SOFTMAX = 0
+SCORE_SIGMOID_BIAS = 1
+
+
+def sigmoid_bias_select(logits_row: np.ndarray, k: int, bias: np.ndarray):
+    """Bias-corrected sigmoid selection of one row.
+
+    s_e = 1 / (1 + exp(-l_e)); the k largest s_e + b_e are selected (equal keys:
+    the lower expert id first); w_j = s_j / sum over the selected of s_i, so the
+    bias steers which experts are chosen but not their weights. The Ling blog's
+    router top-k "prefetches its bias" (section "PDL: stacking the latency floors
+    of small kernels"); the pages give no more of the rule, so this is the plainest
+    reading of a bias-corrected sigmoid router.
+    """
+    l = np.asarray(logits_row, np.float64)
+    s = 1.0 / (1.0 + np.exp(-l))
+    key = s + np.asarray(bias, np.float64)
+    idx = np.argsort(-key, kind="stable")[:k]
+    return idx.astype(np.int64), s[idx] / s[idx].sum()
+
+
+def select(logits_row: np.ndarray, k: int, score: int = SCORE_SOFTMAX, bias=None):
+    """Selection and weights of one row under a scoring rule (0 softmax, 1 sigmoid + bias)."""
+    if score == SCORE_SOFTMAX:
+        return topk_renorm(logits_row, k)
+    if score == SCORE_SIGMOID_BIAS:
+        return sigmoid_bias_select(logits_row, k, bias)
+    raise ValueError(f"unknown scoring rule {score}")
+
+
+def route(x: np.ndarray, router_w: np.ndarray, k: int, score: int = SCORE_SOFTMAX, bias=None):
     """Per-row routing: (logits [M, E], idx [M, k], w [M, k])."""
     logits = router_logits(x, router_w)
     idx = np.zeros((logits.shape[0], k), np.int64)
     w = np.zeros((logits.shape[0], k), np.float64)
     for m in range(logits.shape[0]):
-        idx[m], w[m] = topk_renorm(logits[m], k)
+        if score == SCORE_SOFTMAX:  # looked up by name so that planted mistakes reach it
+            idx[m], w[m] = topk_renorm(logits[m], k)
+        else:
+            idx[m], w[m] = select(logits[m], k, score, bias)
     return logits, idx, w
 
 
@@ -156,7 +189,7 @@ def expert_swiglu(x_row: np.ndarray, w13: np.ndarray, w2: np.ndarray) -> np.ndar
 
 
 def moe_layer(x, residual, router_w, expert_weights, shared_weights, top_k,
-              routed_scale: float = 1.0):
+              routed_scale: float = 1.0, score: int = SCORE_SOFTMAX, bias=None):
     """One MoE decode layer step for M rows, float64 throughout.
 
     x, residual : float64 [M, H] (the exact values of the bf16 inputs)
@@ -165,11 +198,12 @@ def moe_layer(x, residual, router_w, expert_weights, shared_weights, top_k,
                   for the experts some row selects, so callers can hand over just
                   those experts' weights
     shared_weights : list of (w13, w2), each added with weight 1
+    score, bias : the scoring rule (see ``select``) and the per-expert bias [E]
     Returns (out float64 [M, H], idx int64 [M, k], w float64 [M, k]).
     """
     x = np.asarray(x, np.float64)
     out = np.array(residual, np.float64, copy=True)
-    _, idx, w = route(x, router_w, top_k)
+    _, idx, w = route(x, router_w, top_k, score, bias)
     cache = {}
     for m in range(x.shape[0]):
         routed = np.zeros(x.shape[1])

@@ -1,6 +1,8 @@
 """Test-side glue between the synthetic inputs, the oracle and the GPU library.
 
-Lives under tests/ because it calls the oracle (test infrastructure).
+Lives under tests/ because it calls the oracle (test infrastructure). The GPU
+parity tests compare against the C++ float64 oracle (``oracle.cpp``), which reads
+the exact bf16 / NVFP4 bit patterns the kernels read.
 """
 
 from __future__ import annotations
@@ -9,6 +11,7 @@ import numpy as np
 import torch
 
 import oracle
+from oracle import cpp
 from moe_decode_layer_gb300 import synth
 
 MAX_ABS = 2e-2     # output tolerance against the float64 oracle (bf16 weights)
@@ -29,18 +32,22 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def hidden_with_margin(router_w: torch.Tensor, m_rows: int, top_k: int, seed: int,
-                       rho: float = 0.0, margin: float = 0.05, max_tries: int = 200):
-    """bf16 [M, H] rows whose float64 router logits have a top-k gap >= margin.
+                       rho: float = 0.0, margin: float = 0.05, max_tries: int = 200, score: int = 0,
+                       bias=None):
+    """bf16 [M, H] rows whose float64 selection keys have a top-k gap >= margin
+    (router logits for softmax scoring; sigmoid(logit) + bias for the
+    bias-corrected sigmoid rule).
 
     Each row that misses the margin is redrawn alone (its own stream), so the
     selected expert set is decided by a gap far above fp32 rounding.
     """
-    rw = f64(router_w)
+    rw = bits(router_w)
+    b = None if bias is None else bias.detach().cpu().double().numpy()
     attempts = [0] * m_rows
     for _ in range(max_tries):
         x = synth.hidden_rows(m_rows, rw.shape[1], seed, rho, attempts)
-        logits = oracle.router_logits(f64(x), rw)
-        bad = [m for m in range(m_rows) if oracle.topk_margin(logits[m], top_k) < margin]
+        logits = cpp.router_logits(f64(x), rw)
+        bad = [m for m in range(m_rows) if selection_margin(logits[m], top_k, score, b) < margin]
         if not bad:
             return x
         for m in bad:
@@ -49,29 +56,36 @@ def hidden_with_margin(router_w: torch.Tensor, m_rows: int, top_k: int, seed: in
 
 
 def expert_accessor(shape: synth.LayerShape, layer: dict, prefix: str = ""):
-    """e -> float64 (w13 [2I, H], w2 [H, I]) read from the layer tensors on demand."""
+    """e -> the raw weights of expert e for the C++ oracle, copied from the layer
+    tensors on demand: bf16 bit patterns (w13 [2I, H], w2 [H, I]) or an NVFP4
+    expert (codes, e4m3 scale bytes, tensor scales)."""
     def get(e):
         if shape.wdtype == "bf16":
-            return f64(layer[prefix + "w13"][e]), f64(layer[prefix + "w2"][e])
-        i = shape.inter
-        gs = layer[prefix + "w13_gs"][e].cpu().numpy()
-        q13 = bits(layer[prefix + "w13_q"][e])
-        s13 = bits(layer[prefix + "w13_s"][e])
-        gate = oracle.dequant_nvfp4_rows(q13[:i], s13[:i], float(gs[0]))
-        up = oracle.dequant_nvfp4_rows(q13[i:], s13[i:], float(gs[1]))
-        down = oracle.dequant_nvfp4_rows(bits(layer[prefix + "w2_q"][e]), bits(layer[prefix + "w2_s"][e]),
-                                         float(layer[prefix + "w2_gs"][e].cpu()))
-        return np.vstack([gate, up]), down
+            return bits(layer[prefix + "w13"][e]), bits(layer[prefix + "w2"][e])
+        return cpp.NVFP4Expert(bits(layer[prefix + "w13_q"][e]), bits(layer[prefix + "w13_s"][e]),
+                               layer[prefix + "w13_gs"][e].cpu().numpy(), bits(layer[prefix + "w2_q"][e]),
+                               bits(layer[prefix + "w2_s"][e]), np.float32(layer[prefix + "w2_gs"][e].cpu()))
     return get
 
 
 def oracle_layer(shape: synth.LayerShape, layer: dict, x: torch.Tensor, residual: torch.Tensor,
-                 routed_scale: float = 1.0):
-    """Run the oracle on the exact values of the given tensors (copied to host)."""
+                 routed_scale: float = 1.0, score: int = 0, bias=None):
+    """Run the C++ oracle on the exact values of the given tensors (copied to host).
+
+    Returns (out float64 [M, H], idx int64 [M, k], w float64 [M, k])."""
     shared_get = expert_accessor(shape, layer, "sh_")
     shared = [shared_get(s) for s in range(shape.num_shared)]
-    return oracle.moe_layer(f64(x), f64(residual), f64(layer["router_w"]),
-                            expert_accessor(shape, layer), shared, shape.top_k, routed_scale)
+    b = None if bias is None else bias.detach().cpu().double().numpy()
+    return cpp.moe_layer(f64(x), f64(residual), bits(layer["router_w"]), expert_accessor(shape, layer), shared,
+                         shape.top_k, routed_scale, score, b)
+
+
+def selection_margin(logits_row: np.ndarray, k: int, score: int = 0, bias=None) -> float:
+    """Gap between the k-th and (k+1)-th selection key of one row (float64)."""
+    key = np.asarray(logits_row, np.float64)
+    if score == 1:
+        key = 1.0 / (1.0 + np.exp(-key)) + np.asarray(bias, np.float64)
+    return oracle.topk_margin(key, k)
 
 
 def assert_close(got_bf16: torch.Tensor, ref: np.ndarray, max_abs=MAX_ABS, rel_l2=REL_L2, what="out"):

@@ -9,8 +9,8 @@ Stack: 12 distinct Ling-shaped layers, M=6 correlated rows, pre-norm
 h_{l+1} = h_l + MoE_l(bf16(RMSNorm(h_l))), run in place through the C ABI. Each
 layer is checked teacher-forced (the oracle takes the GPU's bf16 input of that
 layer); where the oracle's own top-k gap is below 1e-3 the two expert sets may
-legitimately differ, so such rows are compared on outputs only when the sets
-agree. The end-to-end result is also compared with the oracle chained through
+legitimately differ, so each row is compared on outputs when its sets agree, and
+at most two of the 72 layer rows may be left out. The end-to-end result is also compared with the oracle chained through
 all layers on its own bf16-rounded outputs.
 """
 
@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import cpp
 from moe_decode_layer_gb300 import _lib, synth
 from moe_decode_layer_gb300.layer import MoEDecodeLayer
 from tests import helpers
@@ -103,28 +104,39 @@ def test_stack_12_layers_m6():
         assert md.status() == _lib.MOE_OK
     final = h.cpu()
     outputs = inputs[1:] + [final]
-    # teacher-forced per layer
+    # teacher-forced per layer: every row whose expert set matches the oracle's is
+    # compared (a row whose float64 top-k gap is below 1e-3 may legitimately pick
+    # another set in fp32; such a row alone is skipped, the others still count)
+    compared = 0
     for l in range(n_layers):
         h_in = inputs[l]
-        xb = torch.from_numpy(oracle.stack_layer_input(helpers.bits(h_in)).view(np.int16)).view(torch.bfloat16)
+        xb = torch.from_numpy(cpp.stack_layer_input(helpers.bits(h_in)).view(np.int16)).view(torch.bfloat16)
         ref, ridx, _ = helpers.oracle_layer(shape, layers[l], xb, h_in)
-        logits = oracle.router_logits(helpers.f64(xb), helpers.f64(layers[l]["router_w"]))
+        logits = cpp.router_logits(helpers.f64(xb), helpers.bits(layers[l]["router_w"]))
         gi = idxs[l].cpu().numpy()
+        rows = []
         for r in range(m):
+            same = sorted(gi[r].tolist()) == sorted(ridx[r].tolist())
             if oracle.topk_margin(logits[r], shape.top_k) >= 1e-3:
-                assert sorted(gi[r].tolist()) == sorted(ridx[r].tolist()), f"layer {l} row {r}"
-        same = all(sorted(gi[r].tolist()) == sorted(ridx[r].tolist()) for r in range(m))
-        if same:
-            helpers.assert_close(outputs[l], ref, what=f"layer {l}")
-    # end to end: the oracle chained on its own bf16-rounded outputs
+                assert same, f"layer {l} row {r}: expert sets differ"
+            if same:
+                rows.append(r)
+        if rows:
+            helpers.assert_close(outputs[l][rows], ref[rows], what=f"layer {l} rows {rows}")
+            compared += len(rows)
+    assert compared >= n_layers * m - 2, f"only {compared} of {n_layers * m} layer rows compared"
+    # end to end: the oracle chained on its own bf16-rounded outputs. Routing near
+    # ties can flip between fp32 and float64 in later layers, so the chain drifts
+    # apart slowly; 2e-2 relative L2 after 12 layers bounds that drift (the
+    # per-layer check above holds every layer to the contract's 5e-3).
     hb = helpers.bits(h0)
     for l in range(n_layers):
-        xb = oracle.stack_layer_input(hb)
+        xb = cpp.stack_layer_input(hb)
         xt = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
         rt = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16)
         ref, _, _ = helpers.oracle_layer(shape, layers[l], xt, rt)
-        hb = oracle.f64_to_bf16_bits(ref)
-    ref_final = oracle.bf16_bits_to_f64(hb)
+        hb = cpp.f64_to_bf16_bits(ref)
+    ref_final = cpp.bf16_bits_to_f64(hb)
     got = helpers.f64(final)
     rl2 = np.linalg.norm(got - ref_final) / np.linalg.norm(ref_final)
     assert rl2 < 2e-2, f"12-layer end-to-end rel L2 {rl2:.3e}"

@@ -114,11 +114,18 @@ def test_repeated_runs_and_inplace(tiny):
     assert torch.equal(buf, first)
 
 
-def test_zero_rows_give_zero(tiny):
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_zero_rows_give_zero(tiny, sched):
+    """Zero rows: all logits tie at 0, so the tie rule (lower expert id first)
+    decides the whole selection -- experts 0..k-1 in that order, equal weights --
+    and silu(0) * 0 makes the output exactly zero."""
     x = torch.zeros((3, synth.TINY.hidden), dtype=torch.bfloat16)
-    _, out, _, w = _run(synth.TINY, tiny, x)
+    _, out, idx, w = _run(synth.TINY, tiny, x, sched=sched)
     assert torch.count_nonzero(out.float()) == 0
     np.testing.assert_allclose(w.numpy(), 1.0 / synth.TINY.top_k, rtol=0, atol=1e-7)
+    assert idx.tolist() == [list(range(synth.TINY.top_k))] * 3
+    _, ridx, _ = helpers.oracle_layer(synth.TINY, tiny, x, x)
+    assert ridx.tolist() == idx.tolist()
 
 
 def test_run_host_matches_device(tiny):

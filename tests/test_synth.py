@@ -5,6 +5,8 @@ import math
 import numpy as np
 import torch
 
+import oracle
+
 from moe_decode_layer_gb300 import synth
 from tests import helpers
 
@@ -48,8 +50,10 @@ def test_nvfp4_layer_shapes():
     assert layer["w2_q"].shape == (4, 256, 128) and layer["w2_s"].shape == (4, 256, 16)
     assert layer["w13_gs"].shape == (4, 2) and layer["sh_w2_gs"].shape == (1,)
     # dequantised weights track the float draw's spread
-    get = helpers.expert_accessor(shape, layer)
-    w13, w2 = get(0)
+    ex = helpers.expert_accessor(shape, layer)(0)
+    w13 = np.vstack([oracle.dequant_nvfp4_rows(ex.q13[:256], ex.s13[:256], float(ex.gs13[0])),
+                     oracle.dequant_nvfp4_rows(ex.q13[256:], ex.s13[256:], float(ex.gs13[1]))])
+    w2 = oracle.dequant_nvfp4_rows(ex.q2, ex.s2, float(ex.gs2))
     assert abs(w13.std() - 0.02) < 0.003 and abs(w2.std() - 0.02) < 0.003
 
 

@@ -1,7 +1,10 @@
 """moe_decode_run_static, the entry point that allocates nothing (its scratch is
-a fixed array of device memory defined in the library), against the handle-based
-moe_decode_run on the same weights and inputs, on two calls in a row with
-different inputs. Kept in a file of its own that pytest collects last."""
+a fixed array of device memory defined in the library), on two calls in a row
+with different inputs: against the C++ float64 oracle within the layer
+tolerances, and bit for bit against the handle-based moe_decode_run on the same
+weights and inputs (same kernel, same plan, so any difference would be state
+left over in the shared array). Kept in a file of its own that pytest collects
+last."""
 
 import ctypes
 
@@ -70,9 +73,11 @@ def test_static_entry_matches_handle_entry(case):
         ref = mod.run(x, x, None, ref_idx, ref_w)
         assert mod.status() == _lib.MOE_OK
         out, idx, wt = _run_static(lib, cfg, w, x, m, shape.top_k)
-        helpers.assert_close(out.cpu(), helpers.f64(ref.cpu()), what=f"{case} call {call}")
-        helpers.assert_routing(idx.cpu(), wt.cpu(), ref_idx.cpu().numpy().astype("int64"),
-                               ref_w.cpu().numpy().astype("float64"))
+        oref, oidx, ow = helpers.oracle_layer(shape, layer, x.cpu(), x.cpu())
+        helpers.assert_routing(idx.cpu(), wt.cpu(), oidx, ow)
+        helpers.assert_close(out.cpu(), oref, what=f"{case} call {call}")
+        assert torch.equal(out, ref), f"{case} call {call}: differs from the handle entry"
+        assert torch.equal(idx, ref_idx) and torch.equal(wt, ref_w)
     mod.close()
 
 
@@ -90,3 +95,27 @@ def test_static_entry_rejects_oversized_scratch():
     st = lib.moe_decode_run_static(ctypes.byref(big), ctypes.byref(w), vp(x), vp(x), vp(x), 1, None, None,
                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_static_entry_refuses_stream_capture():
+    """The call waits for its step, which a stream under capture cannot do: it
+    must refuse before any device work and leave the capture intact."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = _lib.load()
+    shape = synth.TINY
+    layer = synth.make_layer(shape, seed=29, device="cuda")
+    cfg, w = _cfg(shape, 1), _weights(shape, layer)
+    x = helpers.hidden_with_margin(layer["router_w"], 1, shape.top_k, seed=5).cuda()
+    out = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    with torch.cuda.graph(g, stream=s):
+        st = lib.moe_decode_run_static(ctypes.byref(cfg), ctypes.byref(w), vp(x), vp(x), vp(out), 1, None, None,
+                                       ctypes.c_void_p(s.cuda_stream))
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    # outside capture the same call works
+    ref = _run_static(lib, cfg, w, x, 1, shape.top_k)[0]
+    oref, _, _ = helpers.oracle_layer(shape, layer, x.cpu(), x.cpu())
+    helpers.assert_close(ref.cpu(), oref)
