@@ -2,7 +2,8 @@
 """Benchmark of the MoE decode layer step on GB300 (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ling_m1]
-                    [--impl ours|reference] [--sched persistent|pdl_chain|chain]
+                    [--impl ours|reference] [--sched persistent|...]
+                    [--extra tiny_m1,ling_m6,stack_m6,nvfp4_m1,nvfp4_m6]
 
 A step is one MoE layer step (router, top-k, expert gate/up, down, combine with
 the shared expert into the residual) over one batch of M token rows; for the
@@ -10,15 +11,24 @@ the shared expert into the residual) over one batch of M token rows; for the
 rotate over several distinct full-size layer copies (far more bytes than the
 129 MB L2) and over 64 distinct inputs, so the routed experts change every step.
 
-``value`` is algorithmic HBM GB/s over the whole job: the bytes a step must read
-(router + each distinct routed expert + shared experts) summed over all steps
-and ranks, divided by the max-over-ranks device time of the timed region.
+Timed region: exactly K steps, replayed from CUDA graphs that hold them (a graph
+of P = min(K, 64) steps replayed K // P times, then a graph of the K % P rest),
+bracketed by CUDA events on the launching stream. ``value`` is algorithmic HBM
+GB/s over the whole job: the bytes the K steps must read (router + each distinct
+routed expert + shared experts) summed over ranks, divided by the max-over-ranks
+time. ``step_latency_us`` adds p10 / p50 / p90 over at least 200 single steps,
+each launched directly and bracketed by its own events.
+
+The headline workload fills the top-level keys; every other configuration of the
+layer step (tiny, Ling M=6, the 12-layer stack, NVFP4 M=1 and M=6) gets a block
+of the same fields under ``workloads``, each with its roofline, its CPU-oracle
+baseline (1 thread and all cores) and its end-to-end figure.
 
 Multi-GPU: the layer step does not shard (one GPU, no collectives); N processes
 run N independent replicas, the timed region is bracketed by barriers and the
 max over ranks is taken (weak scaling).
 
-``--impl reference`` times the float64 CPU oracle on the host cores instead
+``--impl reference`` times the C++ float64 CPU oracle on the host cores instead
 (the only reference that exists for this layer step), on the same workload.
 """
 
@@ -28,7 +38,6 @@ import argparse
 import csv
 import io
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -41,6 +50,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE decode layer-step µs and achieved HBM GB/s (% of roofline), M=1 and M=6"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+DEFAULT_EXTRA = "tiny_m1,ling_m6,stack_m6,nvfp4_m1,nvfp4_m6"
 
 from moe_decode_layer_gb300.synth import WORKLOADS  # noqa: E402
 
@@ -57,16 +67,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel: str, workload: str):
-    """dram read+write bytes per launch from profiles/, if recorded for the
-    current kernel sources (a changed kernel invalidates the number)."""
+def sources_digest() -> str:
+    """Digest of the CUDA sources: a traffic record holds only for the sources it
+    was captured with."""
     import hashlib
     csrc = os.path.join(ROOT, "moe_decode_layer_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
-    digest = h.hexdigest()[:16]
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel: str, workload: str):
+    """dram read+write bytes per launch from profiles/, if recorded for the
+    current kernel sources (a changed kernel invalidates the number)."""
+    digest = sources_digest()
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None, digest
@@ -135,29 +151,48 @@ def reduce_over_ranks(dist, maxes, sums, device):
     return t.tolist(), b.tolist()
 
 
+def percentiles(v):
+    v = sorted(v)
+    q = lambda f: v[min(len(v) - 1, int(f * len(v)))]  # noqa: E731
+    return {"p10": round(q(0.10), 3), "p50": round(statistics.median(v), 3), "p90": round(q(0.90), 3),
+            "n": len(v)}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 
-def run_ours(args, rank, world, dist):
+class LayerPool:
+    """Distinct full-size layer copies on the device, shared by the workloads that
+    use the same layer shape (the stack's 12 layers also serve as the cold copies
+    of the single-layer Ling workloads)."""
+
+    def __init__(self, rank: int):
+        self.rank = rank
+        self.layers = {}
+
+    def get(self, shape_name: str, shape, n: int):
+        from moe_decode_layer_gb300 import synth
+        have = self.layers.setdefault(shape_name, [])
+        while len(have) < n:
+            have.append(synth.make_layer(shape, seed=1000 + 97 * self.rank + len(have), device="cuda"))
+        return have[:n]
+
+    def drop(self, shape_name: str):
+        self.layers.pop(shape_name, None)
+
+
+def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, e2e_steps, cpu_seconds):
+    """Measure one workload: timed graph replay, latency distribution, e2e, roofline."""
     import torch
     from moe_decode_layer_gb300 import _lib, synth
     from moe_decode_layer_gb300.layer import MoEDecodeLayer
 
-    wl = WORKLOADS[args.workload]
-    shape = synth.workload_shape(args.workload)
+    wl = WORKLOADS[name]
+    shape = synth.workload_shape(name)
     m, nl = wl["m"], wl["layers"]
-    dev = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(dev)
-    clocks = ClockSampler(dev)
-    clocks.start()
-
-    # distinct layer copies: enough bytes that no weight stays in L2 between uses
     copies = nl if nl > 1 else args.copies
-    layers = [synth.make_layer(shape, seed=1000 + 97 * rank + i, device="cuda") for i in range(copies)]
+    layers = pool.get(wl["shape"], shape, copies)
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=args.sched, pre_rmsnorm=nl > 1) for i in range(copies)]
-    if args.ring_slots:
-        for md in mods:
-            md.set_option(_lib.MOE_OPT_RING_SLOTS, min(args.ring_slots, md.info(_lib.MOE_INFO_RING_SLOTS)))
     n_in = 64
     xs = [synth.hidden_rows(m, shape.hidden, seed=50_000 + 1000 * rank + j, rho=wl["rho"]).cuda()
           for j in range(n_in)]
@@ -173,7 +208,7 @@ def run_ours(args, rank, world, dist):
                 layer.run(out, out, out)  # pre-norm, residual and output in place
 
     # algorithmic bytes of each distinct step of the rotation (from the routing)
-    period = n_in if nl == 1 else n_in
+    period = n_in
     step_bytes = []
     idx = torch.empty((m, shape.top_k), dtype=torch.int32, device="cuda")
     for s in range(period):
@@ -192,26 +227,36 @@ def run_ours(args, rank, world, dist):
         if st != _lib.MOE_OK:
             raise RuntimeError(f"device status {_lib.status_string(st)}")
 
-    for s in range(args.warmup):
+    for s in range(warmup):
         step(s)
     torch.cuda.synchronize()
 
-    # The timed steps are replayed from a CUDA graph of one rotation period (as a
-    # decode loop launches them); the remainder of K steps launches directly.
-    K = args.steps
-    graph = torch.cuda.CUDAGraph()
+    # The K timed steps replay from CUDA graphs holding exactly those steps, as a
+    # decode loop launches them: P = min(K, period) steps per graph, replayed
+    # K // P times, then a graph of the remaining K % P steps.
+    K = steps
+    P = min(K, period)
+    R = K % P
     cs = torch.cuda.Stream()
     cs.wait_stream(stream)
-    with torch.cuda.stream(cs):
-        for s in range(period):
-            step(s)
+    graphs = []
+    for count, first in ((P, 0), (R, K - R)):
+        if count == 0:
+            graphs.append(None)
+            continue
+        with torch.cuda.stream(cs):
+            for s in range(first, first + count):
+                step(s)  # warm the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for s in range(first, first + count):
+                step(s)
+        graphs.append(g)
     torch.cuda.synchronize()
-    with torch.cuda.graph(graph, stream=cs):
-        for s in range(period):
-            step(s)
-    torch.cuda.synchronize()
-    for _ in range(2):
-        graph.replay()
+    for g in graphs:
+        if g is not None:
+            g.replay()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
@@ -219,66 +264,52 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("timed")  # ncu --nvtx --nvtx-include "timed/" selects these launches
     t0.record(stream)
-    for _ in range(K // period):
-        graph.replay()
-    for s in range(K - K % period, K):
-        step(s)
+    for _ in range(K // P):
+        graphs[0].replay()
+    if graphs[1] is not None:
+        graphs[1].replay()
     t1.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)
+    # the graph replays cover step s = i mod P for i < K - R, then steps K - R .. K - 1
+    bytes_total = sum(step_bytes[(i % P) % period] for i in range(K - R)) + \
+        sum(step_bytes[s % period] for s in range(K - R, K))
 
-    # kernel time per launch (CUDA events around sampled direct launches) and the
-    # same steps launched one by one from the host
-    K2 = min(K, 4000)
-    stride = max(1, K2 // 1000)
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(0, K2, stride)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(0, K2, stride)]
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for s in range(K2):
-        if s % stride == 0:
-            ev_a[s // stride].record(stream)
-            step(s)
-            ev_b[s // stride].record(stream)
-        else:
-            step(s)
-    d1.record(stream)
+    # per-step latency: single direct launches, each bracketed by its own events
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * lat_steps)]
+    for s in range(lat_steps):
+        ev[2 * s].record(stream)
+        step(s)
+        ev[2 * s + 1].record(stream)
     torch.cuda.synchronize()
-    direct_ms = d0.elapsed_time(d1)
-    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    lat_us = [ev[2 * s].elapsed_time(ev[2 * s + 1]) * 1e3 / nl for s in range(lat_steps)]
     for md in mods:
         st = md.status()
         if st != _lib.MOE_OK:
             raise RuntimeError(f"device status {_lib.status_string(st)}")
-    clk = clocks.stop()
-
-    bytes_total = sum(step_bytes[s % period] for s in range(K))
-    sampled_bytes = statistics.mean(step_bytes[s % period] for s in range(0, K2, stride))
 
     # end to end through the host-buffer entry point (copies + sync every step)
-    k_e2e = min(K, args.e2e_steps)
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = torch.empty_like(xh[0]).pin_memory()
     if nl == 1:
-        xh = [x.cpu().pin_memory() for x in xs]
-        oh = torch.empty_like(xh[0]).pin_memory()
-        for s in range(min(10, k_e2e)):
+        for s in range(min(10, e2e_steps)):
             mods[s % copies].run_host(xh[s % n_in], xh[s % n_in], oh)
         if dist is not None:
             dist.barrier()
         te = time.perf_counter()
-        for s in range(k_e2e):
+        for s in range(e2e_steps):
             mods[s % copies].run_host(xh[s % n_in], xh[s % n_in], oh)
         e2e_s = time.perf_counter() - te
-        h2d, d2h = 2 * m * shape.hidden * 2, m * shape.hidden * 2
+        h2d, d2h = m * shape.hidden * 2, m * shape.hidden * 2  # x (also the residual) in, out back
+        e2e_path = "moe_decode_run_host (pinned host buffers; x doubles as the residual; copies + sync each step)"
     else:
-        xh = [x.cpu().pin_memory() for x in xs]
-        oh = torch.empty_like(xh[0]).pin_memory()
         if dist is not None:
             dist.barrier()
         te = time.perf_counter()
-        for s in range(k_e2e):
+        for s in range(e2e_steps):
             out.copy_(xh[s % n_in], non_blocking=True)
             for layer in mods:
                 layer.run(out, out, out)
@@ -286,31 +317,40 @@ def run_ours(args, rank, world, dist):
             torch.cuda.synchronize()
         e2e_s = time.perf_counter() - te
         h2d, d2h = m * shape.hidden * 2, m * shape.hidden * 2
-    e2e_bytes = sum(step_bytes[s % period] for s in range(k_e2e))
+        e2e_path = "pinned host copy in, 12 x moe_decode_run in place, copy out, sync"
+    e2e_bytes = sum(step_bytes[s % period] for s in range(e2e_steps))
 
-    direct_bytes = sum(step_bytes[s % period] for s in range(K2))
-    # max over ranks of the times, sum over ranks of the bytes
+    lat_sorted_us = lat_us
     if dist is not None:
-        (elapsed_ms, e2e_s, launch_ms, direct_ms), (bytes_total, e2e_bytes, direct_bytes) = reduce_over_ranks(
-            dist, [elapsed_ms, e2e_s, launch_ms, direct_ms], [bytes_total, e2e_bytes, direct_bytes], "cuda")
+        (elapsed_ms, e2e_s), (bytes_total, e2e_bytes) = reduce_over_ranks(
+            dist, [elapsed_ms, e2e_s], [bytes_total, e2e_bytes], "cuda")
 
-    kernels_per_run = mods[0].info(_lib.MOE_INFO_KERNELS_PER_RUN)
+    kernels_per_layer = mods[0].info(_lib.MOE_INFO_KERNELS_PER_RUN)
     peak, peak_kind = measured_peak()
-    if mods[0].info(_lib.MOE_INFO_INTERLEAVED_ROWS) >> (m - 1) & 1:
+    if kernels_per_layer > 1:
+        kernel_name = "moe_layer_kernel_chain"
+    elif mods[0].info(_lib.MOE_INFO_FLAT_ROWS) >> (m - 1) & 1:
+        kernel_name = "moe_flat_kernel"
+    elif mods[0].info(_lib.MOE_INFO_INTERLEAVED_ROWS) >> (m - 1) & 1:
         kernel_name = "moe_ilv_kernel"
     else:
-        kernel_name = "moe_layer_kernel" if args.sched in ("persistent", "phased", "interleaved") else "moe_layer_kernel_chain"
-    traffic, digest = traffic_record(kernel_name, args.workload)
+        kernel_name = "moe_layer_kernel"
+    traffic, digest = traffic_record(kernel_name, name)
     ms_step = elapsed_ms / K
+    launches_per_step = kernels_per_layer * nl
+    # the dominant (single-kernel schedules: only) kernel's mean launch duration
+    # over the timed region, and the algorithmic bytes one launch streams
+    launch_us = ms_step * 1e3 / launches_per_step
+    bytes_per_launch = bytes_total / K / nl / world
+    achieved = bytes_per_launch / (launch_us * 1e-6) / 1e9 if kernels_per_layer == 1 else None
     gbs = bytes_total / (elapsed_ms * 1e-3) / 1e9
-    launch_gbs = sampled_bytes / (launch_ms * 1e-3) / 1e9 / (nl if False else 1)
     res = {
         "metric": METRIC,
         "value": round(gbs, 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
-        "warmup": args.warmup,
+        "warmup": warmup,
         "ms_per_step": round(ms_step, 6),
         "higher_is_better": True,
         "scaling": "weak",
@@ -318,122 +358,125 @@ def run_ours(args, rank, world, dist):
         "dtype": "bf16" if shape.wdtype == "bf16" else "nvfp4",
         "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: {wl['desc']}",
+            "workload": f"{name}: {wl['desc']}",
             "rows_M": m,
             "layers_per_step": nl,
             "sched": args.sched,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": f"CUDA graph of {period} captured steps, replayed (remainder launched directly)",
-            "l2": (f"no flush; weights cold: {copies} distinct full layer copies "
+            "launch": (f"CUDA graph replay of exactly {K} steps (a {P}-step graph x {K // P}"
+                       + (f" + a {R}-step graph" if R else "") + ")"),
+            "l2": (f"no flush; inputs larger than L2: weights cold, {copies} distinct full layer copies "
                    f"({copies * (shape.router_bytes() + (shape.num_experts + shape.num_shared) * shape.expert_bytes()) / 1e9:.1f} GB) "
                    f"and {n_in} distinct inputs rotate, far above the 129 MB L2"),
         },
         "us_per_layer_step": round(ms_step * 1e3 / nl, 3),
-        "direct_launch": {"value": round(direct_bytes / (direct_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                          "us_per_layer_step": round(direct_ms * 1e3 / K2 / nl, 3), "steps": K2,
-                          "note": "the same steps launched one by one from the host"},
+        "step_latency_us": dict(percentiles(lat_sorted_us),
+                                note="single steps launched directly, each bracketed by CUDA events "
+                                     "(per layer for the stack)"),
         "tokens_per_s_equiv": round(world * m / (ms_step * 1e-3), 1),
         "bytes_per_step_avg": round(bytes_total / K / world),
         "roofline": {
             "bound": "hbm",
-            "achieved": round(launch_gbs, 1),
+            "achieved": None if achieved is None else round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
-            "frac": round(launch_gbs / peak, 4),
-            "peak_kind": f"{peak_kind} (STREAM-style copy)",
-            "frac_of_nominal_8TBs": round(launch_gbs / NOMINAL_HBM_GBS, 4),
+            "frac": None if achieved is None else round(achieved / peak, 4),
+            "peak_kind": f"{peak_kind} (STREAM-style copy, MEASURED_PEAKS.json hbm_gbs)",
+            "frac_of_nominal_8TBs": None if achieved is None else round(achieved / NOMINAL_HBM_GBS, 4),
             "kernel": kernel_name,
-            "kernel_us_per_launch": round(launch_ms * 1e3 / (nl * (1 if args.sched == "persistent" else 1)), 3),
+            "kernel_us_per_launch": round(launch_us, 3),
+            "algorithmic_bytes_per_launch": round(bytes_per_launch),
+            "timing": "launch duration = timed-region time / launches (one launch per layer step)",
             "traffic": traffic,
             "traffic_note": f"ncu dram read+write per launch for kernel sources {digest}" if traffic
             else "no ncu record for the current kernel sources",
         },
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
-                "us_per_step": round(e2e_s / k_e2e * 1e6, 2), "steps": k_e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "moe_decode_run_host (pinned host buffers, copies + sync each step)" if nl == 1
-                else "host copy in, 12 x moe_decode_run, copy out, sync"},
-        "gpu_launches": K * kernels_per_run * nl,
-        "clocks": clk,
+                "us_per_step": round(e2e_s / e2e_steps * 1e6, 2), "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": e2e_path},
+        "gpu_launches": K * launches_per_step,
     }
-    return res, (layers, mods, xs, shape, m, nl)
+    if rank == 0 and world == 1 and cpu_seconds > 0:
+        res["cpu_baseline"] = cpu_baseline(name, cpu_seconds)
+    for md in mods:
+        md.close()
+    del mods, xs, graphs
+    return res
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 
 
-def oracle_step_time(shape, m, rho, target_s, seed=7):
-    """Time the float64 oracle on one layer step, repeated for about target_s."""
-    import numpy as np
-    import torch
-    import oracle
-    from moe_decode_layer_gb300 import synth
+class OracleWorkload:
+    """A layer of the workload's shape for the C++ oracle on the host.
 
-    layer = synth.make_layer(shape, seed=seed, device="cpu") if shape.num_experts <= 64 else None
-    rng_experts = {}
+    Ling-sized layers are not materialised: the router is drawn once and each
+    expert's weights are drawn when a step first selects it (same N(0, 0.02^2)
+    recipe as the device layers, from a CPU generator, so not the GPU's values;
+    the oracle's cost does not depend on them)."""
 
-    # Ling-sized layers are not materialised on the CPU: each step reads the
-    # router and only the experts it selects, drawn lazily (same distribution).
-    if layer is None:
+    def __init__(self, name: str, seed: int = 7):
+        import numpy as np
+        import torch
+        from moe_decode_layer_gb300 import synth
+        self.np, self.torch, self.synth = np, torch, synth
+        self.wl = WORKLOADS[name]
+        self.shape = synth.workload_shape(name)
+        self.seed = seed
         g = torch.Generator().manual_seed(seed)
-        router = (torch.randn((shape.num_experts, shape.hidden), generator=g) * 0.02).to(torch.bfloat16)
-    else:
-        router = layer["router_w"]
+        r = (torch.randn((self.shape.num_experts, self.shape.hidden), generator=g) * 0.02).to(torch.bfloat16)
+        self.router = r.view(torch.int16).numpy().view(np.uint16)
+        self.cache = {}
 
-    def bits(t):
-        return t.contiguous().view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 \
-            else t.contiguous().numpy()
-
-    def expert_bits(e, prefix=""):
-        key = (prefix, e)
-        if key not in rng_experts:
-            if layer is not None:
-                rng_experts[key] = (bits(layer[prefix + "w13"][e]), bits(layer[prefix + "w2"][e]))
+    def expert(self, e, shared=False):
+        from oracle import cpp
+        key = (shared, e)
+        if key not in self.cache:
+            torch, np, sh = self.torch, self.np, self.shape
+            gg = torch.Generator().manual_seed(self.seed * 1009 + e + (100_003 if shared else 0))
+            w13 = torch.randn((2 * sh.inter, sh.hidden), generator=gg) * 0.02
+            w2 = torch.randn((sh.hidden, sh.inter), generator=gg) * 0.02
+            if sh.wdtype == "bf16":
+                bits = lambda t: t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+                self.cache[key] = (bits(w13), bits(w2))
             else:
-                gg = torch.Generator().manual_seed(seed * 1009 + e + (7 if prefix else 0))
-                if shape.wdtype == "bf16":
-                    w13 = (torch.randn((2 * shape.inter, shape.hidden), generator=gg) * 0.02).to(torch.bfloat16)
-                    w2 = (torch.randn((shape.hidden, shape.inter), generator=gg) * 0.02).to(torch.bfloat16)
-                    rng_experts[key] = (bits(w13), bits(w2))
-                else:
-                    w13 = torch.randn((2 * shape.inter, shape.hidden), generator=gg) * 0.02
-                    w2 = torch.randn((shape.hidden, shape.inter), generator=gg) * 0.02
-                    q13, s13, t13 = synth.quantize_nvfp4(w13)
-                    q2, s2, t2 = synth.quantize_nvfp4(w2)
-                    rng_experts[key] = ((bits(q13), bits(s13), float(t13)), (bits(q2), bits(s2), float(t2)))
-        return rng_experts[key]
+                qg, sg, tg = self.synth.quantize_nvfp4(w13[:sh.inter])
+                qu, su, tu = self.synth.quantize_nvfp4(w13[sh.inter:])
+                q2, s2, t2 = self.synth.quantize_nvfp4(w2)
+                self.cache[key] = cpp.NVFP4Expert(torch.cat([qg, qu]).numpy(), torch.cat([sg, su]).numpy(),
+                                                  np.array([float(tg), float(tu)], np.float32), q2.numpy(),
+                                                  s2.numpy(), np.float32(t2))
+            if len(self.cache) > 192:
+                self.cache.pop(next(iter(self.cache)))
+        return self.cache[key]
 
-    def accessor(prefix=""):
-        def get(e):
-            a, b = expert_bits(e, prefix)
-            if shape.wdtype == "bf16":
-                return oracle.bf16_bits_to_f64(a), oracle.bf16_bits_to_f64(b)
-            return (oracle.dequant_nvfp4_rows(a[0], a[1], a[2]), oracle.dequant_nvfp4_rows(b[0], b[1], b[2]))
-        return get
+    def prepare(self, step: int):
+        from oracle import cpp
+        x = self.synth.hidden_rows(self.wl["m"], self.shape.hidden, seed=90_000 + step, rho=self.wl["rho"])
+        xb = x.view(self.torch.int16).numpy().view(self.np.uint16)
+        xf = cpp.bf16_bits_to_f64(xb)
+        shared = [self.expert(s, True) for s in range(self.shape.num_shared)]
+        return cpp.Prepared(xf, xf, self.router, self.expert, shared, self.shape.top_k)
 
-    rbits = bits(router)
-    steps, t_total, step_bytes = 0, 0.0, 0
+
+def oracle_timing(name: str, target_s: float, threads: int):
+    """Time the C++ oracle on layer steps of the workload for about target_s of
+    oracle time (weights gathered outside the timed calls). Returns (s per layer
+    step, algorithmic bytes per layer step, steps)."""
+    from moe_decode_layer_gb300 import synth
+    ow = OracleWorkload(name)
+    t_total, b_total, n = 0.0, 0, 0
+    wall0 = time.perf_counter()
     while True:
-        x = synth.hidden_rows(m, shape.hidden, seed=90_000 + steps, rho=rho)
-        xb = bits(x)
-        # warm the lazily drawn weights outside the timed part
-        _, idx, _ = oracle.route(oracle.bf16_bits_to_f64(xb), oracle.bf16_bits_to_f64(rbits), shape.top_k)
-        for e in set(idx.ravel().tolist()):
-            expert_bits(e)
-        for s in range(shape.num_shared):
-            expert_bits(s, "sh_")
+        prep = ow.prepare(n)
         t = time.perf_counter()
-        xf = oracle.bf16_bits_to_f64(xb)
-        shared_get = accessor("sh_")
-        oracle.moe_layer(xf, xf, oracle.bf16_bits_to_f64(rbits), accessor(),
-                         [shared_get(s) for s in range(shape.num_shared)], shape.top_k)
+        prep.run(threads)
         t_total += time.perf_counter() - t
-        step_bytes += synth.algorithmic_bytes(shape, len(set(idx.ravel().tolist())))
-        steps += 1
-        rng_experts.clear() if len(rng_experts) > 256 else None
-        if t_total >= target_s and steps >= 3:
+        b_total += synth.algorithmic_bytes(ow.shape, len(prep.needed))
+        n += 1
+        if (t_total >= target_s and n >= 2) or time.perf_counter() - wall0 > 4 * target_s + 10:
             break
-    return t_total / steps, step_bytes / steps, steps
+    return t_total / n, b_total / n, n
 
 
 def cores_used():
@@ -444,42 +487,48 @@ def cores_used():
 
 
 def cpu_baseline(workload, target_s):
-    from moe_decode_layer_gb300 import synth
+    """The oracle, as it stands, on the host cores: one thread and all cores."""
+    from oracle import cpp
     wl = WORKLOADS[workload]
-    shape = synth.workload_shape(workload)
-    t_step, b_step, n = oracle_step_time(shape, wl["m"], wl["rho"], target_s)
-    t_step *= wl["layers"]  # the stack runs the same layer arithmetic per layer
-    b_step *= wl["layers"]
-    return {"value": round(b_step / t_step / 1e9, 4), "unit": "GB/s",
-            "us_per_step": round(t_step * 1e6, 1), "cores": cores_used(), "kind": "oracle",
-            "sample": f"{n} layer steps of the {workload} workload through the float64 numpy oracle "
-                      f"(router over all experts + the selected experts), ~{target_s:.0f} s of CPU time; "
-                      f"numpy BLAS threads over {cores_used()} cores"}
+    nl = wl["layers"]
+    cores = min(cores_used(), cpp.max_threads())
+    t1, b1, n1 = oracle_timing(workload, target_s / 2, 1)
+    tn, bn, nn = oracle_timing(workload, target_s / 2, cores)
+    return {"value": round(bn / tn / 1e9, 4), "unit": "GB/s", "us_per_step": round(tn * nl * 1e6, 1),
+            "cores": cores, "kind": "oracle",
+            "one_thread": {"value": round(b1 / t1 / 1e9, 4), "unit": "GB/s", "us_per_step": round(t1 * nl * 1e6, 1),
+                           "cores": 1, "steps": n1},
+            "sample": f"{nn} (all cores) and {n1} (one thread) layer steps of the {workload} workload through "
+                      f"the C++ float64 oracle (router over all experts + the selected and shared experts, "
+                      f"OpenMP over output elements), ~{target_s / 2:.1f} s each"
+                      + (f"; a step of the {nl}-layer stack is timed as {nl} such layer steps" if nl > 1 else "")
+                      + "; expert weights drawn on the CPU with the device recipe, not the GPU's values"}
 
 
 def run_reference(args, rank, world):
     """The oracle as the reference arm: rank 0 only."""
     if rank != 0:
         return None
-    from moe_decode_layer_gb300 import synth
+    from oracle import cpp
     wl = WORKLOADS[args.workload]
-    shape = synth.workload_shape(args.workload)
-    # each step is a bounded sample; total CPU time ~ a few minutes at most
+    nl = wl["layers"]
     budget = getattr(args, "ref_seconds", None)
     if budget is None:
-        budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup))) * (args.steps + args.warmup)
-    t_step, b_step, n = oracle_step_time(shape, wl["m"], wl["rho"], budget)
-    t_step *= wl["layers"]
-    b_step *= wl["layers"]
+        budget = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup))) * (args.steps + args.warmup)
+    cores = min(cores_used(), cpp.max_threads())
+    t_step, b_step, n = oracle_timing(args.workload, budget, cores)
+    t_step *= nl
+    b_step *= nl
     v = b_step / t_step / 1e9
-    base = {"value": round(v, 4), "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
-            "sample": f"{n} oracle layer steps on the host cores, workload {args.workload}"}
+    base = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} layer steps of the {args.workload} workload through the C++ float64 oracle on "
+                      f"{cores} host cores (OpenMP)"}
     return {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {wl['desc']}", "rows_M": wl["m"], "layers_per_step": wl["layers"]},
+        "config": {"workload": f"{args.workload}: {wl['desc']}", "rows_M": wl["m"], "layers_per_step": nl},
         "cpu_baseline": base,
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -491,19 +540,21 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="ling_m1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sched", default="persistent", choices=["persistent", "phased", "interleaved", "pdl_chain", "chain"])
+    ap.add_argument("--sched", default="persistent",
+                    choices=["persistent", "phased", "interleaved", "flat", "pdl_chain", "chain"])
     ap.add_argument("--copies", type=int, default=8, help="distinct layer copies (single-layer workloads)")
-    ap.add_argument("--e2e-steps", type=int, default=2000)
-    ap.add_argument("--ring-slots", type=int, default=0, help="cap on shared-memory ring slots (0 = planned)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle CPU baseline sample length")
+    ap.add_argument("--lat-steps", type=int, default=256, help="single steps for the latency percentiles (>= 200)")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle CPU baseline sample per workload")
     ap.add_argument("--ref-seconds", type=float, default=None,
-                    help="--impl reference: total oracle time (default: ~20 s per step, <= 2 min)")
-    ap.add_argument("--secondary", default="ling_m6",
-                    help="extra workload measured in the same run ('' to skip)")
+                    help="--impl reference: total oracle time (default: ~10 s per step, <= 2 min)")
+    ap.add_argument("--extra", default=DEFAULT_EXTRA,
+                    help="other workloads measured in the same run (comma list, '' to skip)")
+    ap.add_argument("--extra-steps", type=int, default=400, help="timed steps of each extra workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -526,22 +577,32 @@ def main(argv=None):
             dist.destroy_process_group()
         return 0
 
-    res, keep = run_ours(args, rank, world, dist)
-    del keep
-    if args.secondary and args.secondary != args.workload and world == 1:
-        import torch
-        torch.cuda.empty_cache()
-        sec_args = argparse.Namespace(**vars(args))
-        sec_args.workload = args.secondary
-        sec_args.steps = max(100, args.steps // 4)
-        sec_args.warmup = max(10, args.warmup // 4)
-        sec, keep = run_ours(sec_args, rank, world, None)
-        del keep
-        res["secondary"] = {k: sec[k] for k in ("value", "unit", "ms_per_step", "us_per_layer_step",
-                                                "tokens_per_s_equiv", "bytes_per_step_avg", "roofline",
-                                                "config", "steps", "clocks")}
-    if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    import torch
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    pool = LayerPool(rank)
+    lat = max(200, args.lat_steps)
+    res = run_workload(args.workload, args, rank, world, dist, pool, args.steps, args.warmup, lat,
+                       min(args.e2e_steps, max(args.steps, 50)), args.cpu_seconds)
+    extras = [w for w in args.extra.split(",") if w and w != args.workload] if world == 1 else []
+    blocks = {}
+    order = sorted(extras, key=lambda w: WORKLOADS[w]["shape"] != WORKLOADS[args.workload]["shape"])
+    for name in order:
+        shape_name = WORKLOADS[name]["shape"]
+        blk = run_workload(name, args, rank, world, None, pool, max(args.extra_steps, 64), max(args.warmup, 10),
+                           lat, min(args.e2e_steps, 200), args.cpu_seconds)
+        blocks[name] = {k: blk[k] for k in ("value", "unit", "ms_per_step", "us_per_layer_step", "step_latency_us",
+                                           "tokens_per_s_equiv", "bytes_per_step_avg", "roofline", "e2e",
+                                           "cpu_baseline", "config", "steps", "gpu_launches", "dtype")
+                        if k in blk}
+        if not any(WORKLOADS[w]["shape"] == shape_name for w in order[order.index(name) + 1:]):
+            pool.drop(shape_name)
+            torch.cuda.empty_cache()
+    if blocks:
+        res["workloads"] = {k: blocks[k] for k in extras if k in blocks}
+    res["clocks"] = clocks.stop()
     if rank == 0:
         print(json.dumps(res), flush=True)
     if dist is not None:

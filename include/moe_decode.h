@@ -74,7 +74,7 @@ typedef enum moe_sched {
  *   0 <= num_shared <= 4;  1 <= max_rows <= 8;
  *   bf16:  hidden % 8 == 0, 64 <= hidden <= 4096; inter % 8 == 0 and inter / 8
  *          either a power of two <= 32 or a multiple of 32 no larger than 384;
- *   nvfp4: hidden % 256 == 0, 256 <= hidden <= 8192; inter % 256 == 0, inter <= 12288;
+ *   nvfp4: hidden % 256 == 0, 256 <= hidden <= 4096; inter % 256 == 0, inter <= 12288;
  *   routed_scale finite; rms_eps > 0 when pre_rmsnorm.
  */
 typedef struct moe_decode_config {
@@ -124,15 +124,23 @@ typedef struct moe_decode_weights {
 
 typedef struct moe_decode_handle moe_decode_handle;
 
-/* Validates a config on the host. Makes no CUDA call. */
+/*
+ * Validates a config on the host. Makes no CUDA call. This is the "guard" of the
+ * SGLang Low-Latency Mode page, section "Plugin System: Design and Integration":
+ * declared requirements are checked before any weight is touched, so an
+ * unsupported configuration fails early. The shapes it accepts cover the pages'
+ * layers: Ling-3.0-flash (model table: hidden 2560, 512 routed + 1 shared expert,
+ * top-8, moe_intermediate 768) and Muse Spark ("The model": 8 of 256 experts, NVFP4).
+ */
 moe_status moe_decode_config_check(const moe_decode_config* cfg);
 
 /*
  * The launch layout create would plan for cfg on a device with `sms` SMs and
  * `smem_optin` bytes of opt-in shared memory per block, computed on the host
  * (no CUDA call). `interleaved` = 1 asks for the slot-interleaved single kernel's
- * layout (MOE_ERR_UNSUPPORTED when it does not fit), 0 for the phase-ordered
- * kernels'. All fields in bytes or counts; filled only on MOE_OK.
+ * layout, 2 for the expert-range kernel's (MOE_ERR_UNSUPPORTED when it does not
+ * fit), 0 for the phase-ordered kernels'. All fields in bytes or counts; filled
+ * only on MOE_OK.
  */
 typedef struct moe_decode_plan_info {
   int32_t smem_bytes;        /* dynamic shared memory per CTA (incl. alignment slack)   */
@@ -156,7 +164,10 @@ moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t sm
                            moe_decode_plan_info* out);
 
 /*
- * Builds a handle for the current CUDA device: validates cfg and the weight
+ * Builds a handle for the current CUDA device -- the "build" step of the SGLang
+ * Low-Latency Mode page, section "Plugin System: Design and Integration":
+ * execution resources are set up once at initialisation and reused by every
+ * request. It validates cfg and the weight
  * pointers, allocates the handle's device scratch (control words, tagged
  * logits and intermediate activations, host-call staging buffers) and plans the
  * launch shape from the device's SM count and shared memory. Copies nothing and
@@ -169,7 +180,13 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
                              moe_decode_handle** out);
 
 /*
- * Enqueues one layer step on `stream`; returns without waiting.
+ * Enqueues one layer step on `stream`; returns without waiting. The step is the
+ * router chain (norm -> gate matvec -> top-k) and the MoE chain (up-GEMM ->
+ * activation -> down-GEMM -> combine) of the Ling-3.0-flash batch-1 decode blog,
+ * section "PDL: stacking the latency floors of small kernels", fused into one
+ * persistent kernel or chained with programmatic dependent launch (cfg.sched);
+ * the "runtime" step of the plugin section above (a dispatch that a CUDA graph
+ * can record once and replay).
  *   x        bf16 [M, H] device, layer input (normalised inside when pre_rmsnorm)
  *   residual bf16 [M, H] device
  *   out      bf16 [M, H] device; may be the same buffer as residual and/or x
@@ -195,7 +212,10 @@ moe_status moe_decode_run_host(moe_decode_handle* h, const void* x_host, const v
                                float* topk_w_host, moe_stream_t stream);
 
 /*
- * Synchronises `stream`, reads and clears the handle's device status word.
+ * Synchronises `stream`, reads and clears the handle's device status word. Every
+ * device-side wait is bounded (the Muse Spark page, "Megakernel internals": a
+ * missed deadline stops the launch instead of hanging the server), and a wait that
+ * gives up is reported here.
  * MOE_ERR_DEVICE_TIMEOUT means some device-side wait of an earlier run on this
  * handle gave up after the wait limit; that run's outputs are undefined.
  */
@@ -218,6 +238,14 @@ enum {
                                   measured faster; 2 always; 0 never (the phase-
                                   ordered kernel). get_info: the mode, 0 when the
                                   interleaved layout does not fit.                   */
+  MOE_OPT_FLAT = 7,            /* MOE_SCHED_PERSISTENT runs with the expert-range
+                                  kernel (each CTA owns a contiguous range of the
+                                  routed experts' rows and output blocks; bf16
+                                  weights, at most one shared expert) when its layout
+                                  fits and: 1 (default) for one token row, where it
+                                  measured faster; 2 always; 0 never. It takes
+                                  precedence over MOE_OPT_INTERLEAVE. get_info: the
+                                  mode, 0 when the layout does not fit.              */
   MOE_INFO_GRID = 16,          /* CTAs per kernel                                   */
   MOE_INFO_THREADS = 17,       /* threads per CTA                                   */
   MOE_INFO_SMEM = 18,          /* dynamic shared memory per CTA, bytes              */
@@ -225,9 +253,10 @@ enum {
   MOE_INFO_SLOT_BYTES = 20,    /*                            bytes per slot         */
   MOE_INFO_KERNELS_PER_RUN = 21,
   MOE_INFO_SCRATCH_BYTES = 22,
-  MOE_INFO_INTERLEAVED_ROWS = 23 /* bit m-1 set: a run of m rows under the current
-                                    schedule and MOE_OPT_INTERLEAVE takes the
-                                    slot-interleaved kernel                        */
+  MOE_INFO_INTERLEAVED_ROWS = 23, /* bit m-1 set: a run of m rows under the current
+                                    schedule and options takes the slot-interleaved
+                                    kernel                                         */
+  MOE_INFO_FLAT_ROWS = 24        /* the same for the expert-range kernel            */
 };
 moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value);
 moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value);
@@ -251,13 +280,17 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
  * flag per SM) exceeds it
  * return MOE_ERR_UNSUPPORTED before any device work. The first call on a device
  * sets the array up (resolves its device address and fills it, a blocking
- * memset); make that first call before any CUDA stream capture. Every call
- * shares the array and it keeps the last call's contents; calls that overlap on
- * the GPU (from different streams or threads, on one device) race, so issue
- * them one after another.
+ * memset). The array's address is looked up again on every call; a call that
+ * finds it moved (the module was reloaded, as after cudaDeviceReset) sets the new
+ * array up the same way. Every call shares the array and it keeps the last call's
+ * contents; calls that overlap on the GPU (from different streams or threads, on
+ * one device) race, so issue them one after another.
  *
  * Blocking: the call waits for the step on `stream` and returns its device
- * status (MOE_OK or MOE_ERR_DEVICE_TIMEOUT), as moe_decode_run_host does.
+ * status (MOE_OK or MOE_ERR_DEVICE_TIMEOUT), as moe_decode_run_host does. So it
+ * must never be made on a stream that is being captured into a CUDA graph: such
+ * a call returns MOE_ERR_INVALID_ARG before any device work. MOE_ERR_UNSUPPORTED
+ * also when one CTA of the launch does not fit an SM.
  * Never calls cudaMalloc, cudaFree or any allocating library routine.
  */
 #define MOE_DECODE_STATIC_SCRATCH_BYTES (4u << 20)

@@ -19,12 +19,16 @@ struct moe_decode_handle {
   moe_decode_config cfg;
   Params base;       // everything but the per-run pointers and M
   Params ilv;        // the same for the slot-interleaved single kernel (when has_ilv)
+  Params flat;       // the same for the expert-range single kernel (when has_flat)
   bool has_ilv = false;
-  int ilv_mode = 1;  // MOE_OPT_INTERLEAVE
+  bool has_flat = false;
+  int ilv_mode = 1;   // MOE_OPT_INTERLEAVE
+  int flat_mode = 0;  // MOE_OPT_FLAT
   int device = 0;
   int sched = MOE_SCHED_PERSISTENT;
   int max_slots = 0;  // ring slots the planned shared memory holds
   int max_slots_ilv = 0;
+  int max_slots_flat = 0;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   uint16_t* stage_x = nullptr;  // run_host staging
@@ -32,6 +36,7 @@ struct moe_decode_handle {
   uint16_t* stage_out = nullptr;
   int32_t* stage_idx = nullptr;
   float* stage_w = nullptr;
+  uint32_t* host_status = nullptr;  // pinned host words: the status read back by run_host
 };
 
 namespace {
@@ -210,6 +215,81 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   return MOE_OK;
 }
 
+// The layout of the expert-range single kernel (moe_flat.cuh): the shape fields
+// of plan(), then its own shared memory: three h buffers (one per down segment)
+// that the routing scratch overlaps, and a ring of gate/up / down stages.
+// MOE_ERR_UNSUPPORTED when the kernel does not cover cfg (bf16 weights, at most
+// one shared expert, routed slots no more than the grid's CTAs, I <= 1024).
+moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params& p) {
+  moe_status st = plan(c, sms, smem_optin, p, false);
+  if (st != MOE_OK) return st;
+  if (p.fmt != moe::FMT_BF16 || p.S > 1 || p.nslot_max - p.S > p.grid ||
+      p.nslot_max > moe::CTRL_WORDS - moe::CTRL_SLOTCNT || p.nchunk_i > moe::kFlatMaxChunks)
+    return MOE_ERR_UNSUPPORTED;
+  const int H = p.H, I = p.I, E = p.E, K = p.K, maxm = p.maxm;
+  size_t off = 0;
+  auto take = [&](size_t bytes, size_t align) {
+    off = round_up(off, align);
+    const size_t at = off;
+    off += bytes;
+    return static_cast<int>(at);
+  };
+  p.off_full = take(moe::kMaxSlots * 8, 8);
+  p.off_empty = take(moe::kMaxSlots * 8, 8);
+  p.off_xbar = take(8, 8);
+  p.off_hbar = take(moe::kFlatSegs * 8, 8);
+  p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
+  p.off_x = take((size_t)maxm * H * 2, 128);
+  p.off_sel_e = take((size_t)maxm * K * 4, 4);
+  p.off_sel_w = take((size_t)maxm * K * 4, 4);
+  p.off_emask = take((size_t)E * 4, 4);
+  p.off_bitmap = take((size_t)(E + 31) / 32 * 4, 4);
+  p.off_slot_of = take((size_t)E * 4, 4);
+  p.off_slot_e = take((size_t)p.nslot_max * 4, 4);
+  p.off_slot_mask = take((size_t)p.nslot_max * 4, 4);
+  p.off_slot_w = take((size_t)p.nslot_max * maxm * 4, 4);
+  p.off_pair_base = take((size_t)(p.nslot_max + 1) * 4, 4);
+  p.off_pair_sr = take((size_t)p.npair_max * 4, 4);
+  p.off_red = take((size_t)moe::kNC * 8 * 4, 16);
+  p.off_misc = take(moe::MISC_WORDS * 4, 16);
+  p.off_acnt = take((size_t)p.nslot_max * 4, 4);
+  p.off_fin = take((size_t)(1 + p.nslot_max) * 4, 4);
+  const size_t fixed = round_up(off, 128);
+  // h buffers; the routing scratch overlaps them (routing is over before any h lands)
+  p.off_hs = (int)fixed;
+  const size_t hbytes = (size_t)moe::kFlatSegs * maxm * I * 4;
+  size_t ro = fixed;
+  auto rtake = [&](size_t bytes, size_t align) {
+    ro = round_up(ro, align);
+    const size_t at = ro;
+    ro += bytes;
+    return static_cast<int>(at);
+  };
+  p.off_lg = rtake((size_t)maxm * E * 4, 16);
+  p.off_cand = rtake((size_t)maxm * moe::kCandMax * 8, 16);
+  p.off_lmax = rtake((size_t)maxm * 32 * 4, 16);
+  p.off_thr = rtake((size_t)maxm * 8, 8);
+  p.off_ccount = rtake((size_t)maxm * 4, 4);
+  p.off_wtmp = rtake((size_t)maxm * 16 * 4, 16);
+  p.off_wpc = rtake(32 * 4, 16);
+  p.off_ring = (int)round_up(std::max(ro, fixed + hbytes), 128);
+  const size_t q0 = std::max<size_t>(1, std::min<size_t>(moe::kNC, moe::kStageTarget / p.pair_bytes));
+  const size_t slot = round_up(std::max({q0 * p.pair_bytes, (size_t)p.rpair_bytes, (size_t)p.pair_bytes,
+                                         (size_t)p.row2}), 128);
+  const long long ring_budget = (long long)smem_optin - 1024 - p.off_ring;
+  const long long ns = ring_budget > 0 ? ring_budget / (long long)slot : 0;
+  if (ns < 3) return MOE_ERR_UNSUPPORTED;
+  p.slot_bytes = (int)slot;
+  p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
+  p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
+  p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
+  p.d_rows_stage = p.slot_bytes / p.row2;
+  p.nslots_x = p.nslots_d = p.hs_pairs = p.hs_perslot = 0;
+  p.hs_nbuf = 1;
+  p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
+  return MOE_OK;
+}
+
 const void* kernel_for(const Params& p, int maxm_t, int phases) {
   return p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, phases) : moe::kernel_nvfp4(maxm_t, phases);
 }
@@ -259,19 +339,31 @@ void bind_pointers(const Params& from, Params& to) {
 // Whether a persistent run of m rows takes the slot-interleaved kernel: always
 // when forced (mode 2), else where it measured faster on GB300 -- bf16 weights,
 // one token row (mode 1).
+// Whether a persistent run of m rows takes the expert-range kernel: always when
+// forced (mode 2), else (mode 1) where it measured faster on GB300.
+bool use_flat(const moe_decode_handle* h, int m) {
+  if (h->sched != MOE_SCHED_PERSISTENT || !h->has_flat) return false;
+  return h->flat_mode == 2 || (h->flat_mode == 1 && m == 1);
+}
 bool interleaved(const moe_decode_handle* h, int m) {
-  if (h->sched != MOE_SCHED_PERSISTENT || !h->has_ilv) return false;
+  if (h->sched != MOE_SCHED_PERSISTENT || !h->has_ilv || use_flat(h, m)) return false;
   return h->ilv_mode == 2 || (h->ilv_mode == 1 && h->base.fmt == moe::FMT_BF16 && m == 1);
 }
 // The layout a run of m rows uses.
-const Params& active_params(const moe_decode_handle* h, int m) { return interleaved(h, m) ? h->ilv : h->base; }
+const Params& active_params(const moe_decode_handle* h, int m) {
+  return use_flat(h, m) ? h->flat : interleaved(h, m) ? h->ilv : h->base;
+}
+int threads_for(const moe_decode_handle* h, int m) {
+  return use_flat(h, m) ? moe::kThreadsFlat : interleaved(h, m) ? moe::kThreadsIlv : moe::kThreads;
+}
 
 moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
   const int maxm_t = p.M == 1 ? 1 : 8;
   const bool ilv = interleaved(h, p.M);
+  const bool flat = use_flat(h, p.M);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(ilv ? moe::kThreadsIlv : moe::kThreads);
+  cfg.blockDim = dim3(threads_for(h, p.M));
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -281,9 +373,8 @@ moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelExC(&cfg, kernel_for(p, maxm_t, ilv ? moe::PH_ILV : moe::PH_ALL), args) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
+    const void* k = flat ? moe::kernel_flat(maxm_t) : kernel_for(p, maxm_t, ilv ? moe::PH_ILV : moe::PH_ALL);
+    if (cudaLaunchKernelExC(&cfg, k, args) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
   const int phases[3] = {moe::PH_R, moe::PH_U, moe::PH_D};
@@ -347,11 +438,13 @@ moe_status moe_decode_config_check(const moe_decode_config* cfg) { return check_
 
 moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t smem_optin, int32_t interleaved,
                            moe_decode_plan_info* out) {
-  if (!out || sms <= 0 || smem_optin <= 0 || interleaved < 0 || interleaved > 1) return MOE_ERR_INVALID_ARG;
+  if (!out || sms <= 0 || smem_optin <= 0 || interleaved < 0 || interleaved > 2) return MOE_ERR_INVALID_ARG;
   moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
   Params p;
-  if ((st = plan(*cfg, sms, smem_optin, p, interleaved != 0)) != MOE_OK) return st;
+  if ((st = interleaved == 2 ? plan_flat(*cfg, sms, smem_optin, p)
+                             : plan(*cfg, sms, smem_optin, p, interleaved != 0)) != MOE_OK)
+    return st;
   out->smem_bytes = p.smem_bytes;
   out->ring_slots = p.nslots;
   out->slot_bytes = p.slot_bytes;
@@ -365,9 +458,9 @@ moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t sm
   out->h_per_slot = p.hs_perslot;
   out->slots_max = p.nslot_max;
   out->pairs_max = p.npair_max;
-  out->lag = interleaved ? p.ilv_lag : 0;
-  out->down_h_offset = interleaved ? p.d_hoff : 0;
-  out->threads = interleaved ? moe::kThreadsIlv : moe::kThreads;
+  out->lag = interleaved == 1 ? p.ilv_lag : 0;
+  out->down_h_offset = interleaved == 1 ? p.d_hoff : 0;
+  out->threads = interleaved == 2 ? moe::kThreadsFlat : interleaved ? moe::kThreadsIlv : moe::kThreads;
   return MOE_OK;
 }
 
@@ -386,6 +479,8 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   Params p, pi;
   if ((st = plan(*cfg, sms, optin, p, false)) != MOE_OK) return st;
   const bool has_ilv = plan(*cfg, sms, optin, pi, true) == MOE_OK;
+  Params pf;
+  bool has_flat = plan_flat(*cfg, sms, optin, pf) == MOE_OK;
   // Every kernel this handle may launch gets the shared-memory size, and one
   // CTA of the single-kernel schedule must fit on every SM.
   const int phases[4] = {moe::PH_ALL, moe::PH_R, moe::PH_U, moe::PH_D};
@@ -399,6 +494,14 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, moe::kThreads, p.smem_bytes) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (blocks < 1) return MOE_ERR_UNSUPPORTED;
+    }
+    if (has_flat) {
+      const void* k = moe::kernel_flat(mt);
+      int blocks = 0;
+      if (!k || cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pf.smem_bytes) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, moe::kThreadsFlat, pf.smem_bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (blocks < 1) has_flat = false;
     }
     if (has_ilv) {
       const void* k = kernel_for(pi, mt, moe::PH_ILV);
@@ -424,6 +527,9 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   const size_t o_xf = take((size_t)p.grid * 8);
 
   const size_t tag_end = off;
+  // expert-range kernel: per-slot outputs and per-block counts (zeroed)
+  const size_t o_y = has_flat ? take((size_t)p.nslot_max * maxm * H * 4) : 0;
+  const size_t o_bc = has_flat ? take((size_t)p.grid * 4) : 0;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
   const size_t o_so = take(maxm * H * 2);
@@ -436,10 +542,19 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
     delete h;
     return MOE_ERR_OOM;
   }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&h->host_status), 2 * sizeof(uint32_t), cudaHostAllocDefault) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->scratch);
+    delete h;
+    return MOE_ERR_OOM;
+  }
   uint8_t* base = static_cast<uint8_t*>(h->scratch);
   if (cudaMemset(base, 0, o_logits) != cudaSuccess ||
       cudaMemset(base + o_logits, 0xff, tag_end - o_logits) != cudaSuccess ||
+      (has_flat && cudaMemset(base + o_bc, 0, (size_t)p.grid * 4) != cudaSuccess) ||
       cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFreeHost(h->host_status);
     cudaFree(h->scratch);
     delete h;
     return MOE_ERR_CUDA;
@@ -474,6 +589,14 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->base = p;
   h->max_slots = p.nslots;
   h->has_ilv = has_ilv;
+  h->has_flat = has_flat;
+  h->max_slots_flat = has_flat ? pf.nslots : 0;
+  if (has_flat) {
+    bind_pointers(p, pf);
+    pf.ybuf = reinterpret_cast<float*>(base + o_y);
+    pf.blkcnt = reinterpret_cast<uint32_t*>(base + o_bc);
+    h->flat = pf;
+  }
   if (has_ilv) {
     // the interleaved layout, with the same weights and scratch
     bind_pointers(p, pi);
@@ -526,21 +649,29 @@ moe_status moe_decode_run_host(moe_decode_handle* h, const void* x_host, const v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)m_rows * h->cfg.hidden * 2;
   const size_t kb = (size_t)m_rows * h->cfg.top_k * 4;
+  // one copy per distinct input buffer: a residual that is x itself is not sent twice
+  const bool same = residual_host == x_host;
   if (cudaMemcpyAsync(h->stage_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->stage_r, residual_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      (!same && cudaMemcpyAsync(h->stage_r, residual_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess))
     return MOE_ERR_CUDA;
-  moe_status st = moe_decode_run(h, h->stage_x, h->stage_r, h->stage_out, m_rows,
+  moe_status st = moe_decode_run(h, h->stage_x, same ? h->stage_x : h->stage_r, h->stage_out, m_rows,
                                  topk_idx_host ? h->stage_idx : nullptr,
                                  topk_w_host ? h->stage_w : nullptr, stream);
   if (st != MOE_OK) return st;
-  if (cudaMemcpyAsync(out_host, h->stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  // results and the device status word back in the same stream, then one wait
+  if (cudaMemcpyAsync(out_host, h->stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (topk_idx_host &&
+       cudaMemcpyAsync(topk_idx_host, h->stage_idx, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+      (topk_w_host && cudaMemcpyAsync(topk_w_host, h->stage_w, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+      cudaMemcpyAsync(h->host_status, h->base.ctrl + moe::CTRL_STATUS, 2 * sizeof(uint32_t),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (topk_idx_host &&
-      cudaMemcpyAsync(topk_idx_host, h->stage_idx, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (h->host_status[0] == 0) return MOE_OK;
+  if (cudaMemsetAsync(h->base.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (topk_w_host && cudaMemcpyAsync(topk_w_host, h->stage_w, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return moe_decode_get_status(h, stream);
+  return MOE_ERR_DEVICE_TIMEOUT;
 }
 
 moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value) {
@@ -552,24 +683,31 @@ moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t v
       return MOE_OK;
     case MOE_OPT_WAIT_TIMEOUT_NS:
       if (value <= 0) return MOE_ERR_INVALID_ARG;
-      h->base.timeout_ns = h->ilv.timeout_ns = (unsigned long long)value;
+      h->base.timeout_ns = h->ilv.timeout_ns = h->flat.timeout_ns = (unsigned long long)value;
       return MOE_OK;
     case MOE_OPT_TEST_FLAGS:
       if (value < 0 || value > moe::TEST_SKIP_LOGITS) return MOE_ERR_INVALID_ARG;
-      h->base.test_flags = h->ilv.test_flags = (int)value;
+      h->base.test_flags = h->ilv.test_flags = h->flat.test_flags = (int)value;
       return MOE_OK;
     case MOE_OPT_RING_SLOTS:
-      if (value < 2 || value > std::max(h->max_slots, h->max_slots_ilv)) return MOE_ERR_INVALID_ARG;
+      if (value < 2 || value > std::max({h->max_slots, h->max_slots_ilv, h->max_slots_flat}))
+        return MOE_ERR_INVALID_ARG;
       h->base.nslots = std::min((int)value, h->max_slots);
       h->ilv.nslots = std::min((int)value, h->max_slots_ilv);
+      h->flat.nslots = std::max(3, std::min((int)value, h->max_slots_flat));
       return MOE_OK;
     case MOE_OPT_STAMPS:
       if (value & 7) return MOE_ERR_INVALID_ARG;
-      h->base.stamps = h->ilv.stamps = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+      h->base.stamps = h->ilv.stamps = h->flat.stamps =
+          reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
       return MOE_OK;
     case MOE_OPT_INTERLEAVE:
       if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       h->ilv_mode = (int)value;
+      return MOE_OK;
+    case MOE_OPT_FLAT:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      h->flat_mode = (int)value;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -584,8 +722,16 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_OPT_RING_SLOTS: *value = active_params(h, 1).nslots; return MOE_OK;
     case MOE_OPT_STAMPS: *value = (int64_t)reinterpret_cast<uintptr_t>(h->base.stamps); return MOE_OK;
     case MOE_OPT_INTERLEAVE: *value = h->has_ilv ? h->ilv_mode : 0; return MOE_OK;
+    case MOE_OPT_FLAT: *value = h->has_flat ? h->flat_mode : 0; return MOE_OK;
+    case MOE_INFO_FLAT_ROWS: {
+      int64_t mask = 0;
+      for (int m = 1; m <= h->cfg.max_rows; ++m)
+        if (use_flat(h, m)) mask |= int64_t(1) << (m - 1);
+      *value = mask;
+      return MOE_OK;
+    }
     case MOE_INFO_GRID: *value = h->base.grid; return MOE_OK;
-    case MOE_INFO_THREADS: *value = interleaved(h, 1) ? moe::kThreadsIlv : moe::kThreads; return MOE_OK;
+    case MOE_INFO_THREADS: *value = threads_for(h, 1); return MOE_OK;
     case MOE_INFO_SMEM: *value = active_params(h, 1).smem_bytes; return MOE_OK;
     case MOE_INFO_RING_SLOTS: *value = active_params(h, 1).nslots; return MOE_OK;
     case MOE_INFO_SLOT_BYTES: *value = active_params(h, 1).slot_bytes; return MOE_OK;
@@ -605,8 +751,9 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
 moe_status moe_decode_destroy(moe_decode_handle* h) {
   if (!h) return MOE_OK;
   cudaError_t e = cudaFree(h->scratch);  // cudaFree waits for outstanding work
+  const cudaError_t eh = h->host_status ? cudaFreeHost(h->host_status) : cudaSuccess;
   delete h;
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return e == cudaSuccess && eh == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // extern "C"

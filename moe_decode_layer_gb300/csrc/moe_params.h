@@ -29,6 +29,12 @@ enum Phase : int { PH_R = 1, PH_U = 2, PH_D = 4, PH_ALL = 7 };
 // schedule -- each CTA computes a block of rows of every union slot's gate/up
 // items, and the down stage of slot s follows the gate/up items of slot s + lag.
 constexpr int PH_ILV = 8;
+// Kernel selector: the expert-range single kernel (each CTA owns a contiguous
+// range of (expert, gate/up row) items and of (expert, output block) down stages).
+constexpr int PH_FLAT = 16;
+constexpr int kThreadsFlat = kThreadsIlv;  // consumers, producer, publisher, fetcher
+constexpr int kFlatSegs = 3;               // down segments per CTA: shared block + <= 2 routed slots
+constexpr int kFlatMaxChunks = 128;        // 16-byte chunks of a down row (I <= 1024 bf16)
 constexpr int kIlvRot = 37;  // per slot, the CTA -> row-block map rotates by this many CTAs
 constexpr int kIlvCnt = 8;   // per-CTA arrival counters of the interleaved schedule (slot s uses s % 8)
 // Interleaved-schedule words in shared memory (off_ucnt): the arrival counters,
@@ -162,6 +168,11 @@ struct Params {
   unsigned long long timeout_ns;
   int test_flags;
   unsigned long long* stamps;  // optional [grid][kStampSlots]
+  // expert-range kernel
+  float* ybuf;         // [nslot_max][maxm][H]: each union slot's down output, per row
+  uint32_t* blkcnt;    // [grid]: slots whose output rows of block b are stored (reset by the last)
+  int off_acnt;        // [nslot_max] consumer warps done with a slot's gate/up items
+  int off_fin;         // [1 + nslot_max] output blocks this CTA finishes (count, ids)
 };
 
 }  // namespace moe

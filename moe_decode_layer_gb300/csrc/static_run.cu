@@ -26,28 +26,33 @@ static_assert(kCtrlBytes >= moe::CTRL_WORDS * 4, "control words exceed their are
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Once per device, with that device current: the array's device address (the
-// name g_static_scratch in host code is only a stand-in, not that address),
-// control words zeroed and every tagged word set to a tag no run ever uses.
+// With the device current: the array's device address (the name
+// g_static_scratch in host code is only a stand-in, not that address). The
+// address is resolved on every call, which is cheap; the first call on a device,
+// and any call that finds a new address (the module was reloaded, e.g. after a
+// cudaDeviceReset, which also zeroes the array), sets the array up again: control
+// words zeroed and every tagged word set to a tag no run ever uses (a blocking
+// memset).
 moe_status setup_device(int dev, unsigned char** out) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (g_scratch_ptr[dev] != p) {
     unsigned char* b = static_cast<unsigned char*>(p);
     if (cudaMemset(b, 0, kCtrlBytes) != cudaSuccess ||
         cudaMemset(b + kCtrlBytes, 0xff, MOE_DECODE_STATIC_SCRATCH_BYTES - kCtrlBytes) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
       cudaGetLastError();
+      g_scratch_ptr[dev] = nullptr;
       return MOE_ERR_CUDA;
     }
     g_scratch_ptr[dev] = p;
   }
-  *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
+  *out = static_cast<unsigned char*>(p);
   return MOE_OK;
 }
 
@@ -82,6 +87,15 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   const size_t need = o_xf + round256((size_t)p.grid * 8);
   if (need > MOE_DECODE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
   if ((st = moe::check_weights_host(*cfg, w)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the call waits for its step and reads the status back, which a stream under
+  // capture cannot do: refuse before any device work
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return MOE_ERR_INVALID_ARG;
   unsigned char* base = nullptr;
   if ((st = setup_device(dev, &base)) != MOE_OK) return st;
 
@@ -106,7 +120,13 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   if (!kernel) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one CTA of the cooperative launch must fit on every SM (registers and threads
+  // as well as shared memory), as moe_decode_create checks
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, ilv ? moe::kThreadsIlv : moe::kThreads,
+                                                    p.smem_bytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (blocks < 1) return MOE_ERR_UNSUPPORTED;
   // a status left by an earlier call must not stop this one
   if (cudaMemsetAsync(p.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaLaunchConfig_t lc = {};

@@ -27,10 +27,11 @@ class MoEDecodeLayer:
 
     ``weights`` is the dict layout of :func:`synth.make_layer` (device tensors).
     The tensors are borrowed: this object keeps references so they outlive the
-    C handle. ``sched``: "persistent" (one kernel; slot-interleaved where that
-    measured faster), "phased" (one kernel, phases in order), "interleaved" (one
-    kernel, slot-interleaved whenever its layout fits), "pdl_chain" or "chain"
-    (three kernels).
+    C handle. ``sched``: "persistent" (one kernel; the expert-range or
+    slot-interleaved kernel where that measured faster), "phased" (one kernel,
+    phases in order), "interleaved" (one kernel, slot-interleaved whenever its
+    layout fits), "flat" (the expert-range kernel whenever its layout fits),
+    "pdl_chain" or "chain" (three kernels).
     """
 
     def __init__(self, shape: LayerShape, weights: dict, max_rows: int, sched: str = "persistent",
@@ -44,7 +45,8 @@ class MoEDecodeLayer:
                           wdtype=_lib.MOE_W_BF16 if shape.wdtype == "bf16" else _lib.MOE_W_NVFP4,
                           score=_lib.MOE_SCORE_SOFTMAX_TOPK_RENORM, routed_scale=routed_scale,
                           pre_rmsnorm=int(pre_rmsnorm), rms_eps=rms_eps,
-                          sched=_lib.SCHED_NAMES["persistent" if sched in ("phased", "interleaved") else sched])
+                          sched=_lib.SCHED_NAMES["persistent" if sched in ("phased", "interleaved", "flat")
+                                                  else sched])
         w = _lib.Weights()
         g = weights.get
         w.router_w = _ptr(g("router_w"))
@@ -66,7 +68,10 @@ class MoEDecodeLayer:
                    "moe_decode_create")
         self.handle = h
         if sched in ("phased", "interleaved"):  # the single kernel in phase order / always interleaved
+            self.set_option(_lib.MOE_OPT_FLAT, 0)
             self.set_option(_lib.MOE_OPT_INTERLEAVE, 0 if sched == "phased" else 2)
+        elif sched == "flat":  # the expert-range kernel whenever it fits
+            self.set_option(_lib.MOE_OPT_FLAT, 2)
 
     # ------------------------------------------------------------------ runs
     def run(self, x: torch.Tensor, residual: torch.Tensor | None = None, out: torch.Tensor | None = None,

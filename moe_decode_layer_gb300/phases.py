@@ -93,12 +93,13 @@ def main():
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--sweep-ring", default="", help="comma list of ring slot counts to compare")
     ap.add_argument("--hot", action="store_true", help="one layer copy and one input: weights stay in L2")
+    ap.add_argument("--sched", default="persistent", help="schedule (see MoEDecodeLayer)")
     a = ap.parse_args()
     sweep = [int(v) for v in a.sweep_ring.split(",") if v] or [a.ring_slots]
     for rs in sweep:
-        rows, total, used = timeline(a.workload, 1 if a.hot else a.copies, a.runs, rs,
+        rows, total, used = timeline(a.workload, 1 if a.hot else a.copies, a.runs, rs, sched=a.sched,
                                      n_inputs=1 if a.hot else 64)
-        print(f"# {a.workload}{' (hot: weights in L2)' if a.hot else ''}: ring slots {used}, "
+        print(f"# {a.workload} [{a.sched}]{' (hot: weights in L2)' if a.hot else ''}: ring slots {used}, "
               f"median first-entry -> last-exit {total:.2f} us")
         print(f"{'event':>16} {'median':>8} {'p10':>8} {'p90':>8} {'max':>8}")
         for name, med, p10, p90, mx in rows:

@@ -86,11 +86,13 @@ def test_nvfp4_small_shapes():
         assert torch.equal(outs[0], outs[1])
 
 
-def test_stack_12_layers_m6():
+@pytest.mark.parametrize("sched", ["persistent", "flat"])
+def test_stack_12_layers_m6(sched):
     shape = synth.LING
     n_layers, m = 12, 6
     layers = [synth.make_layer(shape, seed=100 + i, device="cuda") for i in range(n_layers)]
-    mods = [MoEDecodeLayer(shape, layers[i], m, pre_rmsnorm=True, rms_eps=1e-6) for i in range(n_layers)]
+    mods = [MoEDecodeLayer(shape, layers[i], m, sched=sched, pre_rmsnorm=True, rms_eps=1e-6)
+            for i in range(n_layers)]
     h0 = synth.hidden_rows(m, shape.hidden, seed=77, rho=0.5)
     h = h0.cuda()
     inputs, idxs = [], []

@@ -24,9 +24,10 @@ def tiny():
     return synth.make_layer(synth.TINY, seed=0, device="cuda")
 
 
-@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "pdl_chain", "chain"])
-def test_withheld_router_results_time_out(tiny, sched):
-    x = helpers.hidden_with_margin(tiny["router_w"], 2, synth.TINY.top_k, seed=3)
+@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "flat", "pdl_chain", "chain"])
+@pytest.mark.parametrize("m", [1, 2])
+def test_withheld_router_results_time_out(tiny, sched, m):
+    x = helpers.hidden_with_margin(tiny["router_w"], m, synth.TINY.top_k, seed=3)
     mod = MoEDecodeLayer(synth.TINY, tiny, 2, sched=sched)
     xd = x.cuda()
     good = mod.run(xd, xd).clone()

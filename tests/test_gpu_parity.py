@@ -6,7 +6,9 @@ relative L2 5e-3 of the oracle. Cases span the tiny layer, the Ling-shaped layer
 at full size (M = 1 and M = 6 correlated rows) in the launch configuration the
 bench times, ragged and degenerate shapes, all three schedules (which must agree
 bit for bit), in-place outputs, repeated runs, graph capture and the host-buffer
-entry point.
+entry point. The expert-range kernel ("flat") sums each output over the experts in
+another order (per expert, then over experts), so it is held to the oracle and to
+bitwise repeatability rather than to bit equality with the others.
 """
 
 import numpy as np
@@ -19,7 +21,9 @@ from tests import helpers
 
 pytestmark = pytest.mark.gpu
 
-SCHEDS = ["persistent", "phased", "interleaved", "pdl_chain", "chain"]
+SCHEDS = ["persistent", "phased", "interleaved", "flat", "pdl_chain", "chain"]
+# schedules that sum every output in the same order (bit-identical results)
+SAME_ORDER = ["phased", "interleaved", "pdl_chain", "chain"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -92,11 +96,31 @@ def test_tiny_moe_part_alone(tiny):
     assert np.linalg.norm(g - ref) / np.linalg.norm(ref) < 3e-3
 
 
-def test_schedules_bitwise_identical(tiny):
-    x = helpers.hidden_with_margin(tiny["router_w"], 4, synth.TINY.top_k, seed=9, rho=0.5)
-    outs = [_run(synth.TINY, tiny, x, sched=s)[1] for s in SCHEDS]
+@pytest.mark.parametrize("m", [1, 4])
+def test_schedules_bitwise_identical(tiny, m):
+    x = helpers.hidden_with_margin(tiny["router_w"], m, synth.TINY.top_k, seed=9, rho=0.5)
+    outs = [_run(synth.TINY, tiny, x, sched=s)[1] for s in SAME_ORDER]
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_flat_kernel_repeatable_and_inplace(tiny, m):
+    """The expert-range kernel: the same bits on every run (the block that finishes
+    last sums its slots in a fixed order), in place as well."""
+    x = helpers.hidden_with_margin(tiny["router_w"], m, synth.TINY.top_k, seed=40 + m, rho=0.5)
+    mod = MoEDecodeLayer(synth.TINY, tiny, 8, sched="flat")
+    assert mod.info(_lib.MOE_INFO_FLAT_ROWS) >> (m - 1) & 1
+    xd = x.cuda()
+    first = mod.run(xd, xd).clone()
+    for _ in range(30):
+        assert torch.equal(mod.run(xd, xd), first)
+    buf = xd.clone()
+    mod.run(buf, buf, buf)
+    assert mod.status() == _lib.MOE_OK
+    assert torch.equal(buf, first)
+    ref, _, _ = helpers.oracle_layer(synth.TINY, tiny, x, x)
+    helpers.assert_close(first.cpu(), ref)
 
 
 def test_repeated_runs_and_inplace(tiny):
@@ -176,7 +200,7 @@ def test_shapes(cfg, m):
     layer = synth.make_layer(shape, seed=3, device="cuda")
     margin = 0.05 if cfg["top_k"] < cfg["num_experts"] else 0.0
     x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=21, rho=0.5, margin=margin)
-    outs = []
+    outs = {}
     for sched in SCHEDS:
         _, out, idx, w = _run(shape, layer, x, sched=sched, max_rows=8)
         if cfg["top_k"] < cfg["num_experts"]:
@@ -184,9 +208,9 @@ def test_shapes(cfg, m):
         else:
             ref, _, _ = helpers.oracle_layer(shape, layer, x, x)
             helpers.assert_close(out, ref)
-        outs.append(out)
-    for o in outs[1:]:
-        assert torch.equal(outs[0], o)
+        outs[sched] = out
+    for s in SAME_ORDER[1:]:
+        assert torch.equal(outs[SAME_ORDER[0]], outs[s]), s
 
 
 # ----------------------------------------------------------------------------- Ling-shaped layer
@@ -199,7 +223,7 @@ def test_ling_m1(ling, sched):
     _check(synth.LING, ling, x, out, idx, w)
 
 
-@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "pdl_chain"])
+@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "flat", "pdl_chain"])
 def test_ling_m6_correlated(ling, sched):
     x = helpers.hidden_with_margin(ling["router_w"], 6, synth.LING.top_k, seed=1, rho=0.5)
     _, out, idx, w = _run(synth.LING, ling, x, sched=sched)
@@ -216,11 +240,36 @@ def test_ling_interleave_modes(ling):
         assert MoEDecodeLayer(synth.LING, ling, m).info(_lib.MOE_OPT_INTERLEAVE) == 1
         assert MoEDecodeLayer(synth.LING, ling, m, sched="interleaved").info(_lib.MOE_OPT_INTERLEAVE) == 2
         assert MoEDecodeLayer(synth.LING, ling, m, sched="phased").info(_lib.MOE_OPT_INTERLEAVE) == 0
-    assert MoEDecodeLayer(synth.LING, ling, 6).info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0b1
+    dflt = MoEDecodeLayer(synth.LING, ling, 6)
+    flat_rows = dflt.info(_lib.MOE_INFO_FLAT_ROWS)
+    assert dflt.info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0b1 & ~flat_rows
     assert MoEDecodeLayer(synth.LING, ling, 6, sched="interleaved").info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0b111111
+    assert MoEDecodeLayer(synth.LING, ling, 6, sched="interleaved").info(_lib.MOE_INFO_FLAT_ROWS) == 0
     assert MoEDecodeLayer(synth.LING, ling, 6, sched="phased").info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0
+    assert MoEDecodeLayer(synth.LING, ling, 6, sched="phased").info(_lib.MOE_INFO_FLAT_ROWS) == 0
+    fl = MoEDecodeLayer(synth.LING, ling, 6, sched="flat")
+    assert fl.info(_lib.MOE_INFO_FLAT_ROWS) == 0b111111 and fl.info(_lib.MOE_INFO_INTERLEAVED_ROWS) == 0
+    assert fl.info(_lib.MOE_OPT_FLAT) == 2
     assert MoEDecodeLayer(synth.LING, ling, 1).info(_lib.MOE_INFO_THREADS) == 480
     assert MoEDecodeLayer(synth.LING, ling, 1, sched="phased").info(_lib.MOE_INFO_THREADS) == 416
+
+
+@pytest.mark.parametrize("m", [1, 6])
+def test_ling_flat_inplace_repeat(ling, m):
+    """The expert-range kernel at full Ling size, in place (x, residual and output
+    one buffer), run twice on fresh copies: identical bits, within the oracle's
+    tolerance."""
+    x = helpers.hidden_with_margin(ling["router_w"], m, synth.LING.top_k, seed=70 + m, rho=0.5)
+    mod = MoEDecodeLayer(synth.LING, ling, m, sched="flat")
+    outs = []
+    for _ in range(2):
+        buf = x.cuda()
+        mod.run(buf, buf, buf)
+        assert mod.status() == _lib.MOE_OK
+        outs.append(buf.cpu())
+    assert torch.equal(outs[0], outs[1])
+    ref, _, _ = helpers.oracle_layer(synth.LING, ling, x, x)
+    helpers.assert_close(outs[0], ref)
 
 
 def test_ling_moe_part_alone(ling):
@@ -240,7 +289,7 @@ def test_small_ring_wraps(tiny, slots, sched):
     _, ref_out, _, _ = _run(synth.TINY, tiny, x, sched=sched, max_rows=8)
     mod = MoEDecodeLayer(synth.TINY, tiny, 8, sched=sched)
     mod.set_option(_lib.MOE_OPT_RING_SLOTS, slots)
-    assert mod.info(_lib.MOE_OPT_RING_SLOTS) == slots
+    assert mod.info(_lib.MOE_OPT_RING_SLOTS) == (max(slots, 3) if sched == "flat" else slots)
     xd = x.cuda()
     for _ in range(3):
         out = mod.run(xd, xd)

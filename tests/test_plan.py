@@ -90,6 +90,38 @@ def test_planned_layouts_fit(sms, optin):
     assert n_checked > 500 and n_ilv > 100 and n_unfit < n_checked // 10
 
 
+@pytest.mark.parametrize("sms,optin", [(152, 232448), (132, 232448), (152, 166912)])
+def test_planned_flat_layouts_fit(sms, optin):
+    """The expert-range kernel's layout: bf16 weights, at most one shared expert,
+    no more routed slots than CTAs, I <= 1024; then it fits shared memory, every
+    stage fits a ring slot and the slot counters stay inside the control words."""
+    lib = _lib.load()
+    n_flat = 0
+    for fp4, h, i, e, k, s, m in _sweep():
+        cfg = _cfg(h, i, e, k, s, m, fp4)
+        if lib.moe_decode_config_check(ctypes.byref(cfg)) != _lib.MOE_OK:
+            continue
+        st, p = _plan(lib, cfg, sms, optin, 2)
+        what = f"H={h} I={i} E={e} k={k} S={s} M={m} fp4={fp4} sms={sms}"
+        covered = not fp4 and s <= 1 and min(e, m * k) <= sms and i <= 1024
+        if st != _lib.MOE_OK:
+            assert st == _lib.MOE_ERR_UNSUPPORTED, what
+            # on a GB300's shared memory only the kernel's coverage, a base layout that
+            # does not fit either, or three large h buffers (M x I >= 6144) rule it out
+            base, _ = _plan(lib, cfg, sms, optin, 0)
+            assert base != _lib.MOE_OK or not covered or optin < 232448 or m * i >= 6144, what
+            continue
+        assert covered, what
+        n_flat += 1
+        assert p.smem_bytes <= optin and p.slot_bytes % 128 == 0, what
+        assert 3 <= p.ring_slots <= K_MAX_SLOTS, what
+        assert 1 <= p.pairs_per_stage <= K_NC and p.pairs_per_stage * 4 * h <= p.slot_bytes, what
+        assert p.router_pairs_per_stage * 4 * h <= p.slot_bytes, what
+        assert p.down_rows_per_stage >= 1 and p.down_rows_per_stage * 2 * i <= p.slot_bytes, what
+        assert p.slots_max <= K_SLOT_COUNTERS and p.threads == 480 and p.lag == 0, what
+    assert n_flat > 200
+
+
 def test_plan_of_the_benchmarked_layers():
     """The Ling-shaped layer on 152 SMs: both single-kernel layouts fit, with the
     numbers the kernels were measured with."""
@@ -103,6 +135,11 @@ def test_plan_of_the_benchmarked_layers():
         assert st == _lib.MOE_OK and q.lag == 5 and q.down_rows_per_stage == 17
     st, p = _plan(lib, _cfg(2560, 768, 512, 8, 1, 1, False), 152, 232448, 0)
     assert p.ring_slots == 6 and p.h_pairs == 9 and p.h_buffers == 1
+    # the expert-range kernel: 30 KB stages of 3 gate/up pairs or 20 down rows
+    for m, slots in ((1, 6), (6, 4)):
+        st, f = _plan(lib, _cfg(2560, 768, 512, 8, 1, m, False), 152, 232448, 2)
+        assert st == _lib.MOE_OK and f.slot_bytes == 30720 and f.pairs_per_stage == 3
+        assert f.down_rows_per_stage == 20 and f.ring_slots == slots, (m, f.ring_slots)
 
 
 def test_plan_rejects_bad_arguments():
@@ -110,7 +147,7 @@ def test_plan_rejects_bad_arguments():
     cfg = _cfg(2560, 768, 512, 8, 1, 1, False)
     info = _lib.PlanInfo()
     assert lib.moe_decode_plan(ctypes.byref(cfg), 0, 232448, 0, ctypes.byref(info)) == _lib.MOE_ERR_INVALID_ARG
-    assert lib.moe_decode_plan(ctypes.byref(cfg), 152, 232448, 2, ctypes.byref(info)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_plan(ctypes.byref(cfg), 152, 232448, 3, ctypes.byref(info)) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_decode_plan(ctypes.byref(cfg), 152, 232448, 0, None) == _lib.MOE_ERR_INVALID_ARG
     bad = _cfg(2560, 776, 512, 8, 1, 1, False)  # 97 threads per down group
     assert lib.moe_decode_plan(ctypes.byref(bad), 152, 232448, 0, ctypes.byref(info)) == _lib.MOE_ERR_UNSUPPORTED
