@@ -6,7 +6,8 @@
  *   1. router GEMV      l[m,e] = sum_h x[m,h] Wr[e,h]          (bf16 in, fp32 acc)
  *   2. top-k select     the k largest l[m,:], ties to the lower expert id, with
  *                       renormalised weights w_j = exp(l_j - l_max) / sum_sel exp(.)
- *                       (= softmax over all experts -> top-k -> renormalise)
+ *                       (= softmax over all experts -> top-k -> renormalise); or
+ *                       the bias-corrected sigmoid rule (see moe_score)
  *   3. routed experts   h = silu(Wg_e x) * (Wu_e x),  y_e = Wd_e h   (fp32)
  *   4. shared experts   the same SwiGLU MLP with the shared weights, weight 1
  *   5. combine          out = bf16_rne(r + routed_scale * sum_j w_j y_{e_j} + sum_s y_s)
@@ -22,7 +23,8 @@
  * experts, NVFP4 expert weights); "SGLang Low-Latency Mode: kernels and
  * runtime", section "Low-Latency-Specific Optimizations" item 3 (at most eight
  * rows: expert row sets placed by bitmap and population count). The pages do not
- * fix the scoring rule; softmax -> top-k -> renormalise is the one implemented.
+ * fix the scoring rule; softmax -> top-k -> renormalise is the default, and a
+ * bias-corrected sigmoid rule is the second (moe_score).
  *
  * Threading: a handle may be used from one host thread at a time. Runs on one
  * handle must not overlap on the GPU (they share the handle's scratch); issue
@@ -38,7 +40,7 @@
 extern "C" {
 #endif
 
-#define MOE_DECODE_ABI_VERSION 1
+#define MOE_DECODE_ABI_VERSION 2
 
 /* A cudaStream_t. NULL means the legacy default stream. */
 typedef struct CUstream_st* moe_stream_t;
@@ -57,8 +59,18 @@ typedef enum moe_wdtype {
   MOE_W_NVFP4 = 1  /* expert weights e2m1 codes + e4m3 block-16 scales + fp32 */
 } moe_wdtype;
 
+/*
+ * Router scoring rules. The pages do not fix one: the Ling blog's router top-k
+ * "prefetches its bias" (section "PDL: stacking the latency floors of small
+ * kernels"), which points at a bias-corrected router; softmax -> top-k ->
+ * renormalise is the default reading.
+ */
 typedef enum moe_score {
-  MOE_SCORE_SOFTMAX_TOPK_RENORM = 0 /* softmax over E -> top-k -> renormalise */
+  MOE_SCORE_SOFTMAX_TOPK_RENORM = 0, /* softmax over E -> top-k -> renormalise:
+                                        w_j = exp(l_j - l_max) / sum_sel exp(l_i - l_max) */
+  MOE_SCORE_SIGMOID_BIAS = 1         /* s_e = sigmoid(l_e); the k largest s_e + bias_e are
+                                        selected (ties to the lower id); w_j = s_j / sum_sel s_i.
+                                        The bias steers the choice only.                   */
 } moe_score;
 
 typedef enum moe_sched {
@@ -104,7 +116,9 @@ typedef struct moe_decode_config {
  *           w13_gscale fp32 [E, 2]     tensor scale of the gate rows, of the up rows
  *           w2      uint8 [E, H, I/2], w2_scale uint8 [E, H, I/16], w2_gscale fp32 [E]
  *   sh_*            the same for the S shared experts (leading dim S)
- * Unused pointers (scales for bf16, shared for S = 0) may be NULL.
+ *   router_bias     fp32  [E] selection bias, 4-byte aligned (MOE_SCORE_SIGMOID_BIAS)
+ * Unused pointers (scales for bf16, shared for S = 0, the bias under softmax
+ * scoring) may be NULL.
  */
 typedef struct moe_decode_weights {
   const void* router_w;
@@ -120,6 +134,7 @@ typedef struct moe_decode_weights {
   const void* sh_w2_scale;
   const float* sh_w13_gscale;
   const float* sh_w2_gscale;
+  const float* router_bias;
 } moe_decode_weights;
 
 typedef struct moe_decode_handle moe_decode_handle;

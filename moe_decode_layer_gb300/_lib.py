@@ -22,6 +22,7 @@ MOE_ERR_OOM = 5
 MOE_W_BF16 = 0
 MOE_W_NVFP4 = 1
 MOE_SCORE_SOFTMAX_TOPK_RENORM = 0
+MOE_SCORE_SIGMOID_BIAS = 1
 MOE_SCHED_PERSISTENT = 0
 MOE_SCHED_PDL_CHAIN = 1
 MOE_SCHED_CHAIN = 2
@@ -71,7 +72,7 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router_w", "w13", "w2", "w13_scale", "w2_scale", "w13_gscale", "w2_gscale",
-        "sh_w13", "sh_w2", "sh_w13_scale", "sh_w2_scale", "sh_w13_gscale", "sh_w2_gscale")]
+        "sh_w13", "sh_w2", "sh_w13_scale", "sh_w2_scale", "sh_w13_gscale", "sh_w2_gscale", "router_bias")]
 
 
 class PlanInfo(ctypes.Structure):

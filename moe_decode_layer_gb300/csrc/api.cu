@@ -52,7 +52,7 @@ moe_status check_config(const moe_decode_config* c) {
   const int H = c->hidden, I = c->inter, E = c->num_experts, K = c->top_k;
   if (H <= 0 || I <= 0 || E <= 0 || K <= 0 || c->num_shared < 0 || c->max_rows <= 0)
     return MOE_ERR_INVALID_ARG;
-  if (c->score != MOE_SCORE_SOFTMAX_TOPK_RENORM) return MOE_ERR_UNSUPPORTED;
+  if (c->score != MOE_SCORE_SOFTMAX_TOPK_RENORM && c->score != MOE_SCORE_SIGMOID_BIAS) return MOE_ERR_UNSUPPORTED;
   if (c->sched < MOE_SCHED_PERSISTENT || c->sched > MOE_SCHED_CHAIN) return MOE_ERR_UNSUPPORTED;
   if (E < 2 || E > 1024 || (E & 1)) return MOE_ERR_UNSUPPORTED;
   if (K > 16 || K > E) return MOE_ERR_UNSUPPORTED;
@@ -84,6 +84,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   const int maxm = c.max_rows;
   p.H = H; p.I = I; p.E = E; p.K = K; p.S = S; p.maxm = maxm;
   p.fmt = c.wdtype == MOE_W_BF16 ? moe::FMT_BF16 : moe::FMT_NVFP4;
+  p.score = c.score == MOE_SCORE_SIGMOID_BIAS ? 1 : 0;
   p.routed_scale = c.routed_scale;
   p.rms_eps = c.rms_eps;
   p.pre_rmsnorm = c.pre_rmsnorm ? 1 : 0;
@@ -130,6 +131,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   p.off_misc = take(moe::MISC_WORDS * 4, 16);
   p.off_ucnt = take(moe::ILV_WORDS * 4, 16);
   p.off_dslot = take((size_t)p.nslot_max * 4, 4);
+  p.off_bias = p.score ? take((size_t)E * 4, 16) : 0;
   const size_t fixed = round_up(off, 128);
   const long long avail = (long long)smem_optin - 1024 - (long long)fixed;
   // ring slot: one stage of ~kStageTarget bytes, at least one router pair, one
@@ -253,7 +255,7 @@ moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params
   p.off_red = take((size_t)moe::kNC * 8 * 4, 16);
   p.off_misc = take(moe::MISC_WORDS * 4, 16);
   p.off_acnt = take((size_t)p.nslot_max * 4, 4);
-  p.off_fin = take((size_t)(1 + p.nslot_max) * 4, 4);
+  p.off_bias = p.score ? take((size_t)E * 4, 16) : 0;
   const size_t fixed = round_up(off, 128);
   // h buffers; the routing scratch overlaps them (routing is over before any h lands)
   p.off_hs = (int)fixed;
@@ -284,6 +286,9 @@ moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params
   p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
   p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
   p.d_rows_stage = p.slot_bytes / p.row2;
+  // the final combine stages its block's (slot, row, output) values in the ring
+  p.flat_rb = ((H + p.grid - 1) / p.grid + 1) / 2 * 2;
+  if ((long long)p.nslots * p.slot_bytes / 4 < (long long)p.nslot_max * maxm * p.flat_rb) return MOE_ERR_UNSUPPORTED;
   p.nslots_x = p.nslots_d = p.hs_pairs = p.hs_perslot = 0;
   p.hs_nbuf = 1;
   p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
@@ -298,6 +303,8 @@ moe_status check_weights(const moe_decode_config& c, const moe_decode_weights* w
   if (!w) return MOE_ERR_INVALID_ARG;
   auto need = [](const void* q) { return q != nullptr && aligned16(q); };
   if (!need(w->router_w) || !need(w->w13) || !need(w->w2)) return MOE_ERR_INVALID_ARG;
+  if (c.score == MOE_SCORE_SIGMOID_BIAS && (!w->router_bias || (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)))
+    return MOE_ERR_INVALID_ARG;
   const bool fp4 = c.wdtype == MOE_W_NVFP4;
   if (fp4 && (!need(w->w13_scale) || !need(w->w2_scale) || !w->w13_gscale || !w->w2_gscale))
     return MOE_ERR_INVALID_ARG;
@@ -318,6 +325,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // Weight and scratch pointers of `from` into `to` (two layouts of one handle).
 void bind_pointers(const Params& from, Params& to) {
   to.router_w = from.router_w;
+  to.router_bias = from.router_bias;
   to.w13 = from.w13;
   to.w13_s = from.w13_s;
   to.w13_gs = from.w13_gs;
@@ -403,6 +411,7 @@ moe_status plan_host(const moe_decode_config& cfg, int sms, int smem_optin, Para
 }
 void bind_weights_host(const moe_decode_weights& w, Params& p) {
   p.router_w = static_cast<const uint8_t*>(w.router_w);
+  p.router_bias = w.router_bias;
   p.w13 = static_cast<const uint8_t*>(w.w13);
   p.w2 = static_cast<const uint8_t*>(w.w2);
   p.w13_s = static_cast<const uint8_t*>(w.w13_scale);
@@ -526,10 +535,9 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   const size_t o_h = take((size_t)moe::kHRep * p.npair_max * I * 4);
   const size_t o_xf = take((size_t)p.grid * 8);
 
+  // expert-range kernel: tagged per-(block, slot, row) outputs
+  const size_t o_y = has_flat ? take((size_t)p.grid * p.nslot_max * maxm * pf.flat_rb * 8) : 0;
   const size_t tag_end = off;
-  // expert-range kernel: per-slot outputs and per-block counts (zeroed)
-  const size_t o_y = has_flat ? take((size_t)p.nslot_max * maxm * H * 4) : 0;
-  const size_t o_bc = has_flat ? take((size_t)p.grid * 4) : 0;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
   const size_t o_so = take(maxm * H * 2);
@@ -552,7 +560,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   uint8_t* base = static_cast<uint8_t*>(h->scratch);
   if (cudaMemset(base, 0, o_logits) != cudaSuccess ||
       cudaMemset(base + o_logits, 0xff, tag_end - o_logits) != cudaSuccess ||
-      (has_flat && cudaMemset(base + o_bc, 0, (size_t)p.grid * 4) != cudaSuccess) ||
+
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFreeHost(h->host_status);
     cudaFree(h->scratch);
@@ -564,6 +572,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->sched = cfg->sched;
   h->scratch_bytes = off;
   p.router_w = static_cast<const uint8_t*>(w->router_w);
+  p.router_bias = w->router_bias;
   p.w13 = static_cast<const uint8_t*>(w->w13);
   p.w2 = static_cast<const uint8_t*>(w->w2);
   p.w13_s = static_cast<const uint8_t*>(w->w13_scale);
@@ -593,8 +602,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->max_slots_flat = has_flat ? pf.nslots : 0;
   if (has_flat) {
     bind_pointers(p, pf);
-    pf.ybuf = reinterpret_cast<float*>(base + o_y);
-    pf.blkcnt = reinterpret_cast<uint32_t*>(base + o_bc);
+    pf.ybuf = reinterpret_cast<unsigned long long*>(base + o_y);
     h->flat = pf;
   }
   if (has_ilv) {

@@ -20,11 +20,13 @@
 // while the h of their slot is still on its way.
 //
 // The combine (Ling-3.0-flash batch-1 decode blog, section "PDL: stacking the
-// latency floors of small kernels": one fp32 sum, one final cast): every stage
-// stores its rows' fp32 results per (slot, row) in global memory; after its last
-// stage a CTA counts each of its output blocks once, and the CTA that completes
-// a block's count (all S + |U| slots stored) sums the block's slots in slot order,
-// adds the residual and writes bf16. No CTA waits for another at the end.
+// latency floors of small kernels": one fp32 sum, one final cast): every down
+// stage stores its rows' fp32 results per (output block, slot, token row) in
+// global memory as run-tagged 64-bit words (run tag << 32 | value: the data is
+// its own readiness flag, no fence -- "Muse Spark Open Ultrafast", section
+// "Megakernel internals"); CTA b owns output block b and, after its own down
+// stages, polls the block's words of every slot until all carry this run's tag,
+// sums them in slot order, adds the residual and writes bf16 once.
 //
 // Code size matters here: the kernel runs once per layer step, so every
 // instruction it executes is fetched again at each launch unless the SM's
@@ -110,16 +112,23 @@ __device__ __forceinline__ Ring flat_items(const Ctx& c, const Route& rt, int lo
   return ring;
 }
 
-// One down stage: rows [0, nr) of the stage (W2 rows of one expert) against the
-// slot's h (hs: the slot's pairs in ascending row order), fp32 sums stored to
-// yout[m * H + r] (yout = the slot's output at the stage's first row). 16 threads
-// per row, each with chunks sub, sub + 16, ... of the row; every lane of a warp
-// runs the same number of passes (rows past nr repeat the last one and are not
-// stored), so the 16-lane reductions stay converged.
+// Output block of row o (blocks split H over the grid: block b starts at
+// floor(H b / grid)).
+__device__ __forceinline__ int flat_block(const Params& p, int o) {
+  return (int)(((unsigned)(o + 1) * (unsigned)p.grid - 1u) / (unsigned)p.H);
+}
+
+// One down stage: rows [0, nr) of the stage (W2 rows o = R0 + r of one expert)
+// against the slot's h (hs: the slot's pairs in ascending row order); the fp32
+// sums are stored tagged to the owner block's words (rows that did not choose
+// the expert store a tagged zero, so the owner finds every word of the run).
+// 16 threads per row, each with chunks sub, sub + 16, ... of the row; every lane
+// of a warp runs the same number of passes (rows past nr repeat the last one and
+// are not stored), so the 16-lane reductions stay converged.
 template <int MAXM>
 __device__ __forceinline__ void flat_down_stage(const Params& p, const uint8_t* st, int nr, const float* hs,
-                                                uint32_t mask, const float (&hr)[kDChunk][8], float* yout,
-                                                int tid) {
+                                                uint32_t mask, const float (&hr)[kDChunk][8], int sl, int R0,
+                                                uint32_t ep, int tid) {
   const int sub = tid & (kDRowLanes - 1);
   const int nch = p.nchunk_i;
 #pragma unroll 1
@@ -156,9 +165,11 @@ __device__ __forceinline__ void flat_down_stage(const Params& p, const uint8_t* 
 #pragma unroll
       for (int o = kDRowLanes / 2; o; o >>= 1) acc[m] += __shfl_xor_sync(kFull, acc[m], o);
     if (sub == 0 && r < nr) {
+      const int o = R0 + r, b = flat_block(p, o);
+      unsigned long long* y = p.ybuf + ((size_t)b * p.nslot_max + sl) * p.maxm * p.flat_rb + (o - flat_row(p, b));
 #pragma unroll
       for (int m = 0; m < MAXM; ++m)
-        if (mask >> m & 1u) yout[(size_t)m * p.H + r] = acc[m];
+        if (m < p.M) st_tagged(y + (size_t)m * p.flat_rb, ep, (mask >> m & 1u) ? acc[m] : 0.0f);
     }
   }
 }
@@ -191,13 +202,12 @@ __device__ __forceinline__ Ring flat_down(const Ctx& c, const Route& rt, const F
     }
     if (k == 0 && c.tid == 0) c.stamp(ST_D_FIRST);
     const int R1 = flat_row(p, sg.b1[k]);
-    float* yslot = p.ybuf + (size_t)sl * p.maxm * p.H;
 #pragma unroll 1
     for (int r0 = flat_row(p, sg.b0[k]); r0 < R1; r0 += drs, ring.next(p.nslots)) {
       const int nr = min(drs, R1 - r0);
       const bool got = !c.aborted() && c.wait_full(ring);
       if (got && have)
-        flat_down_stage<MAXM>(p, c.slot_ptr(ring.slot), nr, hs, mask, hr, yslot + r0, c.tid);
+        flat_down_stage<MAXM>(p, c.slot_ptr(ring.slot), nr, hs, mask, hr, sl, r0, c.epoch(), c.tid);
       __syncwarp();
       if (got && c.lane == 0) c.release(ring, 1);
     }
@@ -205,50 +215,70 @@ __device__ __forceinline__ Ring flat_down(const Ctx& c, const Route& rt, const F
   return ring;
 }
 
-// After the last down stage: count this CTA's slots of each output block it
-// stored; the CTA completing a block's count sums the block (slot order), adds
-// the residual and writes bf16 with one rounding.
+// After its own down stages, CTA b finishes output block b: it polls the block's
+// tagged words of every slot (bounded) until all carry this run's tag, then sums
+// each output row over the slots in slot order, adds the residual and writes
+// bf16 with one rounding.
 template <int MAXM>
-__device__ __forceinline__ void flat_finish(const Ctx& c, const Route& rt, const FlatSegs& sg, int nsl) {
+__device__ __forceinline__ void flat_finish(const Ctx& c, int nsl) {
   const Params& p = c.p;
-  int* fin = reinterpret_cast<int*>(c.sm + p.off_fin);
-  if (c.tid == 0) fin[0] = 0;
-  bar_sync(kBarConsumers, kNC * 32);  // every ybuf store of this CTA is done; fin[0] is clear
-  // one thread per (segment, block): release this CTA's stores with the count
-  int t = c.tid;
-  for (int k = 0; k < sg.n; ++k) {
-    const int nb = sg.b1[k] - sg.b0[k];
-    if (t >= 0 && t < nb && !c.aborted()) {
-      const int b = sg.b0[k] + t;
-      __threadfence();
-      const uint32_t prev = atomicAdd(p.blkcnt + b, 1u);
-      if (prev == (uint32_t)nsl - 1u) {
-        __threadfence();  // acquire the other CTAs' stores of this block
-        p.blkcnt[b] = 0u;  // this run's last use of the count
-        fin[1 + atomicAdd(fin, 1)] = b;
+  const int b = blockIdx.x, o0 = flat_row(p, b), nr = flat_row(p, b + 1) - o0;
+  if (nr == 0) return;
+  float* stg = reinterpret_cast<float*>(c.sm + p.off_ring);  // the ring is idle now: [slot][row m][nr]
+  const uint32_t ep = c.epoch();
+  const unsigned long long* yb = p.ybuf + (size_t)b * p.nslot_max * p.maxm * p.flat_rb;
+  const int n = nsl * p.M * nr;
+  const int nthr = kNC * 32;
+  uint32_t spins = 0;
+  bool ok = !c.aborted();
+  for (int base = c.tid; ok && base < n; base += nthr * kStageBatch) {
+    uint32_t pending = 0;
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k)
+      if (base + k * nthr < n) pending |= 1u << k;
+    while (pending) {
+      unsigned long long v[kStageBatch];
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        v[k] = 0;
+        const int i = base + k * nthr;
+        if (pending >> k & 1u) {
+          const int sl = i / (p.M * nr), m = (i / nr) % p.M, j = i % nr;
+          v[k] = ld_relaxed_u64(yb + ((size_t)sl * p.maxm + m) * p.flat_rb + j);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        if ((pending >> k & 1u) && (uint32_t)(v[k] >> 32) == ep) {
+          stg[base + k * nthr] = __uint_as_float((uint32_t)v[k]);
+          pending &= ~(1u << k);
+        }
+      }
+      if (!pending) break;
+      __nanosleep(32);
+      if ((++spins & 15) == 0) {
+        if (c.aborted() || c.peer_failed()) {
+          ok = false;
+          break;
+        }
+        if (c.expired()) {
+          c.fail(SITE_HIDDEN);
+          ok = false;
+          break;
+        }
       }
     }
-    t -= nb;
   }
+  if (p.out_aliases_x && ok) wait_xflags(c);
   bar_sync(kBarConsumers, kNC * 32);
-  const int nfin = fin[0];
-  if (nfin == 0) return;
-  if (p.out_aliases_x) {
-    if (!c.aborted()) wait_xflags(c);
-    bar_sync(kBarConsumers, kNC * 32);
-  }
-  for (int f = 0; f < nfin; ++f) {
-    const int b = fin[1 + f];
-    const int o0 = flat_row(p, b), nr = flat_row(p, b + 1) - o0;
-    for (int i = c.tid; i < nr * p.M; i += kNC * 32) {
-      const int m = i / nr, o = o0 + i % nr;
-      float y = 0.0f;
-      const float* src = p.ybuf + (size_t)m * p.H + o;
-      for (int sl = 0; sl < nsl; ++sl)  // the slots row m uses (others hold no value for it)
-        if (rt.slot_mask[sl] >> m & 1u) y += __ldcg(src + (size_t)sl * p.maxm * p.H);
-      const float rv = __uint_as_float((uint32_t)p.resid[(size_t)m * p.H + o] << 16);
-      p.out[(size_t)m * p.H + o] = f32_to_bf16_bits(rv + y);
-    }
+  if (c.aborted()) return;
+  for (int i = c.tid; i < p.M * nr; i += nthr) {
+    const int m = i / nr, j = i % nr;
+    float y = 0.0f;
+    for (int sl = 0; sl < nsl; ++sl) y += stg[((size_t)sl * p.M + m) * nr + j];  // zeros where row m has no value
+    const size_t at = (size_t)m * p.H + o0 + j;
+    const float rv = __uint_as_float((uint32_t)p.resid[at] << 16);
+    p.out[at] = f32_to_bf16_bits(rv + y);
   }
 }
 
@@ -401,11 +431,10 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
   for (int e = c.tid; e < (p.E + 31) / 32; e += kThreadsFlat) rt.bitmap[e] = 0u;
   __syncthreads();
 
-  const int nrw = ilv_nrw(p);
   if (c.warp > kNC) {
     // ------------------------------------------------------------ hand-off warps
     __syncwarp();
-    bar_sync(kBarRoute, ilv_route_threads(p));
+    bar_sync(kBarRoute, kThreadsFlat);
     if (c.lane == 0) {
       if (c.warp == kNC + 1) {
         flat_publish(c);
@@ -424,11 +453,11 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
       c.stamp(ST_START);
       pr.x_rows();
       pr.router();
-      flat_produce_pairs(pr, rt, slo, shi, ilv_sq(p), true);
+      flat_produce_pairs(pr, rt, slo, shi, p.q, true);
       c.stamp(ST_P_R_ISSUED);
     }
     __syncwarp();
-    bar_sync(kBarRoute, ilv_route_threads(p));
+    bar_sync(kBarRoute, kThreadsFlat);
     if (c.lane == 0) {
       c.stamp(ST_P_ROUTE);
       const FlatSegs sg = flat_segs(p, c.misc[MISC_NROUTED]);
@@ -459,18 +488,15 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
       count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
-    if (c.warp < nrw) {
-      route_rows(c, rt, true, nrw * 32, kBarRouting);
-      fence_proxy_async_shared();  // the routing scratch becomes the h buffers (bulk copies)
-      bar_arrive(kBarRoute, ilv_route_threads(p));
-      if (c.tid == 0) c.stamp(ST_ROUTED);
-    }
+    // every consumer warp routes (the logits staged by all of them, each row's
+    // top-k spread over several warps); the shared expert's items follow
+    route_rows(c, rt, true, kNC * 32, kBarRouting);
+    fence_proxy_async_shared();  // the routing scratch becomes the h buffers (bulk copies)
+    bar_arrive(kBarRoute, kThreadsFlat);
+    if (c.tid == 0) c.stamp(ST_ROUTED);
     int slo, shi;
     split_range(p.S * p.I, blockIdx.x, p.grid, slo, shi);
-    // the shared expert's items: the non-routing warps compute them while routing
-    // runs; the routing warps walk the same stages (without items) afterwards
-    ring = flat_items<FMT, MAXM>(c, rt, slo, shi, 0, true, ring, nrw, kNC - nrw, ilv_sq(p));
-    bar_sync(kBarConsumers, kNC * 32);  // the routing tables, for every warp
+    ring = flat_items<FMT, MAXM>(c, rt, slo, shi, 0, true, ring, 0, kNC, p.q);
     if (c.tid == 0) c.stamp(ST_R_DONE);
     const int nrouted = c.misc[MISC_NROUTED];
     ring = flat_items<FMT, MAXM>(c, rt, c.misc[MISC_ULO], c.misc[MISC_UHI], p.S, false, ring, 0, kNC, p.q);
@@ -478,7 +504,8 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
     const FlatSegs sg = flat_segs(p, nrouted);
     ring = flat_down<MAXM>(c, rt, sg, ring);
     if (c.tid == 0) c.stamp(ST_D_SUMMED);
-    flat_finish<MAXM>(c, rt, sg, p.S + nrouted);
+    bar_sync(kBarConsumers, kNC * 32);  // every consumer is done with the ring
+    flat_finish<MAXM>(c, p.S + nrouted);
     if (c.tid == 0) {
       c.stamp(ST_D_DONE);
       if (p.stamps) {
@@ -494,8 +521,6 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
       p.ctrl[CTRL_EXIT] = 0u;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       for (int i = 0; i < p.nslot_max; ++i) p.ctrl[CTRL_SLOTCNT + i] = 0u;
-      // block counts left by a run that gave up (a completed block resets its own)
-      for (int b = 0; b < p.grid; ++b) p.blkcnt[b] = 0u;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;
       p.ctrl[CTRL_EPOCH] = e;

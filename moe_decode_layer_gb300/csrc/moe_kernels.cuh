@@ -613,14 +613,38 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
   }
 }
 
+// Power-of-two exponent k that puts a row whose largest |x| has bf16 bits
+// `maxbits` into [2^14, 2^15): x * 2^k is then inside fp16's range, and every
+// bf16 value of the row down to 2^-29 of the maximum keeps all its bits in fp16
+// (smaller ones are below the fp32 rounding of any sum the maximum enters).
+__device__ __forceinline__ int xscale_exp(uint32_t maxbits) {
+  const int e = (int)(maxbits >> 7);
+  if (maxbits == 0u) return 0;
+  if (e == 0) return 14 + 133 - (31 - __clz(maxbits & 0x7fu));  // bf16 subnormal: mantissa * 2^-133
+  return 14 - (e - 127);
+}
+
 // NVFP4 experts multiply e2m1 codes (exact in fp16) with fp16 activations:
 // once the bf16 router no longer needs them, the CTA's x rows are converted in
-// place (exact for values inside the fp16 range).
+// place, each row scaled by its power of two 2^k (xscale_exp) so that no value
+// overflows or loses bits to fp16's smaller exponent range; the gate/up sums are
+// scaled back by 2^-k, exactly.
 static __device__ __forceinline__ void x_to_f16(const Ctx& c) {
   uint32_t* xw = reinterpret_cast<uint32_t*>(c.sm + c.p.off_x);
-  for (int i = c.tid; i < c.p.M * c.p.H / 2; i += kNC * 32) {
+  uint32_t* xmax = reinterpret_cast<uint32_t*>(c.misc + MISC_XMAX);
+  const int hw = c.p.H / 2;  // words per row
+  if (c.tid < c.p.M) xmax[c.tid] = 0u;
+  bar_sync(kBarConsumers, kNC * 32);
+  for (int i = c.tid; i < c.p.M * hw; i += kNC * 32) {
     const uint32_t v = xw[i];
-    const __half2 h = __floats2half2_rn(bf16lo(v), bf16hi(v));
+    const uint32_t a = max(v & 0x7fffu, (v >> 16) & 0x7fffu);  // |x| as bits: larger bits, larger value
+    if (a) atomicMax(xmax + i / hw, a);
+  }
+  bar_sync(kBarConsumers, kNC * 32);
+  for (int i = c.tid; i < c.p.M * hw; i += kNC * 32) {
+    const uint32_t v = xw[i];
+    const int k = xscale_exp(xmax[i / hw]);
+    const __half2 h = __floats2half2_rn(ldexpf(bf16lo(v), k), ldexpf(bf16hi(v), k));
     xw[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
 }
@@ -700,6 +724,7 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
     const uint32_t mask = shared ? (1u << p.M) - 1u : rt.slot_mask[slot];
     const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane);
     float gsg = 1.0f, gsu = 1.0f, gs2 = 1.0f;
+    int xk = 0;  // NVFP4: the row's power-of-two scale of x (x_to_f16)
     if (FMT == FMT_NVFP4) {
       const int e = shared ? -1 - slot : rt.slot_e[slot];
       const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
@@ -708,7 +733,9 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
       gs2 = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];  // the down weights' tensor scale, applied once here
     }
     if (rs.m >= 0) {
-      float h = silu_f32(rs.g * gsg) * (rs.u * gsu);
+      if (FMT == FMT_NVFP4) xk = xscale_exp(reinterpret_cast<const uint32_t*>(c.misc + MISC_XMAX)[rs.m]);
+      float h = FMT == FMT_NVFP4 ? silu_f32(ldexpf(rs.g, -xk) * gsg) * (ldexpf(rs.u, -xk) * gsu)
+                                 : silu_f32(rs.g * gsg) * (rs.u * gsu);
       if (!shared) h *= rt.slot_w[slot * p.maxm + rs.m];
       if (FMT == FMT_NVFP4) h *= gs2;
       // pair index: a shared slot holds every row (pairs s * M + m); a routed
@@ -810,130 +837,128 @@ __device__ __forceinline__ unsigned long long pack_key(float v, int e) {
 __device__ __forceinline__ int key_expert(unsigned long long k) { return (int)(0xffffffffu - (uint32_t)k); }
 __device__ __forceinline__ float key_value(unsigned long long k) { return order_key_f32((uint32_t)(k >> 32)); }
 
-// Row m's top-k on warp m, from the logits staged in shared memory. Lane l
-// holds experts 32 i + l. The K-th largest of the 32 lane maxima (by value, with
-// multiplicity) bounds the K-th largest logit from below -- those K lane maxima
-// are K distinct logits -- so every selected expert has a logit at or above it;
-// the few candidates at or above it are ranked in parallel on exact keys (ties:
-// the lower expert id). With many exact ties the candidates can exceed kCandMax;
-// then K rounds of a warp-wide max select instead.
+__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
+  const uint32_t lo = __shfl_sync(kFull, (uint32_t)v, src), hi = __shfl_sync(kFull, (uint32_t)(v >> 32), src);
+  return ((unsigned long long)hi << 32) | lo;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+  const uint32_t hi = warp_max_u32((uint32_t)(v >> 32));
+  const uint32_t lo = warp_max_u32((uint32_t)(v >> 32) == hi ? (uint32_t)v : 0u);
+  return ((unsigned long long)hi << 32) | lo;
+}
+__device__ __forceinline__ float sigmoid_f32(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+// Row m's top-k on warp m from the logits staged in shared memory (lg[e]), with
+// every expert's selection key in registers (lane l holds experts l + 32 i,
+// PM * 32 >= E). The K-th largest of the 32 lane maxima bounds the K-th largest
+// key from below -- those K lane maxima are K distinct experts -- so every
+// selected expert's key is at or above it; the few candidates at or above it go
+// to shared memory at positions from a warp scan and a per-lane bit count, and
+// each is ranked against all of them on exact 64-bit keys (ties: the lower
+// expert id). With more than kCandMax candidates (many keys tied in value), K
+// rounds of a warp-wide maximum select instead. Each step is kept short and
+// independent: one warp's chain of dependent shuffles and shared loads is the
+// routing latency every CTA waits for.
 template <int PM>
 __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
   const Params& p = c.p;
-  float* lg = reinterpret_cast<float*>(c.sm + p.off_lg) + (size_t)m * p.E;
+  const int E = p.E, K = p.K, lane = c.lane;
+  float* lg = reinterpret_cast<float*>(c.sm + p.off_lg) + (size_t)m * E;
+  const float* bias = p.score ? reinterpret_cast<const float*>(c.sm + p.off_bias) : nullptr;
   uint32_t* lmax = reinterpret_cast<uint32_t*>(c.sm + p.off_lmax) + m * 32;
-  unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + m * kCandMax;
-  uint32_t* thr = reinterpret_cast<uint32_t*>(c.sm + p.off_thr) + m * 2;
-  const int lane = c.lane;
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + (size_t)m * kCandMax;
   uint32_t key[PM];
-  uint32_t best = 0;
 #pragma unroll
   for (int i = 0; i < PM; ++i) {
-    const int e = 32 * i + lane;
-    key[i] = e < p.E ? f32_order_key(lg[e]) : 0u;
-    best = key[i] > best ? key[i] : best;
+    const int e = lane + 32 * i;
+    float v = 0.0f;
+    if (e < E) v = bias ? sigmoid_f32(lg[e]) + bias[e] : lg[e];
+    key[i] = e < E ? f32_order_key(v) : 0u;
   }
-  lmax[lane] = best;
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < PM; ++i) mx = max(mx, key[i]);
+  lmax[lane] = mx;
   __syncwarp();
   int gt = 0, ge = 0;
   const uint4* l4 = reinterpret_cast<const uint4*>(lmax);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint4 q = l4[j];
-    gt += (q.x > best) + (q.y > best) + (q.z > best) + (q.w > best);
-    ge += (q.x >= best) + (q.y >= best) + (q.z >= best) + (q.w >= best);
+    gt += (q.x > mx) + (q.y > mx) + (q.z > mx) + (q.w > mx);
+    ge += (q.x >= mx) + (q.y >= mx) + (q.z >= mx) + (q.w >= mx);
   }
-  if (gt <= p.K - 1 && ge >= p.K) *thr = best;  // the K-th largest lane max (ties write the same value)
-  __syncwarp();
-  const uint32_t t = *thr;
-  int cnt = 0;
+  // the K-th largest lane maximum (lanes tied on it hold the same value)
+  const uint32_t bt = __ballot_sync(kFull, mx != 0u && gt <= K - 1 && ge >= K);
+  const uint32_t T = __shfl_sync(kFull, mx, __ffs(bt) - 1);
+  uint32_t fm = 0;
 #pragma unroll
-  for (int i = 0; i < PM; ++i) cnt += key[i] != 0u && key[i] >= t;
-  // candidate positions: exclusive warp scan of the lanes' counts
-  int o = cnt;
+  for (int i = 0; i < PM; ++i) fm |= (uint32_t)(key[i] != 0u && key[i] >= T) << i;
+  const int cnt = __popc(fm);
+  int incl = cnt;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(kFull, o, d);
-    if (lane >= d) o += y;
+    const int y = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += y;
   }
-  const int C = __shfl_sync(kFull, o, 31);
-  o -= cnt;
-  if (cnt) {
-#pragma unroll
-    for (int i = 0; i < PM; ++i) {
-      if (key[i] != 0u && key[i] >= t) {
-        const int e = 32 * i + lane;
-        if (o < kCandMax) cand[o] = ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)e);
-        ++o;
-      }
-    }
-  }
-  __syncwarp();
-  int* sel_e = rt.sel_e + m * p.K;
-  float* sel_v = rt.sel_w + m * p.K;  // logits first, weights after
+  const int C = __shfl_sync(kFull, incl, 31);
+  int* sel_e = rt.sel_e + m * K;
+  float* sel_w = rt.sel_w + m * K;
   if (C <= kCandMax) {
-    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
+    const int o = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < PM; ++i)
+      if (fm >> i & 1u)
+        cand[o + __popc(fm & ((1u << i) - 1u))] =
+            ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)(lane + 32 * i));
+    __syncwarp();
     for (int ci = lane; ci < C; ci += 32) {
       const unsigned long long v = cand[ci];
-      int r0 = 0, r1 = 0;
-      for (int j = 0; 2 * j < C; ++j) {
+      int r = 0;
+      const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
+#pragma unroll 4
+      for (int j = 0; j < (C + 1) / 2; ++j) {
         const ulonglong2 q = c2[j];
-        r0 += q.x > v;
-        r1 += (2 * j + 1 < C) && q.y > v;
+        r += (q.x > v) + (2 * j + 1 < C && q.y > v);
       }
-      const int rank = r0 + r1;
-      if (rank < p.K) {
-        sel_e[rank] = key_expert(v);
-        sel_v[rank] = key_value(v);
-      }
+      if (r < K) sel_e[r] = key_expert(v);
     }
   } else {
-    unsigned long long kk[PM];
-    unsigned long long lb = 0;
+    unsigned long long last = ~0ull;
+    for (int j = 0; j < K; ++j) {
+      unsigned long long b = 0;
 #pragma unroll
-    for (int i = 0; i < PM; ++i) {
-      const int e = 32 * i + lane;
-      kk[i] = key[i] ? ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)e) : 0ull;
-      lb = kk[i] > lb ? kk[i] : lb;
-    }
-    for (int j = 0; j < p.K; ++j) {
-      const uint32_t hi = (uint32_t)(lb >> 32);
-      const uint32_t ghi = warp_max_u32(hi);
-      const uint32_t lo = hi == ghi ? (uint32_t)lb : 0u;
-      const uint32_t glo = warp_max_u32(lo);  // ~e: the lowest expert id among the max
-      if (hi == ghi && (uint32_t)lb == glo) {
-        sel_e[j] = key_expert(lb);
-        sel_v[j] = key_value(lb);
-#pragma unroll
-        for (int i = 0; i < PM; ++i)
-          if (kk[i] == lb) kk[i] = 0;
-        lb = 0;
-#pragma unroll
-        for (int i = 0; i < PM; ++i) lb = kk[i] > lb ? kk[i] : lb;
+      for (int i = 0; i < PM; ++i) {
+        const unsigned long long k =
+            key[i] ? ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)(lane + 32 * i)) : 0ull;
+        if (k < last && k > b) b = k;
       }
-      __syncwarp();
+      last = warp_max_u64(b);
+      if (lane == 0) sel_e[j] = key_expert(last);
     }
   }
   __syncwarp();
-  // renormalised softmax over the selection (a butterfly sum: a fixed order)
-  const float v = lane < p.K ? sel_v[lane] : 0.0f;
-  const float v0 = __shfl_sync(kFull, v, 0);  // every lane takes part in the shuffle
-  const float ex = lane < p.K ? expf(v - v0) : 0.0f;
-  float sum = ex;
+  // weights in selection order: exp(l_j - l_0) / sum (softmax rule, l_0 the
+  // largest selected logit) or sigmoid(l_j) / sum (bias rule); a butterfly sum,
+  // one fixed order
+  const int ej = lane < K ? sel_e[lane] : 0;
+  const float lj = lane < K ? lg[ej] : 0.0f;
+  const float l0 = __shfl_sync(kFull, lj, 0);  // every lane takes part in the shuffle
+  const float num = lane < K ? (bias ? sigmoid_f32(lj) : expf(lj - l0)) : 0.0f;
+  float sum = num;
 #pragma unroll
   for (int d = 16; d; d >>= 1) sum += __shfl_xor_sync(kFull, sum, d);
-  if (lane < p.K) {
-    const float w = ex / sum;
-    const int e = sel_e[lane];
-    atomicOr(&rt.emask[e], 1u << m);
-    atomicOr(&rt.bitmap[e >> 5], 1u << (e & 31));
+  __syncwarp();  // every lane has read lg before it holds weights
+  if (lane < K) {
+    const float w = num / sum;
+    atomicOr(&rt.emask[ej], 1u << m);
+    atomicOr(&rt.bitmap[ej >> 5], 1u << (ej & 31));
     if (write_topk && blockIdx.x == 0) {
-      if (p.topk_idx) p.topk_idx[m * p.K + lane] = e;
-      if (p.topk_w) p.topk_w[m * p.K + lane] = w;
+      if (p.topk_idx) p.topk_idx[m * K + lane] = ej;
+      if (p.topk_w) p.topk_w[m * K + lane] = w;
     }
-    __syncwarp((1u << p.K) - 1u);
-    sel_v[lane] = w;
-    lg[e] = w;  // the union reads the combine weight of (row m, expert e) here
+    sel_w[lane] = w;
+    lg[ej] = w;  // the union reads the combine weight of (row m, expert e) here
   }
 }
 
@@ -1029,7 +1054,9 @@ __device__ __forceinline__ void union_one_row(const Ctx& c, const Route& rt) {
   const int e = lane < K ? rt.sel_e[lane] : 0x7fffffff;
   const float w = lane < K ? rt.sel_w[lane] : 0.0f;
   int rank = 0;
-  for (int j = 0; j < K; ++j) rank += __shfl_sync(kFull, e, j) < e;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)  // K <= 16; the bound is the same on every lane
+    if (j < K) rank += __shfl_sync(kFull, e, j) < e;
   if (lane < K) {
     const int sl = S + rank;
     rt.slot_of[e] = sl;
@@ -1062,6 +1089,12 @@ __device__ __forceinline__ void union_one_row(const Ctx& c, const Route& rt) {
 static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk,
                                                   int nthr = kNC * 32, int bar = kBarConsumers) {
   const Params& p = c.p;
+  // the selection bias (bias-corrected sigmoid rule) into shared memory while
+  // the logits are still on their way
+  if (p.score) {
+    float* bs = reinterpret_cast<float*>(c.sm + p.off_bias);
+    for (int e = c.tid; e < p.E; e += nthr) bs[e] = __ldg(p.router_bias + e);
+  }
   // every CTA's router logits stored (count), before reading any of them
   if (c.tid == 0) {
     if (!c.aborted()) wait_count(c, CTRL_RCOUNT, SITE_FLAGS);

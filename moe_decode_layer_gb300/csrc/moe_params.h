@@ -93,17 +93,21 @@ enum Stamp : int {
 };
 
 // Shared-memory words kept in the misc block.
+// MISC_XMAX + m: bf16 bits of the largest |x| of row m (NVFP4: sets the row's
+// power-of-two scale into fp16's range).
 enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_ULO = 3, MISC_UHI = 4, MISC_WTOT = 8,
-                  MISC_WORDS = 32 };
+                  MISC_XMAX = 16, MISC_WORDS = 32 };
 
 struct Params {
   // shapes
   int H, I, E, K, S, M, maxm, fmt;
+  int score;         // 0: softmax -> top-k -> renormalise; 1: sigmoid + bias selection
   float routed_scale;
   float rms_eps;
   int pre_rmsnorm;
   // weights (device, borrowed)
   const uint8_t* router_w;
+  const float* router_bias;  // [E] selection bias (score 1)
   const uint8_t* w13;
   const uint8_t* w13_s;
   const float* w13_gs;
@@ -164,15 +168,16 @@ struct Params {
                      // per counter), down stages issued, producer done
   int off_dslot;     // [nslot_max] ring slot of each slot's down stage (producer)
   int off_red, off_misc, off_ring;
+  int off_bias;      // [E] fp32 selection bias (score 1)
   int smem_bytes;  // dynamic shared memory requested (includes alignment slack)
   unsigned long long timeout_ns;
   int test_flags;
   unsigned long long* stamps;  // optional [grid][kStampSlots]
   // expert-range kernel
-  float* ybuf;         // [nslot_max][maxm][H]: each union slot's down output, per row
-  uint32_t* blkcnt;    // [grid]: slots whose output rows of block b are stored (reset by the last)
+  unsigned long long* ybuf;  // [grid][nslot_max][maxm][flat_rb] tagged: each union slot's down
+                             // output of output block b (run tag << 32 | fp32 bits)
+  int flat_rb;         // rows of the largest output block, rounded up to even
   int off_acnt;        // [nslot_max] consumer warps done with a slot's gate/up items
-  int off_fin;         // [1 + nslot_max] output blocks this CTA finishes (count, ids)
 };
 
 }  // namespace moe

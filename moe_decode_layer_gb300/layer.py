@@ -25,7 +25,9 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
 class MoEDecodeLayer:
     """One MoE layer's decode step on the current CUDA device.
 
-    ``weights`` is the dict layout of :func:`synth.make_layer` (device tensors).
+    ``weights`` is the dict layout of :func:`synth.make_layer` (device tensors);
+    ``score`` 1 selects the bias-corrected sigmoid rule, whose fp32 [E] bias is
+    ``weights["router_bias"]``.
     The tensors are borrowed: this object keeps references so they outlive the
     C handle. ``sched``: "persistent" (one kernel; the expert-range or
     slot-interleaved kernel where that measured faster), "phased" (one kernel,
@@ -35,7 +37,8 @@ class MoEDecodeLayer:
     """
 
     def __init__(self, shape: LayerShape, weights: dict, max_rows: int, sched: str = "persistent",
-                 pre_rmsnorm: bool = False, rms_eps: float = 1e-6, routed_scale: float = 1.0):
+                 pre_rmsnorm: bool = False, rms_eps: float = 1e-6, routed_scale: float = 1.0,
+                 score: int = 0):
         self.lib = _lib.load()
         self.shape = shape
         self.max_rows = max_rows
@@ -43,13 +46,14 @@ class MoEDecodeLayer:
         cfg = _lib.Config(hidden=shape.hidden, inter=shape.inter, num_experts=shape.num_experts,
                           top_k=shape.top_k, num_shared=shape.num_shared, max_rows=max_rows,
                           wdtype=_lib.MOE_W_BF16 if shape.wdtype == "bf16" else _lib.MOE_W_NVFP4,
-                          score=_lib.MOE_SCORE_SOFTMAX_TOPK_RENORM, routed_scale=routed_scale,
+                          score=score, routed_scale=routed_scale,
                           pre_rmsnorm=int(pre_rmsnorm), rms_eps=rms_eps,
                           sched=_lib.SCHED_NAMES["persistent" if sched in ("phased", "interleaved", "flat")
                                                   else sched])
         w = _lib.Weights()
         g = weights.get
         w.router_w = _ptr(g("router_w"))
+        w.router_bias = _ptr(g("router_bias"))
         if shape.wdtype == "bf16":
             w.w13, w.w2 = _ptr(g("w13")), _ptr(g("w2"))
             if shape.num_shared:

@@ -199,6 +199,13 @@ def _nvfp4_experts(n, inter, hidden, seed, device, std):
     return w13q, w13s, w13g, w2q, w2s, w2g
 
 
+def router_bias(num_experts: int, seed: int, device="cpu", std: float = 0.05) -> torch.Tensor:
+    """fp32 [E] selection bias for the bias-corrected sigmoid rule, ~N(0, std^2)
+    (of the order of the gaps between the top sigmoid scores, so the bias changes
+    which experts are chosen)."""
+    return _normal((num_experts,), _gen(seed * 7919 + 11, device), device, std)
+
+
 def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) -> dict:
     """All weights of one layer as torch tensors on ``device``.
 

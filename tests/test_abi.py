@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported():
 
 def test_abi_version_and_strings():
     lib = _lib.load()
-    assert lib.moe_decode_abi_version() == 1
+    assert lib.moe_decode_abi_version() == 2
     for s in range(6):
         assert _lib.status_string(s)
     assert _lib.status_string(0) == "ok"
@@ -75,7 +75,7 @@ def test_supported_configs():
     (dict(inter=4096), _lib.MOE_ERR_UNSUPPORTED),     # more than one CTA's consumers
     (dict(wdtype=1, hidden=2176), _lib.MOE_ERR_UNSUPPORTED),  # not a multiple of 256
     (dict(wdtype=2), _lib.MOE_ERR_UNSUPPORTED),
-    (dict(score=1), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(score=2), _lib.MOE_ERR_UNSUPPORTED),
     (dict(sched=3), _lib.MOE_ERR_UNSUPPORTED),
     (dict(num_shared=5), _lib.MOE_ERR_UNSUPPORTED),
     (dict(num_shared=-1), _lib.MOE_ERR_INVALID_ARG),

@@ -144,3 +144,36 @@ def test_stack_12_layers_m6(sched):
     assert rl2 < 2e-2, f"12-layer end-to-end rel L2 {rl2:.3e}"
     del layers, mods
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("sched", ["persistent", "phased", "pdl_chain"])
+def test_nvfp4_activations_outside_fp16_range(sched):
+    """NVFP4 experts multiply fp16 activations: rows far outside fp16's range --
+    one with entries of 1e5 (fp16 tops out at 65504), one scaled by 2^-20 (fp16
+    subnormals keep only a few bits there) -- must come out as the float64 oracle
+    computes them from the exact bf16 values. The kernels scale each row by a
+    power of two into fp16's range and scale the sums back. Zero residual, so
+    the check bites on the MoE sum; tolerance per element: one bf16 rounding of
+    the output (2^-8 relative) plus the layer's 2e-2."""
+    shape = synth.LayerShape(hidden=512, inter=256, num_experts=32, top_k=4, num_shared=1, wdtype="nvfp4")
+    layer = synth.make_layer(shape, seed=13, device="cuda")
+    x = helpers.hidden_with_margin(layer["router_w"], 3, shape.top_k, seed=17)
+    xf = x.float()
+    xf[0, 0], xf[0, 7] = 1.0e5, -7.0e4
+    xf[1] = xf[1] * 2.0 ** -20  # exact in bf16; the logits' top-k gap scales with it
+    xf[2, 5] = 3.0e-7
+    x = xf.to(torch.bfloat16)
+    r = torch.zeros_like(x)
+    mod = MoEDecodeLayer(shape, layer, 3, sched=sched)
+    idx = torch.empty((3, shape.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((3, shape.top_k), dtype=torch.float32, device="cuda")
+    out = mod.run(x.cuda(), r.cuda(), None, idx, w)
+    assert mod.status() == _lib.MOE_OK
+    ref, ridx, rw = helpers.oracle_layer(shape, layer, x, r)
+    helpers.assert_routing(idx.cpu(), w.cpu(), ridx, rw)
+    got = helpers.f64(out.cpu())
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 2e-2), float((err - 2.0 ** -8 * np.abs(ref)).max())
+    for m in range(3):  # each row on its own scale
+        assert np.linalg.norm(got[m] - ref[m]) <= 5e-3 * np.linalg.norm(ref[m]), m

@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import cpp
 from moe_decode_layer_gb300 import _lib, synth
 from moe_decode_layer_gb300.layer import MoEDecodeLayer
 from tests import helpers
@@ -211,6 +212,46 @@ def test_shapes(cfg, m):
         outs[sched] = out
     for s in SAME_ORDER[1:]:
         assert torch.equal(outs[SAME_ORDER[0]], outs[s]), s
+
+
+# ----------------------------------------------------------------------------- bias-corrected sigmoid rule
+
+
+def _sigmoid_case(shape, layer, m, seed, sched, bias, routed_scale=2.5, max_rows=8):
+    lay = dict(layer, router_bias=bias)
+    x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=seed, rho=0.5, margin=1e-3,
+                                   score=1, bias=bias)
+    mod = MoEDecodeLayer(shape, lay, max(m, max_rows), sched=sched, routed_scale=routed_scale, score=1)
+    xd = x.cuda()
+    out = torch.empty_like(xd)
+    idx = torch.empty((m, shape.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((m, shape.top_k), dtype=torch.float32, device="cuda")
+    mod.run(xd, xd, out, idx, w)
+    assert mod.status() == _lib.MOE_OK
+    ref, ridx, rw = helpers.oracle_layer(shape, lay, x, x, routed_scale=routed_scale, score=1, bias=bias)
+    helpers.assert_routing(idx.cpu(), w.cpu(), ridx, rw, by_weight=False)
+    helpers.assert_close(out.cpu(), ref)
+    return x, ridx
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("m", [1, 5])
+def test_tiny_sigmoid_bias(tiny, sched, m):
+    """Selection by sigmoid(logit) + bias, weights sigmoid(logit) / sum, routed
+    scale 2.5; the bias is large enough that it changes some row's choice."""
+    bias = synth.router_bias(synth.TINY.num_experts, seed=3, device="cuda", std=0.2)
+    x, ridx = _sigmoid_case(synth.TINY, tiny, m, 90 + m, sched, bias)
+    if m == 5:
+        plain = cpp.route(helpers.f64(x), helpers.bits(tiny["router_w"]), synth.TINY.top_k, 1,
+                          np.zeros(synth.TINY.num_experts))[1]
+        assert any(sorted(a) != sorted(b) for a, b in zip(plain.tolist(), ridx.tolist()))
+
+
+@pytest.mark.parametrize("sched", ["persistent", "flat", "pdl_chain"])
+@pytest.mark.parametrize("m", [1, 6])
+def test_ling_sigmoid_bias(ling, sched, m):
+    bias = synth.router_bias(synth.LING.num_experts, seed=5, device="cuda")
+    _sigmoid_case(synth.LING, ling, m, 120 + m, sched, bias, max_rows=m)
 
 
 # ----------------------------------------------------------------------------- Ling-shaped layer
