@@ -180,8 +180,9 @@ __device__ __forceinline__ Ring flat_down(const Ctx& c, const Route& rt, const F
   const Params& p = c.p;
   const uint32_t hbar0 = smem_u32(c.sm + p.off_hbar);
   const int drs = p.d_rows_stage;
-#pragma unroll 1
-  for (int k = 0; k < sg.n; ++k) {
+#pragma unroll
+  for (int k = 0; k < kFlatSegs; ++k) {  // unrolled: the segment table stays in registers
+    if (k >= sg.n) break;
     const int sl = sg.sl[k];
     const uint32_t mask = rt.slot_mask[sl];
     const float* hs = reinterpret_cast<const float*>(c.sm + p.off_hs) + (size_t)k * p.maxm * p.I;
@@ -343,7 +344,9 @@ __device__ __forceinline__ void flat_fetch(const Ctx& c, const Route& rt, const 
   const float* rep = p.hbuf + (size_t)(blockIdx.x % kHRep) * p.npair_max * p.I;
   int issued = 0;
   uint32_t spins = 0;
-  for (int k = 0; k < sg.n && !c.aborted(); ++k) {
+#pragma unroll
+  for (int k = 0; k < kFlatSegs; ++k) {
+    if (k >= sg.n || c.aborted()) break;
     const int sl = sg.sl[k];
     while (ld_acquire_u32(p.ctrl + CTRL_SLOTCNT + sl) < (uint32_t)p.I) {
       __nanosleep(32);
@@ -393,7 +396,9 @@ __device__ __forceinline__ void flat_produce_pairs(Producer& pr, const Route& rt
 
 __device__ __forceinline__ void flat_produce_down(Producer& pr, const Route& rt, const FlatSegs& sg) {
   const Params& p = pr.c.p;
-  for (int k = 0; k < sg.n; ++k) {
+#pragma unroll
+  for (int k = 0; k < kFlatSegs; ++k) {
+    if (k >= sg.n) break;
     const int sl = sg.sl[k];
     const int e = sl < p.S ? -1 - sl : rt.slot_e[sl];
     const uint8_t* wt = e >= 0 ? p.w2 : p.sh_w2;

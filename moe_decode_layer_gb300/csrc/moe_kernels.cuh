@@ -138,7 +138,7 @@ struct Ctx {
   long long c0;
   int tid, warp, lane;
 
-  __device__ Ctx(const Params& pp, uint8_t* base) : p(pp), sm(base) {
+  __device__ __forceinline__ Ctx(const Params& pp, uint8_t* base) : p(pp), sm(base) {
     misc = reinterpret_cast<int*>(sm + p.off_misc);
     slot_seq = reinterpret_cast<volatile int*>(sm + p.off_slot_seq);
     full0 = smem_u32(sm + p.off_full);
@@ -150,35 +150,35 @@ struct Ctx {
     warp = tid >> 5;
     lane = tid & 31;
   }
-  __device__ bool aborted() const { return *reinterpret_cast<volatile int*>(misc + MISC_ABORT) != 0; }
-  __device__ void fail(uint32_t site) const {
+  __device__ __forceinline__ bool aborted() const { return *reinterpret_cast<volatile int*>(misc + MISC_ABORT) != 0; }
+  __device__ __forceinline__ void fail(uint32_t site) const {
     *reinterpret_cast<volatile int*>(misc + MISC_ABORT) = 1;
     atomicOr(&p.ctrl[CTRL_STATUS], DEV_ERR_TIMEOUT);
     atomicCAS(&p.ctrl[CTRL_WHERE], 0u, site);
   }
   // Stop this CTA's waits without a status of its own (another CTA set one).
-  __device__ void abort_local() const { *reinterpret_cast<volatile int*>(misc + MISC_ABORT) = 1; }
-  __device__ bool expired() const { return global_ns() - t0 > p.timeout_ns; }
+  __device__ __forceinline__ void abort_local() const { *reinterpret_cast<volatile int*>(misc + MISC_ABORT) = 1; }
+  __device__ __forceinline__ bool expired() const { return global_ns() - t0 > p.timeout_ns; }
   // Another CTA gave up: stop waiting on data it will never publish.
-  __device__ bool peer_failed() const { return ld_relaxed_u32(&p.ctrl[CTRL_STATUS]) != 0; }
-  __device__ uint32_t epoch() const { return static_cast<uint32_t>(misc[MISC_EPOCH]); }
+  __device__ __forceinline__ bool peer_failed() const { return ld_relaxed_u32(&p.ctrl[CTRL_STATUS]) != 0; }
+  __device__ __forceinline__ uint32_t epoch() const { return static_cast<uint32_t>(misc[MISC_EPOCH]); }
   // Slots past nslots: in the gate/up phase extra slots in the h area, in the
   // down phase (d) the x area.
-  __device__ uint8_t* slot_ptr(int slot, bool d = false) const {
+  __device__ __forceinline__ uint8_t* slot_ptr(int slot, bool d = false) const {
     return slot < p.nslots ? sm + p.off_ring + (size_t)slot * p.slot_bytes
            : d             ? sm + p.off_x
                            : sm + p.off_xslot + (size_t)(slot - p.nslots) * p.slot_bytes;
   }
   // Phase timestamp (one plain store; off unless the handle has a stamp buffer).
-  __device__ void stamp(int ev) const {
+  __device__ __forceinline__ void stamp(int ev) const {
     if (p.stamps) p.stamps[(size_t)blockIdx.x * kStampSlots + ev] = global_ns();
   }
-  __device__ void count(int ev, unsigned long long v) const {
+  __device__ __forceinline__ void count(int ev, unsigned long long v) const {
     if (p.stamps) atomicAdd(&p.stamps[(size_t)blockIdx.x * kStampSlots + ev], v);
   }
 
   // Bounded wait on an mbarrier phase. False on abort / timeout.
-  __device__ bool wait_bar(uint32_t bar, uint32_t par, uint32_t site) const {
+  __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t par, uint32_t site) const {
     while (!mbar_try_wait(bar, par)) {
       if (aborted()) return false;
       if (expired()) {
@@ -194,7 +194,7 @@ struct Ctx {
   // ahead of its slot; an mbarrier parity only tells adjacent phases apart. The
   // producer therefore records which stage owns a slot before arming it, and the
   // parity wait starts only once `seq` owns the slot.
-  __device__ bool wait_full(const Ring& r) const {
+  __device__ __forceinline__ bool wait_full(const Ring& r) const {
     for (uint32_t spin = 0; slot_seq[r.slot] != r.seq; ++spin) {
       __nanosleep(64);  // leave the issue slots to the warps doing arithmetic
       if ((spin & 15) == 15) {
@@ -208,10 +208,10 @@ struct Ctx {
     return wait_bar(full0 + 8u * r.slot, r.phase(), SITE_RING_FULL);
   }
   // Producer side: bounded wait for the slot of stage `r` to be free.
-  __device__ bool wait_empty(const Ring& r) const {
+  __device__ __forceinline__ bool wait_empty(const Ring& r) const {
     return wait_bar(empty0 + 8u * r.slot, r.phase() ^ 1u, SITE_RING_EMPTY);
   }
-  __device__ void release(const Ring& r, uint32_t count) const { mbar_arrive(empty0 + 8u * r.slot, count); }
+  __device__ __forceinline__ void release(const Ring& r, uint32_t count) const { mbar_arrive(empty0 + 8u * r.slot, count); }
 };
 
 // Routing tables in shared memory.
@@ -225,7 +225,7 @@ struct Route {
   uint32_t* slot_mask;  // [nslot_max] rows that use the slot
   float* slot_w;        // [nslot_max][maxm] combine weight (routed_scale folded in)
   int* pair_base;       // [nslot_max + 1] first (slot, row) pair index of each slot
-  __device__ Route(const Params& p, uint8_t* sm)
+  __device__ __forceinline__ Route(const Params& p, uint8_t* sm)
       : sel_e(reinterpret_cast<int*>(sm + p.off_sel_e)),
         sel_w(reinterpret_cast<float*>(sm + p.off_sel_w)),
         emask(reinterpret_cast<uint32_t*>(sm + p.off_emask)),
@@ -1460,7 +1460,7 @@ struct Producer {
   uint64_t pol;
   Ring ring;            // next stage to issue
   uint64_t used = 0;    // slots that received copies
-  __device__ Producer(const Ctx& cc) : c(cc) { pol = policy_evict_first(); }
+  __device__ __forceinline__ Producer(const Ctx& cc) : c(cc) { pol = policy_evict_first(); }
 
   // Claims the next stage's slot and announces its bytes. False on abort.
   bool x_free = false;  // the consumers are done with x and the h area (down-phase slot in the x area)
@@ -1471,11 +1471,11 @@ struct Producer {
   // this CTA is done with the h area, counted on the slot's own mbarrier.
   const Route* h_rt = nullptr;  // set: fetches active
   int h_next = 0, h_nsl = 0;
-  __device__ bool test_x_free() {
+  __device__ __forceinline__ bool test_x_free() {
     if (!x_free && mbar_test_wait(smem_u32(c.sm + c.p.off_xfree), 0)) x_free = true;
     return x_free;
   }
-  __device__ void poll_h() {
+  __device__ __forceinline__ void poll_h() {
     const Params& p = c.p;
     if (!h_rt || h_next >= h_nsl || !test_x_free()) return;
     const float* rep = p.hbuf + (size_t)(blockIdx.x % kHRep) * p.npair_max * p.I;
@@ -1492,7 +1492,7 @@ struct Producer {
     }
   }
   // Bounded: the remaining fetches once every down stage is issued.
-  __device__ void finish_h() {
+  __device__ __forceinline__ void finish_h() {
     uint32_t spins = 0;
     while (h_rt && h_next < h_nsl && !c.aborted()) {
       poll_h();
@@ -1508,7 +1508,7 @@ struct Producer {
     }
   }
   // After an abort: the fetches issued must land before exit.
-  __device__ void drain_h() const {
+  __device__ __forceinline__ void drain_h() const {
     const uint64_t t = global_ns();
     for (int sl = 0; sl < h_next; ++sl)
       while (!mbar_try_wait(c.full0 + 8u * (kHSlotBar + sl), 0) && global_ns() - t < c.p.timeout_ns) {
@@ -1520,7 +1520,7 @@ struct Producer {
   // stage; the hand-off warp adds the h rows (counted on the same full barrier)
   // once every CTA has counted the slot's gate/up items as stored.
   // Gate/up stages of union slot s: this CTA's block of the slot's rows.
-  __device__ void ilv_pairs(const Route& rt, int s, int q) {
+  __device__ __forceinline__ void ilv_pairs(const Route& rt, int s, int q) {
     const Params& p = c.p;
     int lo, hi;
     ilv_rows(p, s, lo, hi);
@@ -1535,7 +1535,7 @@ struct Producer {
   }
   // The down stage of union slot s: this CTA's output rows of the expert's down
   // matrix now; the hand-off warp adds the slot's h rows later.
-  __device__ void ilv_down(const Route& rt, int s) {
+  __device__ __forceinline__ void ilv_down(const Route& rt, int s) {
     const Params& p = c.p;
     int r_lo, r_hi;
     cta_rows(p, r_lo, r_hi);
@@ -1556,7 +1556,7 @@ struct Producer {
     ring.next(p.nslots);
   }
 
-  __device__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar, bool d = false) {
+  __device__ __forceinline__ bool begin(uint32_t bytes, uint32_t& dst, uint32_t& bar, bool d = false) {
     if (c.aborted()) return false;
     if (h_rt) {  // poll the h fetches while the slot is busy
       uint32_t spins = 0;
@@ -1587,14 +1587,14 @@ struct Producer {
   }
 
   // x rows straight into shared memory, ahead of any weights.
-  __device__ void x_rows() {
+  __device__ __forceinline__ void x_rows() {
     const Params& p = c.p;
     const uint32_t bytes = (uint32_t)p.M * p.H * 2;
     mbar_arrive_expect_tx(c.xbar, bytes);
     bulk_g2s(smem_u32(c.sm + p.off_x), p.x, bytes, c.xbar, pol);
   }
 
-  __device__ void router() {
+  __device__ __forceinline__ void router() {
     const Params& p = c.p;
     int lo, hi;
     split_range(p.E / 2, blockIdx.x, p.grid, lo, hi);
@@ -1617,7 +1617,7 @@ struct Producer {
 
   // Rows j .. j + nq - 1 of expert e (shared expert -1 - e when e < 0) as a
   // gate block and an up block (plus the two scale blocks for NVFP4).
-  __device__ void copy_pairs(int e, int j, int nq, uint32_t dst, uint32_t bar) const {
+  __device__ __forceinline__ void copy_pairs(int e, int j, int nq, uint32_t dst, uint32_t bar) const {
     const Params& p = c.p;
     const uint8_t* wt = e >= 0 ? p.w13 : p.sh_w13;
     const uint8_t* ws = e >= 0 ? p.w13_s : p.sh_w13_s;
@@ -1635,7 +1635,7 @@ struct Producer {
 
   // Gate/up stages: consecutive rows of one expert as a gate block and an up
   // block (plus the two scale blocks for NVFP4).
-  __device__ void pairs(bool shared_phase, const Route& rt) {
+  __device__ __forceinline__ void pairs(bool shared_phase, const Route& rt) {
     const Params& p = c.p;
     int lo, hi;
     if (shared_phase) {
@@ -1658,7 +1658,7 @@ struct Producer {
 
   // Down stages (row block rb, union slot sl) for sl in [sl_lo, sl_hi).
   // nd: down-phase slots in the x area (0 or 1)
-  __device__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi, int nd) {
+  __device__ __forceinline__ void down_block(const Route& rt, int rb, int sl_lo, int sl_hi, int nd) {
     const Params& p = c.p;
     int r_lo, r_hi;
     cta_rows(p, r_lo, r_hi);
@@ -1680,14 +1680,14 @@ struct Producer {
     }
   }
 
-  __device__ int down_blocks() const {
+  __device__ __forceinline__ int down_blocks() const {
     int r_lo, r_hi;
     cta_rows(c.p, r_lo, r_hi);
     return (r_hi - r_lo + c.p.d_rows_stage - 1) / c.p.d_rows_stage;
   }
 
   // Shared experts' down rows of this CTA into L2 ahead of time.
-  __device__ void prefetch_shared_down() {
+  __device__ __forceinline__ void prefetch_shared_down() {
     const Params& p = c.p;
     int r_lo, r_hi;
     cta_rows(p, r_lo, r_hi);
@@ -1701,7 +1701,7 @@ struct Producer {
 
   // Before exit: wait (bounded) for this CTA's copies still in flight: the
   // newest use of every slot that received copies.
-  __device__ void drain() {
+  __device__ __forceinline__ void drain() {
     const Params& p = c.p;
     const uint64_t t = global_ns();
     for (uint64_t u = used; u; u &= u - 1) {
