@@ -50,7 +50,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE decode layer-step µs and achieved HBM GB/s (% of roofline), M=1 and M=6"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_EXTRA = "tiny_m1,ling_m6,stack_m6,nvfp4_m1,nvfp4_m6"
+DEFAULT_EXTRA = "tiny_m1,ling_m6,ling_m16,stack_m6,nvfp4_m1,nvfp4_m6,ling_fp8_m1,ling_fp8_m6"
 
 from moe_decode_layer_gb300.synth import WORKLOADS  # noqa: E402
 

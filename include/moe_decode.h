@@ -1,7 +1,7 @@
 /*
  * moe_decode.h -- C ABI of the GB300 small-batch MoE decode layer step.
  *
- * One call computes, for M = 1..8 token rows, the MoE block of a decoder layer:
+ * One call computes, for M = 1..16 token rows, the MoE block of a decoder layer:
  *
  *   1. router GEMV      l[m,e] = sum_h x[m,h] Wr[e,h]          (bf16 in, fp32 acc)
  *   2. top-k select     the k largest l[m,:], ties to the lower expert id, with
@@ -55,8 +55,11 @@ typedef enum moe_status {
 } moe_status;
 
 typedef enum moe_wdtype {
-  MOE_W_BF16 = 0,  /* expert weights bf16                                     */
-  MOE_W_NVFP4 = 1  /* expert weights e2m1 codes + e4m3 block-16 scales + fp32 */
+  MOE_W_BF16 = 0,      /* expert weights bf16                                     */
+  MOE_W_NVFP4 = 1,     /* expert weights e2m1 codes + e4m3 block-16 scales + fp32 */
+  MOE_W_FP8_BLOCK = 2  /* expert weights e4m3 + one fp32 scale per 128 x 128 block
+                          (Ling-3.0-flash blog, "Where the time goes now": fp8
+                          weights halve the bytes; block 128)                     */
 } moe_wdtype;
 
 /*
@@ -83,10 +86,13 @@ typedef enum moe_sched {
  * Layer configuration. Supported (create/config_check return MOE_ERR_UNSUPPORTED
  * otherwise):
  *   2 <= num_experts <= 1024, even;  1 <= top_k <= min(16, num_experts);
- *   0 <= num_shared <= 4;  1 <= max_rows <= 8;
+ *   0 <= num_shared <= 4;  1 <= max_rows <= 16 (a run of more than 8 rows launches
+ *   row groups of at most 8, one after another: the wider verify batch of the Muse
+ *   Spark page, "Speculative decoding", checks 16 tokens per step);
  *   bf16:  hidden % 8 == 0, 64 <= hidden <= 4096; inter % 8 == 0 and inter / 8
  *          either a power of two <= 32 or a multiple of 32 no larger than 384;
  *   nvfp4: hidden % 256 == 0, 256 <= hidden <= 4096; inter % 256 == 0, inter <= 12288;
+ *   fp8:   hidden % 128 == 0, hidden <= 4096; inter % 128 == 0 and inter / 8 as for bf16;
  *   routed_scale finite; rms_eps > 0 when pre_rmsnorm.
  */
 typedef struct moe_decode_config {
@@ -115,6 +121,9 @@ typedef struct moe_decode_config {
  *           w13_scale uint8 [E, 2I, H/16] e4m3 scale per 16 consecutive elements
  *           w13_gscale fp32 [E, 2]     tensor scale of the gate rows, of the up rows
  *           w2      uint8 [E, H, I/2], w2_scale uint8 [E, H, I/16], w2_gscale fp32 [E]
+ *   fp8:    w13     uint8 [E, 2I, H]   e4m3 codes; w13_scale fp32 [E, 2I/128, H/128]
+ *           w2      uint8 [E, H, I]    e4m3 codes; w2_scale  fp32 [E, H/128, I/128]
+ *           (w = e4m3(code) * scale[row / 128][col / 128]; gscale pointers unused)
  *   sh_*            the same for the S shared experts (leading dim S)
  *   router_bias     fp32  [E] selection bias, 4-byte aligned (MOE_SCORE_SIGMOID_BIAS)
  * Unused pointers (scales for bf16, shared for S = 0, the bias under softmax

@@ -21,6 +21,8 @@ MOE_ERR_OOM = 5
 
 MOE_W_BF16 = 0
 MOE_W_NVFP4 = 1
+MOE_W_FP8_BLOCK = 2
+WDTYPE = {"bf16": MOE_W_BF16, "nvfp4": MOE_W_NVFP4, "fp8": MOE_W_FP8_BLOCK}
 MOE_SCORE_SOFTMAX_TOPK_RENORM = 0
 MOE_SCORE_SIGMOID_BIAS = 1
 MOE_SCHED_PERSISTENT = 0

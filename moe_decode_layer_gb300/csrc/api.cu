@@ -56,7 +56,7 @@ moe_status check_config(const moe_decode_config* c) {
   if (c->sched < MOE_SCHED_PERSISTENT || c->sched > MOE_SCHED_CHAIN) return MOE_ERR_UNSUPPORTED;
   if (E < 2 || E > 1024 || (E & 1)) return MOE_ERR_UNSUPPORTED;
   if (K > 16 || K > E) return MOE_ERR_UNSUPPORTED;
-  if (c->num_shared > 4 || c->max_rows > 8) return MOE_ERR_UNSUPPORTED;
+  if (c->num_shared > 4 || c->max_rows > moe::kMaxRowsRun) return MOE_ERR_UNSUPPORTED;
   if (!std::isfinite(c->routed_scale)) return MOE_ERR_INVALID_ARG;
   if (c->pre_rmsnorm && !(c->rms_eps > 0.0f && std::isfinite(c->rms_eps))) return MOE_ERR_INVALID_ARG;
   if (c->wdtype == MOE_W_BF16) {
@@ -67,6 +67,11 @@ moe_status check_config(const moe_decode_config* c) {
   } else if (c->wdtype == MOE_W_NVFP4) {
     if (H % 256 || H < 256 || H > 4096) return MOE_ERR_UNSUPPORTED;
     if (I % 256 || I / 32 > moe::kNC * 32) return MOE_ERR_UNSUPPORTED;
+  } else if (c->wdtype == MOE_W_FP8_BLOCK) {
+    // 128 x 128 scale blocks; 8-code down chunks, I / 8 threads per down row as bf16
+    if (H % moe::kFp8Block || H > 4096 || I % moe::kFp8Block) return MOE_ERR_UNSUPPORTED;
+    const int tg = I / 8;
+    if (!((tg <= 32 && pow2(tg)) || (tg % 32 == 0 && tg <= moe::kNC * 32))) return MOE_ERR_UNSUPPORTED;
   } else {
     return MOE_ERR_UNSUPPORTED;
   }
@@ -81,9 +86,10 @@ moe_status check_config(const moe_decode_config* c) {
 moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, bool ilv) {
   std::memset(&p, 0, sizeof(p));
   const int H = c.hidden, I = c.inter, E = c.num_experts, K = c.top_k, S = c.num_shared;
-  const int maxm = c.max_rows;
+  // one launch handles at most kMaxRowsLaunch rows; a run of more splits into launches
+  const int maxm = std::min(c.max_rows, moe::kMaxRowsLaunch);
   p.H = H; p.I = I; p.E = E; p.K = K; p.S = S; p.maxm = maxm;
-  p.fmt = c.wdtype == MOE_W_BF16 ? moe::FMT_BF16 : moe::FMT_NVFP4;
+  p.fmt = c.wdtype == MOE_W_BF16 ? moe::FMT_BF16 : c.wdtype == MOE_W_NVFP4 ? moe::FMT_NVFP4 : moe::FMT_FP8;
   p.score = c.score == MOE_SCORE_SIGMOID_BIAS ? 1 : 0;
   p.routed_scale = c.routed_scale;
   p.rms_eps = c.rms_eps;
@@ -91,6 +97,9 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   if (p.fmt == moe::FMT_BF16) {
     p.nchunk_h = H / 8; p.row13 = 2 * H; p.sc13 = 0;
     p.nchunk_i = I / 8; p.row2 = 2 * I; p.sc2 = 0;
+  } else if (p.fmt == moe::FMT_FP8) {  // block scales are read by the consumers, not staged
+    p.nchunk_h = H / 16; p.row13 = H; p.sc13 = 0;
+    p.nchunk_i = I / 8; p.row2 = I; p.sc2 = 0;
   } else {
     p.nchunk_h = H / 32; p.row13 = H / 2; p.sc13 = H / 16;
     p.nchunk_i = I / 32; p.row2 = I / 2; p.sc2 = I / 16;
@@ -193,7 +202,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   // routed gate/up items are split by cost: streaming the pair plus the FMA work
   // of each row that chose the expert (fitted on GB300 per-CTA phase times: an
   // extra row adds ~1/6 of a bf16 item's time and about one NVFP4 item's)
-  p.item_base = p.fmt == moe::FMT_BF16 ? 6 : 1;
+  p.item_base = p.fmt == moe::FMT_BF16 ? 6 : p.fmt == moe::FMT_FP8 ? 3 : 1;
   p.off_xslot = (int)fixed;
   // the x rows are dead once the gate/up items are done: their area holds one
   // more down-phase slot when it is large enough
@@ -296,7 +305,9 @@ moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params
 }
 
 const void* kernel_for(const Params& p, int maxm_t, int phases) {
-  return p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, phases) : moe::kernel_nvfp4(maxm_t, phases);
+  return p.fmt == moe::FMT_BF16    ? moe::kernel_bf16(maxm_t, phases)
+         : p.fmt == moe::FMT_NVFP4 ? moe::kernel_nvfp4(maxm_t, phases)
+                                   : moe::kernel_fp8(maxm_t, phases);
 }
 
 moe_status check_weights(const moe_decode_config& c, const moe_decode_weights* w) {
@@ -305,14 +316,16 @@ moe_status check_weights(const moe_decode_config& c, const moe_decode_weights* w
   if (!need(w->router_w) || !need(w->w13) || !need(w->w2)) return MOE_ERR_INVALID_ARG;
   if (c.score == MOE_SCORE_SIGMOID_BIAS && (!w->router_bias || (reinterpret_cast<uintptr_t>(w->router_bias) & 3u)))
     return MOE_ERR_INVALID_ARG;
-  const bool fp4 = c.wdtype == MOE_W_NVFP4;
+  const bool fp4 = c.wdtype == MOE_W_NVFP4, fp8 = c.wdtype == MOE_W_FP8_BLOCK;
   if (fp4 && (!need(w->w13_scale) || !need(w->w2_scale) || !w->w13_gscale || !w->w2_gscale))
     return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!need(w->w13_scale) || !need(w->w2_scale))) return MOE_ERR_INVALID_ARG;
   if (c.num_shared > 0) {
     if (!need(w->sh_w13) || !need(w->sh_w2)) return MOE_ERR_INVALID_ARG;
     if (fp4 && (!need(w->sh_w13_scale) || !need(w->sh_w2_scale) || !w->sh_w13_gscale ||
                 !w->sh_w2_gscale))
       return MOE_ERR_INVALID_ARG;
+    if (fp8 && (!need(w->sh_w13_scale) || !need(w->sh_w2_scale))) return MOE_ERR_INVALID_ARG;
   }
   return MOE_OK;
 }
@@ -487,7 +500,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
     return MOE_ERR_CUDA;
   Params p, pi;
   if ((st = plan(*cfg, sms, optin, p, false)) != MOE_OK) return st;
-  const bool has_ilv = plan(*cfg, sms, optin, pi, true) == MOE_OK;
+  const bool has_ilv = kernel_for(p, 1, moe::PH_ILV) != nullptr && plan(*cfg, sms, optin, pi, true) == MOE_OK;
   Params pf;
   bool has_flat = plan_flat(*cfg, sms, optin, pf) == MOE_OK;
   // Every kernel this handle may launch gets the shared-memory size, and one
@@ -622,16 +635,26 @@ moe_status moe_decode_run(moe_decode_handle* h, const void* x, const void* resid
   if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
     return MOE_ERR_INVALID_ARG;
-  Params p = active_params(h, m_rows);
-  p.M = m_rows;
-  p.x = static_cast<const uint16_t*>(x);
-  p.resid = static_cast<const uint16_t*>(residual);
-  p.out = static_cast<uint16_t*>(out);
-  p.topk_idx = topk_idx;
-  p.topk_w = topk_w;
-  const size_t bytes = (size_t)m_rows * p.H * 2;
-  p.out_aliases_x = overlaps(x, bytes, out, bytes) ? 1 : 0;
-  return launch(h, p, reinterpret_cast<cudaStream_t>(stream));
+  // at most kMaxRowsLaunch rows per launch: a wider verify batch (up to
+  // kMaxRowsRun rows) runs as row groups one after another on the stream, each a
+  // complete layer step of its rows (rows are independent; the groups share the
+  // handle's scratch in stream order)
+  for (int g0 = 0; g0 < m_rows; g0 += moe::kMaxRowsLaunch) {
+    const int mg = std::min(moe::kMaxRowsLaunch, m_rows - g0);
+    Params p = active_params(h, mg);
+    p.M = mg;
+    const size_t row0 = (size_t)g0 * p.H;
+    p.x = static_cast<const uint16_t*>(x) + row0;
+    p.resid = static_cast<const uint16_t*>(residual) + row0;
+    p.out = static_cast<uint16_t*>(out) + row0;
+    p.topk_idx = topk_idx ? topk_idx + (size_t)g0 * p.K : nullptr;
+    p.topk_w = topk_w ? topk_w + (size_t)g0 * p.K : nullptr;
+    const size_t bytes = (size_t)mg * p.H * 2;
+    p.out_aliases_x = overlaps(p.x, bytes, p.out, bytes) ? 1 : 0;
+    const moe_status st = launch(h, p, reinterpret_cast<cudaStream_t>(stream));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_decode_get_status(moe_decode_handle* h, moe_stream_t stream) {
@@ -734,7 +757,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_INFO_FLAT_ROWS: {
       int64_t mask = 0;
       for (int m = 1; m <= h->cfg.max_rows; ++m)
-        if (use_flat(h, m)) mask |= int64_t(1) << (m - 1);
+        if (use_flat(h, std::min(m, moe::kMaxRowsLaunch))) mask |= int64_t(1) << (m - 1);
       *value = mask;
       return MOE_OK;
     }
@@ -748,7 +771,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_INFO_INTERLEAVED_ROWS: {
       int64_t mask = 0;
       for (int m = 1; m <= h->cfg.max_rows; ++m)
-        if (interleaved(h, m)) mask |= int64_t(1) << (m - 1);
+        if (interleaved(h, std::min(m, moe::kMaxRowsLaunch))) mask |= int64_t(1) << (m - 1);
       *value = mask;
       return MOE_OK;
     }

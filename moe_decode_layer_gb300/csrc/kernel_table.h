@@ -6,6 +6,7 @@ namespace moe {
 // Kernel entry for (maxm_t in {1, 8}, phases in Phase). NULL if not instantiated.
 const void* kernel_bf16(int maxm_t, int phases);
 const void* kernel_nvfp4(int maxm_t, int phases);
+const void* kernel_fp8(int maxm_t, int phases);
 // The expert-range single kernel (bf16 weights) for maxm_t in {1, 8}.
 const void* kernel_flat(int maxm_t);
 }  // namespace moe

@@ -523,12 +523,105 @@ __device__ __forceinline__ RowSums dot_rows_fp4(const uint4* qa, const uint4* qb
   return r;
 }
 
+// One FP8 chunk: 16 e4m3 codes (16 bytes, element k in byte k) against 16
+// activations given as fp16 pairs (8 words). Every product e4m3 * fp16 is exact
+// in fp32; the sum is fp32. The caller applies the chunk's 128 x 128 block scale.
+__device__ __forceinline__ float dot16_fp8(const uint4 q, const uint32_t* xh) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  float part = 0.0f;
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const uint32_t wv = e4m3x2_to_f16x2((qw[wi] >> (16 * hb)) & 0xffffu);
+      const uint32_t xv = xh[wi * 2 + hb];
+      asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1; mov.b32 {b0, b1}, %2;\n"
+          " fma.rn.f32.f16 %0, a0, b0, %0; fma.rn.f32.f16 %0, a1, b1, %0;\n}\n"
+          : "+f"(part)
+          : "r"(wv), "r"(xv));
+    }
+  }
+  return part;
+}
+
+// First fp32 block scale of gate/up row j (j < 2I) of expert e (shared expert
+// -1 - e when e < 0): scales are [experts][2I / 128][H / 128].
+__device__ __forceinline__ const float* fp8_scale_row13(const Params& p, int e, int j) {
+  const float* base = reinterpret_cast<const float*>(e >= 0 ? p.w13_s : p.sh_w13_s);
+  const int ex = e >= 0 ? e : -1 - e;
+  const int nb = p.H / kFp8Block;
+  return base + ((size_t)ex * (2 * p.I / kFp8Block) + j / kFp8Block) * nb;
+}
+
+// FP8 rows a, b (codes qa, qb) against one x row held in the lane's registers as
+// fp16 (8 words per 16-element chunk); sg, su: the lane's block scales.
+__device__ __forceinline__ RowSums dot_one_fp8(const uint4* qa, const uint4* qb, const float* sg, const float* su,
+                                               int nch, const uint32_t* xr, int lane) {
+  RowSums r{0, 0.0f, 0.0f};
+#pragma unroll
+  for (int i = 0; i < kCplFp8; ++i) {
+    const int ch = lane + 32 * i;
+    if (ch < nch) {
+      r.g = fmaf(sg[i], dot16_fp8(qa[ch], xr + 8 * i), r.g);
+      r.u = fmaf(su[i], dot16_fp8(qb[ch], xr + 8 * i), r.u);
+    }
+  }
+  warp_sum2(r.g, r.u);
+  if (lane != 0) r.m = -1;
+  return r;
+}
+
+// FP8 rows a, b against the N fp16 x rows of `mask` in shared memory; the block
+// scales are read from the rows' scale vectors (gsr, usr) through the read-only cache.
+template <int N>
+__device__ __forceinline__ RowSums dot_rows_fp8(const uint4* qa, const uint4* qb, const float* gsr, const float* usr,
+                                                int nch, const uint4* xs, int H, uint32_t mask, int lane) {
+  int rows[N];
+  const uint4* xp[N];
+  uint32_t msk = mask;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    rows[k] = __ffs(msk) - 1;
+    msk &= msk - 1;
+    xp[k] = xs + (size_t)rows[k] * (H / 8);
+  }
+  float g[N], u[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) g[k] = u[k] = 0.0f;
+  for (int ch = lane; ch < nch; ch += 32) {
+    const uint4 va = qa[ch], vb = qb[ch];
+    const float s_a = __ldg(gsr + ch / 8), s_b = __ldg(usr + ch / 8);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const uint4 x0 = xp[k][ch * 2], x1 = xp[k][ch * 2 + 1];
+      const uint32_t xh[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      g[k] = fmaf(s_a, dot16_fp8(va, xh), g[k]);
+      u[k] = fmaf(s_b, dot16_fp8(vb, xh), u[k]);
+    }
+  }
+  RowSums r{-1, 0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    warp_sum2(g[k], u[k]);
+    if (lane == k) r = RowSums{rows[k], g[k], u[k]};
+  }
+  return r;
+}
+
+// FP8 block scales of one gate/up item: the gate and up rows' scale vectors, and
+// the lane's scales for the register path (loaded before the stage is waited for).
+struct Fp8Scales {
+  const float* g_row = nullptr;
+  const float* u_row = nullptr;
+  float gv[kCplFp8], uv[kCplFp8];
+};
+
 // The item's gate/up sums: the register path for single-row kernels, else the
 // N-row path for the item's row count.
 template <int FMT, int MAXM>
 __device__ __forceinline__ RowSums item_dot(const uint8_t* st, int iq, int nq, const Params& p,
                                             const uint4* xb, const uint32_t* xh, const uint4* xs, uint32_t mask,
-                                            int lane) {
+                                            int lane, const Fp8Scales& fs) {
   if (FMT == FMT_BF16) {
     const uint4* wa = reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13);
     const uint4* wb = reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13);
@@ -545,6 +638,25 @@ __device__ __forceinline__ RowSums item_dot(const uint8_t* st, int iq, int nq, c
         case 6: return dot_rows_bf16<6>(wa, wb, nch, xs, mask, lane);
         case 7: return dot_rows_bf16<7>(wa, wb, nch, xs, mask, lane);
         case 8: return dot_rows_bf16<8>(wa, wb, nch, xs, mask, lane);
+        default: return RowSums{-1, 0.0f, 0.0f};
+      }
+    }
+  } else if (FMT == FMT_FP8) {
+    const uint4* qa = reinterpret_cast<const uint4*>(st + (size_t)iq * p.row13);
+    const uint4* qb = reinterpret_cast<const uint4*>(st + (size_t)(nq + iq) * p.row13);
+    const int nch = p.nchunk_h;
+    if constexpr (MAXM == 1) {
+      return dot_one_fp8(qa, qb, fs.gv, fs.uv, nch, xh, lane);
+    } else {
+      switch (__popc(mask)) {
+        case 1: return dot_rows_fp8<1>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 2: return dot_rows_fp8<2>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 3: return dot_rows_fp8<3>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 4: return dot_rows_fp8<4>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 5: return dot_rows_fp8<5>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 6: return dot_rows_fp8<6>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 7: return dot_rows_fp8<7>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
+        case 8: return dot_rows_fp8<8>(qa, qb, fs.g_row, fs.u_row, nch, xs, p.H, mask, lane);
         default: return RowSums{-1, 0.0f, 0.0f};
       }
     }
@@ -580,7 +692,7 @@ template <int FMT, int MAXM>
 struct XRegs {
   // MAXM == 1: the lane's x chunks, loaded once per phase.
   uint4 b[(MAXM == 1 && FMT == FMT_BF16) ? kCplBf16 : 1];          // bf16 chunks
-  uint32_t h[(MAXM == 1 && FMT == FMT_NVFP4) ? 16 * kCplFp4 : 1];  // fp16 chunks (NVFP4)
+  uint32_t h[(MAXM == 1 && FMT != FMT_BF16) ? 16 * kCplFp4 : 1];  // fp16 chunks (NVFP4, FP8: 64 words)
 };
 
 template <int FMT, int MAXM>
@@ -594,6 +706,21 @@ __device__ __forceinline__ void load_xregs(const Ctx& c, XRegs<FMT, MAXM>& xr) {
     for (int i = 0; i < kCplBf16; ++i) {
       const int ch = c.lane + 32 * i;
       xr.b[i] = ch < nch8 ? xs[ch] : make_uint4(0, 0, 0, 0);
+    }
+  } else if (FMT == FMT_FP8) {  // x rows are fp16 by now: 16-element chunks, 8 words each
+#pragma unroll
+    for (int i = 0; i < kCplFp8; ++i) {
+      const int ch = c.lane + 32 * i;
+      if (ch < p.H / 16) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint4 v = xs[ch * 2 + q];
+          xr.h[8 * i + 4 * q] = v.x;
+          xr.h[8 * i + 4 * q + 1] = v.y;
+          xr.h[8 * i + 4 * q + 2] = v.z;
+          xr.h[8 * i + 4 * q + 3] = v.w;
+        }
+      }
     }
   } else {  // x rows are fp16 by now
 #pragma unroll
@@ -717,14 +844,29 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
   const size_t rep_stride = (size_t)p.npair_max * p.I;
   const int nq = w.count();
   const int iq = w.offset(c.warp);
+  Fp8Scales fs;
+  if (FMT == FMT_FP8 && iq < nq) {
+    // the item's block scales, requested before the stage is waited for
+    const int e = shared ? -1 - slot : rt.slot_e[slot];
+    fs.g_row = fp8_scale_row13(p, e, w.j + iq);
+    fs.u_row = fp8_scale_row13(p, e, p.I + w.j + iq);
+    if (MAXM == 1) {
+#pragma unroll
+      for (int i = 0; i < kCplFp8; ++i) {
+        const int ch = min(c.lane + 32 * i, p.nchunk_h - 1);
+        fs.gv[i] = __ldg(fs.g_row + ch / 8);
+        fs.uv[i] = __ldg(fs.u_row + ch / 8);
+      }
+    }
+  }
   if (iq < nq && !c.aborted() && c.wait_full(ring)) {
     if (c.warp == 0 && c.lane == 0 && first) c.stamp(ST_U_DATA);
     const uint8_t* st = c.slot_ptr(ring.slot);
     const int j = w.j + iq;
     const uint32_t mask = shared ? (1u << p.M) - 1u : rt.slot_mask[slot];
-    const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane);
+    const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane, fs);
     float gsg = 1.0f, gsu = 1.0f, gs2 = 1.0f;
-    int xk = 0;  // NVFP4: the row's power-of-two scale of x (x_to_f16)
+    int xk = 0;  // NVFP4 / FP8: the row's power-of-two scale of x (x_to_f16)
     if (FMT == FMT_NVFP4) {
       const int e = shared ? -1 - slot : rt.slot_e[slot];
       const float* gs = e >= 0 ? p.w13_gs + 2 * e : p.sh_w13_gs + 2 * (-1 - e);
@@ -733,9 +875,9 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
       gs2 = e >= 0 ? p.w2_gs[e] : p.sh_w2_gs[-1 - e];  // the down weights' tensor scale, applied once here
     }
     if (rs.m >= 0) {
-      if (FMT == FMT_NVFP4) xk = xscale_exp(reinterpret_cast<const uint32_t*>(c.misc + MISC_XMAX)[rs.m]);
-      float h = FMT == FMT_NVFP4 ? silu_f32(ldexpf(rs.g, -xk) * gsg) * (ldexpf(rs.u, -xk) * gsu)
-                                 : silu_f32(rs.g * gsg) * (rs.u * gsu);
+      if (FMT != FMT_BF16) xk = xscale_exp(reinterpret_cast<const uint32_t*>(c.misc + MISC_XMAX)[rs.m]);
+      float h = FMT != FMT_BF16 ? silu_f32(ldexpf(rs.g, -xk) * gsg) * (ldexpf(rs.u, -xk) * gsu)
+                                : silu_f32(rs.g * gsg) * (rs.u * gsu);
       if (!shared) h *= rt.slot_w[slot * p.maxm + rs.m];
       if (FMT == FMT_NVFP4) h *= gs2;
       // pair index: a shared slot holds every row (pairs s * M + m); a routed
@@ -1196,15 +1338,33 @@ __device__ __forceinline__ void issue_h(const Ctx& c, const Route& rt, int sl0, 
   bulk_g2s_plain(smem_u32(dst), src, bytes, bar);
 }
 
+// FP8 down-projection block scales of expert e (shared expert -1 - e when e < 0):
+// [H / 128][I / 128] per expert.
+__device__ __forceinline__ const float* fp8_scale_down(const Params& p, int e) {
+  const float* base = reinterpret_cast<const float*>(e >= 0 ? p.w2_s : p.sh_w2_s);
+  return base + (size_t)(e >= 0 ? e : -1 - e) * (p.H / kFp8Block) * (p.I / kFp8Block);
+}
+
 // One down stage: this thread's rows of the CTA's output block (group g, 16-byte
 // code chunk ch) against the h rows of the slot's pairs (hs, in pair order),
 // accumulated in fp32 over the slots.
+// FP8: s2 = the expert's block scales [H / 128][I / 128], row0 = the global row
+// of the stage's first row.
 template <int FMT, int MAXM>
 __device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, const float* hs, uint32_t mask,
-                                           float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch, int nr) {
+                                           float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch, int nr,
+                                           const float* s2 = nullptr, int row0 = 0) {
   constexpr int RPG = rows_per_group(FMT);
   const int drs = p.d_rows_stage;
   int hp = 0;
+  float sv[FMT == FMT_FP8 ? RPG : 1];
+  if (FMT == FMT_FP8) {  // each row's scale of this thread's 8-code chunk
+#pragma unroll
+    for (int ri = 0; ri < RPG; ++ri) {
+      const int r = min(g + ri * p.ng, nr - 1);
+      sv[ri] = __ldg(s2 + (size_t)((row0 + r) / kFp8Block) * (p.I / kFp8Block) + (8 * ch) / kFp8Block);
+    }
+  }
 #pragma unroll
   for (int m = 0; m < MAXM; ++m) {
     if (!(mask >> m & 1u)) continue;
@@ -1225,6 +1385,35 @@ __device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, c
       }
 #pragma unroll
       for (int ri = 0; ri < RPG; ++ri) dot8_bf16_f32(acc[ri][m], wv[ri], hv);
+    } else if (FMT == FMT_FP8) {
+      // 8 e4m3 codes per thread and row against 8 fp32 h values, summed in
+      // fp32 (one rounding per fused multiply-add), then the row's block scale
+      const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
+      const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
+      const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint2 wv[RPG];
+#pragma unroll
+      for (int ri = 0; ri < RPG; ++ri) {
+        const int r = min(g + ri * p.ng, nr - 1);
+        wv[ri] = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2)[ch];
+      }
+#pragma unroll
+      for (int ri = 0; ri < RPG; ++ri) {
+        const uint32_t qw[2] = {wv[ri].x, wv[ri].y};
+        float part = 0.0f;
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint32_t f = e4m3x2_to_f16x2((qw[wi] >> (16 * hb)) & 0xffffu);
+            const __half2 w2 = *reinterpret_cast<const __half2*>(&f);
+            const int e0 = wi * 4 + hb * 2;
+            part = fmaf(__low2float(w2), hv[e0], part);
+            part = fmaf(__high2float(w2), hv[e0 + 1], part);
+          }
+        }
+        acc[ri][m] = fmaf(sv[ri], part, acc[ri][m]);
+      }
     } else {
       // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
 #pragma unroll
@@ -1423,7 +1612,8 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, global_ns() - tw);
         if (got && have && active)
           down_stage<FMT, MAXM>(p, c.slot_ptr(ring.slot, true), hs + (size_t)(rt.pair_base[sl] - rt.pair_base[sl0]) * p.I,
-                                mask, acc, g, ch, nr);
+                                mask, acc, g, ch, nr, FMT == FMT_FP8 ? fp8_scale_down(p, sl < p.S ? -1 - sl : rt.slot_e[sl]) : nullptr,
+                                rb_lo);
         __syncwarp();
         if (got && c.lane == 0) c.release(ring, 1);
       }
@@ -1838,7 +2028,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       bar_arrive(kBarRoute, kThreads);
       if (c.tid == 0) c.stamp(ST_ROUTED);
     }
-    if (FMT == FMT_NVFP4 && kNeedX) {  // the router is done with the bf16 x rows
+    if (FMT != FMT_BF16 && kNeedX) {  // the router is done with the bf16 x rows
       x_to_f16(c);
       bar_sync(kBarConsumers, kNC * 32);
     }
@@ -2116,7 +2306,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
       count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
-    if (FMT == FMT_NVFP4) {  // the router is done with the bf16 x rows
+    if (FMT != FMT_BF16) {  // the router is done with the bf16 x rows
       x_to_f16(c);
       bar_sync(kBarConsumers, kNC * 32);
     }

@@ -5,14 +5,18 @@
 namespace moe {
 
 constexpr int kNC = 12;                  // consumer warps per CTA
+constexpr int kMaxRowsLaunch = 8;        // token rows one kernel launch handles
+constexpr int kMaxRowsRun = 16;          // token rows one run handles (launches of <= 8 rows)
 constexpr int kThreads = (kNC + 1) * 32; // + one producer warp
 constexpr int kThreadsIlv = kThreads + 64;  // slot-interleaved kernel: + two hand-off warps
 constexpr int kRpgMax = 6;               // down-projection rows per thread group per stage (at most)
 constexpr int kRpgFp4 = 3;               // NVFP4: its 32-element chunks leave more groups, so fewer rows each
-__host__ __device__ constexpr int rows_per_group(int fmt) { return fmt == 0 ? kRpgMax : kRpgFp4; }
+__host__ __device__ constexpr int rows_per_group(int fmt) { return fmt == 1 ? kRpgFp4 : kRpgMax; }
 constexpr int kMaxSlots = 64;            // ring slots (upper bound for the barrier arrays)
 constexpr int kCplBf16 = 16;             // 16-byte x chunks per lane kept in registers (H <= 4096)
 constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVFP4 (H <= 4096)
+constexpr int kCplFp8 = 8;               // 16-element x chunks per lane for FP8 (H <= 4096)
+constexpr int kFp8Block = 128;           // FP8 weights: one fp32 scale per 128 x 128 block
 constexpr int kStageTarget = 32768;      // ring slot size aimed for (bytes)
 constexpr int kMinSlots = 4;             // ring slots kept before shrinking the h staging area
 constexpr int kLogitRep = 4;             // copies of the router logits (spreads the all-CTA read)
@@ -20,7 +24,7 @@ constexpr int kHRep = 4;                 // copies of the h rows (spreads the al
 constexpr int kCandMax = 64;             // top-k candidates ranked in parallel per row
 constexpr int kRouterCopy = 4096;        // bytes per bulk copy of router rows (more copies in flight)
 
-enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1 };
+enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_FP8 = 2 };
 
 // Phases a kernel runs: router + shared gate/up (R), routed gate/up (U),
 // down + combine + residual (D).
@@ -133,9 +137,9 @@ struct Params {
   uint32_t* ctrl;              // CTRL_WORDS
   int out_aliases_x;
   // planned layout
-  int nchunk_h;      // 16-byte code chunks per gate/up row
+  int nchunk_h;      // code chunks per gate/up row (16 bytes; FP8: 16 codes)
   int row13, sc13;   // code / scale bytes per gate/up row
-  int nchunk_i;      // 16-byte code chunks per down row
+  int nchunk_i;      // code chunks per down row (16 bytes; FP8: 8 codes)
   int row2, sc2;     // code / scale bytes per down row
   int pair_bytes;    // one gate row + one up row (codes and scales)
   int rpair_bytes;   // two router rows

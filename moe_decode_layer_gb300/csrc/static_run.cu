@@ -80,7 +80,7 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   const bool ilv = cfg->wdtype == MOE_W_BF16 && m_rows == 1 && moe::plan_host(*cfg, sms, optin, p, true) == MOE_OK;
   if (!ilv && (st = moe::plan_host(*cfg, sms, optin, p, false)) != MOE_OK) return st;
   // scratch layout inside the static array; larger configs are rejected
-  const size_t maxm = cfg->max_rows, E = cfg->num_experts, I = cfg->inter;
+  const size_t maxm = p.maxm, E = cfg->num_experts, I = cfg->inter;
   const size_t o_logits = kCtrlBytes;
   const size_t o_h = o_logits + round256((size_t)moe::kLogitRep * maxm * E * 8);
   const size_t o_xf = o_h + round256((size_t)moe::kHRep * p.npair_max * I * 4);
@@ -104,19 +104,11 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
   p.hbuf = reinterpret_cast<float*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
-  p.M = m_rows;
-  p.x = static_cast<const uint16_t*>(x);
-  p.resid = static_cast<const uint16_t*>(residual);
-  p.out = static_cast<uint16_t*>(out);
-  p.topk_idx = topk_idx;
-  p.topk_w = topk_w;
-  const size_t bytes = (size_t)m_rows * p.H * 2;
-  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
-  p.out_aliases_x = (xa < oa + bytes && oa < xa + bytes) ? 1 : 0;
-
   const int maxm_t = m_rows == 1 ? 1 : 8;
   const int which = ilv ? moe::PH_ILV : moe::PH_ALL;
-  const void* kernel = p.fmt == moe::FMT_BF16 ? moe::kernel_bf16(maxm_t, which) : moe::kernel_nvfp4(maxm_t, which);
+  const void* kernel = p.fmt == moe::FMT_BF16    ? moe::kernel_bf16(maxm_t, which)
+                       : p.fmt == moe::FMT_NVFP4 ? moe::kernel_nvfp4(maxm_t, which)
+                                                 : moe::kernel_fp8(maxm_t, which);
   if (!kernel) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -139,10 +131,25 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   attr[0].val.cooperative = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  void* args[] = {&p};
-  if (cudaLaunchKernelExC(&lc, kernel, args) != cudaSuccess) {
-    cudaGetLastError();
-    return MOE_ERR_CUDA;
+  // rows in groups of at most kMaxRowsLaunch, one launch each (as moe_decode_run)
+  for (int g0 = 0; g0 < m_rows; g0 += moe::kMaxRowsLaunch) {
+    const int mg = m_rows - g0 < moe::kMaxRowsLaunch ? m_rows - g0 : moe::kMaxRowsLaunch;
+    moe::Params q = p;
+    q.M = mg;
+    const size_t row0 = (size_t)g0 * p.H;
+    q.x = static_cast<const uint16_t*>(x) + row0;
+    q.resid = static_cast<const uint16_t*>(residual) + row0;
+    q.out = static_cast<uint16_t*>(out) + row0;
+    q.topk_idx = topk_idx ? topk_idx + (size_t)g0 * p.K : nullptr;
+    q.topk_w = topk_w ? topk_w + (size_t)g0 * p.K : nullptr;
+    const size_t bytes = (size_t)mg * p.H * 2;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(q.x), oa = reinterpret_cast<uintptr_t>(q.out);
+    q.out_aliases_x = (xa < oa + bytes && oa < xa + bytes) ? 1 : 0;
+    void* args[] = {&q};
+    if (cudaLaunchKernelExC(&lc, kernel, args) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
   }
   // wait for the step and report its device status (the status word lives in
   // the shared array too, so it is read and cleared here)

@@ -45,7 +45,7 @@ class MoEDecodeLayer:
         self._weights = weights
         cfg = _lib.Config(hidden=shape.hidden, inter=shape.inter, num_experts=shape.num_experts,
                           top_k=shape.top_k, num_shared=shape.num_shared, max_rows=max_rows,
-                          wdtype=_lib.MOE_W_BF16 if shape.wdtype == "bf16" else _lib.MOE_W_NVFP4,
+                          wdtype=_lib.WDTYPE[shape.wdtype],
                           score=score, routed_scale=routed_scale,
                           pre_rmsnorm=int(pre_rmsnorm), rms_eps=rms_eps,
                           sched=_lib.SCHED_NAMES["persistent" if sched in ("phased", "interleaved", "flat")
@@ -58,6 +58,12 @@ class MoEDecodeLayer:
             w.w13, w.w2 = _ptr(g("w13")), _ptr(g("w2"))
             if shape.num_shared:
                 w.sh_w13, w.sh_w2 = _ptr(g("sh_w13")), _ptr(g("sh_w2"))
+        elif shape.wdtype == "fp8":
+            w.w13, w.w13_scale = _ptr(g("w13_q")), _ptr(g("w13_s"))
+            w.w2, w.w2_scale = _ptr(g("w2_q")), _ptr(g("w2_s"))
+            if shape.num_shared:
+                w.sh_w13, w.sh_w13_scale = _ptr(g("sh_w13_q")), _ptr(g("sh_w13_s"))
+                w.sh_w2, w.sh_w2_scale = _ptr(g("sh_w2_q")), _ptr(g("sh_w2_s"))
         else:
             w.w13, w.w13_scale, w.w13_gscale = _ptr(g("w13_q")), _ptr(g("w13_s")), _ptr(g("w13_gs"))
             w.w2, w.w2_scale, w.w2_gscale = _ptr(g("w2_q")), _ptr(g("w2_s")), _ptr(g("w2_gs"))

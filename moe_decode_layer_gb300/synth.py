@@ -14,7 +14,9 @@ Recipe (the pages publish no weights, so all inputs are synthetic):
     caller that needs a top-k margin can redraw one row alone;
   * NVFP4 weights come from the same bf16-free N(0, 0.02^2) float32 draws,
     quantised with tensor scale amax / (6 * 448), e4m3 block scales
-    amax_block / (6 * tensor_scale) and e2m1 codes rounded to nearest-even.
+    amax_block / (6 * tensor_scale) and e2m1 codes rounded to nearest-even;
+  * FP8 weights from the same draws: one fp32 scale per 128 x 128 block,
+    amax_block / 448, and e4m3 codes rounded to nearest-even (torch's cast).
 """
 
 from __future__ import annotations
@@ -35,13 +37,15 @@ class LayerShape:
     num_experts: int
     top_k: int
     num_shared: int = 1
-    wdtype: str = "bf16"  # "bf16" or "nvfp4"
+    wdtype: str = "bf16"  # "bf16", "nvfp4" or "fp8"
 
     def expert_bytes(self) -> int:
         """HBM bytes of one expert's gate/up/down weights (codes + block scales)."""
         h, i = self.hidden, self.inter
         if self.wdtype == "bf16":
             return 3 * h * i * 2
+        if self.wdtype == "fp8":
+            return 3 * h * i + 3 * (h // 128) * (i // 128) * 4
         return 3 * h * i // 2 + 3 * h * i // 16
 
     def router_bytes(self) -> int:
@@ -55,6 +59,7 @@ LING = LayerShape(hidden=2560, inter=768, num_experts=512, top_k=8, num_shared=1
 MUSE_NVFP4 = LayerShape(hidden=4096, inter=1024, num_experts=256, top_k=8,
                         num_shared=0, wdtype="nvfp4")
 LING_E64 = LayerShape(hidden=2560, inter=768, num_experts=64, top_k=8, num_shared=1)
+LING_FP8 = LayerShape(hidden=2560, inter=768, num_experts=512, top_k=8, num_shared=1, wdtype="fp8")
 
 
 # Workloads of the bench and the profiling tools: layer shape, rows, row
@@ -65,6 +70,9 @@ WORKLOADS = {
     "ling_m6": dict(shape="LING", m=6, rho=0.5, layers=1,
                     desc="Ling-3.0-flash-shaped MoE layer, H=2560, E=512 top-8 + 1 shared, I=768, "
                          "M=6 verify rows correlated rho=0.5"),
+    "ling_m16": dict(shape="LING", m=16, rho=0.5, layers=1,
+                     desc="Ling-3.0-flash-shaped MoE layer, M=16 verify rows correlated rho=0.5 "
+                          "(two launches of 8 rows)"),
     "stack_m6": dict(shape="LING", m=6, rho=0.5, layers=12,
                      desc="12 distinct Ling-shaped MoE layers back to back, RMSNorm(1e-6) + residual "
                           "between layers, M=6 rho=0.5"),
@@ -73,6 +81,11 @@ WORKLOADS = {
                           "E=256 top-8, I=1024, no shared expert, M=1"),
     "nvfp4_m6": dict(shape="MUSE_NVFP4", m=6, rho=0.5, layers=1,
                      desc="NVFP4 experts, H=4096, E=256 top-8, I=1024, M=6 rho=0.5"),
+    "ling_fp8_m1": dict(shape="LING_FP8", m=1, rho=0.0, layers=1,
+                        desc="Ling-shaped MoE layer with FP8 experts (e4m3, fp32 scale per 128 x 128 "
+                             "block), H=2560, E=512 top-8 + 1 shared, I=768, M=1"),
+    "ling_fp8_m6": dict(shape="LING_FP8", m=6, rho=0.5, layers=1,
+                        desc="Ling-shaped MoE layer with FP8 experts, M=6 verify rows correlated rho=0.5"),
     "tiny_m1": dict(shape="TINY", m=1, rho=0.0, layers=1,
                     desc="tiny MoE layer H=256, E=16 top-2 + 1 shared, I=128, M=1"),
     # profiling case: Ling-shaped experts, 64 of them (0.76 GB per copy), same
@@ -206,6 +219,34 @@ def router_bias(num_experts: int, seed: int, device="cpu", std: float = 0.05) ->
     return _normal((num_experts,), _gen(seed * 7919 + 11, device), device, std)
 
 
+def quantize_fp8_block(w: torch.Tensor, block: int = 128):
+    """Quantise float32 [..., R, K] to e4m3 codes with one fp32 scale per block x block
+    tile: scale = amax_tile / 448 (1 for an all-zero tile), codes = the e4m3
+    nearest-even rounding of w / scale. Returns (codes uint8 [..., R, K], scales
+    float32 [..., R / block, K / block])."""
+    *lead, r, k = w.shape
+    t = w.reshape(*lead, r // block, block, k // block, block)
+    amax = t.abs().amax(dim=(-3, -1))
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+    q = (t / sc[..., :, None, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.reshape(*lead, r, k).view(torch.uint8).contiguous(), sc.contiguous()
+
+
+def _fp8_experts(n, inter, hidden, seed, device, std):
+    """FP8 gate/up [n, 2I, H] and down [n, H, I] with their 128 x 128 block scales."""
+    w13q = torch.empty((n, 2 * inter, hidden), dtype=torch.uint8, device=device)
+    w13s = torch.empty((n, 2 * inter // 128, hidden // 128), dtype=torch.float32, device=device)
+    w2q = torch.empty((n, hidden, inter), dtype=torch.uint8, device=device)
+    w2s = torch.empty((n, hidden // 128, inter // 128), dtype=torch.float32, device=device)
+    per = max(1, (1 << 29) // (3 * hidden * inter * 4))
+    for s in range(0, n, per):
+        e = min(n, s + per)
+        g = _gen(seed * 1000003 + s, device)
+        w13q[s:e], w13s[s:e] = quantize_fp8_block(_normal((e - s, 2 * inter, hidden), g, device, std))
+        w2q[s:e], w2s[s:e] = quantize_fp8_block(_normal((e - s, hidden, inter), g, device, std))
+    return w13q, w13s, w2q, w2s
+
+
 def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) -> dict:
     """All weights of one layer as torch tensors on ``device``.
 
@@ -213,6 +254,8 @@ def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) ->
     nvfp4: router_w bf16 [E, H]; w13_q uint8 [E, 2I, H/2], w13_s uint8 [E, 2I, H/16],
            w13_gs f32 [E, 2], w2_q uint8 [E, H, I/2], w2_s uint8 [E, H, I/16],
            w2_gs f32 [E]; the same with an ``sh_`` prefix for the S shared experts.
+    fp8:   router_w bf16 [E, H]; w13_q uint8 e4m3 [E, 2I, H], w13_s f32 [E, 2I/128, H/128],
+           w2_q uint8 e4m3 [E, H, I], w2_s f32 [E, H/128, I/128]; ``sh_`` the same.
     """
     h, i, e, s = shape.hidden, shape.inter, shape.num_experts, shape.num_shared
     g = _gen(seed * 7919 + 1, device)
@@ -227,6 +270,12 @@ def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) ->
         for n, t in zip(names, _nvfp4_experts(e, i, h, seed * 7919 + 2, device, std)):
             layer[n] = t
         for n, t in zip(names, _nvfp4_experts(s, i, h, seed * 7919 + 4, device, std)):
+            layer["sh_" + n] = t
+    elif shape.wdtype == "fp8":
+        names = ("w13_q", "w13_s", "w2_q", "w2_s")
+        for n, t in zip(names, _fp8_experts(e, i, h, seed * 7919 + 2, device, std)):
+            layer[n] = t
+        for n, t in zip(names, _fp8_experts(s, i, h, seed * 7919 + 4, device, std)):
             layer["sh_" + n] = t
     else:
         raise ValueError(f"unknown weight dtype {shape.wdtype!r}")

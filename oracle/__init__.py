@@ -11,7 +11,8 @@ Two independent restatements of the same definitions, both float64:
                 output elements), loaded through ctypes. The GPU parity tests and
                 the bench's CPU baseline use it.
   moe_oracle -- a numpy restatement (router GEMV, selection, SwiGLU experts,
-                combine, RMSNorm), plus ``nvfp4`` for e2m1 / e4m3 decoding. The
+                combine, RMSNorm), plus ``nvfp4`` for e2m1 / e4m3 decoding and
+                the NVFP4 and FP8 block dequantisation. The
                 tests run every pin against both and cross-check the two on random
                 layers.
 
@@ -38,4 +39,4 @@ from .moe_oracle import (  # noqa: F401
     topk_margin,
     expert_union,
 )
-from .nvfp4 import e2m1_value, e4m3_value, dequant_nvfp4_rows  # noqa: F401
+from .nvfp4 import e2m1_value, e4m3_value, dequant_nvfp4_rows, dequant_fp8_block  # noqa: F401

@@ -8,7 +8,8 @@ run against both.
 Expert weights are handed over per expert by a callable ``e -> weights``:
   * ``(w13, w2)`` float64 arrays [2I, H], [H, I] (any values), or
   * ``(w13, w2)`` uint16 arrays of bf16 bit patterns, or
-  * an :class:`NVFP4Expert` of codes, e4m3 scale bytes and tensor scales.
+  * an :class:`NVFP4Expert` of codes, e4m3 scale bytes and tensor scales, or
+  * an :class:`FP8Expert` of e4m3 codes and float32 128 x 128 block scales.
 Only the experts some row selects (and the shared ones) are requested.
 """
 
@@ -23,11 +24,14 @@ from . import build as _build
 
 SCORE_SOFTMAX = 0
 SCORE_SIGMOID_BIAS = 1
-FMT_F64, FMT_BF16, FMT_NVFP4 = 0, 1, 2
+FMT_F64, FMT_BF16, FMT_NVFP4, FMT_FP8 = 0, 1, 2, 3
 
 # gate/up codes [2I, H/2], scales [2I, H/16], tensor scales (gate, up); down
 # codes [H, I/2], scales [H, I/16], tensor scale
 NVFP4Expert = namedtuple("NVFP4Expert", "q13 s13 gs13 q2 s2 gs2")
+# e4m3 gate/up codes [2I, H], float32 scales [2I/128, H/128]; down codes [H, I],
+# scales [H/128, I/128]
+FP8Expert = namedtuple("FP8Expert", "q13 s13 q2 s2")
 
 
 class _Experts(ctypes.Structure):
@@ -177,6 +181,15 @@ def route(x, router_w, k: int, score: int = SCORE_SOFTMAX, bias=None, threads: i
 # ----------------------------------------------------------------------------- the layer
 
 
+def _inter_of(w) -> int:
+    """The expert intermediate size I from one expert's weights."""
+    if isinstance(w, NVFP4Expert):
+        return np.asarray(w.q2).shape[1] * 2
+    if isinstance(w, FP8Expert):
+        return np.asarray(w.q2).shape[1]
+    return np.asarray(w[1]).shape[1]
+
+
 class _ExpertTable:
     """ctypes pointer tables for a set of experts (keeps the arrays alive)."""
 
@@ -188,7 +201,14 @@ class _ExpertTable:
         self.gs2 = np.zeros(max(n, 1), np.float32)
         fmt = None
         for e, wts in entries.items():
-            if isinstance(wts, NVFP4Expert):
+            if isinstance(wts, FP8Expert):
+                f = FMT_FP8
+                q13, q2 = (np.ascontiguousarray(a, dtype=np.uint8) for a in (wts.q13, wts.q2))
+                s13, s2 = (np.ascontiguousarray(a, dtype=np.float32) for a in (wts.s13, wts.s2))
+                self.keep += [q13, s13, q2, s2]
+                self.w13[e], self.w2[e] = q13.ctypes.data, q2.ctypes.data
+                self.s13[e], self.s2[e] = s13.ctypes.data, s2.ctypes.data
+            elif isinstance(wts, NVFP4Expert):
                 f = FMT_NVFP4
                 q13, s13, q2, s2 = (np.ascontiguousarray(a, dtype=np.uint8) for a in (wts.q13, wts.s13, wts.q2, wts.s2))
                 self.keep += [q13, s13, q2, s2]
@@ -230,8 +250,7 @@ def moe_layer(x, residual, router_w, expert_weights, shared_weights, top_k, rout
     routed = _ExpertTable(e_count, {e: expert_weights(e) for e in needed})
     shared = _ExpertTable(len(shared_weights), dict(enumerate(shared_weights)))
     any_w = expert_weights(needed[0]) if needed else shared_weights[0]
-    inter = (np.asarray(any_w.q2).shape[1] * 2 if isinstance(any_w, NVFP4Expert)
-             else np.asarray(any_w[1]).shape[1])
+    inter = _inter_of(any_w)
     shape = _Shape(h, inter, e_count, top_k, len(shared_weights), m, score, rfmt, float(routed_scale), threads)
     out = np.empty((m, h), np.float64)
     idx = np.empty((m, top_k), np.int64)
@@ -261,8 +280,7 @@ class Prepared:
         self.routed = _ExpertTable(self.r.shape[0], {e: expert_weights(e) for e in needed})
         self.shared = _ExpertTable(len(shared_weights), dict(enumerate(shared_weights)))
         any_w = expert_weights(needed[0])
-        inter = (np.asarray(any_w.q2).shape[1] * 2 if isinstance(any_w, NVFP4Expert)
-                 else np.asarray(any_w[1]).shape[1])
+        inter = _inter_of(any_w)
         self.shape = _Shape(h, inter, self.r.shape[0], top_k, len(shared_weights), m, score, rfmt,
                             float(routed_scale), 0)
         self.out = np.empty((m, h), np.float64)

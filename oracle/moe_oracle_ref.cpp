@@ -40,6 +40,10 @@
 //          float32 tensor scale per (expert, projection): w = e2m1 * e4m3 * ts.
 //          (Muse Spark Open Ultrafast, section "The model": NVFP4 experts; the
 //          format follows the OCP microscaling definitions of e2m1 and e4m3.)
+//   FP8    one e4m3 code byte per element and one float32 scale per 128 x 128
+//          block of the matrix, [rows / 128][cols / 128]: w = e4m3 * scale
+//          (Ling-3.0-flash blog, section "Where the time goes now": fp8 weights,
+//          block 128).
 //
 // Threads: the router loops over experts, and each expert's gate/up rows and
 // down rows, split over OpenMP threads; every output element is one sequential
@@ -77,9 +81,10 @@ enum Mutant {
   MUT_NIBBLE_ORDER = 12,
   MUT_E4M3_BIAS = 13,
   MUT_NO_ROUTED_SCALE = 14,
+  MUT_FP8_SCALE_TRANSPOSED = 15,
 };
 
-enum { FMT_F64 = 0, FMT_BF16 = 1, FMT_NVFP4 = 2 };
+enum { FMT_F64 = 0, FMT_BF16 = 1, FMT_NVFP4 = 2, FMT_FP8 = 3 };
 enum { SCORE_SOFTMAX = 0, SCORE_SIGMOID_BIAS = 1 };
 enum { OK = 0, ERR_ARG = 1, ERR_MISSING_EXPERT = 2 };
 
@@ -126,11 +131,11 @@ extern "C" {
 
 // One weight matrix set per expert; entries of unused experts may be NULL.
 typedef struct {
-  int32_t fmt;                      // FMT_F64, FMT_BF16 or FMT_NVFP4
-  const void* const* w13;           // [n] -> [2I, H] values, or e2m1 codes [2I, H/2]
-  const void* const* w2;            // [n] -> [H, I] values, or e2m1 codes [H, I/2]
-  const uint8_t* const* w13_scale;  // NVFP4: [n] -> e4m3 [2I, H/16]
-  const uint8_t* const* w2_scale;   // NVFP4: [n] -> e4m3 [H, I/16]
+  int32_t fmt;                      // FMT_F64, FMT_BF16, FMT_NVFP4 or FMT_FP8
+  const void* const* w13;           // [n] -> [2I, H] values or e4m3 codes, or e2m1 codes [2I, H/2]
+  const void* const* w2;            // [n] -> [H, I] values or e4m3 codes, or e2m1 codes [H, I/2]
+  const uint8_t* const* w13_scale;  // NVFP4: [n] -> e4m3 [2I, H/16]; FP8: float [2I/128, H/128]
+  const uint8_t* const* w2_scale;   // NVFP4: [n] -> e4m3 [H, I/16]; FP8: float [H/128, I/128]
   const float* w13_gscale;          // NVFP4: [n][2] tensor scale of the gate rows, of the up rows
   const float* w2_gscale;           // NVFP4: [n]
 } moe_oracle_experts;
@@ -290,6 +295,17 @@ bool expert_row(const moe_oracle_experts& ex, int e, int which, int r, int cols,
   } else if (ex.fmt == FMT_BF16) {
     const uint16_t* p = static_cast<const uint16_t*>(base) + row0;
     for (int c = 0; c < cols; ++c) dst[c] = bf16_value(p[c]);
+  } else if (ex.fmt == FMT_FP8) {
+    const uint8_t* q = static_cast<const uint8_t*>(base) + row0;
+    const float* sc = reinterpret_cast<const float*>(which == 0 ? ex.w13_scale[e] : ex.w2_scale[e]);
+    if (!sc) return false;
+    const int rows = which == 0 ? 2 * inter : 0;  // only the transposed-index mutant needs it
+    const int nb = cols / 128;
+    for (int c = 0; c < cols; ++c) {
+      const size_t bi = kMutant == MUT_FP8_SCALE_TRANSPOSED ? (size_t)(c / 128) * ((which == 0 ? rows : cols) / 128) + r / 128
+                                                            : (size_t)(r / 128) * nb + c / 128;
+      dst[c] = e4m3_value(q[c]) * static_cast<double>(sc[bi]);
+    }
   } else {
     const uint8_t* q = static_cast<const uint8_t*>(base) + row0 / 2;
     const uint8_t* sc = (which == 0 ? ex.w13_scale[e] : ex.w2_scale[e]);

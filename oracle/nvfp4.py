@@ -75,3 +75,18 @@ def dequant_nvfp4_rows(codes: np.ndarray, scales: np.ndarray, tensor_scale: floa
     out[:, 1::2] = _E2M1[codes >> 4]
     block = np.repeat(_E4M3[scales], 16, axis=1)
     return out * block * float(tensor_scale)
+
+
+def dequant_fp8_block(codes: np.ndarray, scales: np.ndarray, block: int = 128) -> np.ndarray:
+    """Dequantise FP8 block-scaled weights to float64.
+
+    codes  uint8 [R, K]  e4m3 bit patterns, one per element
+    scales float32 [R / block, K / block], one per block x block tile
+    Returns float64 [R, K] = e4m3(code) * scale of the element's tile. (Ling-3.0-flash
+    blog, "Where the time goes now": fp8 weights with 128-wide blocks.)
+    """
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.float64)
+    r, k = codes.shape
+    assert scales.shape == (r // block, k // block)
+    return _E4M3[codes] * np.repeat(np.repeat(scales, block, axis=0), block, axis=1)

@@ -62,6 +62,9 @@ def expert_accessor(shape: synth.LayerShape, layer: dict, prefix: str = ""):
     def get(e):
         if shape.wdtype == "bf16":
             return bits(layer[prefix + "w13"][e]), bits(layer[prefix + "w2"][e])
+        if shape.wdtype == "fp8":
+            return cpp.FP8Expert(bits(layer[prefix + "w13_q"][e]), layer[prefix + "w13_s"][e].cpu().numpy(),
+                                 bits(layer[prefix + "w2_q"][e]), layer[prefix + "w2_s"][e].cpu().numpy())
         return cpp.NVFP4Expert(bits(layer[prefix + "w13_q"][e]), bits(layer[prefix + "w13_s"][e]),
                                layer[prefix + "w13_gs"][e].cpu().numpy(), bits(layer[prefix + "w2_q"][e]),
                                bits(layer[prefix + "w2_s"][e]), np.float32(layer[prefix + "w2_gs"][e].cpu()))

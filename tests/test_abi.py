@@ -56,6 +56,8 @@ def test_supported_configs():
     assert _check() == 0
     assert _check(hidden=256, inter=128, num_experts=16, top_k=2, max_rows=1) == 0
     assert _check(hidden=4096, inter=1024, num_experts=256, top_k=8, num_shared=0, wdtype=1) == 0
+    assert _check(wdtype=2) == 0  # FP8 block-quantised Ling shape
+    assert _check(wdtype=2, hidden=256, inter=128, max_rows=16) == 0
     assert _check(pre_rmsnorm=1, rms_eps=1e-6) == 0
     assert _check(sched=1) == 0 and _check(sched=2) == 0
     assert _check(top_k=16, num_experts=16) == 0
@@ -67,14 +69,17 @@ def test_supported_configs():
     (dict(num_experts=2048), _lib.MOE_ERR_UNSUPPORTED),
     (dict(top_k=17), _lib.MOE_ERR_UNSUPPORTED),
     (dict(top_k=9, num_experts=8), _lib.MOE_ERR_UNSUPPORTED),
-    (dict(max_rows=9), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(max_rows=17), _lib.MOE_ERR_UNSUPPORTED),
     (dict(max_rows=0), _lib.MOE_ERR_INVALID_ARG),
     (dict(hidden=2564), _lib.MOE_ERR_UNSUPPORTED),
     (dict(hidden=8192), _lib.MOE_ERR_UNSUPPORTED),
     (dict(inter=776), _lib.MOE_ERR_UNSUPPORTED),      # 97 threads per group
     (dict(inter=4096), _lib.MOE_ERR_UNSUPPORTED),     # more than one CTA's consumers
     (dict(wdtype=1, hidden=2176), _lib.MOE_ERR_UNSUPPORTED),  # not a multiple of 256
-    (dict(wdtype=2), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(wdtype=3), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(wdtype=2, hidden=2496), _lib.MOE_ERR_UNSUPPORTED),  # FP8: not a multiple of 128
+    (dict(wdtype=2, inter=640), _lib.MOE_ERR_UNSUPPORTED),    # FP8: not a multiple of 128
+    (dict(wdtype=2, inter=384), _lib.MOE_ERR_UNSUPPORTED),    # FP8: 48 threads per down row
     (dict(score=2), _lib.MOE_ERR_UNSUPPORTED),
     (dict(sched=3), _lib.MOE_ERR_UNSUPPORTED),
     (dict(num_shared=5), _lib.MOE_ERR_UNSUPPORTED),

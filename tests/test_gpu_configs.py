@@ -1,4 +1,4 @@
-"""GPU parity for the NVFP4 expert layer and the 12-layer stack with RMSNorm.
+"""GPU parity for the NVFP4 and FP8 expert layers and the 12-layer stack with RMSNorm.
 
 NVFP4 (Muse Spark Open Ultrafast, section "The model": 8 of 256 experts,
 NVFP4 expert weights): H=4096, E=256 top-8, I=1024, no shared expert, M=1 and
@@ -176,4 +176,92 @@ def test_nvfp4_activations_outside_fp16_range(sched):
     err = np.abs(got - ref)
     assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 2e-2), float((err - 2.0 ** -8 * np.abs(ref)).max())
     for m in range(3):  # each row on its own scale
+        assert np.linalg.norm(got[m] - ref[m]) <= 5e-3 * np.linalg.norm(ref[m]), m
+
+
+# ---------------------------------------------------------------------------
+# FP8 block-quantised experts (e4m3 codes, one fp32 scale per 128 x 128 block)
+# ---------------------------------------------------------------------------
+
+
+@pytest.fixture(scope="module")
+def fp8layer():
+    layer = synth.make_layer(synth.LING_FP8, seed=21, device="cuda")
+    yield layer
+    del layer
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("sched", ["persistent", "phased", "pdl_chain", "chain"])
+@pytest.mark.parametrize("m", [1, 6])
+def test_fp8_ling_layer(fp8layer, sched, m):
+    """Ling-shaped layer (H=2560, E=512 top-8 + 1 shared, I=768) with FP8 experts;
+    the oracle decodes the same codes and block scales itself."""
+    shape = synth.LING_FP8
+    x = helpers.hidden_with_margin(fp8layer["router_w"], m, shape.top_k, seed=70 + m, rho=0.5)
+    mod = MoEDecodeLayer(shape, fp8layer, m, sched=sched)
+    xd = x.cuda()
+    idx = torch.empty((m, shape.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((m, shape.top_k), dtype=torch.float32, device="cuda")
+    out = mod.run(xd, xd, None, idx, w)
+    assert mod.status() == _lib.MOE_OK
+    ref, ridx, rw = helpers.oracle_layer(shape, fp8layer, x, x)
+    helpers.assert_routing(idx.cpu(), w.cpu(), ridx, rw)
+    helpers.assert_close(out.cpu(), ref)
+    z = torch.zeros_like(xd)
+    out2 = mod.run(xd, z, None)
+    assert mod.status() == _lib.MOE_OK
+    ref2, _, _ = helpers.oracle_layer(shape, fp8layer, x, z.cpu())
+    helpers.assert_close(out2.cpu(), ref2)
+
+
+@pytest.mark.parametrize("shape", [
+    synth.LayerShape(hidden=256, inter=128, num_experts=16, top_k=4, num_shared=1, wdtype="fp8"),
+    synth.LayerShape(hidden=384, inter=256, num_experts=40, top_k=6, num_shared=2, wdtype="fp8"),
+], ids=["h256", "h384"])
+def test_fp8_small_shapes(shape):
+    """Small FP8 layers spanning several scale blocks along both axes (and a ragged
+    expert count), every row count 1..16 in groups, two schedules bit-identical."""
+    layer = synth.make_layer(shape, seed=23, device="cuda")
+    for m in (1, 2, 5, 8, 13, 16):
+        x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=80 + m, rho=0.5)
+        outs = []
+        for sched in ("persistent", "chain"):
+            mod = MoEDecodeLayer(shape, layer, 16, sched=sched)
+            xd = x.cuda()
+            idx = torch.empty((m, shape.top_k), dtype=torch.int32, device="cuda")
+            w = torch.empty((m, shape.top_k), dtype=torch.float32, device="cuda")
+            out = mod.run(xd, xd, None, idx, w)
+            assert mod.status() == _lib.MOE_OK
+            ref, ridx, rw = helpers.oracle_layer(shape, layer, x, x)
+            helpers.assert_routing(idx.cpu(), w.cpu(), ridx, rw)
+            helpers.assert_close(out.cpu(), ref, what=f"m={m} {sched}")
+            outs.append(out.cpu())
+        assert torch.equal(outs[0], outs[1])
+
+
+def test_fp8_activations_outside_fp16_range():
+    """FP8 experts also multiply fp16 activations: a row with entries of 1e5 and a
+    row scaled by 2^-20 come out as the float64 oracle computes them (same
+    tolerance as the NVFP4 case)."""
+    shape = synth.LayerShape(hidden=256, inter=128, num_experts=16, top_k=4, num_shared=1, wdtype="fp8")
+    layer = synth.make_layer(shape, seed=29, device="cuda")
+    x = helpers.hidden_with_margin(layer["router_w"], 2, shape.top_k, seed=31)
+    xf = x.float()
+    xf[0, 0], xf[0, 9] = 1.0e5, -7.0e4
+    xf[1] = xf[1] * 2.0 ** -20
+    x = xf.to(torch.bfloat16)
+    r = torch.zeros_like(x)
+    mod = MoEDecodeLayer(shape, layer, 2, sched="persistent")
+    idx = torch.empty((2, shape.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((2, shape.top_k), dtype=torch.float32, device="cuda")
+    out = mod.run(x.cuda(), r.cuda(), None, idx, w)
+    assert mod.status() == _lib.MOE_OK
+    ref, ridx, rw = helpers.oracle_layer(shape, layer, x, r)
+    helpers.assert_routing(idx.cpu(), w.cpu(), ridx, rw)
+    got = helpers.f64(out.cpu())
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 2e-2), float((err - 2.0 ** -8 * np.abs(ref)).max())
+    for m in range(2):
         assert np.linalg.norm(got[m] - ref[m]) <= 5e-3 * np.linalg.norm(ref[m]), m

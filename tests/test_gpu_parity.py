@@ -273,6 +273,22 @@ def test_ling_m6_correlated(ling, sched):
     assert 8 <= distinct <= 48
 
 
+@pytest.mark.parametrize("sched", ["persistent", "flat", "pdl_chain"])
+@pytest.mark.parametrize("m", [9, 16])
+def test_wide_verify_rows(tiny, ling, sched, m):
+    """More than 8 rows (the 16-token verify batch): row groups of at most 8 run
+    one after another; every row is checked against the oracle, in place too."""
+    for shape, layer in ((synth.TINY, tiny), (synth.LING, ling)):
+        x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=130 + m, rho=0.5)
+        _, out, idx, w = _run(shape, layer, x, sched=sched)
+        _check(shape, layer, x, out, idx, w)
+        mod = MoEDecodeLayer(shape, layer, m, sched=sched)
+        buf = x.cuda()
+        mod.run(buf, buf, buf)
+        assert mod.status() == _lib.MOE_OK
+        assert torch.equal(buf.cpu(), out)
+
+
 def test_ling_interleave_modes(ling):
     """The Ling-shaped layer fits the slot-interleaved layout at M = 1 and M = 6:
     the default mode (1) uses it for single-row runs, "interleaved" forces it (2),

@@ -400,7 +400,73 @@ def test_nvfp4_layout_by_hand_cpp():
     np.testing.assert_array_equal(a[0], b[0])
 
 
-@pytest.mark.parametrize("fmt", ["f64", "bf16", "nvfp4"])
+def _fp8_expert(rng, hdim, inter):
+    w13 = torch.from_numpy(rng.standard_normal((2 * inter, hdim)).astype(np.float32)) * 0.05
+    w2 = torch.from_numpy(rng.standard_normal((hdim, inter)).astype(np.float32)) * 0.05
+    q13, s13 = synth.quantize_fp8_block(w13)
+    q2, s2 = synth.quantize_fp8_block(w2)
+    return cpp.FP8Expert(q13.numpy(), s13.numpy(), q2.numpy(), s2.numpy())
+
+
+def _fp8_as_f64(ex):
+    return nvfp4.dequant_fp8_block(ex.q13, ex.s13), nvfp4.dequant_fp8_block(ex.q2, ex.s2)
+
+
+def test_fp8_layout_by_hand_cpp():
+    """A one-expert FP8 layer whose codes and block scales are placed by hand equals
+    the same layer with the hand-decoded float64 weights: e4m3 0x38 = 1.0, 0xC4 =
+    -3.0 (sign, exponent 8, mantissa 4: -1.5 * 2); each 128 x 128 tile of the
+    [256, 256] gate/up matrix and the [128, 256] down matrix has its own scale."""
+    hdim, inter = 128, 128
+    q13 = np.zeros((2 * inter, hdim), np.uint8)
+    q13[:, 0], q13[:, 5] = 0x38, 0xC4
+    s13 = np.array([[0.5], [0.25]], np.float32)  # gate rows, up rows
+    q2 = np.zeros((hdim, inter), np.uint8)
+    q2[:, 3] = 0x38
+    s2 = np.array([[2.0]], np.float32)
+    ex = cpp.FP8Expert(q13, s13, q2, s2)
+    row = np.zeros(hdim)
+    row[0], row[5] = 1.0, -3.0
+    w13 = np.vstack([np.tile(row * 0.5, (inter, 1)), np.tile(row * 0.25, (inter, 1))])
+    w2 = np.zeros((hdim, inter))
+    w2[:, 3] = 2.0
+    x = np.linspace(-1, 1, hdim)[None, :]
+    router = np.ones((1, hdim))
+    a = cpp.moe_layer(x, x, router, lambda e: ex, [], 1)
+    b = cpp.moe_layer(x, x, router, lambda e: (w13, w2), [], 1)
+    np.testing.assert_array_equal(a[0], b[0])
+    # a rectangular scale grid: down [256, 128] with scales [2, 1]
+    q2b = np.zeros((256, 128), np.uint8)
+    q2b[:, 1] = 0x38
+    s2b = np.array([[3.0], [5.0]], np.float32)
+    w2b = np.zeros((256, 128))
+    w2b[:128, 1], w2b[128:, 1] = 3.0, 5.0
+    q13b = np.zeros((256, 256), np.uint8)
+    q13b[:, 7] = 0x38
+    s13b = np.array([[1.0, 2.0], [4.0, 8.0]], np.float32)
+    w13b = np.zeros((256, 256))
+    w13b[:128, 7], w13b[128:, 7] = 1.0, 4.0
+    x2 = np.linspace(-1, 1, 256)[None, :]
+    a = cpp.moe_layer(x2, x2, np.ones((1, 256)), lambda e: cpp.FP8Expert(q13b, s13b, q2b, s2b), [], 1)
+    b = cpp.moe_layer(x2, x2, np.ones((1, 256)), lambda e: (w13b, w2b), [], 1)
+    np.testing.assert_array_equal(a[0], b[0])
+
+
+def test_fp8_quantiser_roundtrip():
+    """The synthetic FP8 quantiser and the oracle's decoder are independent: a tile
+    whose values are e4m3 grid points times amax / 448 comes back exactly, and the
+    tile maximum maps to code 448 (0x7E)."""
+    grid = np.array([nvfp4.e4m3_value(b) for b in range(0x7F)], np.float64)  # 0 .. 448
+    rng = np.random.default_rng(4)
+    vals = rng.choice(grid, size=(128, 128)) * rng.choice([-1.0, 1.0], size=(128, 128))
+    vals[0, 0] = 448.0
+    w = torch.from_numpy((vals * 2.0 ** -9).astype(np.float32))  # scale 2^-9: exact
+    q, sc = synth.quantize_fp8_block(w)
+    assert float(sc[0, 0]) == 2.0 ** -9 and int(q[0, 0]) == 0x7E
+    np.testing.assert_array_equal(nvfp4.dequant_fp8_block(q.numpy(), sc.numpy()), vals * 2.0 ** -9)
+
+
+@pytest.mark.parametrize("fmt", ["f64", "bf16", "nvfp4", "fp8"])
 @pytest.mark.parametrize("score", [0, 1])
 def test_cpp_matches_numpy_restatement(fmt, score):
     rng = np.random.default_rng(41 + score)
@@ -410,6 +476,11 @@ def test_cpp_matches_numpy_restatement(fmt, score):
     if fmt == "nvfp4":
         raw = [_nvfp4_expert(rng, hdim, inter) for _ in range(e + s)]
         f64 = [_nvfp4_as_f64(w) for w in raw]
+    elif fmt == "fp8":
+        hdim, inter = 256, 128
+        router = rng.standard_normal((e, hdim)) * 0.2
+        raw = [_fp8_expert(rng, hdim, inter) for _ in range(e + s)]
+        f64 = [_fp8_as_f64(w) for w in raw]
     else:
         f64 = [(rng.standard_normal((2 * inter, hdim)) * 0.2, rng.standard_normal((hdim, inter)) * 0.2)
                for _ in range(e + s)]
@@ -568,13 +639,18 @@ def test_pins_catch_dropped_residual_numpy(monkeypatch):
 CPP_MUTANTS = {1: "swap_gate_up", 2: "sigmoid_not_silu", 3: "silu_sign", 4: "no_renorm",
                5: "ties_to_higher_id", 6: "router_rows_reversed", 7: "bottom_k", 8: "drop_shared",
                9: "drop_residual", 10: "bias_in_weights", 11: "bf16_truncates", 12: "nibble_order",
-               13: "e4m3_bias", 14: "no_routed_scale"}
+               13: "e4m3_bias", 14: "no_routed_scale", 15: "fp8_scale_transposed"}
 
 
 @pytest.mark.parametrize("mutant", sorted(CPP_MUTANTS), ids=lambda n: CPP_MUTANTS[n])
 def test_pins_catch_planted_mistakes_cpp(mutant, monkeypatch):
     impl = CppOracle(mutant)
     failures = _failures(impl)
+    if CPP_MUTANTS[mutant] == "fp8_scale_transposed":
+        monkeypatch.setattr(cpp, "load", lambda m=0: impl.lib)
+        with pytest.raises(AssertionError):
+            test_fp8_layout_by_hand_cpp()
+        failures += 1
     if CPP_MUTANTS[mutant] == "nibble_order":
         monkeypatch.setattr(cpp, "load", lambda m=0: impl.lib)
         with pytest.raises(AssertionError):
