@@ -126,7 +126,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   p.off_hbar = take(16, 8);
   p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
   p.off_x = take((size_t)maxm * H * 2, 128);
-  p.off_sel_e = take((size_t)maxm * K * 4, 4);
+  p.off_sel_e = take(((size_t)maxm * K * 4 + 15) / 16 * 16 + 16, 16);  // read in 16-byte groups by the one-row union
   p.off_sel_w = take((size_t)maxm * K * 4, 4);
   p.off_emask = take((size_t)E * 4, 4);
   p.off_bitmap = take((size_t)(E + 31) / 32 * 4, 4);
@@ -251,7 +251,7 @@ moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params
   p.off_hbar = take(moe::kFlatSegs * 8, 8);
   p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
   p.off_x = take((size_t)maxm * H * 2, 128);
-  p.off_sel_e = take((size_t)maxm * K * 4, 4);
+  p.off_sel_e = take(((size_t)maxm * K * 4 + 15) / 16 * 16 + 16, 16);  // read in 16-byte groups by the one-row union
   p.off_sel_w = take((size_t)maxm * K * 4, 4);
   p.off_emask = take((size_t)E * 4, 4);
   p.off_bitmap = take((size_t)(E + 31) / 32 * 4, 4);

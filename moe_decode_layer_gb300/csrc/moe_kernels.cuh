@@ -994,74 +994,81 @@ __device__ __forceinline__ float sigmoid_f32(float v) { return 1.0f / (1.0f + ex
 // every expert's selection key in registers (lane l holds experts l + 32 i,
 // PM * 32 >= E). The K-th largest of the 32 lane maxima bounds the K-th largest
 // key from below -- those K lane maxima are K distinct experts -- so every
-// selected expert's key is at or above it; the few candidates at or above it go
-// to shared memory at positions from a warp scan and a per-lane bit count, and
-// each is ranked against all of them on exact 64-bit keys (ties: the lower
-// expert id). With more than kCandMax candidates (many keys tied in value), K
-// rounds of a warp-wide maximum select instead. Each step is kept short and
-// independent: one warp's chain of dependent shuffles and shared loads is the
-// routing latency every CTA waits for.
+// selected expert's key is at or above it. It is found by rounds of a warp-wide
+// maximum (redux) over the lane maxima; the few candidates at or above it go to
+// shared memory at positions given by an exclusive count over the lanes (built
+// from ballots of the count's bits), and each is ranked against all of them on
+// exact 64-bit keys (ties: the lower expert id). With more than kCandMax - 1
+// candidates (many keys tied in value), K rounds of a warp-wide maximum select
+// instead. On this path one warp's dependent chain is the routing latency every
+// CTA waits for, so it uses reductions and ballots rather than shuffles, and
+// shared memory where a value must reach every lane.
 template <int PM>
 __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
   const Params& p = c.p;
   const int E = p.E, K = p.K, lane = c.lane;
   float* lg = reinterpret_cast<float*>(c.sm + p.off_lg) + (size_t)m * E;
-  const float* bias = p.score ? reinterpret_cast<const float*>(c.sm + p.off_bias) : nullptr;
-  uint32_t* lmax = reinterpret_cast<uint32_t*>(c.sm + p.off_lmax) + m * 32;
+  const float* bias = reinterpret_cast<const float*>(c.sm + p.off_bias);
+  float* wx = reinterpret_cast<float*>(c.sm + p.off_lmax) + m * 32;  // numerators of the weights
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + (size_t)m * kCandMax;
   uint32_t key[PM];
+  if (p.score) {  // bias-corrected sigmoid rule: select on sigmoid(l) + b
 #pragma unroll
-  for (int i = 0; i < PM; ++i) {
-    const int e = lane + 32 * i;
-    float v = 0.0f;
-    if (e < E) v = bias ? sigmoid_f32(lg[e]) + bias[e] : lg[e];
-    key[i] = e < E ? f32_order_key(v) : 0u;
+    for (int i = 0; i < PM; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = e < E ? f32_order_key(sigmoid_f32(lg[e]) + bias[e]) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PM; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = e < E ? f32_order_key(lg[e]) : 0u;
+    }
   }
-  uint32_t mx = 0;
+  uint32_t t[PM];
 #pragma unroll
-  for (int i = 0; i < PM; ++i) mx = max(mx, key[i]);
-  lmax[lane] = mx;
-  __syncwarp();
-  int gt = 0, ge = 0;
-  const uint4* l4 = reinterpret_cast<const uint4*>(lmax);
+  for (int i = 0; i < PM; ++i) t[i] = key[i];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint4 q = l4[j];
-    gt += (q.x > mx) + (q.y > mx) + (q.z > mx) + (q.w > mx);
-    ge += (q.x >= mx) + (q.y >= mx) + (q.z >= mx) + (q.w >= mx);
+  for (int h = PM / 2; h >= 1; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < h; ++i) t[i] = max(t[i], t[i + h]);
+  // the K-th largest lane maximum: lanes tied on a value leave in the same round
+  uint32_t T = 0, lk = t[0];
+  for (int got = 0; got < K;) {
+    T = warp_max_u32(lk);
+    const bool hit = lk == T;
+    got += __popc(__ballot_sync(kFull, hit));
+    lk = hit ? 0u : lk;
   }
-  // the K-th largest lane maximum (lanes tied on it hold the same value)
-  const uint32_t bt = __ballot_sync(kFull, mx != 0u && gt <= K - 1 && ge >= K);
-  const uint32_t T = __shfl_sync(kFull, mx, __ffs(bt) - 1);
   uint32_t fm = 0;
 #pragma unroll
-  for (int i = 0; i < PM; ++i) fm |= (uint32_t)(key[i] != 0u && key[i] >= T) << i;
+  for (int i = 0; i < PM; ++i) fm |= (uint32_t)(key[i] >= T && key[i] != 0u) << i;
+  // exclusive count of candidates over the lanes, and the total, bit by bit
   const int cnt = __popc(fm);
-  int incl = cnt;
+  const uint32_t lt = (1u << lane) - 1u;
+  int o = 0, C = 0;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, d);
-    if (lane >= d) incl += y;
+  for (int bit = 0; bit < (PM > 16 ? 6 : 5); ++bit) {
+    const uint32_t bb = __ballot_sync(kFull, (cnt >> bit) & 1);
+    o += __popc(bb & lt) << bit;
+    C += __popc(bb) << bit;
   }
-  const int C = __shfl_sync(kFull, incl, 31);
   int* sel_e = rt.sel_e + m * K;
   float* sel_w = rt.sel_w + m * K;
-  if (C <= kCandMax) {
-    const int o = incl - cnt;
+  if (C < kCandMax) {
 #pragma unroll
     for (int i = 0; i < PM; ++i)
-      if (fm >> i & 1u)
-        cand[o + __popc(fm & ((1u << i) - 1u))] =
-            ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)(lane + 32 * i));
+      if (fm >> i & 1u) cand[o++] = ((unsigned long long)key[i] << 32) | (0xffffffffu - (uint32_t)(lane + 32 * i));
+    if (lane == 0) cand[C] = 0ull;  // pads the pairwise scan below (no key is 0)
     __syncwarp();
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
     for (int ci = lane; ci < C; ci += 32) {
       const unsigned long long v = cand[ci];
       int r = 0;
-      const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
 #pragma unroll 4
       for (int j = 0; j < (C + 1) / 2; ++j) {
         const ulonglong2 q = c2[j];
-        r += (q.x > v) + (2 * j + 1 < C && q.y > v);
+        r += (q.x > v) + (q.y > v);
       }
       if (r < K) sel_e[r] = key_expert(v);
     }
@@ -1081,16 +1088,24 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
   }
   __syncwarp();
   // weights in selection order: exp(l_j - l_0) / sum (softmax rule, l_0 the
-  // largest selected logit) or sigmoid(l_j) / sum (bias rule); a butterfly sum,
-  // one fixed order
+  // largest selected logit) or sigmoid(l_j) / sum (bias rule); every lane sums
+  // the K numerators in selection order
   const int ej = lane < K ? sel_e[lane] : 0;
-  const float lj = lane < K ? lg[ej] : 0.0f;
-  const float l0 = __shfl_sync(kFull, lj, 0);  // every lane takes part in the shuffle
-  const float num = lane < K ? (bias ? sigmoid_f32(lj) : expf(lj - l0)) : 0.0f;
-  float sum = num;
+  const float lj = lg[ej];
+  const float num = lane < K ? (p.score ? sigmoid_f32(lj) : expf(lj - lg[sel_e[0]])) : 0.0f;
+  wx[lane] = num;
+  __syncwarp();
+  float sum = 0.0f;
+  const float4* w4 = reinterpret_cast<const float4*>(wx);
 #pragma unroll
-  for (int d = 16; d; d >>= 1) sum += __shfl_xor_sync(kFull, sum, d);
-  __syncwarp();  // every lane has read lg before it holds weights
+  for (int j = 0; j < 4; ++j) {
+    const float4 q = w4[j];
+    sum += q.x;
+    sum += q.y;
+    sum += q.z;
+    sum += q.w;
+  }
+  __syncwarp();  // every lane has read lg and wx before they are overwritten
   if (lane < K) {
     const float w = num / sum;
     atomicOr(&rt.emask[ej], 1u << m);
@@ -1188,18 +1203,25 @@ __device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
 
 // The union for a single token row on warp 0: the K selected experts in
 // ascending id become slots S.., one pair each; the same tables as union_warp
-// builds, from K lanes and K shuffles instead of bitmap and pair prefixes.
+// builds. Each lane counts the selected ids below its own from shared memory
+// (broadcast loads, no shuffles). The gate/up split bounds of a single row do
+// not depend on the routing and were set before it (one_row_split).
 __device__ __forceinline__ void union_one_row(const Ctx& c, const Route& rt) {
   const Params& p = c.p;
   const int K = p.K, S = p.S, lane = c.lane;
   int* psr = reinterpret_cast<int*>(c.sm + p.off_pair_sr);
   const int e = lane < K ? rt.sel_e[lane] : 0x7fffffff;
-  const float w = lane < K ? rt.sel_w[lane] : 0.0f;
+  const int4* s4 = reinterpret_cast<const int4*>(rt.sel_e);  // K <= 16, 16-byte aligned
   int rank = 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j)  // K <= 16; the bound is the same on every lane
-    if (j < K) rank += __shfl_sync(kFull, e, j) < e;
+  for (int j = 0; j < 4; ++j) {
+    if (4 * j < K) {
+      const int4 q = s4[j];
+      rank += (q.x < e) + (4 * j + 1 < K && q.y < e) + (4 * j + 2 < K && q.z < e) + (4 * j + 3 < K && q.w < e);
+    }
+  }
   if (lane < K) {
+    const float w = rt.sel_w[lane];
     const int sl = S + rank;
     rt.slot_of[e] = sl;
     rt.slot_e[sl] = e;
@@ -1218,12 +1240,16 @@ __device__ __forceinline__ void union_one_row(const Ctx& c, const Route& rt) {
   if (lane == 0) {
     rt.pair_base[S + K] = S + K;
     c.misc[MISC_NROUTED] = K;
-    // every routed item has one row: the cost split is the plain split
-    int lo, hi;
-    split_range(K * p.I, blockIdx.x, p.grid, lo, hi);
-    c.misc[MISC_ULO] = lo;
-    c.misc[MISC_UHI] = hi;
   }
+}
+
+// A single row's gate/up cost split: every routed item has one row, so it is the
+// plain split of K * I items over the CTAs, known before the routing.
+__device__ __forceinline__ void one_row_split(const Ctx& c) {
+  int lo, hi;
+  split_range(c.p.K * c.p.I, blockIdx.x, c.p.grid, lo, hi);
+  c.misc[MISC_ULO] = lo;
+  c.misc[MISC_UHI] = hi;
 }
 
 // nthr threads (the first nthr / 32 consumer warps, at least p.M) route; they
@@ -1237,6 +1263,7 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
     float* bs = reinterpret_cast<float*>(c.sm + p.off_bias);
     for (int e = c.tid; e < p.E; e += nthr) bs[e] = __ldg(p.router_bias + e);
   }
+  if (c.tid == 0 && p.M == 1) one_row_split(c);
   // every CTA's router logits stored (count), before reading any of them
   if (c.tid == 0) {
     if (!c.aborted()) wait_count(c, CTRL_RCOUNT, SITE_FLAGS);
