@@ -170,15 +170,25 @@ class LayerPool:
         self.rank = rank
         self.layers = {}
 
-    def get(self, shape_name: str, shape, n: int):
+    def get(self, shape_name: str, shape, n: int, w2_layout: str = "h_i"):
         from moe_decode_layer_gb300 import synth
-        have = self.layers.setdefault(shape_name, [])
+        have = self.layers.setdefault((shape_name, w2_layout), [])
         while len(have) < n:
-            have.append(synth.make_layer(shape, seed=1000 + 97 * self.rank + len(have), device="cuda"))
+            have.append(synth.make_layer(shape, seed=1000 + 97 * self.rank + len(have), device="cuda",
+                                         w2_layout=w2_layout))
         return have[:n]
 
     def drop(self, shape_name: str):
-        self.layers.pop(shape_name, None)
+        for key in [k for k in self.layers if k[0] == shape_name]:
+            self.layers.pop(key, None)
+
+
+def w2_layout_for(args, shape) -> str:
+    """The down-matrix layout the layer copies are built with: "i_h" (transposed,
+    the split-K kernel) where --w2-layout asks for it and the format allows it."""
+    if args.w2_layout == "i_h" and shape.wdtype != "nvfp4" and args.sched == "persistent":
+        return "i_h"
+    return "h_i"
 
 
 def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, e2e_steps, cpu_seconds):
@@ -191,7 +201,7 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
     shape = synth.workload_shape(name)
     m, nl = wl["m"], wl["layers"]
     copies = nl if nl > 1 else args.copies
-    layers = pool.get(wl["shape"], shape, copies)
+    layers = pool.get(wl["shape"], shape, copies, w2_layout_for(args, shape))
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=args.sched, pre_rmsnorm=nl > 1) for i in range(copies)]
     n_in = 64
     xs = [synth.hidden_rows(m, shape.hidden, seed=50_000 + 1000 * rank + j, rho=wl["rho"]).cuda()
@@ -329,6 +339,8 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
     peak, peak_kind = measured_peak()
     if kernels_per_layer > 1:
         kernel_name = "moe_layer_kernel_chain"
+    elif mods[0].info(_lib.MOE_INFO_SPLIT_K):
+        kernel_name = "moe_sk_kernel"
     elif mods[0].info(_lib.MOE_INFO_FLAT_ROWS) >> (m - 1) & 1:
         kernel_name = "moe_flat_kernel"
     elif mods[0].info(_lib.MOE_INFO_INTERLEAVED_ROWS) >> (m - 1) & 1:
@@ -355,13 +367,14 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if shape.wdtype == "bf16" else "nvfp4",
+        "dtype": shape.wdtype,
         "data": "synthetic",
         "config": {
             "workload": f"{name}: {wl['desc']}",
             "rows_M": m,
             "layers_per_step": nl,
             "sched": args.sched,
+            "w2_layout": w2_layout_for(args, shape),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "launch": (f"CUDA graph replay of exactly {K} steps (a {P}-step graph x {K // P}"
                        + (f" + a {R}-step graph" if R else "") + ")"),
@@ -546,6 +559,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sched", default="persistent",
                     choices=["persistent", "phased", "interleaved", "flat", "pdl_chain", "chain"])
+    ap.add_argument("--w2-layout", default="h_i", choices=["h_i", "i_h"],
+                    help="down matrices [E,H,I] (row-block kernels) or transposed [E,I,H] (split-K kernel; "
+                         "bf16 and fp8 workloads under --sched persistent)")
     ap.add_argument("--copies", type=int, default=8, help="distinct layer copies (single-layer workloads)")
     ap.add_argument("--lat-steps", type=int, default=256, help="single steps for the latency percentiles (>= 200)")
     ap.add_argument("--e2e-steps", type=int, default=500)

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define MOE_DECODE_ABI_VERSION 2
+#define MOE_DECODE_ABI_VERSION 3
 
 /* A cudaStream_t. NULL means the legacy default stream. */
 typedef struct CUstream_st* moe_stream_t;
@@ -76,6 +76,23 @@ typedef enum moe_score {
                                         The bias steers the choice only.                   */
 } moe_score;
 
+/*
+ * Layout of the down matrices (w2, sh_w2 and, for FP8, their block scales).
+ * MOE_W2_I_H stores each expert's down matrix transposed, so that the down
+ * weights of one intermediate row are one contiguous row. A handle built with it
+ * runs the split-K single kernel: each CTA applies the down projection to the
+ * intermediate rows it computed itself and the output is a fixed-order sum of
+ * every CTA's partial sums ("Muse Spark Open Ultrafast", section "A new tensor
+ * parallelism": the second expert GEMM split on the intermediate dimension with
+ * one reduction at the end, here across the CTAs of one GPU). The layer computed
+ * is the same; the order of the down projection's sums differs.
+ */
+typedef enum moe_w2_layout {
+  MOE_W2_H_I = 0,  /* w2 [E, H, I] (output rows), the default                      */
+  MOE_W2_I_H = 1   /* w2 [E, I, H] (intermediate rows); bf16 or FP8, hidden <= 3072,
+                      MOE_SCHED_PERSISTENT only                                     */
+} moe_w2_layout;
+
 typedef enum moe_sched {
   MOE_SCHED_PERSISTENT = 0, /* one cooperative kernel; phases hand off through tagged data */
   MOE_SCHED_PDL_CHAIN = 1,  /* three kernels (router, gate/up, down) chained with PDL      */
@@ -108,6 +125,7 @@ typedef struct moe_decode_config {
   int32_t pre_rmsnorm; /* 1: the layer input is bf16(RMSNorm(x)), gamma = 1  */
   float rms_eps;       /* RMSNorm epsilon (1e-6)                              */
   int32_t sched;       /* moe_sched                                           */
+  int32_t w2_layout;   /* moe_w2_layout                                       */
 } moe_decode_config;
 
 /*
@@ -124,6 +142,8 @@ typedef struct moe_decode_config {
  *   fp8:    w13     uint8 [E, 2I, H]   e4m3 codes; w13_scale fp32 [E, 2I/128, H/128]
  *           w2      uint8 [E, H, I]    e4m3 codes; w2_scale  fp32 [E, H/128, I/128]
  *           (w = e4m3(code) * scale[row / 128][col / 128]; gscale pointers unused)
+ *   w2_layout MOE_W2_I_H: w2 bf16 [E, I, H]; fp8 w2 uint8 [E, I, H] with
+ *           w2_scale fp32 [E, I/128, H/128] (the transpose of the tensors above)
  *   sh_*            the same for the S shared experts (leading dim S)
  *   router_bias     fp32  [E] selection bias, 4-byte aligned (MOE_SCORE_SIGMOID_BIAS)
  * Unused pointers (scales for bf16, shared for S = 0, the bias under softmax
@@ -163,8 +183,9 @@ moe_status moe_decode_config_check(const moe_decode_config* cfg);
  * `smem_optin` bytes of opt-in shared memory per block, computed on the host
  * (no CUDA call). `interleaved` = 1 asks for the slot-interleaved single kernel's
  * layout, 2 for the expert-range kernel's (MOE_ERR_UNSUPPORTED when it does not
- * fit), 0 for the phase-ordered kernels'. All fields in bytes or counts; filled
- * only on MOE_OK.
+ * fit), 0 for the phase-ordered kernels'. A config with w2_layout MOE_W2_I_H has
+ * one layout, the split-K kernel's (interleaved must be 0). All fields in bytes
+ * or counts; filled only on MOE_OK.
  */
 typedef struct moe_decode_plan_info {
   int32_t smem_bytes;        /* dynamic shared memory per CTA (incl. alignment slack)   */
@@ -183,6 +204,8 @@ typedef struct moe_decode_plan_info {
   int32_t lag;               /* interleaved: down stage of slot s after the gate/up of s+lag */
   int32_t down_h_offset;     /* interleaved: h rows' offset in a down stage's slot        */
   int32_t threads;           /* threads per CTA                                           */
+  int32_t h_rows_max;        /* split-K (w2_layout MOE_W2_I_H): h rows one CTA holds      */
+  int32_t down_t_rows_per_stage; /* split-K: transposed down rows per stage             */
 } moe_decode_plan_info;
 moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t smem_optin, int32_t interleaved,
                            moe_decode_plan_info* out);
@@ -280,7 +303,9 @@ enum {
   MOE_INFO_INTERLEAVED_ROWS = 23, /* bit m-1 set: a run of m rows under the current
                                     schedule and options takes the slot-interleaved
                                     kernel                                         */
-  MOE_INFO_FLAT_ROWS = 24        /* the same for the expert-range kernel            */
+  MOE_INFO_FLAT_ROWS = 24,       /* the same for the expert-range kernel            */
+  MOE_INFO_SPLIT_K = 25          /* 1: the handle runs the split-K kernel (w2_layout
+                                    MOE_W2_I_H)                                       */
 };
 moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value);
 moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value);
@@ -301,8 +326,9 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
  * every GPU loading the library holds until exit. Configs whose scratch
  * (control words, 4 copies of the M x E logits as 8-byte words, 4 copies of the
  * I fp32 intermediate values of each of the S*M + k*M (expert, row) pairs, one
- * flag per SM) exceeds it
- * return MOE_ERR_UNSUPPORTED before any device work. The first call on a device
+ * flag per SM) exceeds it, and configs with w2_layout MOE_W2_I_H (the split-K
+ * kernel's partial sums need grid x grid blocks), return MOE_ERR_UNSUPPORTED
+ * before any device work. The first call on a device
  * sets the array up (resolves its device address and fills it, a blocking
  * memset). The array's address is looked up again on every call; a call that
  * finds it moved (the module was reloaded, as after cudaDeviceReset) sets the new

@@ -25,6 +25,9 @@ MOE_W_FP8_BLOCK = 2
 WDTYPE = {"bf16": MOE_W_BF16, "nvfp4": MOE_W_NVFP4, "fp8": MOE_W_FP8_BLOCK}
 MOE_SCORE_SOFTMAX_TOPK_RENORM = 0
 MOE_SCORE_SIGMOID_BIAS = 1
+MOE_W2_H_I = 0
+MOE_W2_I_H = 1
+W2_LAYOUT = {"h_i": MOE_W2_H_I, "i_h": MOE_W2_I_H}
 MOE_SCHED_PERSISTENT = 0
 MOE_SCHED_PDL_CHAIN = 1
 MOE_SCHED_CHAIN = 2
@@ -54,6 +57,7 @@ MOE_INFO_KERNELS_PER_RUN = 21
 MOE_INFO_SCRATCH_BYTES = 22
 MOE_INFO_INTERLEAVED_ROWS = 23
 MOE_INFO_FLAT_ROWS = 24
+MOE_INFO_SPLIT_K = 25
 STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTS = ("moe_decode_config_check", "moe_decode_plan", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",
@@ -68,7 +72,8 @@ class Config(ctypes.Structure):
                 ("num_shared", ctypes.c_int32), ("max_rows", ctypes.c_int32),
                 ("wdtype", ctypes.c_int32), ("score", ctypes.c_int32),
                 ("routed_scale", ctypes.c_float), ("pre_rmsnorm", ctypes.c_int32),
-                ("rms_eps", ctypes.c_float), ("sched", ctypes.c_int32)]
+                ("rms_eps", ctypes.c_float), ("sched", ctypes.c_int32),
+                ("w2_layout", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -81,7 +86,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "smem_bytes", "ring_slots", "slot_bytes", "extra_slots", "down_slot_in_x", "pairs_per_stage",
         "router_pairs_per_stage", "down_rows_per_stage", "h_pairs", "h_buffers", "h_per_slot", "slots_max",
-        "pairs_max", "lag", "down_h_offset", "threads")]
+        "pairs_max", "lag", "down_h_offset", "threads", "h_rows_max", "down_t_rows_per_stage")]
 
 
 class MoEDecodeError(RuntimeError):

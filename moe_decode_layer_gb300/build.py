@@ -25,7 +25,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_decode.so")
 
-SOURCES = ["api.cu", "kernels_bf16.cu", "kernels_nvfp4.cu", "kernels_fp8.cu", "kernels_flat.cu", "static_run.cu"]
+SOURCES = ["api.cu", "kernels_bf16.cu", "kernels_nvfp4.cu", "kernels_fp8.cu", "kernels_flat.cu", "kernels_sk.cu", "static_run.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
          "--expt-relaxed-constexpr"]

@@ -22,6 +22,7 @@ struct moe_decode_handle {
   Params flat;       // the same for the expert-range single kernel (when has_flat)
   bool has_ilv = false;
   bool has_flat = false;
+  bool sk = false;    // down matrices transposed: the split-K single kernel only
   int ilv_mode = 1;   // MOE_OPT_INTERLEAVE
   int flat_mode = 0;  // MOE_OPT_FLAT
   int device = 0;
@@ -59,6 +60,20 @@ moe_status check_config(const moe_decode_config* c) {
   if (c->num_shared > 4 || c->max_rows > moe::kMaxRowsRun) return MOE_ERR_UNSUPPORTED;
   if (!std::isfinite(c->routed_scale)) return MOE_ERR_INVALID_ARG;
   if (c->pre_rmsnorm && !(c->rms_eps > 0.0f && std::isfinite(c->rms_eps))) return MOE_ERR_INVALID_ARG;
+  if (c->w2_layout != MOE_W2_H_I && c->w2_layout != MOE_W2_I_H) return MOE_ERR_UNSUPPORTED;
+  if (c->w2_layout == MOE_W2_I_H) {
+    // the split-K kernel: every output column of the transposed down rows to one
+    // consumer thread (8 per thread), one persistent kernel
+    if (c->sched != MOE_SCHED_PERSISTENT || H / 8 > moe::kNC * 32) return MOE_ERR_UNSUPPORTED;
+    if (c->wdtype == MOE_W_BF16) {
+      if (H % 8 || H < 64 || I % 8) return MOE_ERR_UNSUPPORTED;
+    } else if (c->wdtype == MOE_W_FP8_BLOCK) {
+      if (H % moe::kFp8Block || I % moe::kFp8Block) return MOE_ERR_UNSUPPORTED;
+    } else {
+      return MOE_ERR_UNSUPPORTED;
+    }
+    return MOE_OK;
+  }
   if (c->wdtype == MOE_W_BF16) {
     if (H % 8 || H < 64 || H > 4096) return MOE_ERR_UNSUPPORTED;
     const int tg = I / 8;
@@ -304,6 +319,99 @@ moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params
   return MOE_OK;
 }
 
+// The layout of the split-K single kernel (moe_sk.cuh; down matrices stored
+// transposed): the shape fields of plan(), then its own shared memory -- this
+// CTA's h rows and their tags, the routing scratch (overlapping the h rows:
+// routing is over before any is stored), and a ring of gate/up stages (q row
+// pairs) and transposed-down stages (dq rows). At the end the ring holds the
+// CTA's block of every CTA's partial sums. MOE_ERR_UNSUPPORTED when the kernel
+// does not cover cfg (bf16 or FP8 weights, H <= 8 * kNC * 32).
+moe_status plan_sk(const moe_decode_config& c, int sms, int smem_optin, Params& p) {
+  moe_status st = plan(c, sms, smem_optin, p, false);
+  if (st != MOE_OK) return st;
+  if (p.fmt == moe::FMT_NVFP4 || p.H / 8 > moe::kNC * 32 || p.H % 8) return MOE_ERR_UNSUPPORTED;
+  const int H = p.H, I = p.I, E = p.E, K = p.K, S = p.S, maxm = p.maxm, G = p.grid;
+  p.w2t = 1;
+  p.item_base = p.fmt == moe::FMT_BF16 ? 6 : 3;  // as the row-block schedules: cost of an item with N rows
+  // h rows one CTA may hold: its share of the shared experts' rows plus the
+  // largest routed share the cost split can give (items cost item_base + N with
+  // 1 <= N <= maxm, so a share holds at most (base + maxm) / (base + 1) times the
+  // average, plus the items cut at both ends)
+  const long long base = p.item_base;
+  const long long routed = (long long)std::min(E, maxm * K) * I;
+  const long long tcost = routed * (base + maxm);
+  p.sk_rows_max = (int)((long long)(S * I + G - 1) / G + ((tcost + G - 1) / G + base) / (base + 1) + 4);
+  size_t off = 0;
+  auto take = [&](size_t bytes, size_t align) {
+    off = round_up(off, align);
+    const size_t at = off;
+    off += bytes;
+    return static_cast<int>(at);
+  };
+  p.off_full = take(moe::kMaxSlots * 8, 8);
+  p.off_empty = take(moe::kMaxSlots * 8, 8);
+  p.off_xbar = take(8, 8);
+  p.off_psb = take(8, 8);
+  p.off_slot_seq = take(moe::kMaxSlots * 4, 4);
+  p.off_x = take((size_t)maxm * H * 2, 128);
+  p.off_sel_e = take(((size_t)maxm * K * 4 + 15) / 16 * 16 + 16, 16);  // read in 16-byte groups by the one-row union
+  p.off_sel_w = take((size_t)maxm * K * 4, 4);
+  p.off_emask = take((size_t)E * 4, 4);
+  p.off_bitmap = take((size_t)(E + 31) / 32 * 4, 4);
+  p.off_slot_of = take((size_t)E * 4, 4);
+  p.off_slot_e = take((size_t)p.nslot_max * 4, 4);
+  p.off_slot_mask = take((size_t)p.nslot_max * 4, 4);
+  p.off_slot_w = take((size_t)p.nslot_max * maxm * 4, 4);
+  p.off_pair_base = take((size_t)(p.nslot_max + 1) * 4, 4);
+  p.off_pair_sr = take((size_t)p.npair_max * 4, 4);
+  p.off_red = take((size_t)moe::kNC * 8 * 4, 16);  // the router's partial dot products
+  p.off_misc = take(moe::MISC_WORDS * 4, 16);
+  p.off_psum = take((size_t)moe::kNC * 32 * 4, 16);
+  // offsets of the other kernels' areas, unused here
+  p.off_xfree = p.off_hbar = p.off_ucnt = p.off_dslot = p.off_xslot = p.off_acnt = 0;
+  p.off_htag = take((size_t)p.sk_rows_max * 4, 16);
+  p.off_bias = p.score ? take((size_t)E * 4, 16) : 0;
+  const size_t fixed = round_up(off, 128);
+  p.off_hsk = (int)fixed;
+  p.off_hs = (int)fixed;
+  size_t ro = fixed;
+  auto rtake = [&](size_t bytes, size_t align) {
+    ro = round_up(ro, align);
+    const size_t at = ro;
+    ro += bytes;
+    return static_cast<int>(at);
+  };
+  p.off_lg = rtake((size_t)maxm * E * 4, 16);
+  p.off_cand = rtake((size_t)maxm * moe::kCandMax * 8, 16);
+  p.off_lmax = rtake((size_t)maxm * 32 * 4, 16);
+  p.off_thr = rtake((size_t)maxm * 8, 8);
+  p.off_ccount = rtake((size_t)maxm * 4, 4);
+  p.off_wtmp = rtake((size_t)maxm * 16 * 4, 16);
+  p.off_wpc = rtake(32 * 4, 16);
+  p.off_ring = (int)round_up(std::max(ro, fixed + (size_t)p.sk_rows_max * maxm * 4), 1024);
+  const size_t rowt = (size_t)H * (p.fmt == moe::FMT_BF16 ? 2 : 1);  // one transposed down row
+  const size_t q0 = std::max<size_t>(1, std::min<size_t>(moe::kNC, moe::kStageTarget / p.pair_bytes));
+  const size_t slot = round_up(std::max({q0 * p.pair_bytes, (size_t)p.rpair_bytes, (size_t)p.pair_bytes, rowt}), 128);
+  const long long ring_budget = (long long)smem_optin - 1024 - p.off_ring;
+  const long long ns = ring_budget > 0 ? ring_budget / (long long)slot : 0;
+  if (ns < 3) return MOE_ERR_UNSUPPORTED;
+  p.slot_bytes = (int)slot;
+  p.nslots = (int)std::min<long long>(ns, moe::kMaxSlots);
+  p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
+  p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
+  p.dq = (int)(p.slot_bytes / rowt);
+  p.sk_lag = p.q;
+  // the final reduction stages this CTA's block of every CTA's partial sums in the ring
+  p.nrp = (int)round_up((size_t)(H + G - 1) / G, 4);
+  if ((long long)G * maxm * p.nrp * 4 > (long long)p.nslots * p.slot_bytes || (long long)G * maxm * p.nrp * 4 >= (1 << 20))
+    return MOE_ERR_UNSUPPORTED;
+  p.nslots_x = p.nslots_d = p.hs_pairs = p.hs_perslot = 0;
+  p.hs_nbuf = 1;
+  p.d_rows_stage = p.dq;
+  p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
+  return MOE_OK;
+}
+
 const void* kernel_for(const Params& p, int maxm_t, int phases) {
   return p.fmt == moe::FMT_BF16    ? moe::kernel_bf16(maxm_t, phases)
          : p.fmt == moe::FMT_NVFP4 ? moe::kernel_nvfp4(maxm_t, phases)
@@ -363,11 +471,11 @@ void bind_pointers(const Params& from, Params& to) {
 // Whether a persistent run of m rows takes the expert-range kernel: always when
 // forced (mode 2), else (mode 1) where it measured faster on GB300.
 bool use_flat(const moe_decode_handle* h, int m) {
-  if (h->sched != MOE_SCHED_PERSISTENT || !h->has_flat) return false;
+  if (h->sk || h->sched != MOE_SCHED_PERSISTENT || !h->has_flat) return false;
   return h->flat_mode == 2 || (h->flat_mode == 1 && m == 1);
 }
 bool interleaved(const moe_decode_handle* h, int m) {
-  if (h->sched != MOE_SCHED_PERSISTENT || !h->has_ilv || use_flat(h, m)) return false;
+  if (h->sk || h->sched != MOE_SCHED_PERSISTENT || !h->has_ilv || use_flat(h, m)) return false;
   return h->ilv_mode == 2 || (h->ilv_mode == 1 && h->base.fmt == moe::FMT_BF16 && m == 1);
 }
 // The layout a run of m rows uses.
@@ -394,7 +502,9 @@ moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.numAttrs = 1;
-    const void* k = flat ? moe::kernel_flat(maxm_t) : kernel_for(p, maxm_t, ilv ? moe::PH_ILV : moe::PH_ALL);
+    const void* k = h->sk ? moe::kernel_sk(p.fmt, maxm_t)
+                    : flat ? moe::kernel_flat(maxm_t)
+                           : kernel_for(p, maxm_t, ilv ? moe::PH_ILV : moe::PH_ALL);
     if (cudaLaunchKernelExC(&cfg, k, args) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
@@ -464,9 +574,13 @@ moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t sm
   moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
   Params p;
-  if ((st = interleaved == 2 ? plan_flat(*cfg, sms, smem_optin, p)
-                             : plan(*cfg, sms, smem_optin, p, interleaved != 0)) != MOE_OK)
-    return st;
+  if (cfg->w2_layout == MOE_W2_I_H) {  // one layout: the split-K kernel's
+    if (interleaved != 0) return MOE_ERR_UNSUPPORTED;
+    st = plan_sk(*cfg, sms, smem_optin, p);
+  } else {
+    st = interleaved == 2 ? plan_flat(*cfg, sms, smem_optin, p) : plan(*cfg, sms, smem_optin, p, interleaved != 0);
+  }
+  if (st != MOE_OK) return st;
   out->smem_bytes = p.smem_bytes;
   out->ring_slots = p.nslots;
   out->slot_bytes = p.slot_bytes;
@@ -483,6 +597,8 @@ moe_status moe_decode_plan(const moe_decode_config* cfg, int32_t sms, int32_t sm
   out->lag = interleaved == 1 ? p.ilv_lag : 0;
   out->down_h_offset = interleaved == 1 ? p.d_hoff : 0;
   out->threads = interleaved == 2 ? moe::kThreadsFlat : interleaved ? moe::kThreadsIlv : moe::kThreads;
+  out->h_rows_max = p.sk_rows_max;
+  out->down_t_rows_per_stage = p.dq;
   return MOE_OK;
 }
 
@@ -499,14 +615,26 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   Params p, pi;
-  if ((st = plan(*cfg, sms, optin, p, false)) != MOE_OK) return st;
-  const bool has_ilv = kernel_for(p, 1, moe::PH_ILV) != nullptr && plan(*cfg, sms, optin, pi, true) == MOE_OK;
+  const bool sk = cfg->w2_layout == MOE_W2_I_H;
+  if ((st = sk ? plan_sk(*cfg, sms, optin, p) : plan(*cfg, sms, optin, p, false)) != MOE_OK) return st;
+  const bool has_ilv =
+      !sk && kernel_for(p, 1, moe::PH_ILV) != nullptr && plan(*cfg, sms, optin, pi, true) == MOE_OK;
   Params pf;
-  bool has_flat = plan_flat(*cfg, sms, optin, pf) == MOE_OK;
+  bool has_flat = !sk && plan_flat(*cfg, sms, optin, pf) == MOE_OK;
   // Every kernel this handle may launch gets the shared-memory size, and one
   // CTA of the single-kernel schedule must fit on every SM.
   const int phases[4] = {moe::PH_ALL, moe::PH_R, moe::PH_U, moe::PH_D};
   for (int mt : {1, 8}) {
+    if (sk) {
+      const void* k = moe::kernel_sk(p.fmt, mt);
+      int blocks = 0;
+      if (!k) return MOE_ERR_UNSUPPORTED;
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, moe::kThreads, p.smem_bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (blocks < 1) return MOE_ERR_UNSUPPORTED;
+      continue;
+    }
     for (int ph : phases) {
       const void* k = kernel_for(p, mt, ph);
       if (!k) return MOE_ERR_UNSUPPORTED;
@@ -551,6 +679,8 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   // expert-range kernel: tagged per-(block, slot, row) outputs
   const size_t o_y = has_flat ? take((size_t)p.grid * p.nslot_max * maxm * pf.flat_rb * 8) : 0;
   const size_t tag_end = off;
+  // split-K kernel: every CTA's partial sums, by destination block
+  const size_t o_ps = sk ? take((size_t)p.grid * p.grid * p.maxm * p.nrp * 4) : 0;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
   const size_t o_so = take(maxm * H * 2);
@@ -602,6 +732,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
   p.hbuf = reinterpret_cast<float*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
+  if (sk) p.psum = reinterpret_cast<float*>(base + o_ps);
 
   h->stage_x = reinterpret_cast<uint16_t*>(base + o_sx);
   h->stage_r = reinterpret_cast<uint16_t*>(base + o_sr);
@@ -612,6 +743,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->max_slots = p.nslots;
   h->has_ilv = has_ilv;
   h->has_flat = has_flat;
+  h->sk = sk;
   h->max_slots_flat = has_flat ? pf.nslots : 0;
   if (has_flat) {
     bind_pointers(p, pf);
@@ -710,6 +842,7 @@ moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t v
   switch (option) {
     case MOE_OPT_SCHED:
       if (value < MOE_SCHED_PERSISTENT || value > MOE_SCHED_CHAIN) return MOE_ERR_INVALID_ARG;
+      if (h->sk && value != MOE_SCHED_PERSISTENT) return MOE_ERR_UNSUPPORTED;  // one kernel for transposed down rows
       h->sched = (int)value;
       return MOE_OK;
     case MOE_OPT_WAIT_TIMEOUT_NS:
@@ -754,6 +887,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_OPT_STAMPS: *value = (int64_t)reinterpret_cast<uintptr_t>(h->base.stamps); return MOE_OK;
     case MOE_OPT_INTERLEAVE: *value = h->has_ilv ? h->ilv_mode : 0; return MOE_OK;
     case MOE_OPT_FLAT: *value = h->has_flat ? h->flat_mode : 0; return MOE_OK;
+    case MOE_INFO_SPLIT_K: *value = h->sk ? 1 : 0; return MOE_OK;
     case MOE_INFO_FLAT_ROWS: {
       int64_t mask = 0;
       for (int m = 1; m <= h->cfg.max_rows; ++m)

@@ -9,4 +9,7 @@ const void* kernel_nvfp4(int maxm_t, int phases);
 const void* kernel_fp8(int maxm_t, int phases);
 // The expert-range single kernel (bf16 weights) for maxm_t in {1, 8}.
 const void* kernel_flat(int maxm_t);
+// The split-K single kernel (down matrices transposed) for fmt in {FMT_BF16,
+// FMT_FP8} and maxm_t in {1, 8}.
+const void* kernel_sk(int fmt, int maxm_t);
 }  // namespace moe

@@ -837,9 +837,12 @@ __device__ __forceinline__ Ring consume_router(const Ctx& c, Ring ring) {
 // the x rows that chose the expert, SwiGLU and the combine weight, h stored in
 // pair order (four copies); the slot is handed back for the absent warps too.
 template <int FMT, int MAXM>
+// hsk / htag (split-K schedule): the h values go to this CTA's shared-memory rows
+// (hsk[iq * maxm + m], the stage's first row at hsk) and the row's tag is set once
+// they are stored, instead of to the global h rows.
 __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const ItemWalk& w, const Ring& ring,
                                            int slot, bool shared, const XRegs<FMT, MAXM>& xr, const uint4* xs,
-                                           bool first) {
+                                           bool first, float* hsk = nullptr, volatile int* htag = nullptr) {
   const Params& p = c.p;
   const size_t rep_stride = (size_t)p.npair_max * p.I;
   const int nq = w.count();
@@ -880,6 +883,9 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
                                 : silu_f32(rs.g * gsg) * (rs.u * gsu);
       if (!shared) h *= rt.slot_w[slot * p.maxm + rs.m];
       if (FMT == FMT_NVFP4) h *= gs2;
+      if (hsk) {
+        hsk[iq * p.maxm + rs.m] = h;
+      } else {
       // pair index: a shared slot holds every row (pairs s * M + m); a routed
       // slot's rows follow its pair base in ascending order
       const int pair = shared ? slot * p.M + rs.m : rt.pair_base[slot] + __popc(mask & ((1u << rs.m) - 1u));
@@ -890,9 +896,16 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
       if (FMT == FMT_NVFP4) at = (size_t)pair * p.I + (size_t)((j % 32) >> 2) * (4 * p.tg) + 4 * (j / 32) + (j & 3);
 #pragma unroll
       for (int r = 0; r < kHRep; ++r) p.hbuf[r * rep_stride + at] = h;
+      }
     }
     __syncwarp();
-    if (c.lane == 0) c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
+    if (c.lane == 0) {
+      if (htag) {
+        __threadfence_block();  // the row's h values (every lane's, ordered by the warp barrier) before its tag
+        htag[iq] = 1;
+      }
+      c.release(ring, iq == 0 ? (uint32_t)(kNC - nq + 1) : 1u);
+    }
   }
 }
 

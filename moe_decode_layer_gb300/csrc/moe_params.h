@@ -36,6 +36,10 @@ constexpr int PH_ILV = 8;
 // Kernel selector: the expert-range single kernel (each CTA owns a contiguous
 // range of (expert, gate/up row) items and of (expert, output block) down stages).
 constexpr int PH_FLAT = 16;
+// Kernel selector: the split-K single kernel (down matrices stored transposed;
+// each CTA applies the down projection to the h rows it computed and the output
+// is a fixed-order sum of every CTA's partial sums).
+constexpr int PH_SK = 32;
 constexpr int kThreadsFlat = kThreadsIlv;  // consumers, producer, publisher, fetcher
 constexpr int kFlatSegs = 3;               // down segments per CTA: shared block + <= 2 routed slots
 constexpr int kFlatMaxChunks = 128;        // 16-byte chunks of a down row (I <= 1024 bf16)
@@ -182,6 +186,17 @@ struct Params {
                              // output of output block b (run tag << 32 | fp32 bits)
   int flat_rb;         // rows of the largest output block, rounded up to even
   int off_acnt;        // [nslot_max] consumer warps done with a slot's gate/up items
+  // split-K down schedule (down matrices stored transposed, [I][H] per expert)
+  int w2t;             // 1: w2 / sh_w2 (and FP8 scales) are [E][I][H] ([E][I/128][H/128])
+  int dq;              // transposed down rows per down stage
+  int sk_lag;          // a down stage follows the gate/up stages of its rows by this many rows
+  int sk_rows_max;     // h rows one CTA may hold (checked on the device)
+  int nrp;             // output rows per CTA block, padded to a multiple of 4
+  int off_hsk;         // [sk_rows_max][maxm] fp32 h of this CTA's rows
+  int off_htag;        // [sk_rows_max] 1 once the row's h is stored
+  int off_psb;         // mbarrier: the partial-sum block of this CTA landed
+  int off_psum;        // [nrp] x (parts) fp32 staging for the fixed-order reduction
+  float* psum;         // [grid (destination)][grid (source)][M][nrp] fp32 partial sums
 };
 
 }  // namespace moe

@@ -65,6 +65,8 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
                                             int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
   moe_status st = moe::check_config_host(cfg);
   if (st != MOE_OK) return st;
+  // the split-K kernel's partial sums (grid x grid blocks) do not fit the static array
+  if (cfg->w2_layout != MOE_W2_H_I) return MOE_ERR_UNSUPPORTED;
   if (!x || !residual || !out || m_rows < 1 || m_rows > cfg->max_rows) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))

@@ -33,7 +33,8 @@ class MoEDecodeLayer:
     slot-interleaved kernel where that measured faster), "phased" (one kernel,
     phases in order), "interleaved" (one kernel, slot-interleaved whenever its
     layout fits), "flat" (the expert-range kernel whenever its layout fits),
-    "pdl_chain" or "chain" (three kernels).
+    "pdl_chain" or "chain" (three kernels). Weights whose ``w2_layout`` is "i_h"
+    (down matrices transposed) run the split-K kernel, under "persistent" only.
     """
 
     def __init__(self, shape: LayerShape, weights: dict, max_rows: int, sched: str = "persistent",
@@ -49,7 +50,8 @@ class MoEDecodeLayer:
                           score=score, routed_scale=routed_scale,
                           pre_rmsnorm=int(pre_rmsnorm), rms_eps=rms_eps,
                           sched=_lib.SCHED_NAMES["persistent" if sched in ("phased", "interleaved", "flat")
-                                                  else sched])
+                                                  else sched],
+                          w2_layout=_lib.W2_LAYOUT[weights.get("w2_layout", "h_i")])
         w = _lib.Weights()
         g = weights.get
         w.router_w = _ptr(g("router_w"))

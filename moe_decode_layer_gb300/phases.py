@@ -21,11 +21,11 @@ from .layer import MoEDecodeLayer
 
 
 def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: str = "persistent",
-             n_inputs: int = 64):
+             n_inputs: int = 64, w2_layout: str = "h_i"):
     wl = synth.WORKLOADS[workload]
     shape = synth.workload_shape(workload)
     m = wl["m"]
-    layers = [synth.make_layer(shape, seed=2000 + i, device="cuda") for i in range(copies)]
+    layers = [synth.make_layer(shape, seed=2000 + i, device="cuda", w2_layout=w2_layout) for i in range(copies)]
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=sched) for i in range(copies)]
     grid = mods[0].info(_lib.MOE_INFO_GRID)
     stamps = torch.zeros((grid, _lib.STAMP_SLOTS), dtype=torch.int64, device="cuda")
@@ -94,11 +94,13 @@ def main():
     ap.add_argument("--sweep-ring", default="", help="comma list of ring slot counts to compare")
     ap.add_argument("--hot", action="store_true", help="one layer copy and one input: weights stay in L2")
     ap.add_argument("--sched", default="persistent", help="schedule (see MoEDecodeLayer)")
+    ap.add_argument("--w2-layout", default="h_i", choices=["h_i", "i_h"],
+                    help="down matrices as stored: i_h (transposed) runs the split-K kernel")
     a = ap.parse_args()
     sweep = [int(v) for v in a.sweep_ring.split(",") if v] or [a.ring_slots]
     for rs in sweep:
         rows, total, used = timeline(a.workload, 1 if a.hot else a.copies, a.runs, rs, sched=a.sched,
-                                     n_inputs=1 if a.hot else 64)
+                                     n_inputs=1 if a.hot else 64, w2_layout=a.w2_layout)
         print(f"# {a.workload} [{a.sched}]{' (hot: weights in L2)' if a.hot else ''}: ring slots {used}, "
               f"median first-entry -> last-exit {total:.2f} us")
         print(f"{'event':>16} {'median':>8} {'p10':>8} {'p90':>8} {'max':>8}")

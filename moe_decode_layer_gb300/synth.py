@@ -247,8 +247,23 @@ def _fp8_experts(n, inter, hidden, seed, device, std):
     return w13q, w13s, w2q, w2s
 
 
-def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) -> dict:
+def _transpose_experts(w: torch.Tensor, chunk_bytes=1 << 29) -> torch.Tensor:
+    """[n, a, b] -> [n, b, a] contiguous, a few experts at a time."""
+    n, a, b = w.shape
+    out = torch.empty((n, b, a), dtype=w.dtype, device=w.device)
+    per = max(1, chunk_bytes // max(1, a * b * w.element_size()))
+    for s in range(0, n, per):
+        out[s:s + per] = w[s:s + per].transpose(1, 2)
+    return out
+
+
+def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02, w2_layout: str = "h_i") -> dict:
     """All weights of one layer as torch tensors on ``device``.
+
+    ``w2_layout`` "i_h" stores the down matrices (and FP8 down scales) transposed,
+    [E, I, H] ([E, I/128, H/128]), for the split-K kernel; the weight values are
+    the same as with "h_i" for the same seed. The dict records the layout under
+    "w2_layout".
 
     bf16:  router_w [E, H], w13 [E, 2I, H], w2 [E, H, I], sh_w13 [S, 2I, H], sh_w2 [S, H, I]
     nvfp4: router_w bf16 [E, H]; w13_q uint8 [E, 2I, H/2], w13_s uint8 [E, 2I, H/16],
@@ -279,4 +294,12 @@ def make_layer(shape: LayerShape, seed: int, device="cpu", std: float = 0.02) ->
             layer["sh_" + n] = t
     else:
         raise ValueError(f"unknown weight dtype {shape.wdtype!r}")
+    if w2_layout == "i_h":
+        if shape.wdtype == "nvfp4":
+            raise ValueError("transposed down matrices are bf16 or fp8 only")
+        for n in (("w2", "sh_w2") if shape.wdtype == "bf16" else ("w2_q", "w2_s", "sh_w2_q", "sh_w2_s")):
+            layer[n] = _transpose_experts(layer[n])
+    elif w2_layout != "h_i":
+        raise ValueError(f"unknown down-matrix layout {w2_layout!r}")
+    layer["w2_layout"] = w2_layout
     return layer

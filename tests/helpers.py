@@ -58,13 +58,20 @@ def hidden_with_margin(router_w: torch.Tensor, m_rows: int, top_k: int, seed: in
 def expert_accessor(shape: synth.LayerShape, layer: dict, prefix: str = ""):
     """e -> the raw weights of expert e for the C++ oracle, copied from the layer
     tensors on demand: bf16 bit patterns (w13 [2I, H], w2 [H, I]) or an NVFP4
-    expert (codes, e4m3 scale bytes, tensor scales)."""
+    expert (codes, e4m3 scale bytes, tensor scales). Down matrices stored
+    transposed (w2_layout "i_h") are handed over in the [H, I] orientation."""
+    t = layer.get("w2_layout", "h_i") == "i_h"
+
+    def down(name, e):
+        w = layer[prefix + name][e]
+        return w.transpose(0, 1).contiguous() if t else w
+
     def get(e):
         if shape.wdtype == "bf16":
-            return bits(layer[prefix + "w13"][e]), bits(layer[prefix + "w2"][e])
+            return bits(layer[prefix + "w13"][e]), bits(down("w2", e))
         if shape.wdtype == "fp8":
             return cpp.FP8Expert(bits(layer[prefix + "w13_q"][e]), layer[prefix + "w13_s"][e].cpu().numpy(),
-                                 bits(layer[prefix + "w2_q"][e]), layer[prefix + "w2_s"][e].cpu().numpy())
+                                 bits(down("w2_q", e)), down("w2_s", e).cpu().numpy())
         return cpp.NVFP4Expert(bits(layer[prefix + "w13_q"][e]), bits(layer[prefix + "w13_s"][e]),
                                layer[prefix + "w13_gs"][e].cpu().numpy(), bits(layer[prefix + "w2_q"][e]),
                                bits(layer[prefix + "w2_s"][e]), np.float32(layer[prefix + "w2_gs"][e].cpu()))

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported():
 
 def test_abi_version_and_strings():
     lib = _lib.load()
-    assert lib.moe_decode_abi_version() == 2
+    assert lib.moe_decode_abi_version() == 3
     for s in range(6):
         assert _lib.status_string(s)
     assert _lib.status_string(0) == "ok"

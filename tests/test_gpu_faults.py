@@ -24,11 +24,15 @@ def tiny():
     return synth.make_layer(synth.TINY, seed=0, device="cuda")
 
 
-@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "flat", "pdl_chain", "chain"])
+@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "flat", "pdl_chain", "chain", "split_k"])
 @pytest.mark.parametrize("m", [1, 2])
 def test_withheld_router_results_time_out(tiny, sched, m):
+    layer = tiny
+    if sched == "split_k":  # down matrices transposed: the split-K kernel
+        layer = synth.make_layer(synth.TINY, seed=0, device="cuda", w2_layout="i_h")
+        sched = "persistent"
     x = helpers.hidden_with_margin(tiny["router_w"], m, synth.TINY.top_k, seed=3)
-    mod = MoEDecodeLayer(synth.TINY, tiny, 2, sched=sched)
+    mod = MoEDecodeLayer(synth.TINY, layer, 2, sched=sched)
     xd = x.cuda()
     good = mod.run(xd, xd).clone()
     assert mod.status() == _lib.MOE_OK

@@ -6,6 +6,7 @@ arrays. moe_decode_plan is the library's own planner, called through the C ABI."
 import ctypes
 import itertools
 
+import numpy as np
 import pytest
 
 from moe_decode_layer_gb300 import _lib
@@ -151,3 +152,65 @@ def test_plan_rejects_bad_arguments():
     assert lib.moe_decode_plan(ctypes.byref(cfg), 152, 232448, 0, None) == _lib.MOE_ERR_INVALID_ARG
     bad = _cfg(2560, 776, 512, 8, 1, 1, False)  # 97 threads per down group
     assert lib.moe_decode_plan(ctypes.byref(bad), 152, 232448, 0, ctypes.byref(info)) == _lib.MOE_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# split-K kernel (down matrices transposed)
+# ---------------------------------------------------------------------------
+
+
+def _sk_cfg(**kw):
+    base = dict(hidden=2560, inter=768, num_experts=512, top_k=8, num_shared=1, max_rows=8, wdtype=0, score=0,
+                routed_scale=1.0, pre_rmsnorm=0, rms_eps=1e-6, sched=0, w2_layout=_lib.MOE_W2_I_H)
+    base.update(kw)
+    return _lib.Config(**base)
+
+
+def _split_rows(costs, grid):
+    """Rows (items) of each CTA under the routed cost split: the item boundaries
+    of CTA b are the first items at or after b / grid and (b + 1) / grid of the
+    total cost (the rule the union applies on the device)."""
+    cum = np.concatenate([[0], np.cumsum(costs)])
+    total = int(cum[-1])
+    bounds = [int(np.searchsorted(cum, total * b // grid, side="left")) for b in range(grid + 1)]
+    return [bounds[b + 1] - bounds[b] for b in range(grid)]
+
+
+@pytest.mark.parametrize("maxm", [1, 6, 8])
+def test_split_k_h_rows_bound_covers_the_cost_split(maxm):
+    """The planner's h-row bound holds for the shared share plus the largest
+    routed share the cost split can give: items whose row counts are all 1 next
+    to items with maxm rows (the most rows per unit of cost), at several expert
+    counts."""
+    lib = _lib.load()
+    info = _lib.PlanInfo()
+    assert lib.moe_decode_plan(ctypes.byref(_sk_cfg(max_rows=maxm)), 152, 232448, 0, ctypes.byref(info)) == 0
+    assert info.h_rows_max > 0 and info.down_t_rows_per_stage > 0
+    I, S, grid, base = 768, 1, 152, 6
+    shared = -(-S * I // grid)
+    rng = np.random.default_rng(maxm)
+    worst = 0
+    for n_slots in (1, 7, 8 * maxm // 2, 8 * maxm):
+        for trial in range(4):
+            rows = rng.integers(1, maxm + 1, size=n_slots)
+            if trial == 0:
+                rows[:] = 1
+            if trial == 1:
+                rows[: n_slots // 2] = maxm
+            costs = np.repeat(base + rows, I)
+            worst = max(worst, max(_split_rows(costs, grid)))
+    assert shared + worst <= info.h_rows_max
+
+
+def test_split_k_plan_fits_and_refuses():
+    lib = _lib.load()
+    info = _lib.PlanInfo()
+    for m in (1, 6, 8):
+        assert lib.moe_decode_plan(ctypes.byref(_sk_cfg(max_rows=m)), 152, 232448, 0, ctypes.byref(info)) == 0
+        assert info.smem_bytes <= 232448 and info.ring_slots >= 3 and info.threads == 416
+    # one layout for transposed down rows: no interleaved / expert-range variant
+    assert lib.moe_decode_plan(ctypes.byref(_sk_cfg()), 152, 232448, 1, ctypes.byref(info)) == _lib.MOE_ERR_UNSUPPORTED
+    for kw in (dict(wdtype=1), dict(hidden=4096), dict(sched=1), dict(w2_layout=2), dict(wdtype=2, inter=704)):
+        assert lib.moe_decode_config_check(ctypes.byref(_sk_cfg(**kw))) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_decode_config_check(ctypes.byref(_sk_cfg(wdtype=2))) == 0
+    assert lib.moe_decode_config_check(ctypes.byref(_sk_cfg(hidden=3072, inter=1000))) == 0

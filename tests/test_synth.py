@@ -3,6 +3,7 @@
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -17,8 +18,10 @@ def test_tiny_layer_shapes_and_determinism():
     c = synth.make_layer(synth.TINY, seed=1)
     assert a["w13"].shape == (16, 256, 256) and a["w2"].shape == (16, 256, 128)
     assert a["sh_w13"].shape == (1, 256, 256) and a["router_w"].shape == (16, 256)
+    assert a["w2_layout"] == "h_i"
     for k in a:
-        assert torch.equal(a[k], b[k])
+        if k != "w2_layout":
+            assert torch.equal(a[k], b[k])
     assert not torch.equal(a["w13"], c["w13"])
     std = a["w13"].float().std().item()
     assert abs(std - 0.02) < 0.001
@@ -61,3 +64,21 @@ def test_algorithmic_bytes_ling():
     # 8 routed + 1 shared expert of 3*2560*768*2 B plus the 512x2560 bf16 router
     assert synth.algorithmic_bytes(synth.LING, 8) == 9 * 11_796_480 + 2_621_440
     assert synth.algorithmic_bytes(synth.MUSE_NVFP4, 8) == 8 * 7_077_888 + 2_097_152
+
+
+@pytest.mark.parametrize("shape", [synth.TINY, synth.LayerShape(hidden=256, inter=128, num_experts=4, top_k=2,
+                                                                num_shared=1, wdtype="fp8")], ids=["bf16", "fp8"])
+def test_transposed_down_layout_holds_the_same_weights(shape):
+    """w2_layout "i_h" stores each down matrix (and FP8 scale grid) transposed;
+    the values are the same as in the default layout for the same seed."""
+    a = synth.make_layer(shape, seed=3)
+    b = synth.make_layer(shape, seed=3, w2_layout="i_h")
+    assert b["w2_layout"] == "i_h"
+    names = ("w2", "sh_w2") if shape.wdtype == "bf16" else ("w2_q", "w2_s", "sh_w2_q", "sh_w2_s")
+    for n in names:
+        assert b[n].shape == (a[n].shape[0], a[n].shape[2], a[n].shape[1])
+        assert torch.equal(b[n], a[n].transpose(1, 2))
+        assert b[n].is_contiguous()
+    with pytest.raises(ValueError):
+        synth.make_layer(synth.LayerShape(hidden=256, inter=256, num_experts=4, top_k=2, num_shared=0,
+                                          wdtype="nvfp4"), seed=1, w2_layout="i_h")
