@@ -204,8 +204,19 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
     layers = pool.get(wl["shape"], shape, copies, w2_layout_for(args, shape))
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=args.sched, pre_rmsnorm=nl > 1) for i in range(copies)]
     n_in = 64
-    xs = [synth.hidden_rows(m, shape.hidden, seed=50_000 + 1000 * rank + j, rho=wl["rho"]).cuda()
-          for j in range(n_in)]
+    seq_rho = wl.get("seq_rho")
+    if seq_rho is None:
+        xs = [synth.hidden_rows(m, shape.hidden, seed=50_000 + 1000 * rank + j, rho=wl["rho"]).cuda()
+              for j in range(n_in)]
+    else:
+        # step j runs layer copy j % copies on the next step of that copy's sequence
+        per = n_in // copies
+        seqs = [synth.decode_sequence(per, m, shape.hidden, seed=60_000 + 1000 * rank + c, rho=wl["rho"],
+                                      seq_rho=seq_rho) for c in range(copies)]
+        xs = [seqs[j % copies][j // copies].cuda() for j in range(n_in)]
+    prefetch = wl.get("prefetch", 0) if args.prefetch is None else args.prefetch
+    for md in mods:
+        md.set_option(_lib.MOE_OPT_PREFETCH_EXPERTS, prefetch)
     out = torch.empty_like(xs[0])
     stream = torch.cuda.current_stream()
 
@@ -221,9 +232,11 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
     period = n_in
     step_bytes = []
     idx = torch.empty((m, shape.top_k), dtype=torch.int32, device="cuda")
+    chosen = []
     for s in range(period):
         if nl == 1:
             mods[s % copies].run(xs[s % n_in], xs[s % n_in], out, topk_idx=idx)
+            chosen.append(idx.cpu())
             step_bytes.append(synth.algorithmic_bytes(shape, len(set(idx.cpu().flatten().tolist()))))
         else:
             h = xs[s % n_in].clone()
@@ -236,6 +249,25 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
         st = md.status()
         if st != _lib.MOE_OK:
             raise RuntimeError(f"device status {_lib.status_string(st)}")
+    # speculative prefetch: how many of the experts each step prefetched (the
+    # previous visit of its layer copy, by the kernel's rule) it then selected
+    pf_stats = None
+    if prefetch and nl == 1 and period >= 2 * copies:
+        hit = tot = sel = 0
+        for s in range(copies, period):
+            prev, cur = chosen[s - copies], set(chosen[s].flatten().tolist())
+            if m == 1:
+                pred = prev[0].tolist()[:prefetch]
+            else:
+                cnt = {}
+                for e in prev.flatten().tolist():
+                    cnt[e] = cnt.get(e, 0) + 1
+                pred = sorted(cnt, key=lambda e: (-cnt[e], e))[:prefetch]
+            hit += len(set(pred) & cur)
+            tot += len(pred)
+            sel += len(cur)
+        pf_stats = {"experts": prefetch, "prefetched_then_selected": round(hit / max(tot, 1), 3),
+                    "selected_that_were_prefetched": round(hit / max(sel, 1), 3)}
 
     for s in range(warmup):
         step(s)
@@ -375,6 +407,7 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
             "layers_per_step": nl,
             "sched": args.sched,
             "w2_layout": w2_layout_for(args, shape),
+            "expert_prefetch": pf_stats if pf_stats else prefetch,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "launch": (f"CUDA graph replay of exactly {K} steps (a {P}-step graph x {K // P}"
                        + (f" + a {R}-step graph" if R else "") + ")"),
@@ -563,6 +596,8 @@ def main(argv=None):
                     help="down matrices [E,H,I] (row-block kernels) or transposed [E,I,H] (split-K kernel; "
                          "bf16 and fp8 workloads under --sched persistent)")
     ap.add_argument("--copies", type=int, default=8, help="distinct layer copies (single-layer workloads)")
+    ap.add_argument("--prefetch", type=int, default=None,
+                    help="experts of the previous step prefetched into L2 while routing (default: the workload's)")
     ap.add_argument("--lat-steps", type=int, default=256, help="single steps for the latency percentiles (>= 200)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle CPU baseline sample per workload")

@@ -289,10 +289,20 @@ enum {
                                   kernel (each CTA owns a contiguous range of the
                                   routed experts' rows and output blocks; bf16
                                   weights, at most one shared expert) when its layout
-                                  fits and: 1 (default) for one token row, where it
-                                  measured faster; 2 always; 0 never. It takes
-                                  precedence over MOE_OPT_INTERLEAVE. get_info: the
-                                  mode, 0 when the layout does not fit.              */
+                                  fits and: 0 (default) never; 1 for one token row;
+                                  2 always. It measured slower than the other
+                                  single kernels on GB300. It takes precedence over
+                                  MOE_OPT_INTERLEAVE. get_info: the mode, 0 when the
+                                  layout does not fit.                               */
+  MOE_OPT_PREFETCH_EXPERTS = 8, /* 0 (default) .. 16: while a run routes, its producer
+                                  warps pull into L2 the weights of this many experts
+                                  that the handle's previous run used most (most token
+                                  rows, ties to the lower id; with one row, the first
+                                  selected), each CTA its 1/grid share ("Muse Spark Open
+                                  Ultrafast", section "Speculative expert prefetching":
+                                  consecutive steps tend to route alike). Results do
+                                  not change. Phase-ordered, interleaved, chained and
+                                  split-K kernels; the expert-range kernel ignores it. */
   MOE_INFO_GRID = 16,          /* CTAs per kernel                                   */
   MOE_INFO_THREADS = 17,       /* threads per CTA                                   */
   MOE_INFO_SMEM = 18,          /* dynamic shared memory per CTA, bytes              */
@@ -304,8 +314,11 @@ enum {
                                     schedule and options takes the slot-interleaved
                                     kernel                                         */
   MOE_INFO_FLAT_ROWS = 24,       /* the same for the expert-range kernel            */
-  MOE_INFO_SPLIT_K = 25          /* 1: the handle runs the split-K kernel (w2_layout
+  MOE_INFO_SPLIT_K = 25,         /* 1: the handle runs the split-K kernel (w2_layout
                                     MOE_W2_I_H)                                       */
+  MOE_INFO_PREDICTED = 32        /* + i (i < 16): the i-th expert the next run
+                                    prefetches, -1 for none. Waits for the device
+                                    (cudaDeviceSynchronize) and reads device memory.  */
 };
 moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t value);
 moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value);

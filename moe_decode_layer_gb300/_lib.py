@@ -41,6 +41,7 @@ MOE_OPT_RING_SLOTS = 4
 MOE_OPT_STAMPS = 5
 MOE_OPT_INTERLEAVE = 6
 MOE_OPT_FLAT = 7
+MOE_OPT_PREFETCH_EXPERTS = 8
 STAMP_NAMES = {0: "start", 1: "x_loaded", 2: "R_done", 3: "routed", 4: "U_done", 5: "D_first",
                6: "D_done", 8: "prod_R_issued", 9: "prod_route", 10: "prod_U_issued",
                11: "prod_D_issued", 12: "logits_seen", 13: "topk_row0", 14: "ucount_full",
@@ -58,6 +59,7 @@ MOE_INFO_SCRATCH_BYTES = 22
 MOE_INFO_INTERLEAVED_ROWS = 23
 MOE_INFO_FLAT_ROWS = 24
 MOE_INFO_SPLIT_K = 25
+MOE_INFO_PREDICTED = 32
 STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTS = ("moe_decode_config_check", "moe_decode_plan", "moe_decode_create", "moe_decode_run", "moe_decode_run_host",

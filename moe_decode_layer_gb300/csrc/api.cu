@@ -463,6 +463,8 @@ void bind_pointers(const Params& from, Params& to) {
   to.hbuf = from.hbuf;
   to.xflags = from.xflags;
   to.ctrl = from.ctrl;
+  to.hist = from.hist;
+  to.psum = from.psum;
 }
 
 // Whether a persistent run of m rows takes the slot-interleaved kernel: always
@@ -681,6 +683,9 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   const size_t tag_end = off;
   // split-K kernel: every CTA's partial sums, by destination block
   const size_t o_ps = sk ? take((size_t)p.grid * p.grid * p.maxm * p.nrp * 4) : 0;
+  // speculative expert prefetch: the predicted expert lists by run parity (-1: none)
+  const size_t o_hist = take(2 * moe::kPfMax * 4);
+  const size_t hist_end = off;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
   const size_t o_so = take(maxm * H * 2);
@@ -703,6 +708,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   uint8_t* base = static_cast<uint8_t*>(h->scratch);
   if (cudaMemset(base, 0, o_logits) != cudaSuccess ||
       cudaMemset(base + o_logits, 0xff, tag_end - o_logits) != cudaSuccess ||
+      cudaMemset(base + o_hist, 0xff, hist_end - o_hist) != cudaSuccess ||
 
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFreeHost(h->host_status);
@@ -733,6 +739,8 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   p.hbuf = reinterpret_cast<float*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
   if (sk) p.psum = reinterpret_cast<float*>(base + o_ps);
+  p.hist = reinterpret_cast<int*>(base + o_hist);
+  p.pf_n = 0;
 
   h->stage_x = reinterpret_cast<uint16_t*>(base + o_sx);
   h->stage_r = reinterpret_cast<uint16_t*>(base + o_sr);
@@ -873,12 +881,30 @@ moe_status moe_decode_set_option(moe_decode_handle* h, int32_t option, int64_t v
       if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       h->flat_mode = (int)value;
       return MOE_OK;
+    case MOE_OPT_PREFETCH_EXPERTS:
+      if (value < 0 || value > moe::kPfMax) return MOE_ERR_INVALID_ARG;
+      h->base.pf_n = h->ilv.pf_n = h->flat.pf_n = (int)value;
+      return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
 
 moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* value) {
   if (!h || !value) return MOE_ERR_INVALID_ARG;
+  if (what >= MOE_INFO_PREDICTED && what < MOE_INFO_PREDICTED + moe::kPfMax) {
+    // the next run's prefetch list: its parity is the run tag the next run takes
+    uint32_t ep = 0;
+    int32_t e = -1;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&ep, h->base.ctrl + moe::CTRL_EPOCH, sizeof(ep), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(&e, h->base.hist + (size_t)(ep & 1u) * moe::kPfMax + (what - MOE_INFO_PREDICTED), sizeof(e),
+                   cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    *value = e;
+    return MOE_OK;
+  }
   switch (what) {
     case MOE_OPT_SCHED: *value = h->sched; return MOE_OK;
     case MOE_OPT_WAIT_TIMEOUT_NS: *value = (int64_t)h->base.timeout_ns; return MOE_OK;
@@ -888,6 +914,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
     case MOE_OPT_INTERLEAVE: *value = h->has_ilv ? h->ilv_mode : 0; return MOE_OK;
     case MOE_OPT_FLAT: *value = h->has_flat ? h->flat_mode : 0; return MOE_OK;
     case MOE_INFO_SPLIT_K: *value = h->sk ? 1 : 0; return MOE_OK;
+    case MOE_OPT_PREFETCH_EXPERTS: *value = h->base.pf_n; return MOE_OK;
     case MOE_INFO_FLAT_ROWS: {
       int64_t mask = 0;
       for (int m = 1; m <= h->cfg.max_rows; ++m)

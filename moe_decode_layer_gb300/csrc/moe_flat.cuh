@@ -430,6 +430,7 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;
     c.misc[MISC_NROUTED] = 0;
+    c.misc[MISC_ROUTED] = 0;
   }
   for (int i = c.tid; i < p.nslot_max; i += kThreadsFlat) reinterpret_cast<int*>(sm + p.off_acnt)[i] = 0;
   for (int e = c.tid; e < p.E; e += kThreadsFlat) rt.emask[e] = 0u;
@@ -497,6 +498,7 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
     // top-k spread over several warps); the shared expert's items follow
     route_rows(c, rt, true, kNC * 32, kBarRouting);
     fence_proxy_async_shared();  // the routing scratch becomes the h buffers (bulk copies)
+    if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
     bar_arrive(kBarRoute, kThreadsFlat);
     if (c.tid == 0) c.stamp(ST_ROUTED);
     int slo, shi;

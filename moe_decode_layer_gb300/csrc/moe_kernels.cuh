@@ -1265,6 +1265,41 @@ __device__ __forceinline__ void one_row_split(const Ctx& c) {
   c.misc[MISC_UHI] = hi;
 }
 
+// The experts the next run of this handle prefetches (speculative expert
+// prefetch, off unless pf_n > 0): the routed experts of this run used by the
+// most token rows, ties to the lower expert id; with one row, the selected
+// experts in selection order (descending weight). Written by warp 0 of CTA 0
+// after its work, from the routing tables still in shared memory, into the list
+// of the next run's parity.
+__device__ __forceinline__ void write_prediction(const Ctx& c, const Route& rt) {
+  const Params& p = c.p;
+  if (p.pf_n <= 0 || p.hist == nullptr || blockIdx.x != 0 || c.warp != 0) return;
+  int* out = p.hist + (size_t)((c.epoch() + 1u) & 1u) * kPfMax;
+  const int P = min(p.pf_n, kPfMax);
+  if (p.M == 1) {
+    if (c.lane < kPfMax) out[c.lane] = c.lane < P && c.lane < p.K ? rt.sel_e[c.lane] : -1;
+    return;
+  }
+  const int nr = c.misc[MISC_NROUTED];
+  uint32_t key[4];  // routed slots lane + 32 i: (rows << 16) | (0xffff - slot); 0 = none
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int u = c.lane + 32 * i;
+    key[i] = u < nr ? ((uint32_t)__popc(rt.slot_mask[p.S + u]) << 16) | (0xffffu - (uint32_t)u) : 0u;
+  }
+  for (int j = 0; j < kPfMax; ++j) {
+    uint32_t best = 0;
+    if (j < P) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) best = max(best, key[i]);
+      best = warp_max_u32(best);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) key[i] = key[i] == best ? 0u : key[i];
+    }
+    if (c.lane == 0) out[j] = best ? rt.slot_e[p.S + (int)(0xffffu - (best & 0xffffu))] : -1;
+  }
+}
+
 // nthr threads (the first nthr / 32 consumer warps, at least p.M) route; they
 // meet at named barrier `bar`.
 static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk,
@@ -1916,6 +1951,44 @@ struct Producer {
     return (r_hi - r_lo + c.p.d_rows_stage - 1) / c.p.d_rows_stage;
   }
 
+  // Speculative expert prefetch ("Muse Spark Open Ultrafast", section
+  // "Speculative expert prefetching": consecutive steps tend to route alike, so
+  // the experts the previous step used most are pulled into L2 while the router
+  // runs and HBM is otherwise idle). This CTA's 1/grid share of every byte of
+  // each listed expert (gate/up and down codes and scales) into L2; the list is
+  // the one the previous run of this handle left for this run's parity.
+  // Issued in 16 KB pieces, one at a time and only until the routing warps flag
+  // the routing as done: the CTA's bulk-copy unit handles its operations in
+  // order, and a long prefetch queued ahead of the routed stages would delay them.
+  __device__ __forceinline__ void prefetch_predicted() const {
+    const Params& p = c.p;
+    if (p.pf_n <= 0 || p.hist == nullptr) return;
+    const volatile int* routed = reinterpret_cast<const volatile int*>(c.misc) + MISC_ROUTED;
+    const uint32_t ep = ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
+    const int* list = p.hist + (size_t)(ep & 1u) * kPfMax;
+    const size_t n13 = (size_t)2 * p.I, n2 = (size_t)p.H;  // rows per expert (transposed down: same bytes)
+    constexpr uint32_t kPiece = 16384;
+    for (int i = 0; i < p.pf_n && i < kPfMax; ++i) {
+      const int e = list[i];
+      if (e < 0 || e >= p.E) continue;
+      const uint8_t* base[4] = {p.w13 + (size_t)e * n13 * p.row13, p.w2 + (size_t)e * n2 * p.row2,
+                                p.sc13 ? p.w13_s + (size_t)e * n13 * p.sc13 : nullptr,
+                                p.sc2 ? p.w2_s + (size_t)e * n2 * p.sc2 : nullptr};
+      const size_t len[4] = {n13 * p.row13, n2 * p.row2, n13 * p.sc13, n2 * p.sc2};
+      for (int r = 0; r < 4; ++r) {
+        if (!base[r]) continue;
+        int lo, hi;  // 16-byte units of this CTA's share
+        split_range((int)(len[r] / 16), blockIdx.x, p.grid, lo, hi);
+        for (size_t o = (size_t)lo * 16; o < (size_t)hi * 16; o += kPiece) {
+          if (*routed || c.aborted()) return;
+          const uint32_t n = (uint32_t)min((size_t)kPiece, (size_t)hi * 16 - o);
+          bulk_prefetch_l2(base[r] + o, n);
+          __nanosleep(200);
+        }
+      }
+    }
+  }
+
   // Shared experts' down rows of this CTA into L2 ahead of time.
   __device__ __forceinline__ void prefetch_shared_down() {
     const Params& p = c.p;
@@ -1979,6 +2052,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;
     c.misc[MISC_NROUTED] = 0;
+    c.misc[MISC_ROUTED] = 0;
   }
   for (int e = c.tid; e < p.E; e += kThreads) rt.emask[e] = 0u;
   for (int e = c.tid; e < (p.E + 31) / 32; e += kThreads) rt.bitmap[e] = 0u;
@@ -2006,6 +2080,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         pr.pairs(true, rt);
         c.stamp(ST_P_R_ISSUED);
         if (PHASES & PH_D) pr.prefetch_shared_down();
+        pr.prefetch_predicted();
       } else if (PHASES == PH_D) {
         // The shared experts' down rows of the first row block need no routing.
         if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, 0);
@@ -2065,6 +2140,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     }
     if (kRoute) {
       route_rows(c, rt, (PHASES & PH_U) != 0);
+      if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
       bar_arrive(kBarRoute, kThreads);
       if (c.tid == 0) c.stamp(ST_ROUTED);
     }
@@ -2105,6 +2181,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     if (PHASES & PH_D)
       consume_down<FMT, MAXM>(c, rt, PHASES == PH_ALL && p.out_aliases_x, PHASES == PH_ALL, ring,
                               PHASES == PH_ALL ? p.nslots_d : 0);
+    if (kLast) write_prediction(c, rt);
     if (c.tid == 0) {
       c.stamp(ST_D_DONE);
       if (p.stamps) {
@@ -2279,6 +2356,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;
     c.misc[MISC_NROUTED] = 0;
+    c.misc[MISC_ROUTED] = 0;
   }
   if (c.tid < ILV_WORDS) reinterpret_cast<int*>(sm + p.off_ucnt)[c.tid] = 0;
   for (int e = c.tid; e < p.E; e += kThreadsIlv) rt.emask[e] = 0u;
@@ -2309,6 +2387,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
       for (int s = 0; s < p.S; ++s) pr.ilv_pairs(rt, s, ilv_sq(p));
       c.stamp(ST_P_R_ISSUED);
       pr.prefetch_shared_down();
+      pr.prefetch_predicted();
     }
     __syncwarp();
     bar_sync(kBarRoute, ilv_route_threads(p));
@@ -2353,6 +2432,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     const int nrw = ilv_nrw(p);
     if (c.warp < nrw) {
       route_rows(c, rt, true, nrw * 32, kBarRouting);
+      if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
       bar_arrive(kBarRoute, ilv_route_threads(p));
       if (c.tid == 0) c.stamp(ST_ROUTED);
     }
@@ -2387,6 +2467,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
       }
       write_rows<FMT, MAXM>(c, acc, g, ch, active, nr, r_lo);
     }
+    write_prediction(c, rt);
     if (c.tid == 0) {
       c.stamp(ST_D_DONE);
       if (p.stamps) {

@@ -22,6 +22,7 @@ constexpr int kMinSlots = 4;             // ring slots kept before shrinking the
 constexpr int kLogitRep = 4;             // copies of the router logits (spreads the all-CTA read)
 constexpr int kHRep = 4;                 // copies of the h rows (spreads the all-CTA read)
 constexpr int kCandMax = 64;             // top-k candidates ranked in parallel per row
+constexpr int kPfMax = 16;               // experts a run may prefetch into L2 from the previous run's routing
 constexpr int kRouterCopy = 4096;        // bytes per bulk copy of router rows (more copies in flight)
 
 enum WFmt : int { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_FP8 = 2 };
@@ -103,7 +104,8 @@ enum Stamp : int {
 // Shared-memory words kept in the misc block.
 // MISC_XMAX + m: bf16 bits of the largest |x| of row m (NVFP4: sets the row's
 // power-of-two scale into fp16's range).
-enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_ULO = 3, MISC_UHI = 4, MISC_WTOT = 8,
+enum Misc : int { MISC_EPOCH = 0, MISC_NROUTED = 1, MISC_ABORT = 2, MISC_ULO = 3, MISC_UHI = 4, MISC_ROUTED = 5,
+                  MISC_WTOT = 8,
                   MISC_XMAX = 16, MISC_WORDS = 32 };
 
 struct Params {
@@ -197,6 +199,10 @@ struct Params {
   int off_psb;         // mbarrier: the partial-sum block of this CTA landed
   int off_psum;        // [nrp] x (parts) fp32 staging for the fixed-order reduction
   float* psum;         // [grid (destination)][grid (source)][M][nrp] fp32 partial sums
+  // speculative expert prefetch
+  int pf_n;            // experts to prefetch into L2 while routing runs (0: off)
+  int* hist;           // [2][kPfMax] expert ids (-1: none) by run parity: run r reads list r & 1
+                       // and writes the list for run r + 1
 };
 
 }  // namespace moe

@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
     mbar_init_fence();
     c.misc[MISC_ABORT] = 0;
     c.misc[MISC_NROUTED] = 0;
+    c.misc[MISC_ROUTED] = 0;
   }
   for (int e = c.tid; e < p.E; e += kThreads) rt.emask[e] = 0u;
   for (int e = c.tid; e < (p.E + 31) / 32; e += kThreads) rt.bitmap[e] = 0u;
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
       pr.router();
       sk_produce<FMT>(pr, rt, s_lo, s_hi, true);
       c.stamp(ST_P_R_ISSUED);
+      pr.prefetch_predicted();
     }
     __syncwarp();
     bar_sync(kBarRoute, kThreads);
@@ -335,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
       c.stamp(ST_RFLAG);
     }
     route_rows(c, rt, true);
+    if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
     bar_arrive(kBarRoute, kThreads);
     if (c.tid == 0) c.stamp(ST_ROUTED);
     if (FMT != FMT_BF16) {  // the router is done with the bf16 x rows
@@ -353,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
     ring = sk_consume<FMT, MAXM>(c, rt, ring, c.misc[MISC_ULO], c.misc[MISC_UHI], false, s_hi - s_lo, xr, acc);
     if (c.tid == 0) c.stamp(ST_U_DONE);
     sk_finish<FMT, MAXM>(c, acc);
+    write_prediction(c, rt);
     if (c.tid == 0) {
       c.stamp(ST_D_DONE);
       if (p.stamps) {

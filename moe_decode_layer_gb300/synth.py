@@ -86,6 +86,20 @@ WORKLOADS = {
                              "block), H=2560, E=512 top-8 + 1 shared, I=768, M=1"),
     "ling_fp8_m6": dict(shape="LING_FP8", m=6, rho=0.5, layers=1,
                         desc="Ling-shaped MoE layer with FP8 experts, M=6 verify rows correlated rho=0.5"),
+    # decode sequences: each layer copy sees successive steps whose hidden rows
+    # follow x_t = sqrt(0.8) x_{t-1} + sqrt(0.2) z_t (about half of the top-8
+    # experts repeat from one step to the next), with and without the
+    # speculative prefetch of the previous step's most-used experts
+    "ling_m1_seq": dict(shape="LING", m=1, rho=0.0, layers=1, seq_rho=0.8, prefetch=4,
+                        desc="Ling-shaped layer, M=1, successive decode steps correlated 0.8, "
+                             "4 experts of the previous step prefetched into L2 while routing"),
+    "ling_m1_seq_off": dict(shape="LING", m=1, rho=0.0, layers=1, seq_rho=0.8, prefetch=0,
+                            desc="the same decode sequence without the prefetch"),
+    "ling_m6_seq": dict(shape="LING", m=6, rho=0.5, layers=1, seq_rho=0.8, prefetch=4,
+                        desc="Ling-shaped layer, M=6 rho=0.5, successive decode steps correlated 0.8, "
+                             "4 most-used experts of the previous step prefetched into L2 while routing"),
+    "ling_m6_seq_off": dict(shape="LING", m=6, rho=0.5, layers=1, seq_rho=0.8, prefetch=0,
+                            desc="the same decode sequence without the prefetch"),
     "tiny_m1": dict(shape="TINY", m=1, rho=0.0, layers=1,
                     desc="tiny MoE layer H=256, E=16 top-2 + 1 shared, I=128, M=1"),
     # profiling case: Ling-shaped experts, 64 of them (0.76 GB per copy), same
@@ -109,6 +123,20 @@ def algorithmic_bytes(shape: LayerShape, distinct_routed: int) -> int:
 # ----------------------------------------------------------------------------
 # hidden rows
 # ----------------------------------------------------------------------------
+
+
+def decode_sequence(steps: int, m_rows: int, hidden: int, seed: int, rho: float = 0.0,
+                    seq_rho: float = 0.8) -> list:
+    """bf16 [M, H] rows of `steps` successive decode steps: step 0 as
+    hidden_rows, then x_t = sqrt(seq_rho) x_{t-1} + sqrt(1 - seq_rho) z_t, with z_t
+    drawn as hidden_rows (its own seed per step), in float32, rounded to bf16."""
+    x = hidden_rows(m_rows, hidden, seed=seed, rho=rho).float()
+    out = [x.to(torch.bfloat16)]
+    for t in range(1, steps):
+        z = hidden_rows(m_rows, hidden, seed=seed * 1000 + t, rho=rho).float()
+        x = math.sqrt(seq_rho) * x + math.sqrt(1.0 - seq_rho) * z
+        out.append(x.to(torch.bfloat16))
+    return out
 
 
 def hidden_rows(m_rows: int, hidden: int, seed: int, rho: float = 0.0,
