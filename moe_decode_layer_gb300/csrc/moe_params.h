@@ -9,7 +9,7 @@ constexpr int kMaxRowsLaunch = 8;        // token rows one kernel launch handles
 constexpr int kMaxRowsRun = 16;          // token rows one run handles (launches of <= 8 rows)
 constexpr int kThreads = (kNC + 1) * 32; // + one producer warp
 constexpr int kThreadsIlv = kThreads + 64;  // slot-interleaved kernel: + two hand-off warps
-constexpr int kRpgMax = 6;               // down-projection rows per thread group per stage (at most)
+constexpr int kRpgMax = 5;               // down-projection rows per thread group per stage (at most; 4 groups x 5 rows hold the 17 rows of a Ling-shaped CTA block)
 constexpr int kRpgFp4 = 3;               // NVFP4: its 32-element chunks leave more groups, so fewer rows each
 __host__ __device__ constexpr int rows_per_group(int fmt) { return fmt == 1 ? kRpgFp4 : kRpgMax; }
 constexpr int kMaxSlots = 64;            // ring slots (upper bound for the barrier arrays)
