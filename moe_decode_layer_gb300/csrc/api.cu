@@ -488,10 +488,17 @@ int threads_for(const moe_decode_handle* h, int m) {
   return use_flat(h, m) ? moe::kThreadsFlat : interleaved(h, m) ? moe::kThreadsIlv : moe::kThreads;
 }
 
+// The row bound of the kernel instantiation a launch of m rows takes: 1, 6
+// (bf16 / FP8 phase-ordered and chained kernels: fewer registers for the
+// per-row sums) or 8.
+int maxm_for(const Params& p, int m, bool six_ok) {
+  return m == 1 ? 1 : (m <= 6 && six_ok && p.fmt != moe::FMT_NVFP4) ? 6 : 8;
+}
+
 moe_status launch(moe_decode_handle* h, const Params& p, cudaStream_t stream) {
-  const int maxm_t = p.M == 1 ? 1 : 8;
   const bool ilv = interleaved(h, p.M);
   const bool flat = use_flat(h, p.M);
+  const int maxm_t = maxm_for(p, p.M, !h->sk && !ilv && !flat);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(threads_for(h, p.M));
@@ -626,7 +633,8 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   // Every kernel this handle may launch gets the shared-memory size, and one
   // CTA of the single-kernel schedule must fit on every SM.
   const int phases[4] = {moe::PH_ALL, moe::PH_R, moe::PH_U, moe::PH_D};
-  for (int mt : {1, 8}) {
+  for (int mt : {1, 6, 8}) {
+    if (mt == 6 && (sk || kernel_for(p, 6, moe::PH_ALL) == nullptr)) continue;  // bf16 / FP8 only
     if (sk) {
       const void* k = moe::kernel_sk(p.fmt, mt);
       int blocks = 0;
@@ -647,7 +655,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
         return MOE_ERR_CUDA;
       if (blocks < 1) return MOE_ERR_UNSUPPORTED;
     }
-    if (has_flat) {
+    if (has_flat && mt != 6) {
       const void* k = moe::kernel_flat(mt);
       int blocks = 0;
       if (!k || cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pf.smem_bytes) != cudaSuccess ||
@@ -655,7 +663,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
         return MOE_ERR_CUDA;
       if (blocks < 1) has_flat = false;
     }
-    if (has_ilv) {
+    if (has_ilv && mt != 6) {
       const void* k = kernel_for(pi, mt, moe::PH_ILV);
       int blocks = 0;
       if (!k || cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pi.smem_bytes) != cudaSuccess ||

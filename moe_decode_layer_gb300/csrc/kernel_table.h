@@ -3,7 +3,10 @@
 #pragma once
 
 namespace moe {
-// Kernel entry for (maxm_t in {1, 8}, phases in Phase). NULL if not instantiated.
+// Kernel entry for (maxm_t in {1, 6, 8}, phases in Phase). NULL if not
+// instantiated. maxm_t bounds the token rows of a launch; 6 (bf16 and FP8,
+// phase-ordered and chained kernels) keeps the per-thread sums of up to six rows
+// in registers where 8 spills, for runs of 2..6 rows.
 const void* kernel_bf16(int maxm_t, int phases);
 const void* kernel_nvfp4(int maxm_t, int phases);
 const void* kernel_fp8(int maxm_t, int phases);

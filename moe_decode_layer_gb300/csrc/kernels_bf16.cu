@@ -11,13 +11,19 @@ static const void* pick(int phases) {
     case PH_R: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_BF16, MAXM, PH_R>);
     case PH_U: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_BF16, MAXM, PH_U>);
     case PH_D: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_BF16, MAXM, PH_D>);
-    case PH_ILV: return reinterpret_cast<const void*>(&moe_ilv_kernel<FMT_BF16, MAXM>);
+    case PH_ILV:  // the interleaved kernel: one row, or any row count up to 8
+      if constexpr (MAXM == 6) {
+        return nullptr;
+      } else {
+        return reinterpret_cast<const void*>(&moe_ilv_kernel<FMT_BF16, MAXM>);
+      }
     default: return nullptr;
   }
 }
 
 const void* kernel_bf16(int maxm_t, int phases) {
   if (maxm_t == 1) return pick<1>(phases);
+  if (maxm_t == 6) return pick<6>(phases);
   if (maxm_t == 8) return pick<8>(phases);
   return nullptr;
 }

@@ -18,6 +18,7 @@ static const void* pick(int phases) {
 
 const void* kernel_fp8(int maxm_t, int phases) {
   if (maxm_t == 1) return pick<1>(phases);
+  if (maxm_t == 6) return pick<6>(phases);
   if (maxm_t == 8) return pick<8>(phases);
   return nullptr;
 }

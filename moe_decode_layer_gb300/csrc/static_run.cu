@@ -106,7 +106,9 @@ extern "C" moe_status moe_decode_run_static(const moe_decode_config* cfg, const 
   p.logits = reinterpret_cast<unsigned long long*>(base + o_logits);
   p.hbuf = reinterpret_cast<float*>(base + o_h);
   p.xflags = reinterpret_cast<unsigned long long*>(base + o_xf);
-  const int maxm_t = m_rows == 1 ? 1 : 8;
+  // the row bound of the instantiation: 1, 6 (bf16 / FP8 phase-ordered, runs of
+  // up to 6 rows: fewer registers for the per-row sums) or 8
+  const int maxm_t = m_rows == 1 ? 1 : (!ilv && m_rows <= 6 && p.fmt != moe::FMT_NVFP4) ? 6 : 8;
   const int which = ilv ? moe::PH_ILV : moe::PH_ALL;
   const void* kernel = p.fmt == moe::FMT_BF16    ? moe::kernel_bf16(maxm_t, which)
                        : p.fmt == moe::FMT_NVFP4 ? moe::kernel_nvfp4(maxm_t, which)
