@@ -282,7 +282,7 @@ enum {
                                   kernel (gate/up items and down stages alternate
                                   slot by slot) when its layout fits and: 1 (default)
                                   for bf16 weights and one token row, where it
-                                  measured faster; 2 always; 0 never (the phase-
+                                  measured faster; 2 always (bf16 and FP8); 0 never (the phase-
                                   ordered kernel). get_info: the mode, 0 when the
                                   interleaved layout does not fit.                   */
   MOE_OPT_FLAT = 7,            /* MOE_SCHED_PERSISTENT runs with the expert-range

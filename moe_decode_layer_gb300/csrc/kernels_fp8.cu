@@ -11,7 +11,12 @@ static const void* pick(int phases) {
     case PH_R: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_FP8, MAXM, PH_R>);
     case PH_U: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_FP8, MAXM, PH_U>);
     case PH_D: return reinterpret_cast<const void*>(&moe_layer_kernel<FMT_FP8, MAXM, PH_D>);
-    case PH_ILV: return nullptr;  // FP8 runs the phase-ordered kernel and the chain only
+    case PH_ILV:  // the interleaved kernel: one row, or any row count up to 8
+      if constexpr (MAXM == 6) {
+        return nullptr;
+      } else {
+        return reinterpret_cast<const void*>(&moe_ilv_kernel<FMT_FP8, MAXM>);
+      }
     default: return nullptr;
   }
 }

@@ -2248,12 +2248,13 @@ __device__ __forceinline__ Ring ilv_items(const Ctx& c, const Route& rt, int s, 
 template <int FMT, int MAXM>
 __device__ __forceinline__ Ring ilv_down(const Ctx& c, const Route& rt, int s, Ring ring,
                                          float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch, bool active,
-                                         int nr) {
+                                         int nr, int r_lo) {
   const Params& p = c.p;
   const bool got = !c.aborted() && c.wait_full(ring);
   if (got && active) {
     const uint8_t* st = c.slot_ptr(ring.slot);
-    down_stage<FMT, MAXM>(p, st, reinterpret_cast<const float*>(st + p.d_hoff), rt.slot_mask[s], acc, g, ch, nr);
+    down_stage<FMT, MAXM>(p, st, reinterpret_cast<const float*>(st + p.d_hoff), rt.slot_mask[s], acc, g, ch, nr,
+                          FMT == FMT_FP8 ? fp8_scale_down(p, s < p.S ? -1 - s : rt.slot_e[s]) : nullptr, r_lo);
   }
   __syncwarp();
   if (got && c.lane == 0) c.release(ring, 1);
@@ -2457,7 +2458,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
       if (t < nsl) ring = ilv_items<FMT, MAXM>(c, rt, t, ring, rot, 0, kNC, p.q);
       while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t)
-        ring = ilv_down<FMT, MAXM>(c, rt, dnext++, ring, acc, g, ch, active, nr);
+        ring = ilv_down<FMT, MAXM>(c, rt, dnext++, ring, acc, g, ch, active, nr, r_lo);
     }
     if (c.tid == 0) c.stamp(ST_D_SUMMED);
     if (nr > 0) {

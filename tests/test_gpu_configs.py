@@ -192,7 +192,7 @@ def fp8layer():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("sched", ["persistent", "phased", "pdl_chain", "chain"])
+@pytest.mark.parametrize("sched", ["persistent", "phased", "interleaved", "pdl_chain", "chain"])
 @pytest.mark.parametrize("m", [1, 6])
 def test_fp8_ling_layer(fp8layer, sched, m):
     """Ling-shaped layer (H=2560, E=512 top-8 + 1 shared, I=768) with FP8 experts;
@@ -226,7 +226,7 @@ def test_fp8_small_shapes(shape):
     for m in (1, 2, 5, 8, 13, 16):
         x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=80 + m, rho=0.5)
         outs = []
-        for sched in ("persistent", "chain"):
+        for sched in ("persistent", "chain", "interleaved"):
             mod = MoEDecodeLayer(shape, layer, 16, sched=sched)
             xd = x.cuda()
             idx = torch.empty((m, shape.top_k), dtype=torch.int32, device="cuda")
@@ -237,7 +237,7 @@ def test_fp8_small_shapes(shape):
             helpers.assert_routing(idx.cpu(), w.cpu(), ridx, rw)
             helpers.assert_close(out.cpu(), ref, what=f"m={m} {sched}")
             outs.append(out.cpu())
-        assert torch.equal(outs[0], outs[1])
+        assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
 def test_fp8_activations_outside_fp16_range():
