@@ -50,7 +50,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE decode layer-step µs and achieved HBM GB/s (% of roofline), M=1 and M=6"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_EXTRA = "tiny_m1,ling_m6,ling_m16,stack_m6,nvfp4_m1,nvfp4_m6,ling_fp8_m1,ling_fp8_m6"
+DEFAULT_EXTRA = ("tiny_m1,ling_m6,ling_m16,stack_m6,nvfp4_m1,nvfp4_m6,ling_fp8_m1,ling_fp8_m6,"
+                 "ling_m1_seq,ling_m1_seq_off,ling_m6_seq,ling_m6_seq_off")
 
 from moe_decode_layer_gb300.synth import WORKLOADS  # noqa: E402
 
@@ -203,14 +204,14 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
     copies = nl if nl > 1 else args.copies
     layers = pool.get(wl["shape"], shape, copies, w2_layout_for(args, shape))
     mods = [MoEDecodeLayer(shape, layers[i], m, sched=args.sched, pre_rmsnorm=nl > 1) for i in range(copies)]
-    n_in = 64
+    n_in = args.inputs
     seq_rho = wl.get("seq_rho")
     if seq_rho is None:
         xs = [synth.hidden_rows(m, shape.hidden, seed=50_000 + 1000 * rank + j, rho=wl["rho"]).cuda()
               for j in range(n_in)]
     else:
         # step j runs layer copy j % copies on the next step of that copy's sequence
-        per = n_in // copies
+        per = max(1, n_in // copies)
         seqs = [synth.decode_sequence(per, m, shape.hidden, seed=60_000 + 1000 * rank + c, rho=wl["rho"],
                                       seq_rho=seq_rho) for c in range(copies)]
         xs = [seqs[j % copies][j // copies].cuda() for j in range(n_in)]
@@ -596,6 +597,9 @@ def main(argv=None):
                     help="down matrices [E,H,I] (row-block kernels) or transposed [E,I,H] (split-K kernel; "
                          "bf16 and fp8 workloads under --sched persistent)")
     ap.add_argument("--copies", type=int, default=8, help="distinct layer copies (single-layer workloads)")
+    ap.add_argument("--inputs", type=int, default=64,
+                    help="distinct input batches the steps rotate over (1: every step routes alike, for "
+                         "comparing one launch's DRAM traffic with its algorithmic bytes)")
     ap.add_argument("--prefetch", type=int, default=None,
                     help="experts of the previous step prefetched into L2 while routing (default: the workload's)")
     ap.add_argument("--lat-steps", type=int, default=256, help="single steps for the latency percentiles (>= 200)")
