@@ -304,37 +304,56 @@ struct ItemWalk {
 // --------------------------------------------------------------------------
 // consumer: x rows (arrive by bulk copy; optionally RMS-normalised in place)
 // --------------------------------------------------------------------------
-static __device__ __forceinline__ void prepare_x(const Ctx& c) {
+// row_max (NVFP4 / FP8 weights): also each row's largest |x| as bf16 bits into
+// MISC_XMAX + m (one warp per row, after the normalisation), while the router
+// stages are still landing; x_to_f16 scales by it after routing.
+static __device__ __forceinline__ void prepare_x(const Ctx& c, bool row_max = false) {
   const Params& p = c.p;
   if (!c.wait_bar(c.xbar, 0, SITE_RING_FULL)) return;
-  if (!p.pre_rmsnorm) return;
   uint4* xs = reinterpret_cast<uint4*>(c.sm + p.off_x);
   const int nch = p.H / 8;
-  for (int m = c.warp; m < p.M; m += kNC) {
-    float ss = 0.0f;
-    for (int ch = c.lane; ch < nch; ch += 32) {
-      const uint4 v = xs[m * nch + ch];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (p.pre_rmsnorm) {
+    for (int m = c.warp; m < p.M; m += kNC) {
+      float ss = 0.0f;
+      for (int ch = c.lane; ch < nch; ch += 32) {
+        const uint4 v = xs[m * nch + ch];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float a = bf16lo(w[q]), b = bf16hi(w[q]);
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
+        for (int q = 0; q < 4; ++q) {
+          const float a = bf16lo(w[q]), b = bf16hi(w[q]);
+          ss = fmaf(a, a, ss);
+          ss = fmaf(b, b, ss);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+      const float scale = 1.0f / sqrtf(ss / (float)p.H + p.rms_eps);
+      for (int ch = c.lane; ch < nch; ch += 32) {
+        const uint4 v = xs[m * nch + ch];
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t lo = f32_to_bf16_bits(bf16lo(w[q]) * scale);
+          const uint32_t hi = f32_to_bf16_bits(bf16hi(w[q]) * scale);
+          w[q] = lo | (hi << 16);
+        }
+        xs[m * nch + ch] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
+  }
+  if (row_max) {
+    __syncwarp();  // the warp's normalised rows before it reads them back
+    uint32_t* xmax = reinterpret_cast<uint32_t*>(c.misc + MISC_XMAX);
+    for (int m = c.warp; m < p.M; m += kNC) {
+      uint32_t a = 0u;  // |x| as bits: larger bits, larger value
+      for (int ch = c.lane; ch < nch; ch += 32) {
+        const uint4 v = xs[m * nch + ch];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-    const float scale = 1.0f / sqrtf(ss / (float)p.H + p.rms_eps);
-    for (int ch = c.lane; ch < nch; ch += 32) {
-      const uint4 v = xs[m * nch + ch];
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t lo = f32_to_bf16_bits(bf16lo(w[q]) * scale);
-        const uint32_t hi = f32_to_bf16_bits(bf16hi(w[q]) * scale);
-        w[q] = lo | (hi << 16);
+        for (int q = 0; q < 4; ++q) a = max(a, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
       }
-      xs[m * nch + ch] = make_uint4(w[0], w[1], w[2], w[3]);
+      a = warp_max_u32(a);
+      if (c.lane == 0) xmax[m] = a;
     }
   }
 }
@@ -758,21 +777,17 @@ __device__ __forceinline__ int xscale_exp(uint32_t maxbits) {
 // scaled back by 2^-k, exactly.
 static __device__ __forceinline__ void x_to_f16(const Ctx& c) {
   uint32_t* xw = reinterpret_cast<uint32_t*>(c.sm + c.p.off_x);
-  uint32_t* xmax = reinterpret_cast<uint32_t*>(c.misc + MISC_XMAX);
+  const uint32_t* xmax = reinterpret_cast<const uint32_t*>(c.misc + MISC_XMAX);  // prepare_x(row_max)
   const int hw = c.p.H / 2;  // words per row
-  if (c.tid < c.p.M) xmax[c.tid] = 0u;
-  bar_sync(kBarConsumers, kNC * 32);
-  for (int i = c.tid; i < c.p.M * hw; i += kNC * 32) {
-    const uint32_t v = xw[i];
-    const uint32_t a = max(v & 0x7fffu, (v >> 16) & 0x7fffu);  // |x| as bits: larger bits, larger value
-    if (a) atomicMax(xmax + i / hw, a);
-  }
-  bar_sync(kBarConsumers, kNC * 32);
-  for (int i = c.tid; i < c.p.M * hw; i += kNC * 32) {
-    const uint32_t v = xw[i];
-    const int k = xscale_exp(xmax[i / hw]);
-    const __half2 h = __floats2half2_rn(ldexpf(bf16lo(v), k), ldexpf(bf16hi(v), k));
-    xw[i] = *reinterpret_cast<const uint32_t*>(&h);
+  for (int m = 0; m < c.p.M; ++m) {
+    // 2^k as two exact factors, each inside fp32's normal range (|k| <= 147)
+    const int k = xscale_exp(xmax[m]), k1 = k / 2, k2 = k - k1;
+    const float s1 = __int_as_float((k1 + 127) << 23), s2 = __int_as_float((k2 + 127) << 23);
+    for (int i = c.tid; i < hw; i += kNC * 32) {
+      const uint32_t v = xw[m * hw + i];
+      const __half2 h = __floats2half2_rn(bf16lo(v) * s1 * s2, bf16hi(v) * s1 * s2);
+      xw[m * hw + i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
   }
 }
 
@@ -879,7 +894,9 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
     }
     if (rs.m >= 0) {
       if (FMT != FMT_BF16) xk = xscale_exp(reinterpret_cast<const uint32_t*>(c.misc + MISC_XMAX)[rs.m]);
-      float h = FMT != FMT_BF16 ? silu_f32(ldexpf(rs.g, -xk) * gsg) * (ldexpf(rs.u, -xk) * gsu)
+      // 2^-k as two exact factors (each inside fp32's normal range)
+      const float q1 = __int_as_float((127 - xk / 2) << 23), q2 = __int_as_float((127 - (xk - xk / 2)) << 23);
+      float h = FMT != FMT_BF16 ? silu_f32(rs.g * q1 * q2 * gsg) * (rs.u * q1 * q2 * gsu)
                                 : silu_f32(rs.g * gsg) * (rs.u * gsu);
       if (!shared) h *= rt.slot_w[slot * p.maxm + rs.m];
       if (FMT == FMT_NVFP4) h *= gs2;
@@ -2124,7 +2141,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     // ------------------------------------------------------------ consumers
     if (kChain) pdl_wait();
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
-    if (kNeedX) prepare_x(c);
+    if (kNeedX) prepare_x(c, FMT != FMT_BF16);
     bar_sync(kBarConsumers, kNC * 32);
     if (c.tid == 0) c.stamp(ST_X_LOADED);
     if (PHASES == PH_ALL && p.out_aliases_x && c.tid == 0)
@@ -2415,7 +2432,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
   } else {
     // ------------------------------------------------------------ consumers
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
-    prepare_x(c);
+    prepare_x(c, FMT != FMT_BF16);
     bar_sync(kBarConsumers, kNC * 32);
     if (c.tid == 0) c.stamp(ST_X_LOADED);
     if (p.out_aliases_x && c.tid == 0) st_tagged(p.xflags + blockIdx.x, c.epoch(), 0.0f);

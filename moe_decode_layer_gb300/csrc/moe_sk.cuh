@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
   } else {
     // ------------------------------------------------------------ consumers
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
-    prepare_x(c);
+    prepare_x(c, FMT != FMT_BF16);
     bar_sync(kBarConsumers, kNC * 32);
     if (c.tid == 0) c.stamp(ST_X_LOADED);
     Ring ring;
