@@ -16,9 +16,10 @@
 //   R  router rows (bf16) and the shared experts' gate/up rows: router logits and
 //      the shared experts' silu(g) * u; neither needs a routing decision.
 //   T  every CTA reads all logits and selects the top-k of each row itself, then
-//      forms the union of chosen experts from a bitmap with one row mask per
-//      expert and a popcount prefix over the expert ids (SGLang Low-Latency Mode
-//      page, section "Low-Latency-Specific Optimizations", item 3).
+//      forms the union of chosen experts from one row mask per expert and counts
+//      of the chosen ids below each expert (SGLang Low-Latency Mode page, section
+//      "Low-Latency-Specific Optimizations", item 3: with at most eight rows the
+//      experts are placed by row masks and population counts, not by a sort).
 //   U  gate/up rows of the chosen experts: h = w * silu(g) * u per (expert, row),
 //      SwiGLU in fp32 right after the dot products (blog section "Two fusions and
 //      a retune"). Row pairs of a stage go to different consumer warps.
@@ -66,7 +67,7 @@ namespace moe {
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kBarConsumers = 1;  // named barrier: the kNC consumer warps
 constexpr int kBarRoute = 2;      // named barrier: consumers -> producer, routing ready
-constexpr int kBarRouting = 3;    // named barrier: the routing warps (interleaved kernel)
+constexpr int kBarRouting = 3;    // named barrier: the routing warps (single-kernel schedules)
 constexpr int kStageBatch = 8;    // tagged words in flight per thread when staging h
 
 // --------------------------------------------------------------------------
@@ -932,8 +933,11 @@ enum ItemKind : int { ITEM_SHARED = 1, ITEM_ROUTED = 2 };
 // each consumer warp takes its items of every stage, computes the dot products
 // against the rows of x that chose the expert and publishes tagged h values.
 // Returns the ring position after the phase.
+// Warps w0 .. w0 + nw - 1 take the items, in stages of q items (0: the planned
+// stage size); the other warps walk the same stages without items.
 template <int FMT, int MAXM>
-__device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring) {
+__device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int kind, Ring ring, int w0 = 0,
+                                              int nw = kNC, int q = 0) {
   const Params& p = c.p;
   int lo, hi;
   if (kind == ITEM_SHARED) {
@@ -948,7 +952,10 @@ __device__ __forceinline__ Ring consume_items(const Ctx& c, const Route& rt, int
   load_xregs<FMT, MAXM>(c, xr);
   const int nsl_ring = kind == ITEM_ROUTED ? p.nslots + p.nslots_x : p.nslots;
   ring.fit(nsl_ring);
-  for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(nsl_ring)) {
+  ItemWalk w(lo, hi, q > 0 ? q : p.q, p.I);
+  w.w0 = w0;
+  w.nw = nw;
+  for (; w.more(); ring.next(nsl_ring)) {
     item_stage<FMT, MAXM>(c, rt, w, ring, w.u + slot0, kind == ITEM_SHARED, xr, xs, w.a == lo);
     w.advance(w.count());
   }
@@ -1024,22 +1031,26 @@ __device__ __forceinline__ float sigmoid_f32(float v) { return 1.0f / (1.0f + ex
 // every expert's selection key in registers (lane l holds experts l + 32 i,
 // PM * 32 >= E). The K-th largest of the 32 lane maxima bounds the K-th largest
 // key from below -- those K lane maxima are K distinct experts -- so every
-// selected expert's key is at or above it. It is found by rounds of a warp-wide
-// maximum (redux) over the lane maxima; the few candidates at or above it go to
-// shared memory at positions given by an exclusive count over the lanes (built
-// from ballots of the count's bits), and each is ranked against all of them on
-// exact 64-bit keys (ties: the lower expert id). With more than kCandMax - 1
-// candidates (many keys tied in value), K rounds of a warp-wide maximum select
-// instead. On this path one warp's dependent chain is the routing latency every
-// CTA waits for, so it uses reductions and ballots rather than shuffles, and
-// shared memory where a value must reach every lane.
+// selected expert's key is at or above it. It is found by K rounds of a
+// warp-wide maximum (redux) over the lane maxima, each round retiring the lanes
+// that hold the round's value (lanes tied on a value leave together, which can
+// only lower the bound); the first round gives the largest key. The few
+// candidates at or above the bound go to shared memory at positions given by an
+// exclusive count over the lanes (built from ballots of the count's bits), and
+// each is ranked against all of them on exact 64-bit keys (ties: the lower
+// expert id); the lane that ranks a selected expert also computes its weight
+// numerator. With more than kCandMax - 1 candidates (many keys tied in value), K
+// rounds of a warp-wide maximum select instead. On this path one warp's
+// dependent chain is the routing latency every CTA waits for, so it uses
+// reductions and ballots rather than shuffles, and shared memory where a value
+// must reach every lane. The expert row masks (rt.emask) are set for M > 1 only.
 template <int PM>
 __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, bool write_topk) {
   const Params& p = c.p;
   const int E = p.E, K = p.K, lane = c.lane;
-  float* lg = reinterpret_cast<float*>(c.sm + p.off_lg) + (size_t)m * E;
+  const float* lg = reinterpret_cast<const float*>(c.sm + p.off_lg) + (size_t)m * E;
   const float* bias = reinterpret_cast<const float*>(c.sm + p.off_bias);
-  float* wx = reinterpret_cast<float*>(c.sm + p.off_lmax) + m * 32;  // numerators of the weights
+  float* wx = reinterpret_cast<float*>(c.sm + p.off_lmax) + m * 32;  // numerators of the weights, by rank
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(c.sm + p.off_cand) + (size_t)m * kCandMax;
   uint32_t key[PM];
   if (p.score) {  // bias-corrected sigmoid rule: select on sigmoid(l) + b
@@ -1062,13 +1073,14 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
   for (int h = PM / 2; h >= 1; h >>= 1)
 #pragma unroll
     for (int i = 0; i < h; ++i) t[i] = max(t[i], t[i + h]);
-  // the K-th largest lane maximum: lanes tied on a value leave in the same round
-  uint32_t T = 0, lk = t[0];
-  for (int got = 0; got < K;) {
+  // the bound: K rounds over the lane maxima
+  uint32_t lk = t[0];
+  const uint32_t Tmax = warp_max_u32(lk);
+  uint32_t T = Tmax;
+  lk = lk == T ? 0u : lk;
+  for (int r = 1; r < K; ++r) {
     T = warp_max_u32(lk);
-    const bool hit = lk == T;
-    got += __popc(__ballot_sync(kFull, hit));
-    lk = hit ? 0u : lk;
+    lk = lk == T ? 0u : lk;
   }
   uint32_t fm = 0;
 #pragma unroll
@@ -1085,6 +1097,12 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
   }
   int* sel_e = rt.sel_e + m * K;
   float* sel_w = rt.sel_w + m * K;
+  // weight numerator of a selected key: exp(l - l_max) (softmax rule; l_max is
+  // the largest key's logit) or sigmoid(l) (bias rule)
+  const float lmax = order_key_f32(Tmax);
+  auto numer = [&](unsigned long long v) {
+    return p.score ? sigmoid_f32(lg[key_expert(v)]) : expf(key_value(v) - lmax);
+  };
   if (C < kCandMax) {
 #pragma unroll
     for (int i = 0; i < PM; ++i)
@@ -1100,7 +1118,10 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
         const ulonglong2 q = c2[j];
         r += (q.x > v) + (q.y > v);
       }
-      if (r < K) sel_e[r] = key_expert(v);
+      if (r < K) {
+        sel_e[r] = key_expert(v);
+        wx[r] = numer(v);
+      }
     }
   } else {
     unsigned long long last = ~0ull;
@@ -1113,126 +1134,104 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
         if (k < last && k > b) b = k;
       }
       last = warp_max_u64(b);
-      if (lane == 0) sel_e[j] = key_expert(last);
+      if (lane == 0) {
+        sel_e[j] = key_expert(last);
+        wx[j] = numer(last);
+      }
     }
   }
   __syncwarp();
-  // weights in selection order: exp(l_j - l_0) / sum (softmax rule, l_0 the
-  // largest selected logit) or sigmoid(l_j) / sum (bias rule); every lane sums
-  // the K numerators in selection order
-  const int ej = lane < K ? sel_e[lane] : 0;
-  const float lj = lg[ej];
-  const float num = lane < K ? (p.score ? sigmoid_f32(lj) : expf(lj - lg[sel_e[0]])) : 0.0f;
-  wx[lane] = num;
-  __syncwarp();
+  // weights in selection order: every lane sums the K numerators in order
   float sum = 0.0f;
-  const float4* w4 = reinterpret_cast<const float4*>(wx);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float4 q = w4[j];
-    sum += q.x;
-    sum += q.y;
-    sum += q.z;
-    sum += q.w;
-  }
-  __syncwarp();  // every lane has read lg and wx before they are overwritten
+  for (int j = 0; j < K; ++j) sum += wx[j];
   if (lane < K) {
-    const float w = num / sum;
-    atomicOr(&rt.emask[ej], 1u << m);
-    atomicOr(&rt.bitmap[ej >> 5], 1u << (ej & 31));
+    const int ej = sel_e[lane];
+    const float w = wx[lane] / sum;
+    if (p.M > 1) atomicOr(&rt.emask[ej], 1u << m);
     if (write_topk && blockIdx.x == 0) {
       if (p.topk_idx) p.topk_idx[m * K + lane] = ej;
       if (p.topk_w) p.topk_w[m * K + lane] = w;
     }
     sel_w[lane] = w;
-    lg[ej] = w;  // the union reads the combine weight of (row m, expert e) here
   }
 }
 
-// The union of chosen experts on warp 0, in one pass over the bitmap: lane l
-// owns word l (experts 32 l ..); one warp scan of (pairs, experts) per word
-// gives every slot (ascending expert id, after the S shared slots) and its pair
-// base; each lane then writes its slots' tables, combine weights (left by the
-// top-k in the logits array) and (slot, row) pairs, and counts how many slot
-// starts lie at or below the CTA's cost boundaries for the gate/up split.
-__device__ __forceinline__ void union_warp(const Ctx& c, const Route& rt) {
+// The union of the experts chosen by M > 1 rows, one thread per (row, selected
+// expert) pair (nthr threads meeting at named barrier `bar`; M * K <= 64 pairs).
+// Each pair thread marks whether its row is the lowest one that chose its expert;
+// then it counts, over all pairs, the pairs and the distinct experts with a
+// smaller id: its slot is S + (distinct experts below), its (slot, row) pair
+// index follows the slot's pair base in ascending row order. The thread of each
+// expert's lowest row writes the slot's tables and checks whether one of this
+// CTA's gate/up cost boundaries falls in its slot's cost interval
+// [cum(u), cum(u + 1)), cum(u) = I * (item_base * u + pairs before slot u).
+__device__ __forceinline__ void union_rows(const Ctx& c, const Route& rt, int nthr, int bar) {
   const Params& p = c.p;
-  const int lane = c.lane, S = p.S, M = p.M;
-  const int words = (p.E + 31) / 32;
-  const float* wgt = reinterpret_cast<const float*>(c.sm + p.off_lg);  // [M][E]: weights of the selected
+  const int M = p.M, K = p.K, S = p.S, np = M * K;
   int* psr = reinterpret_cast<int*>(c.sm + p.off_pair_sr);
-  const uint32_t w = lane < words ? rt.bitmap[lane] : 0u;
-  int npairs = 0;
-  for (uint32_t b = w; b; b &= b - 1) npairs += __popc(rt.emask[lane * 32 + __ffs(b) - 1]);
-  // exclusive warp scan of (pairs << 16 | experts)
-  const uint32_t v = ((uint32_t)npairs << 16) | (uint32_t)__popc(w);
-  uint32_t inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, inc, o);
-    if (lane >= o) inc += y;
+  int* fl = reinterpret_cast<int*>(c.sm + p.off_cand);  // [np]: expert << 1 | lowest row (the top-k is done with it)
+  for (int t = c.tid; t < np; t += nthr) {
+    const int e = rt.sel_e[t], m = t / K;
+    fl[t] = (e << 1) | (int)(m == __ffs(rt.emask[e]) - 1);
   }
-  const uint32_t exc = inc - v, all = __shfl_sync(kFull, inc, 31);
-  const int total = (int)(all & 0xffffu), tpairs = (int)(all >> 16);
-  // the cost split: cum(u) = I * (item_base * u + pairs before routed slot u)
+  bar_sync(bar, nthr);
   const uint32_t I = (uint32_t)p.I, base = (uint32_t)p.item_base;
-  const uint32_t tcost = I * (base * (uint32_t)total + (uint32_t)tpairs);  // <= 2^23
-  const uint32_t t0 = tcost * blockIdx.x / (uint32_t)p.grid, t1 = tcost * (blockIdx.x + 1) / (uint32_t)p.grid;
-  int n0 = 0, n1 = 0;
-  int u = (int)(exc & 0xffffu), q = (int)(exc >> 16);  // routed slot index and pairs before it
-  for (uint32_t b = w; b; b &= b - 1) {
-    const int e = lane * 32 + __ffs(b) - 1;
+  for (int t = c.tid; t < np; t += nthr) {
+    const int e = rt.sel_e[t], m = t / K;
     const uint32_t msk = rt.emask[e];
-    const int sl = S + u;
-    const uint32_t cu = I * (base * (uint32_t)u + (uint32_t)q);
-    n0 += cu <= t0;
-    n1 += cu <= t1;
-    rt.slot_of[e] = sl;
-    rt.slot_e[sl] = e;
-    rt.slot_mask[sl] = msk;
-    rt.pair_base[sl] = S * M + q;
-    for (uint32_t mm = msk; mm; mm &= mm - 1) {
-      const int m = __ffs(mm) - 1;
-      rt.slot_w[sl * p.maxm + m] = wgt[m * p.E + e] * p.routed_scale;
-      psr[S * M + q] = (sl << 4) | m;
-      ++q;
+    int pb = 0, sb = 0, tot = 0;  // pairs and experts below e, experts in all
+    const int4* f4 = reinterpret_cast<const int4*>(fl);
+    for (int j = 0; j < np / 4; ++j) {
+      const int4 q = f4[j];
+      const int v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int below = (v[k] >> 1) < e;
+        pb += below;
+        sb += below & v[k];
+        tot += v[k] & 1;
+      }
     }
-    ++u;
+    for (int j = np & ~3; j < np; ++j) {
+      const int v = fl[j], below = (v >> 1) < e;
+      pb += below;
+      sb += below & v;
+      tot += v & 1;
+    }
+    const int sl = S + sb;
+    rt.slot_w[sl * p.maxm + m] = rt.sel_w[t] * p.routed_scale;
+    psr[S * M + pb + __popc(msk & ((1u << m) - 1u))] = (sl << 4) | m;
+    if (m == __ffs(msk) - 1) {
+      rt.slot_of[e] = sl;
+      rt.slot_e[sl] = e;
+      rt.slot_mask[sl] = msk;
+      rt.pair_base[sl] = S * M + pb;
+      const uint32_t tcost = I * (base * (uint32_t)tot + (uint32_t)np);  // <= 2^23
+      const uint32_t t0 = tcost * blockIdx.x / (uint32_t)p.grid, t1 = tcost * (blockIdx.x + 1) / (uint32_t)p.grid;
+      const uint32_t wu = base + (uint32_t)__popc(msk);
+      const uint32_t cu = I * (base * (uint32_t)sb + (uint32_t)pb), cn = cu + I * wu;
+      // each boundary: the first item at or after its cost, in the slot whose interval holds it
+      if (cu <= t0 && t0 < cn) c.misc[MISC_ULO] = sb * p.I + (int)((t0 - cu + wu - 1) / wu);
+      if (cu <= t1 && t1 < cn) c.misc[MISC_UHI] = sb * p.I + (int)((t1 - cu + wu - 1) / wu);
+      if (sb == 0) {  // once: the end of the sequence
+        rt.pair_base[S + tot] = S * M + np;
+        c.misc[MISC_NROUTED] = tot;
+        if (tcost <= t0) c.misc[MISC_ULO] = tot * p.I;
+        if (tcost <= t1) c.misc[MISC_UHI] = tot * p.I;
+      }
+    }
   }
-  for (int t = lane; t < S; t += 32) {
+  for (int t = c.tid; t < S; t += nthr) {
     rt.slot_e[t] = -1 - t;
     rt.slot_mask[t] = (1u << M) - 1u;
     rt.pair_base[t] = t * M;
     for (int m = 0; m < p.maxm; ++m) rt.slot_w[t * p.maxm + m] = 1.0f;
     for (int m = 0; m < M; ++m) psr[t * M + m] = (t << 4) | m;
   }
-  if (lane == 0) {
-    rt.pair_base[S + total] = S * M + tpairs;
-    c.misc[MISC_NROUTED] = total;
-    n0 += tcost <= t0;  // the end of the sequence, u = total
-    n1 += tcost <= t1;
-  }
-  const int u0 = (int)__reduce_add_sync(kFull, (uint32_t)n0) - 1;
-  const int u1 = (int)__reduce_add_sync(kFull, (uint32_t)n1) - 1;
-  // each boundary: the first item at or after its cost, found by the lane that owns its slot
-  u = (int)(exc & 0xffffu);
-  q = (int)(exc >> 16);
-  for (uint32_t b = w; b; b &= b - 1) {
-    const int n = __popc(rt.emask[lane * 32 + __ffs(b) - 1]);
-    const uint32_t cu = I * (base * (uint32_t)u + (uint32_t)q), wu = base + (uint32_t)n;
-    if (u == u0) c.misc[MISC_ULO] = u * p.I + (int)((t0 - cu + wu - 1) / wu);
-    if (u == u1) c.misc[MISC_UHI] = u * p.I + (int)((t1 - cu + wu - 1) / wu);
-    q += n;
-    ++u;
-  }
-  if (lane == 0) {
-    if (u0 >= total) c.misc[MISC_ULO] = total * p.I;
-    if (u1 >= total) c.misc[MISC_UHI] = total * p.I;
-  }
 }
 
 // The union for a single token row on warp 0: the K selected experts in
-// ascending id become slots S.., one pair each; the same tables as union_warp
+// ascending id become slots S.., one pair each; the same tables as union_rows
 // builds. Each lane counts the selected ids below its own from shared memory
 // (broadcast loads, no shuffles). The gate/up split bounds of a single row do
 // not depend on the routing and were set before it (one_row_split).
@@ -1351,11 +1350,10 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
   }
   bar_sync(bar, nthr);
   if (c.tid == 0) c.stamp(ST_TOPK);
-  if (c.warp == 0) {
-    if (p.M == 1)
-      union_one_row(c, rt);
-    else
-      union_warp(c, rt);
+  if (p.M == 1) {
+    if (c.warp == 0) union_one_row(c, rt);
+  } else {
+    union_rows(c, rt, nthr, bar);
   }
   bar_sync(bar, nthr);
 }
@@ -1456,6 +1454,36 @@ __device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, c
       const int r = min(g + ri * p.ng, nr - 1);
       sv[ri] = __ldg(s2 + (size_t)((row0 + r) / kFp8Block) * (p.I / kFp8Block) + (8 * ch) / kFp8Block);
     }
+  }
+  if constexpr (FMT == FMT_BF16 && MAXM > 1 && MAXM <= 6) {
+    // each weight widened once and used for every row that chose the expert
+    // (the registers allow it up to six rows)
+    float wf[RPG][8];
+#pragma unroll
+    for (int ri = 0; ri < RPG; ++ri) {
+      const int r = min(g + ri * p.ng, nr - 1);
+      const uint4 v = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        wf[ri][2 * q] = bf16lo(vw[q]);
+        wf[ri][2 * q + 1] = bf16hi(vw[q]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      if (!(mask >> m & 1u)) continue;
+      const float* hrow = hs + (size_t)hp * p.I;
+      ++hp;
+      const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
+      const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
+      const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int ri = 0; ri < RPG; ++ri)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[ri][m] = fmaf(wf[ri][k], hv[k], acc[ri][m]);
+    }
+    return;
   }
 #pragma unroll
   for (int m = 0; m < MAXM; ++m) {
@@ -1917,7 +1945,8 @@ struct Producer {
 
   // Gate/up stages: consecutive rows of one expert as a gate block and an up
   // block (plus the two scale blocks for NVFP4).
-  __device__ __forceinline__ void pairs(bool shared_phase, const Route& rt) {
+  // q: items per stage (0: the planned stage size).
+  __device__ __forceinline__ void pairs(bool shared_phase, const Route& rt, int q = 0) {
     const Params& p = c.p;
     int lo, hi;
     if (shared_phase) {
@@ -1928,7 +1957,7 @@ struct Producer {
     }
     const int nsl_ring = shared_phase ? p.nslots : p.nslots + p.nslots_x;
     ring.fit(nsl_ring);
-    for (ItemWalk w(lo, hi, p.q, p.I); w.more(); ring.next(nsl_ring)) {
+    for (ItemWalk w(lo, hi, q > 0 ? q : p.q, p.I); w.more(); ring.next(nsl_ring)) {
       const int nq = w.count();
       const int slot = w.u + (shared_phase ? 0 : p.S);
       uint32_t dst, bar;
@@ -2094,7 +2123,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
       }
       if (PHASES & PH_R) {
-        pr.pairs(true, rt);
+        // single kernel: the shared stages are sized for the warps that do not route
+        pr.pairs(true, rt, PHASES == PH_ALL ? ilv_sq(p) : 0);
         c.stamp(ST_P_R_ISSUED);
         if (PHASES & PH_D) pr.prefetch_shared_down();
         pr.prefetch_predicted();
@@ -2105,7 +2135,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     }
     if (kRoute) {
       __syncwarp();
-      bar_sync(kBarRoute, kThreads);
+      bar_sync(kBarRoute, PHASES == PH_ALL ? (ilv_nrw(p) + 1) * 32 : kThreads);
     }
     if (c.lane == 0) {
       c.stamp(ST_P_ROUTE);
@@ -2147,40 +2177,68 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     if (PHASES == PH_ALL && p.out_aliases_x && c.tid == 0)
       st_tagged(p.xflags + blockIdx.x, c.epoch(), 0.0f);
     Ring ring;
-    if (PHASES & PH_R) {
+    if constexpr (PHASES == PH_ALL) {
+      // Every warp computes this CTA's router rows; then warps 0 .. nrw - 1
+      // route while the others compute the shared experts' gate/up items.
       ring = consume_router<MAXM>(c, ring);
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
       if (c.tid == 0) {
         count_done(p, CTRL_RCOUNT);
         c.stamp(ST_RFLAG);
       }
-    }
-    if (kRoute) {
-      route_rows(c, rt, (PHASES & PH_U) != 0);
-      if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
-      bar_arrive(kBarRoute, kThreads);
-      if (c.tid == 0) c.stamp(ST_ROUTED);
-    }
-    if (FMT != FMT_BF16 && kNeedX) {  // the router is done with the bf16 x rows
-      x_to_f16(c);
-      bar_sync(kBarConsumers, kNC * 32);
-    }
-    // gate/up items: the shared experts' (their stages were issued before
-    // routing), then the routed experts'; one loop so that the code exists once
-    constexpr int kKind0 = (PHASES & PH_R) ? ITEM_SHARED : ITEM_ROUTED;
-    constexpr int kKind1 = (PHASES & PH_U) ? ITEM_ROUTED : ITEM_SHARED;
-    if (PHASES & (PH_R | PH_U)) {
+      if (FMT != FMT_BF16) {  // the router is done with the bf16 x rows
+        x_to_f16(c);
+        bar_sync(kBarConsumers, kNC * 32);
+      }
+      const int nrw = ilv_nrw(p);
+      if (c.warp < nrw) {
+        route_rows(c, rt, true, nrw * 32, kBarRouting);
+        if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
+        bar_arrive(kBarRoute, (nrw + 1) * 32);
+        if (c.tid == 0) c.stamp(ST_ROUTED);
+      }
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring, nrw, kNC - nrw, ilv_sq(p));
+      fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
+      bar_sync(kBarConsumers, kNC * 32);  // the routing tables, and this CTA's shared h rows all stored
+      if (c.tid == 0) {
+        c.stamp(ST_R_DONE);
+        if (p.S > 0 && p.hs_nbuf == 2) {
+          __threadfence();  // release them with the count
+          count_done(p, CTRL_SCOUNT);
+        }
+      }
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_ROUTED, ring);
+      fence_proxy_async_global();
+      if (c.tid == 0) c.stamp(ST_U_DONE);
+    } else {
+      if (PHASES & PH_R) {
+        ring = consume_router<MAXM>(c, ring);
+        bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
+        if (c.tid == 0) {
+          count_done(p, CTRL_RCOUNT);
+          c.stamp(ST_RFLAG);
+        }
+      }
+      if (kRoute) {
+        route_rows(c, rt, (PHASES & PH_U) != 0);
+        if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
+        bar_arrive(kBarRoute, kThreads);
+        if (c.tid == 0) c.stamp(ST_ROUTED);
+      }
+      if (FMT != FMT_BF16 && kNeedX) {  // the router is done with the bf16 x rows
+        x_to_f16(c);
+        bar_sync(kBarConsumers, kNC * 32);
+      }
+      // gate/up items: the shared experts' (their stages were issued before
+      // routing), then the routed experts'; one loop so that the code exists once
+      constexpr int kKind0 = (PHASES & PH_R) ? ITEM_SHARED : ITEM_ROUTED;
+      constexpr int kKind1 = (PHASES & PH_U) ? ITEM_ROUTED : ITEM_SHARED;
+      if (PHASES & (PH_R | PH_U)) {
 #pragma unroll 1
-      for (int kind = kKind0; kind <= kKind1; ++kind) {
-        ring = consume_items<FMT, MAXM>(c, rt, kind, ring);
-        fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
-        if (c.tid == 0) c.stamp(kind == ITEM_SHARED ? ST_R_DONE : ST_U_DONE);
-        if (PHASES == PH_ALL && kind == ITEM_SHARED && p.S > 0 && p.hs_nbuf == 2) {
-          bar_sync(kBarConsumers, kNC * 32);  // this CTA's shared h rows are all stored
-          if (c.tid == 0) {
-            __threadfence();  // release them with the count
-            count_done(p, CTRL_SCOUNT);
-          }
+        for (int kind = kKind0; kind <= kKind1; ++kind) {
+          ring = consume_items<FMT, MAXM>(c, rt, kind, ring);
+          fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
+          if (c.tid == 0) c.stamp(kind == ITEM_SHARED ? ST_R_DONE : ST_U_DONE);
         }
       }
     }
