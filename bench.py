@@ -347,8 +347,9 @@ def run_workload(name, args, rank, world, dist, pool, steps, warmup, lat_steps, 
         for s in range(e2e_steps):
             mods[s % copies].run_host(xh[s % n_in], xh[s % n_in], oh)
         e2e_s = time.perf_counter() - te
-        h2d, d2h = m * shape.hidden * 2, m * shape.hidden * 2  # x (also the residual) in, out back
-        e2e_path = "moe_decode_run_host (pinned host buffers; x doubles as the residual; copies + sync each step)"
+        h2d, d2h = mods[0].host_copy_bytes(m)  # x (also the residual) in; status words and out back
+        e2e_path = ("moe_decode_run_host (pinned host buffers; x doubles as the residual; one copy in, "
+                    "one copy of status words + outputs back, sync each step)")
     else:
         if dist is not None:
             dist.barrier()

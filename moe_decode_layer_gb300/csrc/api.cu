@@ -37,7 +37,10 @@ struct moe_decode_handle {
   uint16_t* stage_out = nullptr;
   int32_t* stage_idx = nullptr;
   float* stage_w = nullptr;
-  uint32_t* host_status = nullptr;  // pinned host words: the status read back by run_host
+  // run_host read-back: the device block [status words .. top-k .. output rows]
+  // (contiguous after the control words) and its pinned host copy
+  uint8_t* host_rb = nullptr;
+  size_t rb_si = 0, rb_sw = 0, rb_so = 0;  // byte offsets of topk_idx, topk_w, out in the block
 };
 
 namespace {
@@ -673,16 +676,22 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
       if (blocks < 1) return MOE_ERR_UNSUPPORTED;
     }
   }
-  // scratch: control words | logits | h | x flags | run_host staging
+  // scratch: control words and the run_host outputs | logits | h | x flags | run_host inputs
   const size_t H = cfg->hidden, I = cfg->inter, E = cfg->num_experts, K = cfg->top_k;
   const size_t maxm = cfg->max_rows;
-  size_t off = 0;
+  // the control words (the status among them), then run_host's topk_idx, topk_w and
+  // output rows: one device-to-host copy brings back a run's results and status
+  const size_t o_ctrl = 0;
+  const size_t o_si = round_up(moe::CTRL_WORDS * 4, 16);
+  const size_t o_sw = o_si + round_up(maxm * K * 4, 16);
+  const size_t o_so = o_sw + round_up(maxm * K * 4, 16);
+  const size_t rb_bytes = o_so + maxm * H * 2;
+  size_t off = round_up(rb_bytes, 256);
   auto take = [&](size_t bytes) {
     const size_t at = off;
     off = round_up(off + bytes, 256);
     return at;
   };
-  const size_t o_ctrl = take(moe::CTRL_WORDS * 4);
   const size_t o_logits = take(moe::kLogitRep * maxm * E * 8);
   const size_t o_h = take((size_t)moe::kHRep * p.npair_max * I * 4);
   const size_t o_xf = take((size_t)p.grid * 8);
@@ -697,9 +706,6 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   const size_t hist_end = off;
   const size_t o_sx = take(maxm * H * 2);
   const size_t o_sr = take(maxm * H * 2);
-  const size_t o_so = take(maxm * H * 2);
-  const size_t o_si = take(maxm * K * 4);
-  const size_t o_sw = take(maxm * K * 4);
   auto* h = new (std::nothrow) moe_decode_handle();
   if (!h) return MOE_ERR_OOM;
   if (cudaMalloc(&h->scratch, off) != cudaSuccess) {
@@ -707,7 +713,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
     delete h;
     return MOE_ERR_OOM;
   }
-  if (cudaHostAlloc(reinterpret_cast<void**>(&h->host_status), 2 * sizeof(uint32_t), cudaHostAllocDefault) !=
+  if (cudaHostAlloc(reinterpret_cast<void**>(&h->host_rb), rb_bytes, cudaHostAllocDefault) !=
       cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->scratch);
@@ -720,7 +726,7 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
       cudaMemset(base + o_hist, 0xff, hist_end - o_hist) != cudaSuccess ||
 
       cudaDeviceSynchronize() != cudaSuccess) {
-    cudaFreeHost(h->host_status);
+    cudaFreeHost(h->host_rb);
     cudaFree(h->scratch);
     delete h;
     return MOE_ERR_CUDA;
@@ -756,6 +762,9 @@ moe_status moe_decode_create(const moe_decode_config* cfg, const moe_decode_weig
   h->stage_out = reinterpret_cast<uint16_t*>(base + o_so);
   h->stage_idx = reinterpret_cast<int32_t*>(base + o_si);
   h->stage_w = reinterpret_cast<float*>(base + o_sw);
+  h->rb_si = o_si;
+  h->rb_sw = o_sw;
+  h->rb_so = o_so;
   h->base = p;
   h->max_slots = p.nslots;
   h->has_ilv = has_ilv;
@@ -838,16 +847,20 @@ moe_status moe_decode_run_host(moe_decode_handle* h, const void* x_host, const v
                                  topk_idx_host ? h->stage_idx : nullptr,
                                  topk_w_host ? h->stage_w : nullptr, stream);
   if (st != MOE_OK) return st;
-  // results and the device status word back in the same stream, then one wait
-  if (cudaMemcpyAsync(out_host, h->stage_out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      (topk_idx_host &&
-       cudaMemcpyAsync(topk_idx_host, h->stage_idx, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-      (topk_w_host && cudaMemcpyAsync(topk_w_host, h->stage_w, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-      cudaMemcpyAsync(h->host_status, h->base.ctrl + moe::CTRL_STATUS, 2 * sizeof(uint32_t),
-                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  // the status words, top-k outputs and output rows back as one contiguous block
+  // (they follow each other after the control words), then one wait
+  const size_t skip = moe::CTRL_STATUS * sizeof(uint32_t);
+  const size_t end = h->rb_so + bytes;
+  if (cudaMemcpyAsync(h->host_rb + skip, static_cast<uint8_t*>(h->scratch) + skip, end - skip, cudaMemcpyDeviceToHost,
+                      s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (h->host_status[0] == 0) return MOE_OK;
+  std::memcpy(out_host, h->host_rb + h->rb_so, bytes);
+  if (topk_idx_host) std::memcpy(topk_idx_host, h->host_rb + h->rb_si, kb);
+  if (topk_w_host) std::memcpy(topk_w_host, h->host_rb + h->rb_sw, kb);
+  uint32_t status;
+  std::memcpy(&status, h->host_rb + skip, sizeof(status));
+  if (status == 0) return MOE_OK;
   if (cudaMemsetAsync(h->base.ctrl + moe::CTRL_STATUS, 0, 2 * sizeof(uint32_t), s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -952,7 +965,7 @@ moe_status moe_decode_get_info(moe_decode_handle* h, int32_t what, int64_t* valu
 moe_status moe_decode_destroy(moe_decode_handle* h) {
   if (!h) return MOE_OK;
   cudaError_t e = cudaFree(h->scratch);  // cudaFree waits for outstanding work
-  const cudaError_t eh = h->host_status ? cudaFreeHost(h->host_status) : cudaSuccess;
+  const cudaError_t eh = h->host_rb ? cudaFreeHost(h->host_rb) : cudaSuccess;
   delete h;
   return e == cudaSuccess && eh == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

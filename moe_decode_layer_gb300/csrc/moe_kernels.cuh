@@ -1729,16 +1729,20 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         }
         const uint64_t tw = p.stamps ? global_ns() : 0;
         const bool got = !c.aborted() && c.wait_full(ring);
-        if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, global_ns() - tw);
+        const uint64_t tm = p.stamps ? global_ns() : 0;
+        if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, tm - tw);
         if (got && have && active)
           down_stage<FMT, MAXM>(p, c.slot_ptr(ring.slot, true), hs + (size_t)(rt.pair_base[sl] - rt.pair_base[sl0]) * p.I,
                                 mask, acc, g, ch, nr, FMT == FMT_FP8 ? fp8_scale_down(p, sl < p.S ? -1 - sl : rt.slot_e[sl]) : nullptr,
                                 rb_lo);
         __syncwarp();
+        if (p.stamps && c.tid == 0) c.count(ST_D_MATH_NS, global_ns() - tm);
         if (got && c.lane == 0) c.release(ring, 1);
       }
       if (!per_slot) {
+        const uint64_t tb = p.stamps ? global_ns() : 0;
         bar_sync(kBarConsumers, kNC * 32);  // h buffer b is free again
+        if (p.stamps && c.tid == 0) c.count(ST_D_BAR_NS, global_ns() - tb);
         if (c.tid == 0) issue_ready(used + 1 + nbuf, false);
       }
       ++used;

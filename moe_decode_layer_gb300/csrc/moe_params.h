@@ -90,12 +90,12 @@ enum Stamp : int {
   ST_LOGITS = 12,     // all router logits seen (routing warp 0)
   ST_TOPK = 13,       // top-k of row 0 done
   ST_U_FLAGS = 14,    // the gate/up-done count reached the grid size
-  ST_ROUTER_DATA = 15,// warp 0's first router stage landed
   ST_RFLAG = 16,      // this CTA counted its router logits as stored
   ST_U_DATA = 17,     // warp 0's first routed gate/up stage landed
   ST_RCOUNT = 18,     // the router-done count reached the grid size
   ST_D_HWAIT_NS = 7,     // (sum, thread 0) ns waiting for h batches in the down phase
-  ST_LOGIT_ROUNDS = 21,  // (count) poll rounds of the logits
+  ST_D_MATH_NS = 20,     // (sum, thread 0) ns in the down-stage arithmetic
+  ST_D_BAR_NS = 21,      // (sum, thread 0) ns at the down phase's per-batch barriers
   ST_D_WAIT_NS = 22,     // (sum, warp 0) ns down-phase warp 0 waited for its stages
   ST_CLOCK_MHZ = 23,  // (value) SM clock cycles per microsecond over the kernel
   kStampSlots = 24

@@ -112,6 +112,16 @@ class MoEDecodeLayer:
                    "moe_decode_run_host")
         return out
 
+    def host_copy_bytes(self, m: int) -> tuple[int, int]:
+        """Bytes run_host copies per call with m rows and x as the residual: (in, out).
+        Out is one block from the status words to the m-th output row: the rest of the
+        CTRL_WORDS control words, topk_idx and topk_w for max_rows rows (each padded
+        to 16 bytes), then the output rows."""
+        pad16 = lambda v: (v + 15) // 16 * 16  # noqa: E731
+        k = self.shape.top_k
+        out = _lib.CTRL_WORDS * 4 - 8 + 2 * pad16(self.max_rows * k * 4) + m * self.shape.hidden * 2
+        return m * self.shape.hidden * 2, out
+
     def status(self, stream=None) -> int:
         """Synchronise and return (and clear) the device status code."""
         return self.lib.moe_decode_get_status(self.handle, _stream_ptr(stream))
