@@ -125,6 +125,14 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   p.tg = p.nchunk_i;
   p.ng = moe::kNC * 32 / p.tg;
   p.pair_bytes = 2 * (p.row13 + p.sc13);
+  if (p.fmt == moe::FMT_FP8) {
+    // the expert's whole block-scale matrix rides behind each of its stages (bulk
+    // copies need multiples of 16 bytes; else the consumers read them from global)
+    const size_t s13 = (size_t)(2 * I / moe::kFp8Block) * (H / moe::kFp8Block) * 4;
+    const size_t s2 = (size_t)(H / moe::kFp8Block) * (I / moe::kFp8Block) * 4;
+    p.sc13e = (s13 % 16 == 0 && s13 <= (size_t)moe::kFp8StagedScaleMax) ? (int)s13 : 0;
+    p.sc2e = (s2 % 16 == 0 && s2 <= (size_t)moe::kFp8StagedScaleMax) ? (int)s2 : 0;
+  }
   p.rpair_bytes = 4 * H;
   p.grid = sms;
   p.nslot_max = S + std::min(E, maxm * K);
@@ -169,15 +177,19 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
     // every output row of the CTA in one down stage, then the slot's h rows
     // (at most maxm pairs); the counters hold every union slot
     if (drs < rows_per_cta || p.nslot_max > moe::CTRL_WORDS - moe::CTRL_SLOTCNT) return MOE_ERR_UNSUPPORTED;
-    p.d_hoff = (int)round_up((size_t)drs * (p.row2 + p.sc2), 16);
+    p.d_soff = (int)round_up((size_t)drs * (p.row2 + p.sc2), 16);
+    p.d_hoff = (int)round_up((size_t)p.d_soff + p.sc2e, 16);
   }
   // a slot holds a whole number of gate/up pairs (about kStageTarget bytes), so
   // that no slot space is left unused in the gate/up phases
   const size_t q0 = std::max<size_t>(1, std::min<size_t>(moe::kNC, moe::kStageTarget / p.pair_bytes));
   size_t slot = 0;
   for (;;) {
-    const size_t dstage = ilv ? (size_t)p.d_hoff + (size_t)maxm * I * 4 : (size_t)drs * (p.row2 + p.sc2);
-    slot = round_up(std::max({q0 * p.pair_bytes, (size_t)p.rpair_bytes, (size_t)p.pair_bytes, dstage}), 128);
+    const size_t dstage = ilv ? (size_t)p.d_hoff + (size_t)maxm * I * 4
+                              : round_up((size_t)drs * (p.row2 + p.sc2), 16) + p.sc2e;
+    slot = round_up(std::max({q0 * p.pair_bytes + p.sc13e, (size_t)p.rpair_bytes, (size_t)p.pair_bytes + p.sc13e,
+                              dstage}),
+                    128);
     if (ilv || (long long)(moe::kMinSlots * slot) <= avail - (long long)maxm * I * 4 || drs == 1) break;
     drs = (drs + 1) / 2;
   }
@@ -224,7 +236,9 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
   p.off_xslot = (int)fixed;
   // the x rows are dead once the gate/up items are done: their area holds one
   // more down-phase slot when it is large enough
-  p.nslots_d = (!ilv && (size_t)maxm * H * 2 >= slot && p.nslots < moe::kMaxSlots) ? 1 : 0;
+  // (it only ever takes down stages)
+  const size_t dstage_bytes = round_up((size_t)drs * (p.row2 + p.sc2), 16) + p.sc2e;
+  p.nslots_d = (!ilv && (size_t)maxm * H * 2 >= dstage_bytes && p.nslots < moe::kMaxSlots) ? 1 : 0;
   p.nslots_x = ilv ? 0 : (int)std::min<long long>((long long)(area - fixed) / (long long)slot, moe::kMaxSlots - p.nslots);
   // per-slot h fetches: measured faster for NVFP4 (its gate/up phase ends less
   // evenly across CTAs), not for bf16, which keeps one fetch after all h is stored.
@@ -235,7 +249,8 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
                      ? 1
                      : 0;
   p.d_rows_stage = drs;
-  p.q = std::max(1, std::min(moe::kNC, p.slot_bytes / p.pair_bytes));
+  if (!ilv) p.d_soff = (int)round_up((size_t)drs * (p.row2 + p.sc2), 16);
+  p.q = std::max(1, std::min(moe::kNC, (p.slot_bytes - p.sc13e) / p.pair_bytes));
   // router stages: at most kNC / 2 row pairs, so every row gets at least one warp
   p.qr = std::max(1, std::min(moe::kNC / 2, p.slot_bytes / p.rpair_bytes));
   p.smem_bytes = p.off_ring + p.nslots * p.slot_bytes + 1024;
@@ -252,6 +267,7 @@ moe_status plan(const moe_decode_config& c, int sms, int smem_optin, Params& p, 
 moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params& p) {
   moe_status st = plan(c, sms, smem_optin, p, false);
   if (st != MOE_OK) return st;
+  p.sc13e = p.sc2e = p.d_soff = 0;
   if (p.fmt != moe::FMT_BF16 || p.S > 1 || p.nslot_max - p.S > p.grid ||
       p.nslot_max > moe::CTRL_WORDS - moe::CTRL_SLOTCNT || p.nchunk_i > moe::kFlatMaxChunks)
     return MOE_ERR_UNSUPPORTED;
@@ -332,6 +348,7 @@ moe_status plan_flat(const moe_decode_config& c, int sms, int smem_optin, Params
 moe_status plan_sk(const moe_decode_config& c, int sms, int smem_optin, Params& p) {
   moe_status st = plan(c, sms, smem_optin, p, false);
   if (st != MOE_OK) return st;
+  p.sc13e = p.sc2e = p.d_soff = 0;  // this kernel reads the FP8 block scales from global memory
   if (p.fmt == moe::FMT_NVFP4 || p.H / 8 > moe::kNC * 32 || p.H % 8) return MOE_ERR_UNSUPPORTED;
   const int H = p.H, I = p.I, E = p.E, K = p.K, S = p.S, maxm = p.maxm, G = p.grid;
   p.w2t = 1;

@@ -97,7 +97,9 @@ __device__ __forceinline__ void ilv_rows(const Params& p, int s, int& lo, int& h
 // compute the shared experts' gate/up items meanwhile, in stages of at most
 // ilv_sq pairs (one item per warp and stage).
 __device__ __forceinline__ int ilv_nrw(const Params& p) { return max(p.M, 2); }
-__device__ __forceinline__ int ilv_sq(const Params& p) { return min(p.q, kNC - ilv_nrw(p)); }
+// warps that compute the shared experts' items while the routing runs
+__device__ __forceinline__ int ilv_snw(const Params& p) { return kNC - ilv_nrw(p); }
+__device__ __forceinline__ int ilv_sq(const Params& p) { return min(p.q, ilv_snw(p)); }
 // Threads meeting at the routing-ready barrier: the routing warps, the producer
 // and the two hand-off warps.
 __device__ __forceinline__ int ilv_route_threads(const Params& p) { return (ilv_nrw(p) + 3) * 32; }
@@ -592,7 +594,7 @@ __device__ __forceinline__ RowSums dot_one_fp8(const uint4* qa, const uint4* qb,
 }
 
 // FP8 rows a, b against the N fp16 x rows of `mask` in shared memory; the block
-// scales are read from the rows' scale vectors (gsr, usr) through the read-only cache.
+// scales are read from the rows' scale vectors (gsr, usr: in the stage, or global).
 template <int N>
 __device__ __forceinline__ RowSums dot_rows_fp8(const uint4* qa, const uint4* qb, const float* gsr, const float* usr,
                                                 int nch, const uint4* xs, int H, uint32_t mask, int lane) {
@@ -610,7 +612,7 @@ __device__ __forceinline__ RowSums dot_rows_fp8(const uint4* qa, const uint4* qb
   for (int k = 0; k < N; ++k) g[k] = u[k] = 0.0f;
   for (int ch = lane; ch < nch; ch += 32) {
     const uint4 va = qa[ch], vb = qb[ch];
-    const float s_a = __ldg(gsr + ch / 8), s_b = __ldg(usr + ch / 8);
+    const float s_a = gsr[ch / 8], s_b = usr[ch / 8];  // global or shared memory
 #pragma unroll
     for (int k = 0; k < N; ++k) {
       const uint4 x0 = xp[k][ch * 2], x1 = xp[k][ch * 2 + 1];
@@ -864,8 +866,8 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
   const int nq = w.count();
   const int iq = w.offset(c.warp);
   Fp8Scales fs;
-  if (FMT == FMT_FP8 && iq < nq) {
-    // the item's block scales, requested before the stage is waited for
+  if (FMT == FMT_FP8 && iq < nq && !p.sc13e) {
+    // the item's block scales from global memory, requested before the stage is waited for
     const int e = shared ? -1 - slot : rt.slot_e[slot];
     fs.g_row = fp8_scale_row13(p, e, w.j + iq);
     fs.u_row = fp8_scale_row13(p, e, p.I + w.j + iq);
@@ -882,6 +884,21 @@ __device__ __forceinline__ void item_stage(const Ctx& c, const Route& rt, const 
     if (c.warp == 0 && c.lane == 0 && first) c.stamp(ST_U_DATA);
     const uint8_t* st = c.slot_ptr(ring.slot);
     const int j = w.j + iq;
+    if (FMT == FMT_FP8 && p.sc13e) {
+      // the expert's scales behind the stage's rows: [2I / 128][H / 128]
+      const float* scl = reinterpret_cast<const float*>(st + (size_t)2 * nq * p.row13);
+      const int nb = p.H / kFp8Block;
+      fs.g_row = scl + (j / kFp8Block) * nb;
+      fs.u_row = scl + ((p.I + j) / kFp8Block) * nb;
+      if (MAXM == 1) {
+#pragma unroll
+        for (int i = 0; i < kCplFp8; ++i) {
+          const int ch = min(c.lane + 32 * i, p.nchunk_h - 1);
+          fs.gv[i] = fs.g_row[ch / 8];
+          fs.uv[i] = fs.u_row[ch / 8];
+        }
+      }
+    }
     const uint32_t mask = shared ? (1u << p.M) - 1u : rt.slot_mask[slot];
     const RowSums rs = item_dot<FMT, MAXM>(st, iq, nq, p, xr.b, xr.h, xs, mask, c.lane, fs);
     float gsg = 1.0f, gsu = 1.0f, gs2 = 1.0f;
@@ -1435,11 +1452,19 @@ __device__ __forceinline__ const float* fp8_scale_down(const Params& p, int e) {
   return base + (size_t)(e >= 0 ? e : -1 - e) * (p.H / kFp8Block) * (p.I / kFp8Block);
 }
 
+// FP8 down scales of expert e for the down stage in ring slot `ring`: staged in the
+// slot at d_soff, or the expert's scales in global memory (d: the down-phase slot
+// map of the phase-ordered kernel).
+__device__ __forceinline__ const float* fp8_down_scales(const Ctx& c, const Ring& ring, bool d, int e) {
+  if (!c.p.sc2e) return fp8_scale_down(c.p, e);
+  return reinterpret_cast<const float*>(c.slot_ptr(ring.slot, d) + c.p.d_soff);
+}
+
 // One down stage: this thread's rows of the CTA's output block (group g, 16-byte
 // code chunk ch) against the h rows of the slot's pairs (hs, in pair order),
 // accumulated in fp32 over the slots.
-// FP8: s2 = the expert's block scales [H / 128][I / 128], row0 = the global row
-// of the stage's first row.
+// FP8: s2 = the expert's block scales [H / 128][I / 128] (in the stage, or in
+// global memory), row0 = the global row of the stage's first row.
 template <int FMT, int MAXM>
 __device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, const float* hs, uint32_t mask,
                                            float (&acc)[rows_per_group(FMT)][MAXM], int g, int ch, int nr,
@@ -1452,7 +1477,7 @@ __device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, c
 #pragma unroll
     for (int ri = 0; ri < RPG; ++ri) {
       const int r = min(g + ri * p.ng, nr - 1);
-      sv[ri] = __ldg(s2 + (size_t)((row0 + r) / kFp8Block) * (p.I / kFp8Block) + (8 * ch) / kFp8Block);
+      sv[ri] = s2[(size_t)((row0 + r) / kFp8Block) * (p.I / kFp8Block) + (8 * ch) / kFp8Block];
     }
   }
   if constexpr (FMT == FMT_BF16 && MAXM > 1 && MAXM <= 6) {
@@ -1733,7 +1758,7 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
         if (p.stamps && c.tid == 0) c.count(ST_D_WAIT_NS, tm - tw);
         if (got && have && active)
           down_stage<FMT, MAXM>(p, c.slot_ptr(ring.slot, true), hs + (size_t)(rt.pair_base[sl] - rt.pair_base[sl0]) * p.I,
-                                mask, acc, g, ch, nr, FMT == FMT_FP8 ? fp8_scale_down(p, sl < p.S ? -1 - sl : rt.slot_e[sl]) : nullptr,
+                                mask, acc, g, ch, nr, fp8_down_scales(c, ring, true, sl < p.S ? -1 - sl : rt.slot_e[sl]),
                                 rb_lo);
         __syncwarp();
         if (p.stamps && c.tid == 0) c.count(ST_D_MATH_NS, global_ns() - tm);
@@ -1842,7 +1867,7 @@ struct Producer {
     for (ItemWalk w(s * p.I + lo, s * p.I + hi, q, p.I); w.more(); ring.next(p.nslots)) {
       const int nq = w.count();
       uint32_t dst, bar;
-      if (!begin((uint32_t)nq * p.pair_bytes, dst, bar)) return;
+      if (!begin((uint32_t)nq * p.pair_bytes + p.sc13e, dst, bar)) return;
       copy_pairs(e, w.j, nq, dst, bar);
       w.advance(nq);
     }
@@ -1861,9 +1886,11 @@ struct Producer {
     const uint32_t cb = (uint32_t)nr * p.row2, sb = (uint32_t)nr * p.sc2;
     const uint32_t hb = (uint32_t)(rt.pair_base[s + 1] - rt.pair_base[s]) * (uint32_t)p.I * 4u;
     uint32_t dst, bar;
-    if (!begin(cb + sb + hb, dst, bar)) return;
+    if (!begin(cb + sb + (uint32_t)p.sc2e + hb, dst, bar)) return;
     bulk_g2s(dst, wt + row0 * p.row2, cb, bar, pol);
     if (sb) bulk_g2s(dst + (uint32_t)p.d_rows_stage * p.row2, ws + row0 * p.sc2, sb, bar, pol);
+    if (p.sc2e)  // FP8: the expert's down scales
+      bulk_g2s(dst + (uint32_t)p.d_soff, ws + (size_t)(e >= 0 ? e : -1 - e) * p.sc2e, (uint32_t)p.sc2e, bar, pol);
     reinterpret_cast<volatile int*>(c.sm + p.off_dslot)[s] = ring.slot;
     __threadfence_block();  // the barrier's byte count and the slot before the count of issued stages
     reinterpret_cast<volatile int*>(c.sm + p.off_ucnt)[ILV_DISSUED] = s + 1;
@@ -1940,6 +1967,7 @@ struct Producer {
     const uint32_t cb = (uint32_t)nq * p.row13;
     bulk_g2s(dst, wt + rg * p.row13, cb, bar, pol);
     bulk_g2s(dst + cb, wt + ru * p.row13, cb, bar, pol);
+    if (p.sc13e) bulk_g2s(dst + 2 * cb, ws + ex * p.sc13e, (uint32_t)p.sc13e, bar, pol);  // FP8: the expert's scales
     if (p.sc13) {
       const uint32_t sb = (uint32_t)nq * p.sc13;
       bulk_g2s(dst + 2 * cb, ws + rg * p.sc13, sb, bar, pol);
@@ -1965,7 +1993,7 @@ struct Producer {
       const int nq = w.count();
       const int slot = w.u + (shared_phase ? 0 : p.S);
       uint32_t dst, bar;
-      if (!begin((uint32_t)nq * p.pair_bytes, dst, bar)) return;
+      if (!begin((uint32_t)nq * p.pair_bytes + p.sc13e, dst, bar)) return;
       copy_pairs(shared_phase ? -1 - slot : rt.slot_e[slot], w.j, nq, dst, bar);
       w.advance(nq);
     }
@@ -1988,9 +2016,10 @@ struct Producer {
       const size_t row0 = ex * p.H + rb_lo;
       const uint32_t cb = (uint32_t)nr * p.row2, sb = (uint32_t)nr * p.sc2;
       uint32_t dst, bar;
-      if (!begin(cb + sb, dst, bar, true)) return;
+      if (!begin(cb + sb + (uint32_t)p.sc2e, dst, bar, true)) return;
       bulk_g2s(dst, wt + row0 * p.row2, cb, bar, pol);
       if (sb) bulk_g2s(dst + (uint32_t)p.d_rows_stage * p.row2, ws + row0 * p.sc2, sb, bar, pol);
+      if (p.sc2e) bulk_g2s(dst + (uint32_t)p.d_soff, ws + ex * p.sc2e, (uint32_t)p.sc2e, bar, pol);  // FP8 scales
       ring.next(p.nslots + nd);
     }
   }
@@ -2109,69 +2138,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
   __syncthreads();
 
   bool x_issued = false;
-  if (c.warp == kNC) {
-    // ------------------------------------------------------------ producer
-    Producer pr(c);
-    if (c.lane == 0) {
-      c.stamp(ST_START);
-      if (PHASES == PH_ALL) {
-        pr.x_rows();
-        x_issued = true;
-      }
-      if (PHASES & PH_R) pr.router();
-      if (kChain && kNeedX) {
-        pdl_wait();  // x may be the previous kernel's output
-        if (!c.aborted()) {
-          pr.x_rows();
-          x_issued = true;
-        }
-      }
-      if (PHASES & PH_R) {
-        // single kernel: the shared stages are sized for the warps that do not route
-        pr.pairs(true, rt, PHASES == PH_ALL ? ilv_sq(p) : 0);
-        c.stamp(ST_P_R_ISSUED);
-        if (PHASES & PH_D) pr.prefetch_shared_down();
-        pr.prefetch_predicted();
-      } else if (PHASES == PH_D) {
-        // The shared experts' down rows of the first row block need no routing.
-        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, 0);
-      }
-    }
-    if (kRoute) {
-      __syncwarp();
-      bar_sync(kBarRoute, PHASES == PH_ALL ? (ilv_nrw(p) + 1) * 32 : kThreads);
-    }
-    if (c.lane == 0) {
-      c.stamp(ST_P_ROUTE);
-      if (PHASES & PH_U) {
-        pr.pairs(false, rt);
-        c.stamp(ST_P_U_ISSUED);
-      }
-      if (PHASES & PH_D) {
-        const int nsl = p.S + c.misc[MISC_NROUTED];
-        const int first = PHASES == PH_D ? p.S : 0;  // the chain issued these before routing
-        const int nd = PHASES == PH_ALL ? p.nslots_d : 0;
-        if (PHASES == PH_ALL && p.hs_perslot) {
-          pr.h_rt = &rt;
-          pr.h_nsl = nsl;
-        }
-        for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl, nd);
-        pr.finish_h();
-        c.stamp(ST_P_D_ISSUED);
-      }
-      if (c.aborted()) {
-        pr.drain();
-        pr.drain_h();
-      }
-      // the x copy may still be in flight if the consumers gave up before it landed
-      if (x_issued && c.aborted()) {
-        const uint64_t t = global_ns();
-        while (!mbar_try_wait(c.xbar, 0) && global_ns() - t < p.timeout_ns) {
-        }
-      }
-    }
-    __syncwarp();
-  } else {
+  if (c.warp < kNC) {
     // ------------------------------------------------------------ consumers
     if (kChain) pdl_wait();
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
@@ -2201,7 +2168,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         bar_arrive(kBarRoute, (nrw + 1) * 32);
         if (c.tid == 0) c.stamp(ST_ROUTED);
       }
-      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring, nrw, kNC - nrw, ilv_sq(p));
+      ring = consume_items<FMT, MAXM>(c, rt, ITEM_SHARED, ring, nrw, ilv_snw(p), ilv_sq(p));
       fence_proxy_async_global();  // the h stores are read by other CTAs' bulk copies
       bar_sync(kBarConsumers, kNC * 32);  // the routing tables, and this CTA's shared h rows all stored
       if (c.tid == 0) {
@@ -2268,6 +2235,68 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             (unsigned long long)(clock64() - c.c0) * 1000ull / (global_ns() - c.t0 + 1);
       }
     }
+  } else {
+    // ------------------------------------------------------------ producer
+    Producer pr(c);
+    if (c.lane == 0) {
+      c.stamp(ST_START);
+      if (PHASES == PH_ALL) {
+        pr.x_rows();
+        x_issued = true;
+      }
+      if (PHASES & PH_R) pr.router();
+      if (kChain && kNeedX) {
+        pdl_wait();  // x may be the previous kernel's output
+        if (!c.aborted()) {
+          pr.x_rows();
+          x_issued = true;
+        }
+      }
+      if (PHASES & PH_R) {
+        // single kernel: the shared stages are sized for the warps that do not route
+        pr.pairs(true, rt, PHASES == PH_ALL ? ilv_sq(p) : 0);
+        c.stamp(ST_P_R_ISSUED);
+        if (PHASES & PH_D) pr.prefetch_shared_down();
+        pr.prefetch_predicted();
+      } else if (PHASES == PH_D) {
+        // The shared experts' down rows of the first row block need no routing.
+        if (pr.down_blocks() > 0) pr.down_block(rt, 0, 0, p.S, 0);
+      }
+    }
+    if (kRoute) {
+      __syncwarp();
+      bar_sync(kBarRoute, PHASES == PH_ALL ? (ilv_nrw(p) + 1) * 32 : kThreads);
+    }
+    if (c.lane == 0) {
+      c.stamp(ST_P_ROUTE);
+      if (PHASES & PH_U) {
+        pr.pairs(false, rt);
+        c.stamp(ST_P_U_ISSUED);
+      }
+      if (PHASES & PH_D) {
+        const int nsl = p.S + c.misc[MISC_NROUTED];
+        const int first = PHASES == PH_D ? p.S : 0;  // the chain issued these before routing
+        const int nd = PHASES == PH_ALL ? p.nslots_d : 0;
+        if (PHASES == PH_ALL && p.hs_perslot) {
+          pr.h_rt = &rt;
+          pr.h_nsl = nsl;
+        }
+        for (int rb = 0; rb < pr.down_blocks(); ++rb) pr.down_block(rt, rb, rb == 0 ? first : 0, nsl, nd);
+        pr.finish_h();
+        c.stamp(ST_P_D_ISSUED);
+      }
+      if (c.aborted()) {
+        pr.drain();
+        pr.drain_h();
+      }
+      // the x copy may still be in flight if the consumers gave up before it landed
+      if (x_issued && c.aborted()) {
+        const uint64_t t = global_ns();
+        while (!mbar_try_wait(c.xbar, 0) && global_ns() - t < p.timeout_ns) {
+        }
+      }
+    }
+    __syncwarp();
   }
   __syncthreads();
   if (kLast && c.tid == 0) {
@@ -2333,7 +2362,7 @@ __device__ __forceinline__ Ring ilv_down(const Ctx& c, const Route& rt, int s, R
   if (got && active) {
     const uint8_t* st = c.slot_ptr(ring.slot);
     down_stage<FMT, MAXM>(p, st, reinterpret_cast<const float*>(st + p.d_hoff), rt.slot_mask[s], acc, g, ch, nr,
-                          FMT == FMT_FP8 ? fp8_scale_down(p, s < p.S ? -1 - s : rt.slot_e[s]) : nullptr, r_lo);
+                          fp8_down_scales(c, ring, false, s < p.S ? -1 - s : rt.slot_e[s]), r_lo);
   }
   __syncwarp();
   if (got && c.lane == 0) c.release(ring, 1);
@@ -2446,52 +2475,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
   int r_lo, r_hi;
   cta_rows(p, r_lo, r_hi);
   const int nr = r_hi - r_lo;  // every output row of the CTA in one down stage (planned)
-  if (c.warp > kNC) {
-    // ------------------------------------------------------------ hand-off warps
-    __syncwarp();
-    bar_sync(kBarRoute, ilv_route_threads(p));
-    if (c.lane == 0) {
-      if (c.warp == kNC + 1)
-        ilv_publish(c);
-      else
-        ilv_fetcher(c, rt);
-    }
-    __syncwarp();
-  } else if (c.warp == kNC) {
-    // ------------------------------------------------------------ producer
-    Producer pr(c);
-    if (c.lane == 0) {
-      c.stamp(ST_START);
-      pr.x_rows();
-      pr.router();
-      for (int s = 0; s < p.S; ++s) pr.ilv_pairs(rt, s, ilv_sq(p));
-      c.stamp(ST_P_R_ISSUED);
-      pr.prefetch_shared_down();
-      pr.prefetch_predicted();
-    }
-    __syncwarp();
-    bar_sync(kBarRoute, ilv_route_threads(p));
-    if (c.lane == 0) {
-      c.stamp(ST_P_ROUTE);
-      const int nsl = p.S + c.misc[MISC_NROUTED];
-      int dnext = 0;
-      for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
-        if (t < nsl) pr.ilv_pairs(rt, t, p.q);
-        while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t) pr.ilv_down(rt, dnext++);
-      }
-      c.stamp(ST_P_D_ISSUED);
-      __threadfence_block();
-      reinterpret_cast<volatile int*>(sm + p.off_ucnt)[ILV_PDONE] = 1;
-      if (c.aborted()) {
-        pr.drain();  // the hand-off warp completes the h parts of armed down stages
-        // the x copy may still be in flight if the consumers gave up before it landed
-        const uint64_t t = global_ns();
-        while (!mbar_try_wait(c.xbar, 0) && global_ns() - t < p.timeout_ns) {
-        }
-      }
-    }
-    __syncwarp();
-  } else {
+  if (c.warp < kNC) {
     // ------------------------------------------------------------ consumers
     if (c.tid == 0) c.misc[MISC_EPOCH] = (int)ld_relaxed_u32(&p.ctrl[CTRL_EPOCH]);
     prepare_x(c, FMT != FMT_BF16);
@@ -2528,7 +2512,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     // the shared experts' items: the non-routing warps compute them while routing
     // runs; the routing warps walk the same stages (without items) afterwards
 #pragma unroll 1
-    for (int s = 0; s < p.S; ++s) ring = ilv_items<FMT, MAXM>(c, rt, s, ring, rot, nrw, kNC - nrw, ilv_sq(p));
+    for (int s = 0; s < p.S; ++s) ring = ilv_items<FMT, MAXM>(c, rt, s, ring, rot, nrw, ilv_snw(p), ilv_sq(p));
     bar_sync(kBarConsumers, kNC * 32);  // the routing tables, for every warp
     if (c.tid == 0) c.stamp(ST_R_DONE);
     const int nsl = p.S + c.misc[MISC_NROUTED];
@@ -2555,6 +2539,51 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
             (unsigned long long)(clock64() - c.c0) * 1000ull / (global_ns() - c.t0 + 1);
       }
     }
+  } else if (c.warp == kNC) {
+    // ------------------------------------------------------------ producer
+    Producer pr(c);
+    if (c.lane == 0) {
+      c.stamp(ST_START);
+      pr.x_rows();
+      pr.router();
+      for (int s = 0; s < p.S; ++s) pr.ilv_pairs(rt, s, ilv_sq(p));
+      c.stamp(ST_P_R_ISSUED);
+      pr.prefetch_shared_down();
+      pr.prefetch_predicted();
+    }
+    __syncwarp();
+    bar_sync(kBarRoute, ilv_route_threads(p));
+    if (c.lane == 0) {
+      c.stamp(ST_P_ROUTE);
+      const int nsl = p.S + c.misc[MISC_NROUTED];
+      int dnext = 0;
+      for (int t = p.S; t < nsl + p.ilv_lag; ++t) {
+        if (t < nsl) pr.ilv_pairs(rt, t, p.q);
+        while (nr > 0 && dnext < nsl && dnext + p.ilv_lag <= t) pr.ilv_down(rt, dnext++);
+      }
+      c.stamp(ST_P_D_ISSUED);
+      __threadfence_block();
+      reinterpret_cast<volatile int*>(sm + p.off_ucnt)[ILV_PDONE] = 1;
+      if (c.aborted()) {
+        pr.drain();  // the hand-off warp completes the h parts of armed down stages
+        // the x copy may still be in flight if the consumers gave up before it landed
+        const uint64_t t = global_ns();
+        while (!mbar_try_wait(c.xbar, 0) && global_ns() - t < p.timeout_ns) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ hand-off warps
+    __syncwarp();
+    bar_sync(kBarRoute, ilv_route_threads(p));
+    if (c.lane == 0) {
+      if (c.warp == kNC + 1)
+        ilv_publish(c);
+      else
+        ilv_fetcher(c, rt);
+    }
+    __syncwarp();
   }
   __syncthreads();
   if (c.tid == 0) {

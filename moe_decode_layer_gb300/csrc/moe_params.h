@@ -17,6 +17,7 @@ constexpr int kCplBf16 = 16;             // 16-byte x chunks per lane kept in re
 constexpr int kCplFp4 = 4;               // 32-element x chunks per lane for NVFP4 (H <= 4096)
 constexpr int kCplFp8 = 8;               // 16-element x chunks per lane for FP8 (H <= 4096)
 constexpr int kFp8Block = 128;           // FP8 weights: one fp32 scale per 128 x 128 block
+constexpr int kFp8StagedScaleMax = 4096; // FP8: per-expert scale bytes staged with the weights at most
 constexpr int kStageTarget = 32768;      // ring slot size aimed for (bytes)
 constexpr int kMinSlots = 4;             // ring slots kept before shrinking the h staging area
 constexpr int kLogitRep = 4;             // copies of the router logits (spreads the all-CTA read)
@@ -148,6 +149,11 @@ struct Params {
   int nchunk_i;      // code chunks per down row (16 bytes; FP8: 8 codes)
   int row2, sc2;     // code / scale bytes per down row
   int pair_bytes;    // one gate row + one up row (codes and scales)
+  int sc13e;         // FP8: bytes of one expert's gate/up block scales, copied behind every gate/up
+                     // stage of that expert (0: the consumers read them from global memory)
+  int sc2e;          // FP8: bytes of one expert's down block scales, copied into every down stage
+                     // at d_soff (0: read from global memory)
+  int d_soff;        // byte offset of the staged FP8 down scales inside a down stage's ring slot
   int rpair_bytes;   // two router rows
   int q, qr;         // gate/up pairs per stage, router row pairs per stage (<= kNC)
   int slot_bytes, nslots;
