@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
     }
     // every consumer warp routes (the logits staged by all of them, each row's
     // top-k spread over several warps); the shared expert's items follow
-    route_rows(c, rt, true, kNC * 32, kBarRouting);
+    route_rows<MAXM>(c, rt, true, kNC * 32, kBarRouting);
     fence_proxy_async_shared();  // the routing scratch becomes the h buffers (bulk copies)
     if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
     bar_arrive(kBarRoute, kThreadsFlat);

@@ -1334,7 +1334,9 @@ __device__ __forceinline__ void write_prediction(const Ctx& c, const Route& rt) 
 }
 
 // nthr threads (the first nthr / 32 consumer warps, at least p.M) route; they
-// meet at named barrier `bar`.
+// meet at named barrier `bar`. MAXM: the kernel's row bound (MAXM == 1 exactly
+// when the run has one row).
+template <int MAXM>
 static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt, bool write_topk,
                                                   int nthr = kNC * 32, int bar = kBarConsumers) {
   const Params& p = c.p;
@@ -1344,7 +1346,7 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
     float* bs = reinterpret_cast<float*>(c.sm + p.off_bias);
     for (int e = c.tid; e < p.E; e += nthr) bs[e] = __ldg(p.router_bias + e);
   }
-  if (c.tid == 0 && p.M == 1) one_row_split(c);
+  if (MAXM == 1 && c.tid == 0) one_row_split(c);
   // every CTA's router logits stored (count), before reading any of them
   if (c.tid == 0) {
     if (!c.aborted()) wait_count(c, CTRL_RCOUNT, SITE_FLAGS);
@@ -1367,7 +1369,7 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
   }
   bar_sync(bar, nthr);
   if (c.tid == 0) c.stamp(ST_TOPK);
-  if (p.M == 1) {
+  if constexpr (MAXM == 1) {
     if (c.warp == 0) union_one_row(c, rt);
   } else {
     union_rows(c, rt, nthr, bar);
@@ -1508,91 +1510,91 @@ __device__ __forceinline__ void down_stage(const Params& p, const uint8_t* st, c
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[ri][m] = fmaf(wf[ri][k], hv[k], acc[ri][m]);
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int m = 0; m < MAXM; ++m) {
-    if (!(mask >> m & 1u)) continue;
-    const float* hrow = hs + (size_t)hp * p.I;
-    ++hp;
-    if (FMT == FMT_BF16) {
-      const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
-      const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
-      const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      // every row of the group, branch-free: rows past the block repeat
-      // the last one (their sums are never written), so all loads issue
-      // before the arithmetic
-      uint4 wv[RPG];
+    for (int m = 0; m < MAXM; ++m) {
+      if (!(mask >> m & 1u)) continue;
+      const float* hrow = hs + (size_t)hp * p.I;
+      ++hp;
+      if (FMT == FMT_BF16) {
+        const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
+        const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
+        const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        // every row of the group, branch-free: rows past the block repeat
+        // the last one (their sums are never written), so all loads issue
+        // before the arithmetic
+        uint4 wv[RPG];
 #pragma unroll
-      for (int ri = 0; ri < RPG; ++ri) {
-        const int r = min(g + ri * p.ng, nr - 1);
-        wv[ri] = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
-      }
-#pragma unroll
-      for (int ri = 0; ri < RPG; ++ri) dot8_bf16_f32(acc[ri][m], wv[ri], hv);
-    } else if (FMT == FMT_FP8) {
-      // 8 e4m3 codes per thread and row against 8 fp32 h values, summed in
-      // fp32 (one rounding per fused multiply-add), then the row's block scale
-      const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
-      const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
-      const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      uint2 wv[RPG];
-#pragma unroll
-      for (int ri = 0; ri < RPG; ++ri) {
-        const int r = min(g + ri * p.ng, nr - 1);
-        wv[ri] = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2)[ch];
-      }
-#pragma unroll
-      for (int ri = 0; ri < RPG; ++ri) {
-        const uint32_t qw[2] = {wv[ri].x, wv[ri].y};
-        float part = 0.0f;
-#pragma unroll
-        for (int wi = 0; wi < 2; ++wi) {
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const uint32_t f = e4m3x2_to_f16x2((qw[wi] >> (16 * hb)) & 0xffffu);
-            const __half2 w2 = *reinterpret_cast<const __half2*>(&f);
-            const int e0 = wi * 4 + hb * 2;
-            part = fmaf(__low2float(w2), hv[e0], part);
-            part = fmaf(__high2float(w2), hv[e0 + 1], part);
-          }
+        for (int ri = 0; ri < RPG; ++ri) {
+          const int r = min(g + ri * p.ng, nr - 1);
+          wv[ri] = reinterpret_cast<const uint4*>(st + (size_t)r * p.row2)[ch];
         }
-        acc[ri][m] = fmaf(sv[ri], part, acc[ri][m]);
-      }
-    } else {
-      // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        float hv[16];
+        for (int ri = 0; ri < RPG; ++ri) dot8_bf16_f32(acc[ri][m], wv[ri], hv);
+      } else if (FMT == FMT_FP8) {
+        // 8 e4m3 codes per thread and row against 8 fp32 h values, summed in
+        // fp32 (one rounding per fused multiply-add), then the row's block scale
+        const float4 a = *reinterpret_cast<const float4*>(hrow + 8 * ch);
+        const float4 b = *reinterpret_cast<const float4*>(hrow + 8 * ch + 4);
+        const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint2 wv[RPG];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 f = *reinterpret_cast<const float4*>(hrow + 4 * ch + (blk * 4 + q) * 4 * p.tg);
-          hv[4 * q] = f.x;
-          hv[4 * q + 1] = f.y;
-          hv[4 * q + 2] = f.z;
-          hv[4 * q + 3] = f.w;
+        for (int ri = 0; ri < RPG; ++ri) {
+          const int r = min(g + ri * p.ng, nr - 1);
+          wv[ri] = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2)[ch];
         }
 #pragma unroll
         for (int ri = 0; ri < RPG; ++ri) {
-          const int r = g + ri * p.ng;
-          if (r < nr) {
-            const uint2 qv = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2 + 16 * ch)[blk];
-            const uint32_t sb = st[(size_t)drs * p.row2 + (size_t)r * p.sc2 + 2 * ch + blk];
-            const float sv = __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2(sb) & 0xffffu)));
-            const uint32_t qw[2] = {qv.x, qv.y};
-            float part = 0.0f;
+          const uint32_t qw[2] = {wv[ri].x, wv[ri].y};
+          float part = 0.0f;
 #pragma unroll
-            for (int wi = 0; wi < 2; ++wi) {
+          for (int wi = 0; wi < 2; ++wi) {
 #pragma unroll
-              for (int by = 0; by < 4; ++by) {
-                const uint32_t wv = e2m1x2_to_f16x2((qw[wi] >> (8 * by)) & 0xffu);
-                const int e0 = wi * 8 + by * 2;
-                const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
-                part = fmaf(__low2float(wh), hv[e0], part);
-                part = fmaf(__high2float(wh), hv[e0 + 1], part);
-              }
+            for (int hb = 0; hb < 2; ++hb) {
+              const uint32_t f = e4m3x2_to_f16x2((qw[wi] >> (16 * hb)) & 0xffffu);
+              const __half2 w2 = *reinterpret_cast<const __half2*>(&f);
+              const int e0 = wi * 4 + hb * 2;
+              part = fmaf(__low2float(w2), hv[e0], part);
+              part = fmaf(__high2float(w2), hv[e0 + 1], part);
             }
-            acc[ri][m] = fmaf(sv, part, acc[ri][m]);
+          }
+          acc[ri][m] = fmaf(sv[ri], part, acc[ri][m]);
+        }
+      } else {
+        // one 16-element block (one e4m3 scale) at a time: 16 h values in registers
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          float hv[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(hrow + 4 * ch + (blk * 4 + q) * 4 * p.tg);
+            hv[4 * q] = f.x;
+            hv[4 * q + 1] = f.y;
+            hv[4 * q + 2] = f.z;
+            hv[4 * q + 3] = f.w;
+          }
+#pragma unroll
+          for (int ri = 0; ri < RPG; ++ri) {
+            const int r = g + ri * p.ng;
+            if (r < nr) {
+              const uint2 qv = reinterpret_cast<const uint2*>(st + (size_t)r * p.row2 + 16 * ch)[blk];
+              const uint32_t sb = st[(size_t)drs * p.row2 + (size_t)r * p.sc2 + 2 * ch + blk];
+              const float sv = __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2(sb) & 0xffffu)));
+              const uint32_t qw[2] = {qv.x, qv.y};
+              float part = 0.0f;
+#pragma unroll
+              for (int wi = 0; wi < 2; ++wi) {
+#pragma unroll
+                for (int by = 0; by < 4; ++by) {
+                  const uint32_t wv = e2m1x2_to_f16x2((qw[wi] >> (8 * by)) & 0xffu);
+                  const int e0 = wi * 8 + by * 2;
+                  const __half2 wh = *reinterpret_cast<const __half2*>(&wv);
+                  part = fmaf(__low2float(wh), hv[e0], part);
+                  part = fmaf(__high2float(wh), hv[e0 + 1], part);
+                }
+              }
+              acc[ri][m] = fmaf(sv, part, acc[ri][m]);
+            }
           }
         }
       }
@@ -2163,7 +2165,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       }
       const int nrw = ilv_nrw(p);
       if (c.warp < nrw) {
-        route_rows(c, rt, true, nrw * 32, kBarRouting);
+        route_rows<MAXM>(c, rt, true, nrw * 32, kBarRouting);
         if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
         bar_arrive(kBarRoute, (nrw + 1) * 32);
         if (c.tid == 0) c.stamp(ST_ROUTED);
@@ -2191,7 +2193,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
       }
       if (kRoute) {
-        route_rows(c, rt, (PHASES & PH_U) != 0);
+        route_rows<MAXM>(c, rt, (PHASES & PH_U) != 0);
         if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
         bar_arrive(kBarRoute, kThreads);
         if (c.tid == 0) c.stamp(ST_ROUTED);
@@ -2495,7 +2497,7 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     }
     const int nrw = ilv_nrw(p);
     if (c.warp < nrw) {
-      route_rows(c, rt, true, nrw * 32, kBarRouting);
+      route_rows<MAXM>(c, rt, true, nrw * 32, kBarRouting);
       if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
       bar_arrive(kBarRoute, ilv_route_threads(p));
       if (c.tid == 0) c.stamp(ST_ROUTED);

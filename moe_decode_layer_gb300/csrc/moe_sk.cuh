@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
       count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
-    route_rows(c, rt, true);
+    route_rows<MAXM>(c, rt, true);
     if (c.tid == 0) reinterpret_cast<volatile int*>(c.misc)[MISC_ROUTED] = 1;  // hint for the producer's prefetch
     bar_arrive(kBarRoute, kThreads);
     if (c.tid == 0) c.stamp(ST_ROUTED);
