@@ -1677,7 +1677,6 @@ __device__ void consume_down(const Ctx& c, const Route& rt, bool check_xflags, b
   const int ch = ctid % p.tg;  // 16-byte code chunk of a down row
   const bool active = g < p.ng;
   const float* hs0 = reinterpret_cast<const float*>(c.sm + p.off_hs);
-  float* red = reinterpret_cast<float*>(c.sm + p.off_red);
   const uint32_t hbar0 = smem_u32(c.sm + p.off_hbar);
   const int nbuf = p.hs_nbuf, cap = p.hs_pairs / nbuf;
   constexpr int RPG = rows_per_group(FMT);  // rows per thread group and stage
