@@ -249,10 +249,13 @@ moe_status moe_decode_run(moe_decode_handle* h, const void* x, const void* resid
                           int32_t m_rows, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
 
 /*
- * The same step from host memory: copies x and residual (bf16 [M, H], host) into
- * the handle's staging buffers, runs, copies out (and topk_idx / topk_w when not
- * NULL, host) back, and synchronises `stream`. Host buffers should be pinned for
- * speed; pageable memory works. Returns the device status as get_status does.
+ * The same step from host memory: copies x and residual (bf16 [M, H], host; one
+ * copy when they are the same buffer) into the handle's staging buffers, runs,
+ * brings the device status words, topk_idx / topk_w and out back in one
+ * device-to-host copy into a pinned staging block, synchronises `stream` and
+ * copies out (and topk_idx / topk_w when not NULL, host) from there. Host buffers
+ * should be pinned for speed; pageable memory works. Returns the device status as
+ * get_status does.
  */
 moe_status moe_decode_run_host(moe_decode_handle* h, const void* x_host, const void* residual_host,
                                void* out_host, int32_t m_rows, int32_t* topk_idx_host,
