@@ -1347,13 +1347,9 @@ static __device__ __forceinline__ void route_rows(const Ctx& c, const Route& rt,
     for (int e = c.tid; e < p.E; e += nthr) bs[e] = __ldg(p.router_bias + e);
   }
   if (MAXM == 1 && c.tid == 0) one_row_split(c);
-  // every CTA's router logits stored (count), before reading any of them
-  if (c.tid == 0) {
-    if (!c.aborted()) wait_count(c, CTRL_RCOUNT, SITE_FLAGS);
-    c.stamp(ST_RCOUNT);
-  }
-  bar_sync(bar, nthr);
-  // this CTA's replica of the logits into shared memory (coalesced, tag-checked)
+  // this CTA's replica of the logits into shared memory (coalesced): every word
+  // carries its run tag, so each thread polls its words until the tags are this
+  // run's, with no count or flag to wait for first
   float* lg = reinterpret_cast<float*>(c.sm + p.off_lg);
   const unsigned long long* src = p.logits + (size_t)(blockIdx.x % kLogitRep) * p.maxm * p.E;
   bool ok = !c.aborted() && stage_tagged(c, src, lg, p.M * p.E / 2, SITE_LOGITS, nthr);
