@@ -45,7 +45,7 @@ MOE_OPT_PREFETCH_EXPERTS = 8
 STAMP_NAMES = {0: "start", 1: "x_loaded", 2: "R_done", 3: "routed", 4: "U_done", 5: "D_first",
                6: "D_done", 8: "prod_R_issued", 9: "prod_route", 10: "prod_U_issued",
                11: "prod_D_issued", 12: "logits_seen", 13: "topk_row0", 14: "ucount_full",
-               16: "rcount_add", 17: "U_first_data", 18: "rcount_full",
+               16: "logits_stored", 17: "U_first_data",
                19: "D_summed"}
 STAMP_COUNTS = {7: "D_hwait_us(t0)", 20: "D_math_us(t0)", 21: "D_bar_us(t0)", 22: "D_wait_us(warp0)",
                 23: "sm_clock_mhz"}

@@ -491,7 +491,6 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
     ring = consume_router<MAXM>(c, ring);
     bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
     if (c.tid == 0) {
-      count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
     // every consumer warp routes (the logits staged by all of them, each row's
@@ -526,7 +525,6 @@ __global__ void __launch_bounds__(kThreadsFlat, 1) moe_flat_kernel(const __grid_
     const uint32_t prev = atomicAdd(&p.ctrl[CTRL_EXIT], 1u);
     if (prev == gridDim.x - 1) {
       p.ctrl[CTRL_EXIT] = 0u;
-      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       for (int i = 0; i < p.nslot_max; ++i) p.ctrl[CTRL_SLOTCNT + i] = 0u;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;

@@ -2151,7 +2151,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
       ring = consume_router<MAXM>(c, ring);
       bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
       if (c.tid == 0) {
-        count_done(p, CTRL_RCOUNT);
         c.stamp(ST_RFLAG);
       }
       if (FMT != FMT_BF16) {  // the router is done with the bf16 x rows
@@ -2183,7 +2182,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         ring = consume_router<MAXM>(c, ring);
         bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
         if (c.tid == 0) {
-          count_done(p, CTRL_RCOUNT);
           c.stamp(ST_RFLAG);
         }
       }
@@ -2300,7 +2298,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     const uint32_t prev = atomicAdd(&p.ctrl[CTRL_EXIT], 1u);
     if (prev == gridDim.x - 1) {
       p.ctrl[CTRL_EXIT] = 0u;
-      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_UCOUNT) = 0ull;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_SCOUNT) = 0ull;
       if (PHASES == PH_ALL && p.hs_perslot)
@@ -2483,7 +2480,6 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     ring = consume_router<MAXM>(c, ring);
     bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
     if (c.tid == 0) {
-      count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
     if (FMT != FMT_BF16) {  // the router is done with the bf16 x rows
@@ -2587,7 +2583,6 @@ __global__ void __launch_bounds__(kThreadsIlv, 1) moe_ilv_kernel(const __grid_co
     const uint32_t prev = atomicAdd(&p.ctrl[CTRL_EXIT], 1u);
     if (prev == gridDim.x - 1) {
       p.ctrl[CTRL_EXIT] = 0u;
-      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       for (int i = 0; i < p.nslot_max; ++i) p.ctrl[CTRL_SLOTCNT + i] = 0u;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;

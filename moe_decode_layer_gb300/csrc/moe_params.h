@@ -52,10 +52,11 @@ constexpr int kIlvCnt = 8;   // per-CTA arrival counters of the interleaved sche
 enum IlvWord : int { ILV_DISSUED = kIlvCnt, ILV_PDONE = kIlvCnt + 1, ILV_WORDS = kIlvCnt + 4 };
 
 // Control words at the start of the handle's scratch.
-// CTRL_RCOUNT / CTRL_UCOUNT / CTRL_SCOUNT (64-bit, 8-byte aligned word index): CTAs
-// whose router logits / gate-up results / shared experts' gate-up results of the
-// current run are stored; reset by the last CTA.
-enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3, CTRL_RCOUNT = 4,
+// CTRL_UCOUNT / CTRL_SCOUNT (64-bit, 8-byte aligned word index): CTAs whose gate-up
+// results / shared experts' gate-up results of the current run are stored; reset by
+// the last CTA. (Router logits need no count: readers poll their run tags.) Words
+// 4 and 5 are unused.
+enum Ctrl : int { CTRL_EPOCH = 0, CTRL_EXIT = 1, CTRL_STATUS = 2, CTRL_WHERE = 3,
                   CTRL_UCOUNT = 6, CTRL_SCOUNT = 8, CTRL_SLOTCNT = 16, CTRL_WORDS = 176 };
 // CTRL_SLOTCNT + s: gate/up items of union slot s whose h is stored (all CTAs of
 // the run; complete at I). Used when every pair's h fits the h area at once.
@@ -91,9 +92,8 @@ enum Stamp : int {
   ST_LOGITS = 12,     // all router logits seen (routing warp 0)
   ST_TOPK = 13,       // top-k of row 0 done
   ST_U_FLAGS = 14,    // the gate/up-done count reached the grid size
-  ST_RFLAG = 16,      // this CTA counted its router logits as stored
+  ST_RFLAG = 16,      // this CTA's router logits stored
   ST_U_DATA = 17,     // warp 0's first routed gate/up stage landed
-  ST_RCOUNT = 18,     // the router-done count reached the grid size
   ST_D_HWAIT_NS = 7,     // (sum, thread 0) ns waiting for h batches in the down phase
   ST_D_MATH_NS = 20,     // (sum, thread 0) ns in the down-stage arithmetic
   ST_D_BAR_NS = 21,      // (sum, thread 0) ns at the down phase's per-batch barriers

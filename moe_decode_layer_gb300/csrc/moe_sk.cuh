@@ -333,7 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
     ring = consume_router<MAXM>(c, ring);
     bar_sync(kBarConsumers, kNC * 32);  // this CTA's logits are all stored
     if (c.tid == 0) {
-      count_done(p, CTRL_RCOUNT);
       c.stamp(ST_RFLAG);
     }
     route_rows<MAXM>(c, rt, true);
@@ -370,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_sk_kernel(const __grid_consta
     const uint32_t prev = atomicAdd(&p.ctrl[CTRL_EXIT], 1u);
     if (prev == gridDim.x - 1) {
       p.ctrl[CTRL_EXIT] = 0u;
-      *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_RCOUNT) = 0ull;
       *reinterpret_cast<unsigned long long*>(p.ctrl + CTRL_UCOUNT) = 0ull;
       uint32_t e = p.ctrl[CTRL_EPOCH] + 1u;
       if (e == 0xffffffffu) e = 0u;

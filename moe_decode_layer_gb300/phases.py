@@ -54,12 +54,12 @@ def timeline(workload: str, copies: int, runs: int, ring_slots: int = 0, sched: 
                 if v:
                     per_event[k].append((v - t0) / 1000.0)
         totals.append((int(st[:, 6].max()) - t0) / 1000.0)
-        # per-run derived: the last CTA to publish its router flag vs the first
+        # per-run derived: the last CTA to store its router logits vs the first
         # CTA to see all logits
         rf = [v for v in st[:, 16].tolist() if v]
         ls = [v for v in st[:, 12].tolist() if v]
         if rf and ls:
-            derived.setdefault("last_rcount_add", []).append((max(rf) - t0) / 1000.0)
+            derived.setdefault("last_logits_stored", []).append((max(rf) - t0) / 1000.0)
             derived.setdefault("first_logits_seen", []).append((min(ls) - t0) / 1000.0)
         for k, name in _lib.STAMP_COUNTS.items():
             scale = 1e-3 if "_us" in name else 1.0  # ns sums shown in microseconds
