@@ -91,6 +91,65 @@ def test_planned_layouts_fit(sms, optin):
     assert n_checked > 500 and n_ilv > 100 and n_unfit < n_checked // 10
 
 
+def _fp8_cfg(h, i, e, k, s, m):
+    return _lib.Config(hidden=h, inter=i, num_experts=e, top_k=k, num_shared=s, max_rows=m,
+                       wdtype=_lib.MOE_W_FP8_BLOCK, score=0, routed_scale=1.0, pre_rmsnorm=0, rms_eps=1e-6,
+                       sched=0)
+
+
+def _staged(nbytes):
+    """Scale bytes that ride behind an FP8 stage: whole 16-byte multiples up to 4 KB."""
+    return nbytes if nbytes % 16 == 0 and nbytes <= 4096 else 0
+
+
+@pytest.mark.parametrize("sms,optin", [(152, 232448), (132, 232448)])
+def test_planned_fp8_layouts_fit(sms, optin):
+    """FP8 weights: each expert's block-scale matrix may ride behind its gate/up and
+    down stages, so a stage is its rows plus those bytes. Every planned stage, with
+    its scales, fits its ring slot; the interleaved kernel's h rows start after the
+    staged down scales; the x area takes a down-phase slot only when a down stage
+    (rows and scales) fits it."""
+    lib = _lib.load()
+    n_checked = 0
+    for h, i, e, k, s, m in itertools.product((1024, 2560, 4096), (128, 768, 1024, 3072), (64, 512),
+                                               (2, 8), (0, 1), (1, 6, 8)):
+        cfg = _fp8_cfg(h, i, e, k, s, m)
+        if lib.moe_decode_config_check(ctypes.byref(cfg)) != _lib.MOE_OK:
+            continue
+        s13 = _staged((2 * i // 128) * (h // 128) * 4)
+        s2 = _staged((h // 128) * (i // 128) * 4)
+        for ilv in (0, 1):
+            st, p = _plan(lib, cfg, sms, optin, ilv)
+            if st != _lib.MOE_OK:
+                assert st == _lib.MOE_ERR_UNSUPPORTED
+                continue
+            what = f"fp8 H={h} I={i} E={e} k={k} S={s} M={m} ilv={ilv} sms={sms}"
+            assert p.smem_bytes <= optin and p.slot_bytes % 128 == 0, what
+            assert p.pairs_per_stage * 2 * h + s13 <= p.slot_bytes, what
+            rows_bytes = -(-p.down_rows_per_stage * i // 16) * 16
+            if ilv:
+                assert p.down_h_offset % 16 == 0 and p.down_h_offset >= rows_bytes + s2, what
+                assert p.down_h_offset + m * i * 4 <= p.slot_bytes, what
+            else:
+                assert rows_bytes + s2 <= p.slot_bytes, what
+                if p.down_slot_in_x:
+                    assert m * h * 2 >= rows_bytes + s2, what
+            n_checked += 1
+    assert n_checked > 50
+
+
+def test_fp8_ling_layer_stages_its_scales():
+    """The Ling-shaped FP8 layer: 960 B of gate/up and 480 B of down scales per expert
+    ride with the stages, and six gate/up pairs still fit a slot."""
+    lib = _lib.load()
+    for m in (1, 6):
+        st, p = _plan(lib, _fp8_cfg(2560, 768, 512, 8, 1, m), 152, 232448, 0)
+        assert st == _lib.MOE_OK and p.pairs_per_stage == 6
+        assert 6 * 2 * 2560 + 960 <= p.slot_bytes and 17 * 768 + 480 <= p.slot_bytes
+        st, q = _plan(lib, _fp8_cfg(2560, 768, 512, 8, 1, m), 152, 232448, 1)
+        assert st == _lib.MOE_OK and q.down_h_offset == 17 * 768 + 480
+
+
 @pytest.mark.parametrize("sms,optin", [(152, 232448), (132, 232448), (152, 166912)])
 def test_planned_flat_layouts_fit(sms, optin):
     """The expert-range kernel's layout: bf16 weights, at most one shared expert,
