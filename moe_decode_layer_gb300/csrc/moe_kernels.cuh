@@ -1174,7 +1174,7 @@ __device__ __forceinline__ void topk_row(const Ctx& c, const Route& rt, int m, b
 }
 
 // The union of the experts chosen by M > 1 rows, one thread per (row, selected
-// expert) pair (nthr threads meeting at named barrier `bar`; M * K <= 64 pairs).
+// expert) pair (nthr threads meeting at named barrier `bar`; M * K <= 128 pairs).
 // Each pair thread marks whether its row is the lowest one that chose its expert;
 // then it counts, over all pairs, the pairs and the distinct experts with a
 // smaller id: its slot is S + (distinct experts below), its (slot, row) pair
@@ -1223,7 +1223,7 @@ __device__ __forceinline__ void union_rows(const Ctx& c, const Route& rt, int nt
       rt.slot_e[sl] = e;
       rt.slot_mask[sl] = msk;
       rt.pair_base[sl] = S * M + pb;
-      const uint32_t tcost = I * (base * (uint32_t)tot + (uint32_t)np);  // <= 2^23
+      const uint32_t tcost = I * (base * (uint32_t)tot + (uint32_t)np);  // < 2^24
       const uint32_t t0 = tcost * blockIdx.x / (uint32_t)p.grid, t1 = tcost * (blockIdx.x + 1) / (uint32_t)p.grid;
       const uint32_t wu = base + (uint32_t)__popc(msk);
       const uint32_t cu = I * (base * (uint32_t)sb + (uint32_t)pb), cn = cu + I * wu;
