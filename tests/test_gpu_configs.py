@@ -218,10 +218,15 @@ def test_fp8_ling_layer(fp8layer, sched, m):
 @pytest.mark.parametrize("shape", [
     synth.LayerShape(hidden=256, inter=128, num_experts=16, top_k=4, num_shared=1, wdtype="fp8"),
     synth.LayerShape(hidden=384, inter=256, num_experts=40, top_k=6, num_shared=2, wdtype="fp8"),
-], ids=["h256", "h384"])
+    synth.LayerShape(hidden=384, inter=128, num_experts=24, top_k=4, num_shared=1, wdtype="fp8"),
+], ids=["h256", "h384", "h384_i128"])
 def test_fp8_small_shapes(shape):
     """Small FP8 layers spanning several scale blocks along both axes (and a ragged
-    expert count), every row count 1..16 in groups, two schedules bit-identical."""
+    expert count), every row count 1..16 in groups, the schedules bit-identical. The
+    block scales ride with the weights when an expert's scale matrix is a whole number
+    of 16-byte units and are read from global memory otherwise: H=256 / I=128 stages
+    its gate/up scales (16 B) but not its down scales (8 B); H=384 / I=128 stages
+    neither (24 B and 12 B)."""
     layer = synth.make_layer(shape, seed=23, device="cuda")
     for m in (1, 2, 5, 8, 13, 16):
         x = helpers.hidden_with_margin(layer["router_w"], m, shape.top_k, seed=80 + m, rho=0.5)
