@@ -195,7 +195,7 @@ def test_graph_capture_replays(tiny):
     dict(hidden=512, inter=256, num_experts=64, top_k=1, num_shared=1),    # top-1
     dict(hidden=1024, inter=768, num_experts=2, top_k=1, num_shared=1),    # E = 2, 96-thread groups
 ])
-@pytest.mark.parametrize("m", [1, 5])
+@pytest.mark.parametrize("m", [1, 5, 8])  # k = E = 16 at m = 8: 128 (row, expert) pairs, the most a launch has
 def test_shapes(cfg, m):
     shape = synth.LayerShape(**cfg)
     layer = synth.make_layer(shape, seed=3, device="cuda")
